@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-MoE expert FFN over 2-bit experts on one or more GB300s.
+
+A step is one call of ds4moe_expert_ffn over one batch of synthetic input: routing,
+grouping, the SwiGLU experts (packed 2-bit routed experts plus the bf16 shared expert) and
+the gate-weighted combine. The default workload is single-token decode (T=1, d_model 4096,
+d_ff 2048, 256 experts, top-8, bf16 shared expert). Under torchrun every rank runs an
+independent replica (no data-path collective; weak scaling).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line. --impl reference times the oracle (the plain fp64 CPU restatement)
+on the host cores on the same workload and metric.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 10 ** 6
+METRIC = "routed-MoE tokens/s"
+IQ2_PER_EXPERT = lambda D, F: 2 * F * D // 256 * 66  # noqa: E731  gate + up
+Q2K_PER_EXPERT = lambda D, F: D * F // 256 * 84      # noqa: E731  down
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_t1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--weights", choices=["quantized", "random"], default=None,
+                    help="routed-expert blobs: host-quantised N(0,0.02) (default for decode) or random valid blocks")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ multi-rank plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over ranks (a timing reduction, not part of the data path)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank, world, max_seconds):
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return None
+        rows = []
+        for line in open(self.path):
+            p = [s.strip() for s in line.split(",")]
+            if len(p) >= 9 and p[1].replace(".", "").isdigit():
+                rows.append(p)
+        if not rows:
+            return None
+        mhz = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload set-up
+
+def touched_experts(ds4, wl, L):
+    import torch
+    idx, _ = ds4.ds4moe_route(torch.from_numpy(L).cuda(), wl.k)
+    return sorted(set(idx.cpu().numpy().reshape(-1).tolist()))
+
+
+def make_weights(ds4, wl, experts, mode):
+    """Blobs for every expert: the touched ones quantised from N(0, 0.02) by the library's
+    host quantiser (or random valid blocks), the others all-zero blocks (never read)."""
+    if mode == "random":
+        return synth.random_expert_blobs(wl, experts)
+    nbi = ds4.ds4moe_iq2_bytes(wl.F, wl.D)
+    nbq = ds4.ds4moe_q2k_bytes(wl.D, wl.F)
+    zi, zq = np.zeros(nbi, np.uint8), np.zeros(nbq, np.uint8)
+    gate, up, down = [zi] * wl.E, [zi] * wl.E, [zq] * wl.E
+    for e in experts:
+        gate[e] = ds4.ds4moe_quantize_iq2(synth.expert_weight(wl.seed, e, synth.GATE, wl.F, wl.D))
+        up[e] = ds4.ds4moe_quantize_iq2(synth.expert_weight(wl.seed, e, synth.UP, wl.F, wl.D))
+        down[e] = ds4.ds4moe_quantize_q2k(synth.expert_weight(wl.seed, e, synth.DOWN, wl.D, wl.F))
+    return gate, up, down
+
+
+def algorithmic(wl, counts):
+    """Bytes and FLOPs the method must move / compute for one call, per stage."""
+    D, F, T, k = wl.D, wl.F, wl.T, wl.k
+    touched = int(np.count_nonzero(counts))
+    P = T * k
+    sh_up = 2 * F * D * 2 if wl.shared else 0
+    sh_down = D * F * 2 if wl.shared else 0
+    rows = P + (T if wl.shared else 0)
+    up_bytes = touched * IQ2_PER_EXPERT(D, F) + sh_up + T * D * 2 + rows * F * 4
+    down_bytes = touched * Q2K_PER_EXPERT(D, F) + sh_down + rows * F * 4 + rows * D * 4
+    flops_up = 2 * 2 * F * D * rows
+    flops_down = 2 * D * F * rows
+    return {"touched": touched, "up_bytes": up_bytes, "down_bytes": down_bytes,
+            "total_bytes": touched * (IQ2_PER_EXPERT(D, F) + Q2K_PER_EXPERT(D, F)) + sh_up + sh_down,
+            "flops_up": flops_up, "flops_down": flops_down}
+
+
+def src_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "bit_quantized_routed_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+STAGE_KERNEL = {"up_gemv": ("gemv_up_kernel", "gemv.cu"), "down_gemv": ("gemv_down_kernel", "gemv.cu"),
+                "combine": ("combine_kernel", "combine.cu"), "route": ("route_kernel", "route_group.cu"),
+                "group": ("group_kernel", "route_group.cu")}
+
+
+def ncu_traffic(stage, workload):
+    """dram read+write bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if stage not in STAGE_KERNEL or not os.path.exists(path):
+        return None
+    kern, src = STAGE_KERNEL[stage]
+    rec = json.load(open(path)).get("%s@%s" % (kern, workload))
+    if not rec or rec.get("src_sha") != src_sha(src):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return p["hbm_gbs"], p["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import bit_quantized_routed_gb300 as ds4
+    ds4.build()
+    wl = synth.WORKLOADS[args.workload]
+    if world > 1:
+        wl = wl.replace(seed=wl.seed + 1000 * rank)   # each replica its own batch
+    mode = args.weights or ("quantized" if wl.T <= 32 else "random")
+    L, x = synth.draw_inputs(wl)
+    experts = touched_experts(ds4, wl, L)
+    gate, up, down = make_weights(ds4, wl, experts, mode)
+    shared = synth.shared_weights(wl.seed, wl.D, wl.F) if wl.shared else None
+    W = ds4.ds4moe_weights_create(gate, up, down, wl.D, wl.F, shared=shared, max_tokens=wl.T, max_k=wl.k)
+    del gate, up, down
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    Ld = torch.from_numpy(L).cuda()
+    out = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    counts, _, _, _ = ds4.ds4moe_group(ds4.ds4moe_route(Ld, wl.k)[0], wl.E)
+    alg = algorithmic(wl, counts.cpu().numpy())
+    flush = alg["total_bytes"] < 4 * L2_BYTES
+    if flush:
+        fw = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
+        fr = torch.ones(64 * 2 ** 20, dtype=torch.float32, device="cuda")
+
+    def l2_flush():
+        fw.zero_()           # write more than L2 ...
+        fr.sum()             # ... then read more than L2, so no dirty line is left behind
+
+    def step():
+        ds4.ds4moe_expert_ffn(xd, W, Ld, wl.k, out)
+
+    for _ in range(max(3, args.warmup)):
+        if flush:
+            l2_flush()
+        step()
+    st = ds4.ds4moe_last_status(W)
+    if st:
+        raise RuntimeError(ds4.ds4moe_strerror(st))
+
+    # ---- timed region: K steps, device time from CUDA events on the launching stream
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    launches0 = ds4.ds4moe_get_stats(W)["launches"]
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        barrier(world)
+        for i in range(K):
+            if flush:
+                l2_flush()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    launches = ds4.ds4moe_get_stats(W)["launches"] - launches0
+    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
+    max_ms = reduce_max(dev_ms, world, "cuda")
+    value = whole_job_rate(K * wl.T, world, max_ms / 1e3)
+
+    # ---- per-stage device times (events around each stage, same stream)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_PROFILE, 1)
+    stage_tot = {n: 0.0 for n in ds4.STAGES}
+    for i in range(K):
+        if flush:
+            l2_flush()
+        step()
+        for n, v in ds4.ds4moe_get_stats(W)["stage_ms"].items():
+            stage_tot[n] += v
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_PROFILE, 0)
+    dom = max(stage_tot, key=stage_tot.get)
+    dom_ms = stage_tot[dom] / K
+
+    # ---- end to end through the public API: pinned host buffers, copies inside the region
+    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Lh = torch.from_numpy(L).pin_memory()
+    out_in = torch.zeros((wl.T, wl.D), dtype=torch.float32).pin_memory()
+    out_h = torch.empty((wl.T, wl.D), dtype=torch.float32).pin_memory()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        if flush:
+            l2_flush()
+        e2e_ev[i][0].record(stream)
+        xd.copy_(xh, non_blocking=True)
+        Ld.copy_(Lh, non_blocking=True)
+        out.copy_(out_in, non_blocking=True)
+        ds4.ds4moe_expert_ffn(xd, W, Ld, wl.k, out)
+        out_h.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, "cuda")
+    h2d = wl.T * wl.D * 2 + wl.T * wl.E * 4 + wl.T * wl.D * 4
+    d2h = wl.T * wl.D * 4
+    st = ds4.ds4moe_last_status(W)
+    if st:
+        raise RuntimeError(ds4.ds4moe_strerror(st))
+
+    hbm, tflops, peak_src = load_peaks()
+    if dom in ("up_gemv", "down_gemv", "combine", "route", "group"):
+        b = alg["up_bytes"] if dom == "up_gemv" else alg["down_bytes"] if dom == "down_gemv" else None
+        if dom == "combine":
+            b = (wl.T * wl.k + wl.T) * wl.D * 4 + 2 * wl.T * wl.D * 4
+        achieved = (b / (dom_ms / 1e3) / 1e9) if b else None
+        roof = {"bound": "hbm", "kernel": STAGE_KERNEL.get(dom, (dom,))[0], "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": (achieved / hbm) if achieved else None,
+                "traffic": ncu_traffic(dom, wl.name), "algorithmic_bytes": b, "avg_launch_ms": dom_ms,
+                "peak_source": peak_src}
+    else:
+        f = alg["flops_up"] if dom == "up_gemm" else alg["flops_down"]
+        achieved = f / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops, "traffic": None, "algorithmic_flops": f, "avg_launch_ms": dom_ms,
+                "peak_source": peak_src}
+    roof["stage_ms"] = {n: round(v / K, 5) for n, v in stage_tot.items() if v > 0}
+    roof["call_hbm_gbs"] = alg["total_bytes"] / (max_ms / K / 1e3) / 1e9
+    roof["call_hbm_frac"] = roof["call_hbm_gbs"] / hbm
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": max_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F, "experts": wl.E,
+                       "top_k": wl.k, "shared_expert": "bf16" if wl.shared else None,
+                       "routed_weights": "2-bit IQ2-style gate/up + Q2_K-style down, " +
+                                         ("host-quantised N(0,0.02)" if mode == "quantized" else "random valid blocks"),
+                       "experts_touched": alg["touched"],
+                       "l2": "flushed between steps (write then read 256 MB)" if flush else "working set > 4x L2",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "gpu_launches": int(launches),
+            "e2e": {"value": whole_job_rate(K * wl.T, world, e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": roof, "clocks": clocks.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    W.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ the oracle on the host
+
+def cpu_baseline(workload, seconds):
+    """Runs the oracle in a fresh single-threaded process (spawned, not forked)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", "--workload", workload,
+                          "--cpu-seconds", str(seconds)], capture_output=True, text=True, env=env, timeout=900)
+    if out.returncode:
+        return {"value": None, "error": out.stderr.strip().splitlines()[-1:] or ["failed"]}
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_worker(workload, seconds):
+    import oracle
+    oracle.build()
+    wl = synth.WORKLOADS[workload]
+    L, x = synth.draw_inputs(wl)
+    # the oracle's FFN cost does not depend on block contents: random valid blocks stand in
+    # for the quantised experts so that the baseline does not time quantisation
+    per = max(1, min(wl.T, 4))
+    n_tok, calls, el = 0, 0, 0.0
+    rng = np.random.default_rng(0)
+    sh = synth.shared_weights(wl.seed, wl.D, wl.F) if wl.shared else None
+    while el < seconds:
+        toks = np.sort(rng.choice(wl.T, per, replace=False)) if wl.T > per else np.arange(wl.T)
+        idx, _ = oracle.route(L[toks], wl.k)
+        gate, up, down = synth.random_expert_blobs(wl, np.unique(idx))
+        t1 = time.perf_counter()
+        oracle.moe_ffn(x[toks], L[toks], wl.k, gate, up, down, wl.D, wl.F, shared=sh)
+        el += time.perf_counter() - t1
+        n_tok += len(toks)
+        calls += 1
+    print(json.dumps({"value": n_tok / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                      "sample": "%d oracle call(s) of %d token(s) each from %s, %.1f s of oracle time "
+                                "(fp64, one thread; random valid 2-bit blocks; input generation excluded)"
+                                % (calls, per, workload, el)}))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    cb = cpu_baseline(args.workload, max(5.0, min(60.0, args.cpu_seconds)))
+    v = cb.get("value")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": (1e3 * wl.T / v) if v else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F,
+                                            "experts": wl.E, "top_k": wl.k},
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_worker:
+        cpu_worker(args.workload, args.cpu_seconds)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

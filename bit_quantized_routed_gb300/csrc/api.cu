@@ -1,0 +1,352 @@
+// The C ABI: weights handle (validation, repack, upload, workspace), the device entry points
+// and their launch sequence. Arguments are checked here, on the host, before any launch.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+using namespace ds4moe;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <class T>
+int dev_alloc(ds4moe_weights *h, T **p, size_t bytes) {
+    *p = nullptr;
+    if (h->n_allocs >= static_cast<int>(sizeof(h->allocs) / sizeof(h->allocs[0]))) return DS4MOE_ENOMEM;
+    void *q = nullptr;
+    if (cudaMalloc(&q, bytes ? bytes : 16) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ENOMEM;
+    }
+    h->allocs[h->n_allocs++] = q;
+    *p = static_cast<T *>(q);
+    return DS4MOE_OK;
+}
+
+void free_all(ds4moe_weights *h) {
+    for (int i = 0; i < h->n_allocs; i++) cudaFree(h->allocs[i]);
+    h->n_allocs = 0;
+}
+
+int cuda_status(int err) {
+    if (err == 0) return DS4MOE_OK;
+    return DS4MOE_ECUDA;
+}
+
+#define TRY(x)                        \
+    do {                              \
+        const int rc_ = (x);          \
+        if (rc_ != DS4MOE_OK) {       \
+            free_all(h);              \
+            delete h;                 \
+            return rc_;               \
+        }                             \
+    } while (0)
+
+int upload(void *dst, const void *src, size_t bytes) {
+    return cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice) == cudaSuccess ? DS4MOE_OK : DS4MOE_ECUDA;
+}
+
+// Split IQ2-style blocks [rows][nb][66] into payload [rows][nb][64] and scales [rows][nb].
+bool repack_iq2(const uint8_t *src, size_t nblocks, uint8_t *qs, uint16_t *d) {
+    for (size_t b = 0; b < nblocks; b++) {
+        const uint8_t *blk = src + b * 66;
+        const uint16_t dv = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
+        if (!host_f16_finite(dv)) return false;
+        d[b] = dv;
+        std::memcpy(qs + b * 64, blk + 2, 64);
+    }
+    return true;
+}
+
+// Split Q2_K-style blocks [rows][nb][84] into payload [rows][nb][80] and (d, dmin) pairs.
+bool repack_q2k(const uint8_t *src, size_t nblocks, uint8_t *sq, uint32_t *dd) {
+    for (size_t b = 0; b < nblocks; b++) {
+        const uint8_t *blk = src + b * 84;
+        const uint16_t dv = static_cast<uint16_t>(blk[80] | (blk[81] << 8));
+        const uint16_t mv = static_cast<uint16_t>(blk[82] | (blk[83] << 8));
+        if (!host_f16_finite(dv) || !host_f16_finite(mv)) return false;
+        dd[b] = static_cast<uint32_t>(dv) | (static_cast<uint32_t>(mv) << 16);
+        std::memcpy(sq + b * 80, blk, 80);
+    }
+    return true;
+}
+
+// bf16 bits -> fp16 bits, nearest-even (exact for values in fp16's normal range).
+uint16_t bf16_to_f16(uint16_t b) {
+    const uint32_t u = static_cast<uint32_t>(b) << 16;  // the binary32 value of the bf16
+    const uint32_t sign = (u >> 16) & 0x8000u;
+    const uint32_t mag = u & 0x7fffffffu;
+    if (mag >= 0x7f800000u) return static_cast<uint16_t>(sign | (mag > 0x7f800000u ? 0x7e00u : 0x7c00u));
+    const int e = static_cast<int>(mag >> 23) - 127;
+    if (e > 15) return static_cast<uint16_t>(sign | 0x7c00u);
+    if (e < -25) return static_cast<uint16_t>(sign);
+    const uint32_t sig = (mag & 0x7fffffu) | 0x800000u;
+    const int drop = e >= -14 ? 13 : 13 + (-14 - e);
+    uint32_t q = sig >> drop;
+    const uint32_t rem = sig & ((1u << drop) - 1u), half = 1u << (drop - 1);
+    if (rem > half || (rem == half && (q & 1u))) q++;
+    uint32_t h = e >= -14 ? (static_cast<uint32_t>(e + 15) << 10) + (q - 1024u) : q;
+    if (h >= 0x7c00u) h = 0x7c00u;
+    return static_cast<uint16_t>(sign | h);
+}
+
+// Counts launches per stage and, when profiling, records an event at each stage start and
+// one at the end of the call, all on the call's stream.
+struct StageClock {
+    ds4moe_weights *h;
+    cudaStream_t s;
+    StageClock(ds4moe_weights *h_, ds4moe_stream_t s_) : h(h_), s(s_) {
+        for (bool &r : h->stage_ran) r = false;
+        h->events_recorded = false;
+    }
+    int stage(int i) {
+        h->stage_ran[i] = true;
+        h->launches++;
+        if (!h->profile) return 0;
+        return static_cast<int>(cudaEventRecord(static_cast<cudaEvent_t>(h->events[i]), s));
+    }
+    int finish() {
+        if (!h->profile) return 0;
+        h->events_recorded = true;
+        return static_cast<int>(cudaEventRecord(static_cast<cudaEvent_t>(h->events[DS4MOE_N_STAGES]), s));
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out) {
+    if (!desc || !out) return DS4MOE_EINVAL;
+    *out = nullptr;
+    const int D = desc->d_model, F = desc->d_ff, E = desc->n_experts;
+    if (D <= 0 || F <= 0 || D % 256 || F % 256 || E < 1 || E > 1024) return DS4MOE_EINVAL;
+    if (desc->max_tokens < 1 || desc->max_k < 1 || desc->max_k > 32 || desc->max_k > E) return DS4MOE_EINVAL;
+    if (!desc->gate_iq2 || !desc->up_iq2 || !desc->down_q2k) return DS4MOE_EINVAL;
+    for (int e = 0; e < E; e++)
+        if (!desc->gate_iq2[e] || !desc->up_iq2[e] || !desc->down_q2k[e]) return DS4MOE_EINVAL;
+    const int n_shared = (desc->shared_gate_bf16 != nullptr) + (desc->shared_up_bf16 != nullptr) +
+                         (desc->shared_down_bf16 != nullptr);
+    if (n_shared != 0 && n_shared != 3) return DS4MOE_EINVAL;
+    const int64_t P = static_cast<int64_t>(desc->max_tokens) * desc->max_k;
+    if (P > (int64_t(1) << 30)) return DS4MOE_EINVAL;
+
+    ds4moe_weights *h = new (std::nothrow) ds4moe_weights();
+    if (!h) return DS4MOE_ENOMEM;
+    if (cudaGetDevice(&h->device) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return DS4MOE_ECUDA;
+    }
+    h->gemm_min_tokens = 33;
+    h->shared_gemm_min_tokens = 33;
+    DeviceWeights &w = h->dw;
+    w.D = D;
+    w.F = F;
+    w.E = E;
+    w.nbD = D / 256;
+    w.nbF = F / 256;
+    w.has_shared = n_shared == 3;
+    const size_t nb_up = static_cast<size_t>(F) * w.nbD;    // blocks per gate/up matrix
+    const size_t nb_down = static_cast<size_t>(D) * w.nbF;  // blocks per down matrix
+    TRY(dev_alloc(h, &w.gate_qs, E * nb_up * 64));
+    TRY(dev_alloc(h, &w.up_qs, E * nb_up * 64));
+    TRY(dev_alloc(h, &w.gate_d, E * nb_up * 2));
+    TRY(dev_alloc(h, &w.up_d, E * nb_up * 2));
+    TRY(dev_alloc(h, &w.down_sq, E * nb_down * 80));
+    TRY(dev_alloc(h, &w.down_dd, E * nb_down * 4));
+    {
+        std::vector<uint8_t> qs(nb_up * 64), sq(nb_down * 80);
+        std::vector<uint16_t> dv(nb_up);
+        std::vector<uint32_t> dd(nb_down);
+        for (int e = 0; e < E; e++) {
+            const void *mats[2] = {desc->gate_iq2[e], desc->up_iq2[e]};
+            uint8_t *dqs[2] = {w.gate_qs, w.up_qs};
+            uint16_t *dds[2] = {w.gate_d, w.up_d};
+            for (int m = 0; m < 2; m++) {
+                if (!repack_iq2(static_cast<const uint8_t *>(mats[m]), nb_up, qs.data(), dv.data())) TRY(DS4MOE_EBADDATA);
+                TRY(upload(dqs[m] + e * nb_up * 64, qs.data(), nb_up * 64));
+                TRY(upload(dds[m] + e * nb_up, dv.data(), nb_up * 2));
+            }
+            if (!repack_q2k(static_cast<const uint8_t *>(desc->down_q2k[e]), nb_down, sq.data(), dd.data()))
+                TRY(DS4MOE_EBADDATA);
+            TRY(upload(w.down_sq + e * nb_down * 80, sq.data(), nb_down * 80));
+            TRY(upload(w.down_dd + e * nb_down, dd.data(), nb_down * 4));
+        }
+    }
+    if (w.has_shared) {
+        const size_t n = static_cast<size_t>(F) * D;
+        TRY(dev_alloc(h, &w.sh_gate, n * 2));
+        TRY(dev_alloc(h, &w.sh_up, n * 2));
+        TRY(dev_alloc(h, &w.sh_down, n * 2));
+        TRY(dev_alloc(h, &w.sh_down_f16, n * 2));
+        TRY(upload(w.sh_gate, desc->shared_gate_bf16, n * 2));
+        TRY(upload(w.sh_up, desc->shared_up_bf16, n * 2));
+        TRY(upload(w.sh_down, desc->shared_down_bf16, n * 2));
+        std::vector<uint16_t> f16(n);
+        for (size_t i = 0; i < n; i++) f16[i] = bf16_to_f16(desc->shared_down_bf16[i]);
+        TRY(upload(w.sh_down_f16, f16.data(), n * 2));
+    }
+    Workspace &ws = h->ws;
+    ws.max_T = desc->max_tokens;
+    ws.max_k = desc->max_k;
+    const size_t rows = static_cast<size_t>(P) + desc->max_tokens;
+    TRY(dev_alloc(h, &ws.topk_idx, P * 4));
+    TRY(dev_alloc(h, &ws.topk_w, P * 4));
+    TRY(dev_alloc(h, &ws.counts, E * 4));
+    TRY(dev_alloc(h, &ws.offsets, (E + 1) * 4));
+    TRY(dev_alloc(h, &ws.perm, P * 4));
+    TRY(dev_alloc(h, &ws.inv, P * 4));
+    TRY(dev_alloc(h, &ws.gemv_list, E * 4));
+    TRY(dev_alloc(h, &ws.gemm_list, E * 4));
+    TRY(dev_alloc(h, &ws.meta, sizeof(GroupMeta)));
+    TRY(dev_alloc(h, &ws.grid, 2048));
+    TRY(dev_alloc(h, &ws.h32, rows * F * 4));
+    TRY(dev_alloc(h, &ws.h16, rows * F * 2));
+    TRY(dev_alloc(h, &ws.x16, rows * D * 2));
+    TRY(dev_alloc(h, &ws.y, rows * D * 4));
+    TRY(dev_alloc(h, &ws.status, 16));
+    {
+        uint8_t g[2048];
+        host_grid(g);
+        TRY(upload(ws.grid, g, 2048));
+    }
+    if (cudaMemset(ws.status, 0, 16) != cudaSuccess) TRY(DS4MOE_ECUDA);
+    if (cudaDeviceSynchronize() != cudaSuccess) TRY(DS4MOE_ECUDA);
+    *out = h;
+    return DS4MOE_OK;
+}
+
+void ds4moe_weights_destroy(ds4moe_weights *h) {
+    if (!h) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    for (auto &ev : h->events)
+        if (ev) cudaEventDestroy(static_cast<cudaEvent_t>(ev));
+    free_all(h);
+    cudaSetDevice(cur);
+    delete h;
+}
+
+int ds4moe_set_option(ds4moe_weights *h, int option, int value) {
+    if (!h || value < 0) return DS4MOE_EINVAL;
+    switch (option) {
+        case DS4MOE_OPT_GEMM_MIN_TOKENS: h->gemm_min_tokens = value; return DS4MOE_OK;
+        case DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS: h->shared_gemm_min_tokens = value; return DS4MOE_OK;
+        case DS4MOE_OPT_PROFILE:
+            if (value && !h->events[0]) {
+                for (auto &ev : h->events) {
+                    cudaEvent_t e;
+                    if (cudaEventCreate(&e) != cudaSuccess) return DS4MOE_ECUDA;
+                    ev = e;
+                }
+            }
+            h->profile = value ? 1 : 0;
+            return DS4MOE_OK;
+        default: return DS4MOE_EINVAL;
+    }
+}
+
+int ds4moe_weights_dequantize(const ds4moe_weights *h, int expert, int matrix, float *dst_f32, uint16_t *dst_f16,
+                              ds4moe_stream_t stream) {
+    if (!h || expert < 0 || expert >= h->dw.E || matrix < 0 || matrix > 2 || (!dst_f32 && !dst_f16))
+        return DS4MOE_EINVAL;
+    return cuda_status(launch_dequant(h->dw, h->ws.grid, expert, matrix, dst_f32, dst_f16, stream));
+}
+
+int ds4moe_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *topk_idx, float *topk_w,
+                 ds4moe_stream_t stream) {
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return DS4MOE_EINVAL;
+    if (gate_mode != DS4MOE_GATE_SOFTMAX && gate_mode != DS4MOE_GATE_SIGMOID) return DS4MOE_EINVAL;
+    if (T == 0) return DS4MOE_OK;
+    if (!logits || !topk_idx || !topk_w) return DS4MOE_EINVAL;
+    return cuda_status(launch_route(logits, T, E, k, gate_mode, topk_idx, topk_w, stream));
+}
+
+int ds4moe_group(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
+                 int32_t *inv, ds4moe_stream_t stream) {
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32) return DS4MOE_EINVAL;
+    if (static_cast<int64_t>(T) * k > (int64_t(1) << 30)) return DS4MOE_EINVAL;
+    if (!counts || !offsets || (T > 0 && (!topk_idx || !perm || !inv))) return DS4MOE_EINVAL;
+    return cuda_status(launch_group(topk_idx, T, k, E, 0, counts, offsets, perm, inv, nullptr, nullptr, nullptr,
+                                    nullptr, stream));
+}
+
+int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits, int T, int k, int gate_mode,
+                      float *out, ds4moe_stream_t stream) {
+    if (!h) return DS4MOE_EINVAL;
+    if (T < 0 || T > h->ws.max_T || k < 1 || k > h->ws.max_k || k > h->dw.E) return DS4MOE_EINVAL;
+    if (gate_mode != DS4MOE_GATE_SOFTMAX && gate_mode != DS4MOE_GATE_SIGMOID) return DS4MOE_EINVAL;
+    if (T == 0) return DS4MOE_OK;
+    if (!x || !logits || !out || !aligned16(x) || !aligned16(out)) return DS4MOE_EINVAL;
+    const DeviceWeights &w = h->dw;
+    const Workspace &ws = h->ws;
+    StageClock clk(h, stream);
+    int rc = clk.stage(DS4MOE_STAGE_ROUTE);
+    if (!rc) rc = launch_route(logits, T, w.E, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
+    if (!rc) rc = clk.stage(DS4MOE_STAGE_GROUP);
+    if (!rc)
+        rc = launch_group(ws.topk_idx, T, k, w.E, 0, ws.counts, ws.offsets, ws.perm, ws.inv, ws.gemv_list,
+                          ws.gemm_list, ws.meta, ws.status, stream);
+    const bool shared_gemv = w.has_shared;
+    if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMV);
+    if (!rc) rc = launch_gemv_up(w, ws, x, T, k, shared_gemv, stream);
+    if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMV);
+    if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_gemv, stream);
+    if (!rc) rc = clk.stage(DS4MOE_STAGE_COMBINE);
+    if (!rc) rc = launch_combine(w, ws, T, k, out, stream);
+    if (!rc) rc = clk.finish();
+    h->calls++;
+    return cuda_status(rc);
+}
+
+int ds4moe_get_stats(ds4moe_weights *h, ds4moe_stats *out) {
+    if (!h || !out) return DS4MOE_EINVAL;
+    std::memset(out, 0, sizeof *out);
+    out->calls = h->calls;
+    out->launches = h->launches;
+    if (!h->events_recorded) return DS4MOE_OK;
+    if (cudaEventSynchronize(static_cast<cudaEvent_t>(h->events[DS4MOE_N_STAGES])) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ECUDA;
+    }
+    for (int i = 0; i < DS4MOE_N_STAGES; i++) {
+        if (!h->stage_ran[i]) continue;
+        int j = i + 1;  // the next recorded event ends this stage
+        while (j < DS4MOE_N_STAGES && !h->stage_ran[j]) j++;
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, static_cast<cudaEvent_t>(h->events[i]),
+                                 static_cast<cudaEvent_t>(h->events[j])) != cudaSuccess) {
+            cudaGetLastError();
+            return DS4MOE_ECUDA;
+        }
+        out->stage_ms[i] = ms;
+    }
+    return DS4MOE_OK;
+}
+
+int ds4moe_last_status(ds4moe_weights *h, ds4moe_stream_t stream) {
+    if (!h) return DS4MOE_EINVAL;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ECUDA;
+    }
+    int st = 0;
+    if (cudaMemcpy(&st, h->ws.status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return DS4MOE_ECUDA;
+    if (cudaMemset(h->ws.status, 0, sizeof st) != cudaSuccess) return DS4MOE_ECUDA;
+    if (st & ST_RANGE) return DS4MOE_ERANGE;
+    if (st & ST_TIMEOUT) return DS4MOE_ETIMEOUT;
+    if (st & ST_BADIDX) return DS4MOE_EINVAL;
+    return DS4MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Device helpers shared by the kernels: block decoding, warp reductions, status reporting.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace ds4moe {
+
+constexpr int kWarp = 32;
+
+__device__ __forceinline__ void report(int *status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ float f16_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// silu(v) * u with the fast exponential; |error| ~ 1e-7 relative.
+__device__ __forceinline__ float swiglu(float v, float u) { return v / (1.0f + __expf(-v)) * u; }
+
+// ---------------------------------------------------------------- IQ2-style decode
+// One group of 8 weights: w_i = scale * G[idx][i] * sign_i, exact in fp32.
+// grid_entry: the 8 magnitude bytes of G[idx] (lo word = elements 0..3);
+// s7: the 7 stored sign bits; element 7's sign is their parity.
+__device__ __forceinline__ void iq2_group(uint2 grid_entry, uint32_t s7, float scale, float w[8]) {
+    const uint32_t signs = s7 | ((__popc(s7) & 1u) << 7);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const uint32_t m = ((i < 4 ? grid_entry.x : grid_entry.y) >> (8 * (i & 3))) & 0xffu;
+        const float v = __fmul_rn(scale, static_cast<float>(m));
+        w[i] = __uint_as_float(__float_as_uint(v) ^ (((signs >> i) & 1u) << 31));
+    }
+}
+
+// Scale of one 32-weight sub-block: d * (s+1) / 16, exact in fp32.
+__device__ __forceinline__ float iq2_scale(float d, uint32_t word) {
+    return __fmul_rn(__fmul_rn(d, static_cast<float>((word >> 28) + 1u)), 0.0625f);
+}
+
+// ---------------------------------------------------------------- Q2_K-style decode
+// Weight with code q in a sub-block with ds = d*sc and dm = dmin*m (both exact):
+// one rounding of the exact ds*q - dm.
+__device__ __forceinline__ float q2k_weight(float ds, float dm, uint32_t q) {
+    return __fmaf_rn(ds, static_cast<float>(q), -dm);
+}
+
+}  // namespace ds4moe

@@ -1,0 +1,461 @@
+// Fused dequant-GEMV path for decode-sized expert groups (and the shared expert at small T).
+//
+// Memory-bound: each routed expert's packed rows are streamed once per call with 128-bit
+// coalesced loads, decoded in registers (the IQ2 grid lives in shared memory), and dotted
+// with the group's tokens, staged in shared memory. Phase 1 computes
+// h = silu(W_gate x) * (W_up x) for each row of F; phase 2 computes y = W_down h.
+// Everything accumulates in fp32 on exact fp32 weight values.
+//
+// Source: "DwarfStar" README, "运行大于 RAM 的模型" -- every new token is routed through
+// the experts again, so decode streams expert weights; "Part 5: 服务层" §6 -- the ready
+// decode steps of several sessions run in one batched kernel, weights read once.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace ds4moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUpRows = 16;        // routed rows (of F) per phase-1 item: 2 per warp
+constexpr int kUpSharedRows = 8;   // shared-expert rows per phase-1 item: 1 per warp
+constexpr int kDownRows = 32;      // routed rows (of D) per phase-2 item: 4 per warp
+constexpr int kDownSharedRows = 8; // shared-expert rows per phase-2 item: 1 per warp
+
+struct Items {
+    int routed;       // routed items
+    int total;        // routed + shared items
+    int per_group;    // routed items per group
+};
+
+// Contiguous item range of this CTA, so consecutive items usually share a group and the
+// staged tokens are reused.
+__device__ __forceinline__ void cta_range(int total, int &begin, int &end) {
+    const int per = (total + gridDim.x - 1) / gridDim.x;
+    begin = min(total, blockIdx.x * per);
+    end = min(total, begin + per);
+}
+
+// Swizzled index of 16-byte chunk c in a staged token row (bank-conflict-free for the
+// lane-strided access patterns below).
+__device__ __forceinline__ int swz8(int c) { return c ^ ((c >> 3) & 7); }
+__device__ __forceinline__ int swz16(int c) { return c ^ ((c >> 4) & 7); }
+
+__device__ __forceinline__ void dot8_bf16(const float w[8], uint4 xv, float &acc) {
+    acc = fmaf(w[0], bf16_lo(xv.x), acc);
+    acc = fmaf(w[1], bf16_hi(xv.x), acc);
+    acc = fmaf(w[2], bf16_lo(xv.y), acc);
+    acc = fmaf(w[3], bf16_hi(xv.y), acc);
+    acc = fmaf(w[4], bf16_lo(xv.z), acc);
+    acc = fmaf(w[5], bf16_hi(xv.z), acc);
+    acc = fmaf(w[6], bf16_lo(xv.w), acc);
+    acc = fmaf(w[7], bf16_hi(xv.w), acc);
+}
+
+__device__ __forceinline__ void bf16x8(uint4 v, float w[8]) {
+    w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+    w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
+    acc = fmaf(a.z, b.z, acc);
+    return fmaf(a.w, b.w, acc);
+}
+
+struct UpParams {
+    DeviceWeights w;
+    const uint16_t *x;  // bf16 [T][D]
+    const int32_t *perm, *offsets, *gemv_list;
+    const GroupMeta *meta;
+    const uint8_t *grid;  // [256][8]
+    float *h;             // [P+T][F]
+    int T, k, P;
+    int shared;           // shared expert on this path
+};
+
+// Phase 1: h[pos][r] = silu(gate_r . x) * (up_r . x) for the group's tokens.
+template <int NT>
+__global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint2 *grid_s = reinterpret_cast<uint2 *>(smem);              // 256 x 8 B
+    uint4 *xs = reinterpret_cast<uint4 *>(smem + 2048);           // [NT][D/8] swizzled
+    const int D = p.w.D, F = p.w.F, nbD = p.w.nbD, D8 = D / 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 256; i += kThreads) grid_s[i] = reinterpret_cast<const uint2 *>(p.grid)[i];
+
+    const int n_gemv = p.meta->n_gemv;
+    const int per_group = F / kUpRows;
+    const int routed = n_gemv * per_group;
+    const int total = routed + (p.shared ? F / kUpSharedRows : 0);
+    int begin, end;
+    cta_range(total, begin, end);
+    int staged_key = -1, staged_tok0 = -1;  // which tokens sit in xs
+    __syncthreads();
+
+    for (int item = begin; item < end; item++) {
+        const bool is_routed = item < routed;
+        int e = 0, off = 0, n = 0, r0 = 0, key = -2;
+        if (is_routed) {
+            const int gi = item / per_group;
+            e = p.gemv_list[gi];
+            off = p.offsets[e];
+            n = p.offsets[e + 1] - off;
+            r0 = (item % per_group) * kUpRows;
+            key = e;
+        } else {
+            n = p.T;
+            off = p.P;
+            r0 = (item - routed) * kUpSharedRows;
+        }
+        for (int tok0 = 0; tok0 < n; tok0 += NT) {
+            const int nt = min(NT, n - tok0);
+            if (key != staged_key || tok0 != staged_tok0) {
+                __syncthreads();
+                for (int i = threadIdx.x; i < nt * D8; i += kThreads) {
+                    const int j = i / D8, c = i - j * D8;
+                    const int tok = is_routed ? p.perm[off + tok0 + j] / p.k : tok0 + j;
+                    xs[j * D8 + swz8(c)] = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(tok) * D)[c];
+                }
+                __syncthreads();
+                staged_key = key;
+                staged_tok0 = tok0;
+            }
+            if (is_routed) {
+#pragma unroll 1
+                for (int rr = 0; rr < kUpRows / kWarps; rr++) {
+                    const int r = r0 + warp + rr * kWarps;
+                    const size_t rowb = (static_cast<size_t>(e) * F + r) * nbD;
+                    const uint4 *qg = reinterpret_cast<const uint4 *>(p.w.gate_qs + rowb * 64);
+                    const uint4 *qu = reinterpret_cast<const uint4 *>(p.w.up_qs + rowb * 64);
+                    const uint16_t *dg = p.w.gate_d + rowb;
+                    const uint16_t *du = p.w.up_d + rowb;
+                    float ag[NT], au[NT];
+#pragma unroll
+                    for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
+                    for (int c = lane; c < nbD * 4; c += 32) {
+                        const uint4 vg = __ldg(qg + c), vu = __ldg(qu + c);
+                        const float sdg = f16_to_f32(__ldg(dg + (c >> 2)));
+                        const float sdu = f16_to_f32(__ldg(du + (c >> 2)));
+#pragma unroll
+                        for (int sb = 0; sb < 2; sb++) {
+                            const uint32_t ig = sb ? vg.z : vg.x, wgd = sb ? vg.w : vg.y;
+                            const uint32_t iu = sb ? vu.z : vu.x, wud = sb ? vu.w : vu.y;
+                            const float scg = iq2_scale(sdg, wgd), scu = iq2_scale(sdu, wud);
+#pragma unroll
+                            for (int g = 0; g < 4; g++) {
+                                float wg[8], wu[8];
+                                iq2_group(grid_s[(ig >> (8 * g)) & 255u], (wgd >> (7 * g)) & 127u, scg, wg);
+                                iq2_group(grid_s[(iu >> (8 * g)) & 255u], (wud >> (7 * g)) & 127u, scu, wu);
+                                const int xc = swz8(8 * c + 4 * sb + g);
+#pragma unroll
+                                for (int j = 0; j < NT; j++) {
+                                    if (j < nt) {
+                                        const uint4 xv = xs[j * D8 + xc];
+                                        dot8_bf16(wg, xv, ag[j]);
+                                        dot8_bf16(wu, xv, au[j]);
+                                    }
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; j++) {
+                        if (j < nt) {
+                            const float g = warp_sum(ag[j]), u = warp_sum(au[j]);
+                            if (lane == 0) p.h[static_cast<size_t>(off + tok0 + j) * F + r] = swiglu(g, u);
+                        }
+                    }
+                }
+            } else {
+                const int r = r0 + warp;
+                const uint4 *sg = reinterpret_cast<const uint4 *>(p.w.sh_gate + static_cast<size_t>(r) * D);
+                const uint4 *su = reinterpret_cast<const uint4 *>(p.w.sh_up + static_cast<size_t>(r) * D);
+                float ag[NT], au[NT];
+#pragma unroll
+                for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
+                for (int c = lane; c < D8; c += 32) {
+                    float wg[8], wu[8];
+                    bf16x8(__ldg(sg + c), wg);
+                    bf16x8(__ldg(su + c), wu);
+                    const int xc = swz8(c);
+#pragma unroll
+                    for (int j = 0; j < NT; j++) {
+                        if (j < nt) {
+                            const uint4 xv = xs[j * D8 + xc];
+                            dot8_bf16(wg, xv, ag[j]);
+                            dot8_bf16(wu, xv, au[j]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < NT; j++) {
+                    if (j < nt) {
+                        const float g = warp_sum(ag[j]), u = warp_sum(au[j]);
+                        if (lane == 0) p.h[static_cast<size_t>(off + tok0 + j) * F + r] = swiglu(g, u);
+                    }
+                }
+            }
+        }
+    }
+}
+
+struct DownParams {
+    DeviceWeights w;
+    const int32_t *offsets, *gemv_list;
+    const GroupMeta *meta;
+    const float *h;  // [P+T][F]
+    float *y;        // [P+T][D]
+    int T, P;
+    int shared;
+};
+
+// Phase 2: y[pos][r] = down_r . h[pos] for the group's tokens.
+template <int NT>
+__global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    float4 *hs = reinterpret_cast<float4 *>(smem);  // [NT][F/4] swizzled
+    const int D = p.w.D, F = p.w.F, nbF = p.w.nbF, F4 = F / 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n_gemv = p.meta->n_gemv;
+    const int per_group = D / kDownRows;
+    const int routed = n_gemv * per_group;
+    const int total = routed + (p.shared ? D / kDownSharedRows : 0);
+    int begin, end;
+    cta_range(total, begin, end);
+    int staged_key = -1, staged_tok0 = -1;
+
+    for (int item = begin; item < end; item++) {
+        const bool is_routed = item < routed;
+        int e = 0, off = 0, n = 0, r0 = 0, key = -2;
+        if (is_routed) {
+            const int gi = item / per_group;
+            e = p.gemv_list[gi];
+            off = p.offsets[e];
+            n = p.offsets[e + 1] - off;
+            r0 = (item % per_group) * kDownRows;
+            key = e;
+        } else {
+            n = p.T;
+            off = p.P;
+            r0 = (item - routed) * kDownSharedRows;
+        }
+        for (int tok0 = 0; tok0 < n; tok0 += NT) {
+            const int nt = min(NT, n - tok0);
+            if (key != staged_key || tok0 != staged_tok0) {
+                __syncthreads();
+                for (int i = threadIdx.x; i < nt * F4; i += kThreads) {
+                    const int j = i / F4, c = i - j * F4;
+                    hs[j * F4 + swz16(c)] = reinterpret_cast<const float4 *>(p.h + static_cast<size_t>(off + tok0 + j) * F)[c];
+                }
+                __syncthreads();
+                staged_key = key;
+                staged_tok0 = tok0;
+            }
+            if (is_routed) {
+#pragma unroll 1
+                for (int rr = 0; rr < kDownRows / kWarps; rr++) {
+                    const int r = r0 + warp + rr * kWarps;
+                    const size_t rowb = (static_cast<size_t>(e) * D + r) * nbF;
+                    const uint8_t *sq = p.w.down_sq + rowb * 80;
+                    const uint32_t *dd = p.w.down_dd + rowb;
+                    float acc[NT];
+#pragma unroll
+                    for (int j = 0; j < NT; j++) acc[j] = 0.0f;
+                    for (int c = lane; c < nbF * 4; c += 32) {
+                        const int b = c >> 2, part = c & 3;
+                        const uint4 qv = __ldg(reinterpret_cast<const uint4 *>(sq + b * 80 + 16) + part);
+                        const uint32_t scw = __ldg(reinterpret_cast<const uint32_t *>(sq + b * 80) + part);
+                        const uint32_t ddw = __ldg(dd + b);
+                        const float d = f16_to_f32(static_cast<uint16_t>(ddw & 0xffffu));
+                        const float dmin = f16_to_f32(static_cast<uint16_t>(ddw >> 16));
+#pragma unroll
+                        for (int sub = 0; sub < 4; sub++) {
+                            const uint32_t sc = (scw >> (8 * sub)) & 15u, mn = (scw >> (8 * sub + 4)) & 15u;
+                            const float ds = __fmul_rn(d, static_cast<float>(sc));
+                            const float dm = __fmul_rn(dmin, static_cast<float>(mn));
+                            const uint32_t qw = sub == 0 ? qv.x : sub == 1 ? qv.y : sub == 2 ? qv.z : qv.w;
+                            float wv[16];
+#pragma unroll
+                            for (int i = 0; i < 16; i++) wv[i] = q2k_weight(ds, dm, (qw >> (2 * i)) & 3u);
+#pragma unroll
+                            for (int j = 0; j < NT; j++) {
+                                if (j < nt) {
+#pragma unroll
+                                    for (int q4 = 0; q4 < 4; q4++) {
+                                        const float4 hv = hs[j * F4 + swz16(16 * c + 4 * sub + q4)];
+                                        acc[j] = dot4(make_float4(wv[4 * q4], wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]), hv, acc[j]);
+                                    }
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; j++) {
+                        if (j < nt) {
+                            const float v = warp_sum(acc[j]);
+                            if (lane == 0) p.y[static_cast<size_t>(off + tok0 + j) * D + r] = v;
+                        }
+                    }
+                }
+            } else {
+                const int r = r0 + warp;
+                const uint4 *sd = reinterpret_cast<const uint4 *>(p.w.sh_down + static_cast<size_t>(r) * F);
+                float acc[NT];
+#pragma unroll
+                for (int j = 0; j < NT; j++) acc[j] = 0.0f;
+                for (int c = lane; c < F / 8; c += 32) {
+                    float wv[8];
+                    bf16x8(__ldg(sd + c), wv);
+#pragma unroll
+                    for (int j = 0; j < NT; j++) {
+                        if (j < nt) {
+                            const float4 h0 = hs[j * F4 + swz16(2 * c)], h1 = hs[j * F4 + swz16(2 * c + 1)];
+                            acc[j] = dot4(make_float4(wv[0], wv[1], wv[2], wv[3]), h0, acc[j]);
+                            acc[j] = dot4(make_float4(wv[4], wv[5], wv[6], wv[7]), h1, acc[j]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < NT; j++) {
+                    if (j < nt) {
+                        const float v = warp_sum(acc[j]);
+                        if (lane == 0) p.y[static_cast<size_t>(off + tok0 + j) * D + r] = v;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Device dequantisation of one resident matrix (tests): the same decode as the kernels.
+__global__ void dequant_kernel(DeviceWeights w, int expert, int matrix, const uint8_t *grid, float *dst32,
+                               uint16_t *dst16) {
+    const int D = w.D, F = w.F;
+    const int rows = matrix == DS4MOE_DOWN ? D : F, cols = matrix == DS4MOE_DOWN ? F : D;
+    const size_t nchunks = static_cast<size_t>(rows) * cols / 64;  // 64 weights per chunk
+    for (size_t ci = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; ci < nchunks;
+         ci += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t r = ci / (cols / 64);
+        const int c = static_cast<int>(ci - r * (cols / 64));
+        float v[64];
+        if (matrix == DS4MOE_DOWN) {
+            const size_t rowb = (static_cast<size_t>(expert) * D + r) * w.nbF;
+            const uint8_t *sq = w.down_sq + rowb * 80;
+            const int b = c >> 2, part = c & 3;
+            const uint4 qv = *(reinterpret_cast<const uint4 *>(sq + b * 80 + 16) + part);
+            const uint32_t scw = *(reinterpret_cast<const uint32_t *>(sq + b * 80) + part);
+            const uint32_t ddw = w.down_dd[rowb + b];
+            const float d = f16_to_f32(static_cast<uint16_t>(ddw & 0xffffu));
+            const float dmin = f16_to_f32(static_cast<uint16_t>(ddw >> 16));
+            for (int sub = 0; sub < 4; sub++) {
+                const uint32_t sc = (scw >> (8 * sub)) & 15u, mn = (scw >> (8 * sub + 4)) & 15u;
+                const float ds = __fmul_rn(d, static_cast<float>(sc));
+                const float dm = __fmul_rn(dmin, static_cast<float>(mn));
+                const uint32_t qw = sub == 0 ? qv.x : sub == 1 ? qv.y : sub == 2 ? qv.z : qv.w;
+                for (int i = 0; i < 16; i++) v[16 * sub + i] = q2k_weight(ds, dm, (qw >> (2 * i)) & 3u);
+            }
+        } else {
+            const size_t rowb = (static_cast<size_t>(expert) * F + r) * w.nbD;
+            const uint8_t *qs = (matrix == DS4MOE_GATE ? w.gate_qs : w.up_qs) + rowb * 64;
+            const uint16_t *dp = (matrix == DS4MOE_GATE ? w.gate_d : w.up_d) + rowb;
+            const uint4 q = *(reinterpret_cast<const uint4 *>(qs) + c);
+            const float d = f16_to_f32(dp[c >> 2]);
+            for (int sb = 0; sb < 2; sb++) {
+                const uint32_t iw = sb ? q.z : q.x, sw = sb ? q.w : q.y;
+                const float sc = iq2_scale(d, sw);
+                for (int g = 0; g < 4; g++) {
+                    const uint2 ge = reinterpret_cast<const uint2 *>(grid)[(iw >> (8 * g)) & 255u];
+                    iq2_group(ge, (sw >> (7 * g)) & 127u, sc, v + 32 * sb + 8 * g);
+                }
+            }
+        }
+        const size_t o = r * cols + static_cast<size_t>(c) * 64;
+        for (int i = 0; i < 64; i++) {
+            if (dst32) dst32[o + i] = v[i];
+            if (dst16) dst16[o + i] = __half_as_ushort(__float2half_rn(v[i]));
+        }
+    }
+}
+
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+template <int NT>
+int launch_up_nt(const UpParams &p, cudaStream_t s) {
+    const size_t smem = 2048 + static_cast<size_t>(NT) * p.w.D * 2;
+    cudaError_t err = cudaFuncSetAttribute(gemv_up_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return static_cast<int>(err);
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_up_kernel<NT>, kThreads, smem);
+    gemv_up_kernel<NT><<<sm_count() * (per_sm > 0 ? per_sm : 1), kThreads, smem, s>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+template <int NT>
+int launch_down_nt(const DownParams &p, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(NT) * p.w.F * 4;
+    cudaError_t err = cudaFuncSetAttribute(gemv_down_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return static_cast<int>(err);
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_down_kernel<NT>, kThreads, smem);
+    gemv_down_kernel<NT><<<sm_count() * (per_sm > 0 ? per_sm : 1), kThreads, smem, s>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, bool shared_on_gemv,
+                   void *stream) {
+    UpParams p;
+    p.w = w;
+    p.x = x;
+    p.perm = ws.perm;
+    p.offsets = ws.offsets;
+    p.gemv_list = ws.gemv_list;
+    p.meta = ws.meta;
+    p.grid = ws.grid;
+    p.h = ws.h32;
+    p.T = T;
+    p.k = k;
+    p.P = T * k;
+    p.shared = shared_on_gemv && w.has_shared;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return T == 1 ? launch_up_nt<1>(p, s) : launch_up_nt<8>(p, s);
+}
+
+int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream) {
+    DownParams p;
+    p.w = w;
+    p.offsets = ws.offsets;
+    p.gemv_list = ws.gemv_list;
+    p.meta = ws.meta;
+    p.h = ws.h32;
+    p.y = ws.y;
+    p.T = T;
+    p.P = T * k;
+    p.shared = shared_on_gemv && w.has_shared;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return T == 1 ? launch_down_nt<1>(p, s) : launch_down_nt<8>(p, s);
+}
+
+int launch_dequant(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, float *dst32,
+                   uint16_t *dst16, void *stream) {
+    dequant_kernel<<<sm_count() * 4, 128, 0, static_cast<cudaStream_t>(stream)>>>(w, expert, matrix, grid, dst32,
+                                                                                 dst16);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace ds4moe

@@ -1,0 +1,97 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/ds4moe.h"
+
+namespace ds4moe {
+
+void host_grid(uint8_t out[2048]);
+bool host_f16_finite(uint16_t h);
+
+// Device status bits, OR-ed by kernels into the handle's status word.
+enum : int {
+    ST_RANGE = 1,    // a value overflowed fp16 on the tensor-core path
+    ST_TIMEOUT = 2,  // a bounded wait gave up
+    ST_BADIDX = 4,   // an expert index outside [0, E) reached the grouping kernel
+};
+
+// Resident, repacked expert weights. Each IQ2-style row keeps its 64-byte block payloads
+// (8 sub-blocks x 8 bytes) contiguous, 16-byte aligned, and the fp16 block scales in a
+// separate plane; each Q2_K-style row keeps 80-byte payloads (16 B scales + 64 B codes)
+// and a plane of (d, dmin) fp16 pairs. Row-major within an expert, experts back to back.
+struct DeviceWeights {
+    int D, F, E;
+    int nbD, nbF;           // blocks per row of gate/up (D/256) and of down (F/256)
+    uint8_t *gate_qs, *up_qs;  // [E][F][nbD][64]
+    uint16_t *gate_d, *up_d;   // [E][F][nbD]
+    uint8_t *down_sq;          // [E][D][nbF][80]
+    uint32_t *down_dd;         // [E][D][nbF]  (d | dmin << 16)
+    uint16_t *sh_gate, *sh_up; // [F][D] bf16, or null
+    uint16_t *sh_down;         // [D][F] bf16, or null
+    uint16_t *sh_down_f16;     // [D][F] fp16 copy for the tensor-core path, or null
+    bool has_shared;
+};
+
+// Per-call grouping metadata written on the device by the grouping kernel.
+struct GroupMeta {
+    int n_gemv;  // experts with 0 < n_e < gemm_min, listed in gemv_list in expert order
+    int n_gemm;  // experts with n_e >= gemm_min, listed in gemm_list in expert order
+    int pad[2];
+};
+
+struct Workspace {
+    int max_T, max_k;
+    int32_t *topk_idx;  // [T*k]
+    float *topk_w;      // [T*k]
+    int32_t *counts;    // [E]
+    int32_t *offsets;   // [E+1]
+    int32_t *perm;      // [P]
+    int32_t *inv;       // [P]
+    int32_t *gemv_list; // [E]
+    int32_t *gemm_list; // [E]
+    GroupMeta *meta;
+    uint8_t *grid;      // [256][8] IQ2-style grid
+    float *h32;         // [P+T][F] fp32 intermediate of the GEMV path (rows P.. = shared expert)
+    uint16_t *h16;      // [P+T][F] fp16 intermediate of the tensor-core path
+    uint16_t *x16;      // [P+T][D] fp16 tokens gathered per group for the tensor-core path
+    float *y;           // [P+T][D] per-pair expert outputs (rows P.. = shared expert)
+    int *status;        // device status word
+};
+
+}  // namespace ds4moe
+
+struct ds4moe_weights {
+    int device;
+    ds4moe::DeviceWeights dw;
+    ds4moe::Workspace ws;
+    int gemm_min_tokens;
+    int shared_gemm_min_tokens;
+    int profile;
+    void *events[DS4MOE_N_STAGES + 1];  // cudaEvent_t: start of each stage, end of the call
+    bool stage_ran[DS4MOE_N_STAGES];
+    bool events_recorded;
+    uint64_t calls, launches;
+    void *allocs[64];
+    int n_allocs;
+};
+
+namespace ds4moe {
+
+// Launchers (return a cudaError_t as int; 0 = success).
+int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *idx, float *w,
+                 void *stream);
+int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, int32_t *counts,
+                 int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list,
+                 int32_t *gemm_list, GroupMeta *meta, int *status, void *stream);
+int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
+                   bool shared_on_gemv, void *stream);
+int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv,
+                     void *stream);
+int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, float *out, void *stream);
+int launch_dequant(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, float *dst32,
+                   uint16_t *dst16, void *stream);
+
+}  // namespace ds4moe

@@ -1,0 +1,200 @@
+/*
+ * ds4moe.h -- C ABI of the routed-MoE expert FFN over 2-bit block-quantised experts,
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What it computes. One routed mixture-of-experts layer's expert FFN, the hot path of a
+ * DeepSeek-V4-style engine: per token, top-k routing over router logits, grouping of the
+ * (token, slot) pairs by expert, a SwiGLU expert per pair (h = silu(W_gate x) * (W_up x),
+ * y = W_down h), an always-on bf16 shared expert, and the gate-weighted sum added into the
+ * residual. Sources: "DwarfStar" (ds4 README), section "模型权重" (only routed experts are
+ * quantised: up/gate to IQ2_XXS, down to Q2_K; shared expert, projections and router stay
+ * unquantised); "DwarfStar 深度解析" §2.1 (per-token dynamic expert choice, irregular
+ * compute) and §3.4.3 (the quantisation split, the router kept at full precision);
+ * "Part 5: 服务层" §6 "会话批处理" (several sessions' decode steps in one batched kernel).
+ * The block layouts are this library's own IQ2-style and Q2_K-style formats, frozen in
+ * FORMAT.md (the pages name the formats but print no layout).
+ *
+ * Conventions.
+ *   - Every function returns a status (DS4MOE_OK = 0) and never throws or aborts.
+ *   - Host functions are synchronous and thread-safe.
+ *   - Device functions are asynchronous on the given stream; their pointers are device
+ *     memory owned by the caller, and all argument checks happen on the host before any
+ *     launch. Errors a kernel detects are recorded in a device status word of the weights
+ *     handle and returned by ds4moe_last_status().
+ *   - A weights handle owns its workspace, so calls that use one handle must not overlap
+ *     (issue them on one stream, or order them with events).
+ *   - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ */
+#ifndef DS4MOE_H
+#define DS4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *ds4moe_stream_t;
+
+enum ds4moe_status {
+    DS4MOE_OK = 0,
+    DS4MOE_EINVAL = 1,       /* bad argument (null pointer, size, alignment, k > E, ...) */
+    DS4MOE_ENOMEM = 2,       /* device or host allocation failed */
+    DS4MOE_ECUDA = 3,        /* a CUDA runtime call failed (no device, launch error, ...) */
+    DS4MOE_EBADDATA = 4,     /* input data rejected (non-finite weights, bad packed scale) */
+    DS4MOE_ETIMEOUT = 5,     /* a bounded device-side wait gave up */
+    DS4MOE_EUNSUPPORTED = 6, /* shape or device not supported by this build */
+    DS4MOE_ERANGE = 7        /* a value overflowed the fp16 operand range of the tensor-core path */
+};
+
+enum ds4moe_gate_mode {
+    DS4MOE_GATE_SOFTMAX = 0, /* g_s = exp(l_s - l_0) / sum_j exp(l_j - l_0) over the k selected */
+    DS4MOE_GATE_SIGMOID = 1  /* g_s = sigmoid(l_s) / sum_j sigmoid(l_j) over the k selected */
+};
+
+/* Matrices of one expert, for ds4moe_weights_dequantize(). */
+enum ds4moe_matrix { DS4MOE_GATE = 0, DS4MOE_UP = 1, DS4MOE_DOWN = 2 };
+
+/* Options of a weights handle, for ds4moe_set_option(). */
+enum ds4moe_option {
+    /* Expert groups with at least this many tokens run on the tcgen05 tensor-core path;
+     * smaller groups run on the fused dequant-GEMV path. 0 means never use tensor cores;
+     * 1 means always. Default 33. */
+    DS4MOE_OPT_GEMM_MIN_TOKENS = 0,
+    /* Same threshold for the bf16 shared expert (by token count T). Default 33. */
+    DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS = 1,
+    /* 1: record CUDA events around each stage of ds4moe_expert_ffn on its stream, so that
+     * ds4moe_get_stats() can report per-stage device times. Default 0. */
+    DS4MOE_OPT_PROFILE = 2
+};
+
+/* Stages of ds4moe_expert_ffn, in launch order (indices into ds4moe_stats.stage_ms). */
+enum ds4moe_stage {
+    DS4MOE_STAGE_ROUTE = 0,     /* top-k routing */
+    DS4MOE_STAGE_GROUP = 1,     /* grouping of pairs by expert */
+    DS4MOE_STAGE_GATHER = 2,    /* fp16 token gather for the tensor-core path */
+    DS4MOE_STAGE_UP_GEMV = 3,   /* dequant-GEMV gate/up + SwiGLU */
+    DS4MOE_STAGE_UP_GEMM = 4,   /* tensor-core gate/up + SwiGLU */
+    DS4MOE_STAGE_DOWN_GEMV = 5, /* dequant-GEMV down */
+    DS4MOE_STAGE_DOWN_GEMM = 6, /* tensor-core down */
+    DS4MOE_STAGE_COMBINE = 7,   /* gate-weighted combine into the residual */
+    DS4MOE_N_STAGES = 8
+};
+
+typedef struct {
+    uint64_t calls;     /* ds4moe_expert_ffn calls since creation */
+    uint64_t launches;  /* kernels launched by those calls */
+    float stage_ms[DS4MOE_N_STAGES]; /* device time per stage of the last profiled call, 0 if
+                                        the stage did not run or profiling is off */
+} ds4moe_stats;
+
+/* Human-readable text of a status code (static storage). */
+const char *ds4moe_strerror(int status);
+
+/* ------------------------------------------------------------------ host: formats */
+
+/* Bytes of a packed [rows x cols] matrix: rows * cols/256 * 84 (Q2_K-style) or * 66
+ * (IQ2-style). 0 if rows < 0, cols <= 0 or cols % 256 != 0. */
+size_t ds4moe_q2k_bytes(int64_t rows, int64_t cols);
+size_t ds4moe_iq2_bytes(int64_t rows, int64_t cols);
+
+/* The IQ2-style grid (FORMAT.md): 256 entries x 8 magnitudes, entry-major, into out[2048]. */
+int ds4moe_iq2_grid(uint8_t *out);
+
+/* Quantise a row-major fp32 matrix w [rows x cols] (cols % 256 == 0) into dst (dst_bytes
+ * at least the size above) following FORMAT.md's quantisers; the output is byte-identical
+ * to any implementation that follows them. Runs on all host cores.
+ * EINVAL: bad sizes or null pointers; EBADDATA: a non-finite weight or an fp16 scale
+ * overflow (dst is then unspecified). Source: "DwarfStar" README, "模型权重" (up/gate in
+ * IQ2_XXS, down in Q2_K); the quantiser itself is FORMAT.md's reading. */
+int ds4moe_quantize_q2k(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
+int ds4moe_quantize_iq2(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
+
+/* Host dequantisation to fp32 (the exact values of FORMAT.md), for tests and tools. */
+int ds4moe_dequantize_q2k(const void *src, int64_t rows, int64_t cols, float *dst);
+int ds4moe_dequantize_iq2(const void *src, int64_t rows, int64_t cols, float *dst);
+
+/* ------------------------------------------------------------------ weights handle */
+
+typedef struct ds4moe_weights ds4moe_weights;
+
+typedef struct {
+    int d_model;   /* D, a multiple of 256 */
+    int d_ff;      /* F, a multiple of 256 */
+    int n_experts; /* E, 1..1024 */
+    /* Host pointers, one per expert: gate and up are IQ2-style [d_ff x d_model] blobs of
+     * ds4moe_iq2_bytes(d_ff, d_model) bytes; down is a Q2_K-style [d_model x d_ff] blob of
+     * ds4moe_q2k_bytes(d_model, d_ff) bytes. Copied; the caller keeps ownership. */
+    const void *const *gate_iq2;
+    const void *const *up_iq2;
+    const void *const *down_q2k;
+    /* Host bf16 shared expert, or all three NULL for none: gate/up [d_ff x d_model],
+     * down [d_model x d_ff], row-major. Copied. */
+    const uint16_t *shared_gate_bf16;
+    const uint16_t *shared_up_bf16;
+    const uint16_t *shared_down_bf16;
+    int max_tokens; /* largest T of any later call, >= 1 */
+    int max_k;      /* largest k of any later call, 1..min(32, n_experts) */
+} ds4moe_weights_desc;
+
+/* Create a handle on the current CUDA device: validates the blobs (finite fp16 scales),
+ * repacks them into the device layout, uploads them and allocates the workspace for
+ * max_tokens x max_k pairs. Synchronous. EBADDATA names a non-finite fp16 scale. */
+int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out);
+
+/* Free a handle (NULL is allowed). Synchronises the device first. */
+void ds4moe_weights_destroy(ds4moe_weights *w);
+
+int ds4moe_set_option(ds4moe_weights *w, int option, int value);
+
+/* Dequantise one resident expert matrix on the device, through the same device decode
+ * the kernels use: fp32 values into dst_f32 (rows*cols floats, may be NULL) and the
+ * fp16 operand values of the tensor-core path, RN-even of the fp32 value, into
+ * dst_f16 (may be NULL). Asynchronous. */
+int ds4moe_weights_dequantize(const ds4moe_weights *w, int expert, int matrix, float *dst_f32,
+                              uint16_t *dst_f16, ds4moe_stream_t stream);
+
+/* ------------------------------------------------------------------ device: the hot path */
+
+/* Top-k routing: per token t, the k experts with the largest logits (ties to the lower
+ * expert index; NaN orders as -inf), in that order, and their gate weights (mode above).
+ * logits fp32 [T x E] row-major; topk_idx int32 [T x k]; topk_w fp32 [T x k].
+ * 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T = 0 is a no-op).
+ * Source: "DwarfStar 深度解析" §2.1 (per-token dynamic expert choice) and §3.4.3
+ * (router at full precision); tie rule and gate modes are this library's reading. */
+int ds4moe_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *topk_idx,
+                 float *topk_w, ds4moe_stream_t stream);
+
+/* Group the T*k (token, slot) pairs by expert: a stable counting sort in (token, slot)
+ * order. counts int32 [E]; offsets int32 [E+1] (exclusive scan, offsets[E] = T*k);
+ * perm int32 [T*k] (pair id t*k+s at each grouped position); inv int32 [T*k] (grouped
+ * position of pair t*k+s). Deterministic. */
+int ds4moe_group(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                 int32_t *perm, int32_t *inv, ds4moe_stream_t stream);
+
+/* The expert FFN: out[t] += y_shared[t] + sum_s g[t,s] * y_{idx[t,s]}(x[t]), for t < T.
+ *   x       bf16 [T x d_model], 16-byte aligned;
+ *   logits  fp32 [T x n_experts] (router logits, bias already added);
+ *   out     fp32 [T x d_model] residual, updated in place, 16-byte aligned.
+ * Routing, grouping, the SwiGLU experts and the combine all run on the device with no
+ * host synchronisation; results are bit-reproducible run to run. T <= max_tokens and
+ * k <= max_k of the handle. EINVAL on bad arguments; device-side errors (ERANGE, ...)
+ * are reported by ds4moe_last_status(). */
+int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *w, const float *logits, int T, int k,
+                      int gate_mode, float *out, ds4moe_stream_t stream);
+
+/* Counters of the handle, and (when DS4MOE_OPT_PROFILE is on) the per-stage device times of
+ * the last call, read from its CUDA events (waits for them). */
+int ds4moe_get_stats(ds4moe_weights *w, ds4moe_stats *out);
+
+/* Synchronise the stream, then return and clear the handle's device status word
+ * (DS4MOE_OK when no kernel reported an error since the last call). */
+int ds4moe_last_status(ds4moe_weights *w, ds4moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4MOE_H */

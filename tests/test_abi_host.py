@@ -1,0 +1,108 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every symbol the header
+declares, and its host quantisers, dequantisers and grid agree byte for byte with the
+oracle's independent implementation. Device entry points are only called with arguments
+that the host-side checks reject before any CUDA call."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ds4():
+    import bit_quantized_routed_gb300 as m
+    m.build()
+    return m
+
+
+def _declared():
+    hdr = open(os.path.join(ROOT, "include", "ds4moe.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds4moe_[a-z0-9_]+)\s*\(", hdr)))
+
+
+def test_library_exports_every_declared_symbol(ds4):
+    import ctypes
+    declared = _declared()
+    assert len(declared) >= 16
+    L = ctypes.CDLL(ds4.LIB_PATH)
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(ds4.EXPORTED) == declared
+
+
+def test_sizes_and_strerror(ds4):
+    assert ds4.ds4moe_q2k_bytes(4096, 2048) == 4096 * 8 * 84
+    assert ds4.ds4moe_iq2_bytes(2048, 4096) == 2048 * 16 * 66
+    assert ds4.ds4moe_iq2_bytes(1, 255) == 0 and ds4.ds4moe_q2k_bytes(-1, 256) == 0
+    assert ds4.ds4moe_strerror(0) == "ok"
+    assert "invalid" in ds4.ds4moe_strerror(1)
+
+
+def test_grid_matches_oracle(ds4):
+    assert np.array_equal(ds4.ds4moe_iq2_grid(), oracle.iq2_grid())
+
+
+def _weights(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    w[0, :7] = [0.0, -0.0, 1e-9, -1e-9, 0.05, -0.05, 0.0]     # zeros, tiny values
+    w[1, :256] = 0.0                                           # an all-zero block
+    w[2, :256] = np.float32(0.01)                              # a constant block
+    w[3, 256:512] = -np.abs(w[3, 256:512])                     # all-negative block
+    return w
+
+
+@pytest.mark.parametrize("shape,seed", [((6, 512), 1), ((5, 768), 2)])
+def test_quantizers_byte_identical_to_oracle(ds4, shape, seed):
+    w = _weights(*shape, seed)
+    assert np.array_equal(ds4.ds4moe_quantize_q2k(w), oracle.quantize_q2k(w))
+    assert np.array_equal(ds4.ds4moe_quantize_iq2(w), oracle.quantize_iq2(w))
+
+
+def test_quantizers_byte_identical_on_expert_weights(ds4):
+    w = synth.expert_weight(7, 3, synth.GATE, 16, 1024)
+    assert np.array_equal(ds4.ds4moe_quantize_iq2(w), oracle.quantize_iq2(w))
+    w = synth.expert_weight(7, 3, synth.DOWN, 16, 1024)
+    assert np.array_equal(ds4.ds4moe_quantize_q2k(w), oracle.quantize_q2k(w))
+
+
+def test_host_dequantizers_match_oracle_bitwise(ds4):
+    rows, cols = 8, 512
+    b = synth.random_iq2_blob(3, 0, 0, rows, cols)
+    assert np.array_equal(ds4.ds4moe_dequantize_iq2(b, rows, cols).view(np.uint32),
+                          oracle.dequant_iq2(b, rows, cols).view(np.uint32))
+    b = synth.random_q2k_blob(3, 0, 2, rows, cols)
+    assert np.array_equal(ds4.ds4moe_dequantize_q2k(b, rows, cols).view(np.uint32),
+                          oracle.dequant_q2k(b, rows, cols).view(np.uint32))
+
+
+def test_quantizer_rejects_non_finite(ds4):
+    w = np.zeros((2, 256), np.float32)
+    w[1, 3] = np.inf
+    with pytest.raises(ds4.Ds4moeError) as ei:
+        ds4.ds4moe_quantize_iq2(w)
+    assert ei.value.status == ds4.DS4MOE_EBADDATA
+    with pytest.raises(ValueError):
+        ds4.ds4moe_quantize_q2k(np.zeros((2, 100), np.float32))
+
+
+def test_device_entry_points_reject_bad_arguments_on_host(ds4):
+    L = ds4.lib()
+    # k > E, E too large, bad gate mode: rejected before any CUDA call
+    assert L.ds4moe_route(None, 4, 8, 9, 0, None, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_route(None, 4, 2000, 2, 0, None, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_route(None, 4, 8, 2, 7, None, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_route(None, 4, 8, 2, 0, None, None, None) == ds4.DS4MOE_EINVAL  # null pointers
+    assert L.ds4moe_route(None, 0, 8, 2, 0, None, None, None) == ds4.DS4MOE_OK      # T = 0: no-op
+    assert L.ds4moe_group(None, 4, 2, 8, None, None, None, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_expert_ffn(None, None, None, 1, 1, 0, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_set_option(None, 0, 1) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_weights_dequantize(None, 0, 0, None, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_weights_create(None, None) == ds4.DS4MOE_EINVAL
