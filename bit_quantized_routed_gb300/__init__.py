@@ -33,6 +33,7 @@ EXPORTED = [
     "ds4moe_quantize_q2k", "ds4moe_quantize_iq2", "ds4moe_dequantize_q2k", "ds4moe_dequantize_iq2",
     "ds4moe_weights_create", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
     "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
+    "ds4moe_expert_ffn_static",
 ]
 
 
@@ -86,6 +87,7 @@ def lib():
             "ds4moe_expert_ffn": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
             "ds4moe_get_stats": ([vp, ctypes.POINTER(_Stats)], i32),
             "ds4moe_last_status": ([vp, vp], i32),
+            "ds4moe_expert_ffn_static": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -292,3 +294,17 @@ def ds4moe_get_stats(weights):
 
 def ds4moe_last_status(weights, stream=None):
     return lib().ds4moe_last_status(weights.handle, _stream(stream))
+
+
+def ds4moe_expert_ffn_static(x, weights, logits, k, out, gate_mode=DS4MOE_GATE_SOFTMAX, stream=None):
+    """out += expert FFN of x, like ds4moe_expert_ffn, but with the per-call intermediates in
+    the library's static device region: the call allocates no device memory. For callers
+    that may not allocate while they serve (see include/ds4moe.h)."""
+    import torch
+    T = x.shape[0]
+    if x.shape != (T, weights.d_model) or out.shape != (T, weights.d_model) or logits.shape != (T, weights.n_experts):
+        raise ValueError("shape mismatch")
+    _check(lib().ds4moe_expert_ffn_static(_ptr(x, torch.bfloat16, "x"), weights.handle,
+                                          _ptr(logits, torch.float32, "logits"), T, k, gate_mode,
+                                          _ptr(out, torch.float32, "out"), _stream(stream)),
+           "ds4moe_expert_ffn_static")

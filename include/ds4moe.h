@@ -193,6 +193,29 @@ int ds4moe_get_stats(ds4moe_weights *w, ds4moe_stats *out);
  * (DS4MOE_OK when no kernel reported an error since the last call). */
 int ds4moe_last_status(ds4moe_weights *w, ds4moe_stream_t stream);
 
+/* The expert FFN without any device allocation, for callers that cannot allocate device
+ * memory while they run: for example a plug-in whose host framework owns and budgets every
+ * device allocation, or a serving loop that must not call cudaMalloc (it can synchronise the
+ * device and can fail under memory pressure). Such a caller creates the weights handle once
+ * at load time -- it may ask for the smallest workspace, max_tokens = 1 and max_k = 1 -- and
+ * runs its decode batches through this entry point. The pages have no counterpart: this is
+ * a deployment variant of ds4moe_expert_ffn, not a step of the method.
+ *
+ * Same arguments and result as ds4moe_expert_ffn (out += the expert FFN of x), computed with
+ * every expert group on the dequant-GEMV path. The per-call intermediates (top-k arrays,
+ * grouping, h and y) live in one static 3 MiB region of device memory that every GPU which
+ * loads the library holds until the process exits; the handle's own workspace is not used,
+ * so T and k are not limited by the handle's max_tokens and max_k, only by the region:
+ * calls needing more than 3 MiB (about T*(k+1)*(d_model + d_ff)*4 bytes, e.g. more than 8
+ * tokens at top-8 with d_model 7168 and d_ff 2048) return DS4MOE_EINVAL without launching.
+ * The current device must be the handle's. The first call on a device looks up the region's
+ * device address (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the region: calls that overlap on the GPU (other streams, other threads,
+ * other handles) race and must be ordered by the caller. Device-side errors are reported
+ * through the handle, by ds4moe_last_status(). Nothing here calls cudaMalloc or cudaFree. */
+int ds4moe_expert_ffn_static(const uint16_t *x, const ds4moe_weights *w, const float *logits, int T, int k,
+                             int gate_mode, float *out, ds4moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
