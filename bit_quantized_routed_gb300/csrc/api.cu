@@ -2,6 +2,8 @@
 // and their launch sequence. Arguments are checked here, on the host, before any launch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -53,12 +55,17 @@ int upload(void *dst, const void *src, size_t bytes) {
     return cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice) == cudaSuccess ? DS4MOE_OK : DS4MOE_ECUDA;
 }
 
+constexpr double kF16Max = 65504.0;
+
 // Split IQ2-style blocks [rows][nb][66] into payload [rows][nb][64] and scales [rows][nb].
-bool repack_iq2(const uint8_t *src, size_t nblocks, uint8_t *qs, uint16_t *d) {
+// amax: a bound on |weight| over the blocks (7 d).
+bool repack_iq2(const uint8_t *src, size_t nblocks, uint8_t *qs, uint16_t *d, double *amax) {
     for (size_t b = 0; b < nblocks; b++) {
         const uint8_t *blk = src + b * 66;
         const uint16_t dv = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
         if (!host_f16_finite(dv)) return false;
+        const double bound = 7.0 * std::fabs(host_f16_value(dv));
+        if (bound > *amax) *amax = bound;
         d[b] = dv;
         std::memcpy(qs + b * 64, blk + 2, 64);
     }
@@ -66,12 +73,15 @@ bool repack_iq2(const uint8_t *src, size_t nblocks, uint8_t *qs, uint16_t *d) {
 }
 
 // Split Q2_K-style blocks [rows][nb][84] into payload [rows][nb][80] and (d, dmin) pairs.
-bool repack_q2k(const uint8_t *src, size_t nblocks, uint8_t *sq, uint32_t *dd) {
+// amax: a bound on |weight| over the blocks (max(45 |d|, 15 |dmin|) + ...).
+bool repack_q2k(const uint8_t *src, size_t nblocks, uint8_t *sq, uint32_t *dd, double *amax) {
     for (size_t b = 0; b < nblocks; b++) {
         const uint8_t *blk = src + b * 84;
         const uint16_t dv = static_cast<uint16_t>(blk[80] | (blk[81] << 8));
         const uint16_t mv = static_cast<uint16_t>(blk[82] | (blk[83] << 8));
         if (!host_f16_finite(dv) || !host_f16_finite(mv)) return false;
+        const double bound = 45.0 * std::fabs(host_f16_value(dv)) + 15.0 * std::fabs(host_f16_value(mv));
+        if (bound > *amax) *amax = bound;
         dd[b] = static_cast<uint32_t>(dv) | (static_cast<uint32_t>(mv) << 16);
         std::memcpy(sq + b * 80, blk, 80);
     }
@@ -145,8 +155,8 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
         delete h;
         return DS4MOE_ECUDA;
     }
-    h->gemm_min_tokens = 33;
-    h->shared_gemm_min_tokens = 33;
+    h->gemm_min_tokens = 2;
+    h->shared_gemm_min_tokens = 2;
     DeviceWeights &w = h->dw;
     w.D = D;
     w.F = F;
@@ -162,24 +172,29 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     TRY(dev_alloc(h, &w.up_d, E * nb_up * 2));
     TRY(dev_alloc(h, &w.down_sq, E * nb_down * 80));
     TRY(dev_alloc(h, &w.down_dd, E * nb_down * 4));
+    TRY(dev_alloc(h, &w.tc_ok, E));
     {
-        std::vector<uint8_t> qs(nb_up * 64), sq(nb_down * 80);
+        std::vector<uint8_t> qs(nb_up * 64), sq(nb_down * 80), ok(E);
         std::vector<uint16_t> dv(nb_up);
         std::vector<uint32_t> dd(nb_down);
         for (int e = 0; e < E; e++) {
             const void *mats[2] = {desc->gate_iq2[e], desc->up_iq2[e]};
             uint8_t *dqs[2] = {w.gate_qs, w.up_qs};
             uint16_t *dds[2] = {w.gate_d, w.up_d};
+            double amax = 0.0;
             for (int m = 0; m < 2; m++) {
-                if (!repack_iq2(static_cast<const uint8_t *>(mats[m]), nb_up, qs.data(), dv.data())) TRY(DS4MOE_EBADDATA);
+                if (!repack_iq2(static_cast<const uint8_t *>(mats[m]), nb_up, qs.data(), dv.data(), &amax))
+                    TRY(DS4MOE_EBADDATA);
                 TRY(upload(dqs[m] + e * nb_up * 64, qs.data(), nb_up * 64));
                 TRY(upload(dds[m] + e * nb_up, dv.data(), nb_up * 2));
             }
-            if (!repack_q2k(static_cast<const uint8_t *>(desc->down_q2k[e]), nb_down, sq.data(), dd.data()))
+            if (!repack_q2k(static_cast<const uint8_t *>(desc->down_q2k[e]), nb_down, sq.data(), dd.data(), &amax))
                 TRY(DS4MOE_EBADDATA);
             TRY(upload(w.down_sq + e * nb_down * 80, sq.data(), nb_down * 80));
             TRY(upload(w.down_dd + e * nb_down, dd.data(), nb_down * 4));
+            ok[e] = amax <= kF16Max ? 1 : 0;  // otherwise the expert stays on the fp32 GEMV path
         }
+        TRY(upload(w.tc_ok, ok.data(), E));
     }
     if (w.has_shared) {
         const size_t n = static_cast<size_t>(F) * D;
@@ -193,6 +208,12 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
         std::vector<uint16_t> f16(n);
         for (size_t i = 0; i < n; i++) f16[i] = bf16_to_f16(desc->shared_down_bf16[i]);
         TRY(upload(w.sh_down_f16, f16.data(), n * 2));
+        // the tensor-core path holds the shared expert in fp16: only if every weight fits
+        w.shared_tc_ok = true;
+        const uint16_t *mats[3] = {desc->shared_gate_bf16, desc->shared_up_bf16, desc->shared_down_bf16};
+        for (const uint16_t *m : mats)
+            for (size_t i = 0; i < n && w.shared_tc_ok; i++)
+                if ((m[i] & 0x7fffu) > 0x477fu) w.shared_tc_ok = false;  // |bf16| > 65280 (or inf/nan)
     }
     Workspace &ws = h->ws;
     ws.max_T = desc->max_tokens;
@@ -206,11 +227,17 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     TRY(dev_alloc(h, &ws.inv, P * 4));
     TRY(dev_alloc(h, &ws.gemv_list, E * 4));
     TRY(dev_alloc(h, &ws.gemm_list, E * 4));
+    TRY(dev_alloc(h, &ws.single_list, E * 4));
+    TRY(dev_alloc(h, &ws.tile_prefix, (E + 1) * 4));
     TRY(dev_alloc(h, &ws.meta, sizeof(GroupMeta)));
     TRY(dev_alloc(h, &ws.grid, 2048));
     TRY(dev_alloc(h, &ws.h32, rows * F * 4));
-    TRY(dev_alloc(h, &ws.h16, rows * F * 2));
-    TRY(dev_alloc(h, &ws.x16, rows * D * 2));
+    const size_t rows_tc = std::max<size_t>(rows, kGemmBN);  // at least one full token box
+    TRY(dev_alloc(h, &ws.h16, rows_tc * F * 2));
+    TRY(dev_alloc(h, &ws.x16, rows_tc * D * 2));
+    if (encode_token_maps(h->tmap_x16, ws.x16, static_cast<int>(rows_tc), D) ||
+        encode_token_maps(h->tmap_h16, ws.h16, static_cast<int>(rows_tc), F))
+        TRY(DS4MOE_ECUDA);
     TRY(dev_alloc(h, &ws.y, rows * D * 4));
     TRY(dev_alloc(h, &ws.status, 16));
     {
@@ -260,7 +287,11 @@ int ds4moe_weights_dequantize(const ds4moe_weights *h, int expert, int matrix, f
                               ds4moe_stream_t stream) {
     if (!h || expert < 0 || expert >= h->dw.E || matrix < 0 || matrix > 2 || (!dst_f32 && !dst_f16))
         return DS4MOE_EINVAL;
-    return cuda_status(launch_dequant(h->dw, h->ws.grid, expert, matrix, dst_f32, dst_f16, stream));
+    int rc = 0;
+    if (dst_f32) rc = launch_dequant(h->dw, h->ws.grid, expert, matrix, dst_f32, nullptr, stream);
+    // the fp16 values are the tensor-core path's own operand bytes, from its producers
+    if (!rc && dst_f16) rc = launch_producer_dump(h->dw, h->ws.grid, expert, matrix, dst_f16, stream);
+    return cuda_status(rc);
 }
 
 int ds4moe_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *topk_idx, float *topk_w,
@@ -277,8 +308,8 @@ int ds4moe_group(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, 
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32) return DS4MOE_EINVAL;
     if (static_cast<int64_t>(T) * k > (int64_t(1) << 30)) return DS4MOE_EINVAL;
     if (!counts || !offsets || (T > 0 && (!topk_idx || !perm || !inv))) return DS4MOE_EINVAL;
-    return cuda_status(launch_group(topk_idx, T, k, E, 0, counts, offsets, perm, inv, nullptr, nullptr, nullptr,
-                                    nullptr, stream));
+    return cuda_status(launch_group(topk_idx, T, k, E, 0, nullptr, counts, offsets, perm, inv, nullptr, nullptr,
+                                    nullptr, nullptr, nullptr, nullptr, stream));
 }
 
 int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits, int T, int k, int gate_mode,
@@ -291,17 +322,48 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     const DeviceWeights &w = h->dw;
     const Workspace &ws = h->ws;
     StageClock clk(h, stream);
+    // A group holds at most T tokens, so the tensor-core path can only be needed when
+    // T reaches the threshold; the device decides per group after routing.
+    const int gemm_min = (h->gemm_min_tokens > 0 && T >= h->gemm_min_tokens) ? h->gemm_min_tokens : 0;
+    const bool shared_tc = w.has_shared && w.shared_tc_ok && h->shared_gemm_min_tokens > 0 &&
+                           T >= h->shared_gemm_min_tokens;
+    const bool any_tc = gemm_min > 0 || shared_tc;
     int rc = clk.stage(DS4MOE_STAGE_ROUTE);
     if (!rc) rc = launch_route(logits, T, w.E, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
     if (!rc) rc = clk.stage(DS4MOE_STAGE_GROUP);
     if (!rc)
-        rc = launch_group(ws.topk_idx, T, k, w.E, 0, ws.counts, ws.offsets, ws.perm, ws.inv, ws.gemv_list,
-                          ws.gemm_list, ws.meta, ws.status, stream);
-    const bool shared_gemv = w.has_shared;
+        rc = launch_group(ws.topk_idx, T, k, w.E, gemm_min, w.tc_ok, ws.counts, ws.offsets, ws.perm, ws.inv,
+                          ws.gemv_list, ws.gemm_list, ws.single_list, ws.tile_prefix, ws.meta, ws.status, stream);
+    if (any_tc) {
+        if (!rc) rc = clk.stage(DS4MOE_STAGE_GATHER);
+        if (!rc) rc = launch_gather(w, ws, x, T, k, gemm_min, shared_tc, stream);
+    }
+    // one-token groups (every group at T = 1) run on the decode kernels; groups of 2 ..
+    // gemm_min-1 tokens on the multi-token GEMV kernels, which are launched only when such
+    // groups can exist; larger groups on the tensor cores
+    const bool multi_gemv = gemm_min == 0 ? T > 1 : gemm_min > 2;
+    const bool shared_single = w.has_shared && !shared_tc && T == 1;
+    const bool shared_multi = w.has_shared && !shared_tc && T > 1;
     if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMV);
-    if (!rc) rc = launch_gemv_up(w, ws, x, T, k, shared_gemv, stream);
+    if (!rc) rc = launch_decode_up(w, ws, x, T, k, shared_single, stream);
+    if (multi_gemv || shared_multi) {
+        if (!rc) rc = launch_gemv_up(w, ws, x, T, k, shared_multi, stream);
+        h->launches++;
+    }
+    if (any_tc) {
+        if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMM);
+        if (!rc) rc = launch_gemm_up(w, ws, h->tmap_x16, T, k, shared_tc, stream);
+    }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMV);
-    if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_gemv, stream);
+    if (!rc) rc = launch_decode_down(w, ws, T, k, shared_single, stream);
+    if (multi_gemv || shared_multi) {
+        if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_multi, stream);
+        h->launches++;
+    }
+    if (any_tc) {
+        if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMM);
+        if (!rc) rc = launch_gemm_down(w, ws, h->tmap_h16, T, k, shared_tc, stream);
+    }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_COMBINE);
     if (!rc) rc = launch_combine(w, ws, T, k, out, stream);
     if (!rc) rc = clk.finish();

@@ -1,6 +1,7 @@
 // Device helpers shared by the kernels: block decoding, warp reductions, status reporting.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -10,6 +11,19 @@
 namespace ds4moe {
 
 constexpr int kWarp = 32;
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device,
+// once per (kernel, device): the launch path then makes no attribute call per launch.
+// seen: per-kernel array of 64 device slots holding the largest size set so far.
+inline int ensure_smem(const void *kernel, int bytes, int *seen) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && seen[dev] >= bytes) return 0;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev >= 0 && dev < 64) seen[dev] = bytes;
+    return 0;
+}
 
 __device__ __forceinline__ void report(int *status, int bits) {
     if (status) atomicOr(status, bits);

@@ -1,0 +1,855 @@
+// Tensor-core grouped GEMM for prefill-sized expert groups (tcgen05 + TMEM, sm_103a).
+//
+// "DwarfStar" README, "速度" and "基准测试": prefill runs in chunks of thousands of tokens
+// and is compute-rich; with many tokens per expert the expert FFN is a dense contraction,
+// so it runs on the 5th-generation tensor cores. Per (expert, 128 weight rows, up to 256
+// tokens) tile:
+//   * eight producer warps stream the packed 2-bit weight rows from HBM (a ring of register
+//     prefetches per thread), decode them to fp16 (RN-even of the exact fp32 value) and
+//     write them into shared memory in the canonical K-major SWIZZLE_128B layout (one
+//     128-row x 64-column atom column per stage);
+//   * one warp issues TMA loads of the group's token rows (fp16, gathered per group) into
+//     the same layout;
+//   * one thread issues tcgen05.mma (M=128, N=tokens rounded up to 16, K=16) into fp32
+//     accumulators in tensor memory: gate and up side by side for the first GEMM;
+//   * the producer warps then read the accumulators back with tcgen05.ld (two warps per
+//     TMEM lane quarter) and apply the epilogue: h = silu(gate) * up (fp16 out) for the first GEMM, y (fp32 out) for the down
+//     GEMM.
+// Swap-AB: weights are the M side and tokens the N side, so groups of a few dozen tokens
+// still fill MMAs. Every wait on an mbarrier is bounded: after ~2 s it records
+// DS4MOE_ETIMEOUT in the handle's status word and the CTA drains its copies, frees its
+// tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace ds4moe {
+namespace {
+
+constexpr int BM = 128;   // weight rows per tile (MMA M)
+constexpr int BN = kGemmBN;  // token rows per tile (MMA N at most)
+constexpr int BK = 64;    // K elements per stage: one 128-byte swizzle atom
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA (+ TMEM alloc), warps 2..9 producers/epilogue
+constexpr int kProducers = 256;
+constexpr int kTableBytes = 256 * 16 * 8;  // replicated lookup table (grid or code selectors)
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+enum { UP = 0, DOWN = 1 };
+
+template <int KIND>
+struct Cfg;
+template <>
+struct Cfg<UP> {
+    static constexpr int NA = 2;  // gate and up
+    static constexpr int STAGES = 3;
+    static constexpr int TMEM_COLS = 512;
+};
+template <>
+struct Cfg<DOWN> {
+    static constexpr int NA = 1;
+    static constexpr int STAGES = 4;
+    static constexpr int TMEM_COLS = 256;
+};
+
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of the given parity to complete. Gives up (false) when the CTA's
+// abort flag is raised or after kWaitCycles, raising the flag and the status bit itself.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_test(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            report(status, ST_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used to drain copies before exiting).
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity) && clock64() - t0 < kWaitCycles) {
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 32 TMEM lanes x 16 columns of 32-bit: this thread's lane, columns taddr.col .. +15.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: fp16 A and B (K-major), fp32 accumulate, M x N.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-row, 128-byte-wide SWIZZLE_128B tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ tiles
+
+struct GemmParams {
+    DeviceWeights w;
+    const int32_t *offsets, *gemm_list, *tile_prefix;
+    const GroupMeta *meta;
+    const uint8_t *grid;
+    uint16_t *h16;  // UP output, [rows][F]
+    float *y;       // DOWN output, [rows][D]
+    int T, P, shared;
+    int *status;
+};
+
+struct Tile {
+    int shared;  // 1: the shared expert (bf16/fp16 rows), 0: a routed expert
+    int e;       // routed expert
+    int row0;    // first token row (x16 / h16 / y row)
+    int ntok;    // token rows in the tile (1..BN)
+    int m;       // weight-row tile
+};
+
+__device__ __forceinline__ int n_tiles_total(const GemmParams &p, int m_tiles) {
+    const int n_gemm = p.meta->n_gemm;
+    const int routed = p.tile_prefix[n_gemm];
+    const int sh = p.shared ? (p.T + BN - 1) / BN : 0;
+    return (routed + sh) * m_tiles;
+}
+
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_tiles) {
+    Tile ti;
+    ti.m = t % m_tiles;
+    const int nt = t / m_tiles;
+    const int n_gemm = p.meta->n_gemm;
+    const int routed = p.tile_prefix[n_gemm];
+    if (nt < routed) {
+        int lo = 0, hi = n_gemm - 1;  // largest gi with tile_prefix[gi] <= nt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_prefix[mid] <= nt)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int e = p.gemm_list[lo];
+        const int off = p.offsets[e], n = p.offsets[e + 1] - off;
+        const int lt = nt - p.tile_prefix[lo];
+        ti.shared = 0;
+        ti.e = e;
+        ti.row0 = off + lt * BN;
+        ti.ntok = min(BN, n - lt * BN);
+    } else {
+        const int lt = nt - routed;
+        ti.shared = 1;
+        ti.e = -1;
+        ti.row0 = p.P + lt * BN;
+        ti.ntok = min(BN, p.T - lt * BN);
+    }
+    return ti;
+}
+
+// ------------------------------------------------------------------ producers
+//
+// Each of the 256 producer threads owns one tile row of one matrix (first GEMM: gate or up,
+// 64 columns per stage) or one half row (down GEMM, 32 columns per stage). A format fetches
+// the packed data of a stage into registers (a ring of PF stages in flight hides the HBM
+// latency) and emits it as fp16 into the swizzled A tile. Every fp16 value is RN-even of
+// the weight's exact fp32 value.
+
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// fp16 high byte of magnitude m in {1, 3, 5, 7}: their low bytes are zero.
+__device__ __forceinline__ uint32_t mag_hibyte(uint32_t m) {
+    return m == 1u ? 0x3Cu : m == 3u ? 0x42u : m == 5u ? 0x45u : 0x47u;
+}
+
+// IQ2-style rows: 64 weights = 2 sub-blocks = 8 groups per stage.
+struct IQ2Fmt {
+    static constexpr int PF = 4;
+    struct Data {
+        uint4 q;
+        uint32_t d;
+    };
+    const uint8_t *qs;
+    const uint16_t *dp;
+    size_t rowb;
+    const uint2 *gt;  // grid as fp16 high bytes, this lane's replica
+    __device__ __forceinline__ Data fetch(int kb) const {
+        const int b = kb >> 2, part = kb & 3;
+        Data v;
+        v.q = __ldg(reinterpret_cast<const uint4 *>(qs + (rowb + b) * 64) + part);
+        v.d = __ldg(dp + rowb + b);
+        return v;
+    }
+    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
+        const __half2 dh = u2h(v.d | (v.d << 16));
+#pragma unroll
+        for (int sb = 0; sb < 2; sb++) {
+            const uint32_t iw = sb ? v.q.z : v.q.x, sw = sb ? v.q.w : v.q.y;
+            // (s+1)/16, exact in fp16; G*(s+1)/16 is then exact and one multiply by d rounds once
+            const __half2 c16 = __float2half2_rn(static_cast<float>((sw >> 28) + 1u) * 0.0625f);
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                const uint2 ent = gt[((iw >> (8 * g)) & 255u) << 4];
+                const uint32_t s7 = (sw >> (7 * g)) & 127u;
+                const uint32_t lo = ent.x ^ ((s7 * 0x10204080u) & 0x80808080u);
+                const uint32_t hi = ent.y ^ ((s7 * 0x01020408u + (__popc(s7) << 31)) & 0x80808080u);
+                uint4 o;
+                o.x = h2u(__hmul2(__hmul2(u2h(__byte_perm(lo, 0u, 0x1404)), c16), dh));
+                o.y = h2u(__hmul2(__hmul2(u2h(__byte_perm(lo, 0u, 0x3424)), c16), dh));
+                o.z = h2u(__hmul2(__hmul2(u2h(__byte_perm(hi, 0u, 0x1404)), c16), dh));
+                o.w = h2u(__hmul2(__hmul2(u2h(__byte_perm(hi, 0u, 0x3424)), c16), dh));
+                st_shared16(tile + sw128_off(r, sb * 4 + g), o);
+            }
+        }
+    }
+};
+
+// Q2_K-style rows, half row: 32 weights = 2 sub-blocks per stage. The 4 possible values of a
+// sub-block, RN-even(fp32(d*sc*q - dmin*m)) for q = 0..3, are formed once; each code byte
+// then selects its four values with two byte permutations (selectors from a table).
+struct Q2KFmt {
+    static constexpr int PF = 4;
+    struct Data {
+        uint2 q;
+        uint32_t sc;
+        uint32_t dd;
+    };
+    const uint8_t *sq;
+    const uint32_t *ddp;
+    size_t rowb;
+    int half;
+    const uint2 *st;  // code byte -> two byte_perm selectors, this lane's replica
+    __device__ __forceinline__ Data fetch(int kb) const {
+        const int b = kb >> 2, part = kb & 3;
+        const uint8_t *blk = sq + (rowb + b) * 80;
+        Data v;
+        v.q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 16 * part + 8 * half));
+        v.sc = __ldg(reinterpret_cast<const uint16_t *>(blk + 4 * part + 2 * half));
+        v.dd = __ldg(ddp + rowb + b);
+        return v;
+    }
+    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
+        const float d = f16_to_f32(static_cast<uint16_t>(v.dd & 0xffffu));
+        const float dmin = f16_to_f32(static_cast<uint16_t>(v.dd >> 16));
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const uint32_t sc = (v.sc >> (8 * j)) & 15u, mn = (v.sc >> (8 * j + 4)) & 15u;
+            const float ds = __fmul_rn(d, static_cast<float>(sc));
+            const float dm = __fmul_rn(dmin, static_cast<float>(mn));
+            const uint32_t p01 = pack_h2(q2k_weight(ds, dm, 0u), q2k_weight(ds, dm, 1u));
+            const uint32_t p23 = pack_h2(q2k_weight(ds, dm, 2u), q2k_weight(ds, dm, 3u));
+            const uint32_t qw = j ? v.q.y : v.q.x;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                const uint2 s0 = st[((qw >> (16 * hh)) & 255u) << 4];
+                const uint2 s1 = st[((qw >> (16 * hh + 8)) & 255u) << 4];
+                uint4 o;
+                o.x = __byte_perm(p01, p23, s0.x);
+                o.y = __byte_perm(p01, p23, s0.y);
+                o.z = __byte_perm(p01, p23, s1.x);
+                o.w = __byte_perm(p01, p23, s1.y);
+                st_shared16(tile + sw128_off(r, 4 * half + 2 * j + hh), o);
+            }
+        }
+    }
+};
+
+// bf16 rows (shared gate/up), 64 columns per stage -> fp16.
+struct BF16Fmt {
+    static constexpr int PF = 2;
+    struct Data {
+        uint4 v[8];
+    };
+    const uint16_t *row;
+    __device__ __forceinline__ Data fetch(int kb) const {
+        Data d;
+        const uint4 *src = reinterpret_cast<const uint4 *>(row + kb * BK);
+#pragma unroll
+        for (int c = 0; c < 8; c++) d.v[c] = __ldg(src + c);
+        return d;
+    }
+    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+            const uint4 v = d.v[c];
+            st_shared16(tile + sw128_off(r, c),
+                        make_uint4(pack_h2(bf16_lo(v.x), bf16_hi(v.x)), pack_h2(bf16_lo(v.y), bf16_hi(v.y)),
+                                   pack_h2(bf16_lo(v.z), bf16_hi(v.z)), pack_h2(bf16_lo(v.w), bf16_hi(v.w))));
+        }
+    }
+};
+
+// fp16 rows (shared down), half row: 32 columns per stage -> copied.
+struct F16Fmt {
+    static constexpr int PF = 4;
+    struct Data {
+        uint4 v[4];
+    };
+    const uint16_t *row;
+    int half;
+    __device__ __forceinline__ Data fetch(int kb) const {
+        Data d;
+        const uint4 *src = reinterpret_cast<const uint4 *>(row + kb * BK + 32 * half);
+#pragma unroll
+        for (int c = 0; c < 4; c++) d.v[c] = __ldg(src + c);
+        return d;
+    }
+    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
+#pragma unroll
+        for (int c = 0; c < 4; c++) st_shared16(tile + sw128_off(r, 4 * half + c), d.v[c]);
+    }
+};
+
+struct Pipe {  // the producers' view of the stage ring
+    uint64_t *bars;
+    int S;
+    int stage;
+    uint32_t phase;
+    volatile int *abort_flag;
+    int *status;
+};
+
+// Produces the A operand of all K stages of one tile for this thread's row (slice).
+template <class Fmt>
+__device__ __forceinline__ bool produce_tile(const Fmt &f, int num_kb, uint8_t *smem, int stage_bytes, int a_off,
+                                             int r, Pipe &pp) {
+    constexpr int PF = Fmt::PF;
+    typename Fmt::Data ring[PF];
+#pragma unroll
+    for (int i = 0; i < PF; i++) ring[i] = f.fetch(i);  // num_kb >= 4 >= PF
+    for (int kb0 = 0; kb0 < num_kb; kb0 += PF) {
+#pragma unroll
+        for (int i = 0; i < PF; i++) {
+            const typename Fmt::Data cur = ring[i];
+            if (kb0 + i + PF < num_kb) ring[i] = f.fetch(kb0 + i + PF);
+            if (!mbar_wait(smem_u32(pp.bars + 2 * pp.S + pp.stage), pp.phase ^ 1u, pp.abort_flag, pp.status))
+                return false;
+            f.emit(cur, smem_u32(smem + pp.stage * stage_bytes + a_off), r);
+            fence_proxy_async();
+            mbar_arrive(smem_u32(pp.bars + pp.stage));
+            if (++pp.stage == pp.S) {
+                pp.stage = 0;
+                pp.phase ^= 1u;
+            }
+        }
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+// Tensor maps of one token operand with box heights 16, 32, 64, 128 and 256 rows: a tile
+// loads only the smallest box that covers its tokens.
+struct TokenMaps {
+    CUtensorMap m[kTokenBoxes];
+};
+
+__device__ __forceinline__ int box_index(int ntok) {
+    int i = 0;
+    while ((16 << i) < ntok) i++;
+    return i;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ TokenMaps maps, GemmParams p) {
+    using C = Cfg<KIND>;
+    constexpr int S = C::STAGES;
+    constexpr int STAGE_BYTES = C::NA * A_BYTES + B_BYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint2 *table = reinterpret_cast<uint2 *>(smem + S * STAGE_BYTES);  // [256][16] replicated lookup table
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * STAGE_BYTES + kTableBytes);
+    // bars: full_a[S], full_b[S], empty[S], acc_full, acc_empty, spare
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 3 * S + 3);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = p.w.D, F = p.w.F;
+    const int m_tiles = (KIND == UP ? F : D) / BM;
+    const int total = n_tiles_total(p, m_tiles);
+    if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA, before any allocation
+    const int num_kb = (KIND == UP ? D : F) / BK;
+
+    auto full_a = [&](int s) { return smem_u32(bars + s); };
+    auto full_b = [&](int s) { return smem_u32(bars + S + s); };
+    auto empty = [&](int s) { return smem_u32(bars + 2 * S + s); };
+    const uint32_t acc_full = smem_u32(bars + 3 * S), acc_empty = smem_u32(bars + 3 * S + 1);
+    const uint32_t spare = smem_u32(bars + 3 * S + 2);
+    auto a_tile = [&](int s, int a) { return smem_u32(smem + s * STAGE_BYTES + a * A_BYTES); };
+    auto b_tile = [&](int s) { return smem_u32(smem + s * STAGE_BYTES + C::NA * A_BYTES); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full_a(s), kProducers);
+            mbar_init(full_b(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kProducers);
+        mbar_init(spare, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // lookup table, replicated 16 times so that the 16 lanes of a half-warp never share a bank
+    for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
+        const uint32_t e = static_cast<uint32_t>(i >> 4);
+        uint2 v;
+        if (KIND == UP) {  // grid entry e as fp16 high bytes
+            const uint8_t *g = p.grid + 8 * e;
+            v.x = mag_hibyte(g[0]) | (mag_hibyte(g[1]) << 8) | (mag_hibyte(g[2]) << 16) | (mag_hibyte(g[3]) << 24);
+            v.y = mag_hibyte(g[4]) | (mag_hibyte(g[5]) << 8) | (mag_hibyte(g[6]) << 16) | (mag_hibyte(g[7]) << 24);
+        } else {  // code byte e: selectors of values q0, q1 and q2, q3 (value q at bytes 2q, 2q+1)
+            uint32_t sel[4];
+#pragma unroll
+            for (int i2 = 0; i2 < 4; i2++) sel[i2] = (e >> (2 * i2)) & 3u;
+            v.x = (2 * sel[0]) | ((2 * sel[0] + 1) << 4) | ((2 * sel[1]) << 8) | ((2 * sel[1] + 1) << 12);
+            v.y = (2 * sel[2]) | ((2 * sel[2] + 1) << 4) | ((2 * sel[3]) << 8) | ((2 * sel[3] + 1) << 12);
+        }
+        table[i] = v;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA: token tiles
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_parity[S];
+#pragma unroll
+            for (int s = 0; s < S; s++) issued_parity[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile ti = decode_tile(p, t, m_tiles);
+                const int bi = box_index(ti.ntok);
+                const CUtensorMap *map = &maps.m[bi];
+                const uint32_t bytes = static_cast<uint32_t>(16 << bi) * BK * 2;
+                for (int kb = 0; kb < num_kb; kb++) {
+                    if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_b(stage), bytes);
+                    tma_load_2d(b_tile(stage), map, kb * BK, ti.row0, full_b(stage));
+                    issued_parity[stage] = static_cast<int>(phase);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok)  // let copies still in flight land before the CTA exits
+                for (int s = 0; s < S; s++)
+                    if (issued_parity[s] >= 0) mbar_drain(full_b(s), static_cast<uint32_t>(issued_parity[s]));
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue (one thread)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true, issued = false;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile ti = decode_tile(p, t, m_tiles);
+                if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int N = max(16, (ti.ntok + 15) & ~15);
+                const uint32_t idesc = idesc_f16(BM, N);
+                for (int kb = 0; kb < num_kb; kb++) {
+                    if (!mbar_wait(full_a(stage), phase, abort_flag, p.status) ||
+                        !mbar_wait(full_b(stage), phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int a = 0; a < C::NA; a++)
+#pragma unroll
+                        for (int k = 0; k < BK / 16; k++)
+                            tc_mma(tmem + a * BN, sw128_desc(a_tile(stage, a) + k * 32),
+                                   sw128_desc(b_tile(stage) + k * 32), idesc, (kb | k) != 0);
+                    issued = true;
+                    tc_commit(empty(stage));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(acc_full);
+                acc_phase ^= 1u;
+            }
+            if (!ok && issued) {  // wait for the MMAs in flight before the memory goes away
+                tc_commit(spare);
+                mbar_drain(spare, 0);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- producers, then epilogue
+        const int u = (warp - 2) * 32 + lane;  // 0..255
+        const int r = u & 127;                 // tile row == TMEM lane
+        const int sel = u >> 7;                // first GEMM: matrix (gate/up); down GEMM: half row
+        const int q = warp & 3;                // TMEM lane quarter this warp may access
+        const int colhalf = (warp - 2) >> 2;   // epilogue: which 16-column chunks
+        const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+        const uint2 *tab = table + (lane & 15);
+        Pipe pp{bars, S, 0, 0u, abort_flag, p.status};
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile ti = decode_tile(p, t, m_tiles);
+            const int wrow = ti.m * BM + r;
+            if (KIND == UP) {
+                if (ti.shared) {
+                    BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D};
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
+                } else {
+                    const size_t rowb = (static_cast<size_t>(ti.e) * F + wrow) * p.w.nbD;
+                    IQ2Fmt f{sel ? p.w.up_qs : p.w.gate_qs, sel ? p.w.up_d : p.w.gate_d, rowb, tab};
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
+                }
+            } else {
+                if (ti.shared) {
+                    F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, sel};
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
+                } else {
+                    const size_t rowb = (static_cast<size_t>(ti.e) * D + wrow) * p.w.nbF;
+                    Q2KFmt f{p.w.down_sq, p.w.down_dd, rowb, sel, tab};
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
+                }
+            }
+            if (!ok) break;
+            // epilogue: accumulators -> registers -> global; two warps per TMEM lane quarter
+            if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int orow = ti.m * BM + q * 32 + lane;
+            bool range_ok = true;
+            for (int c0 = 16 * colhalf; c0 < ti.ntok; c0 += 32) {
+                if (KIND == UP) {
+                    float g[16], uu[16];
+                    tmem_ld16(tmem + lane_addr + c0, g);
+                    tmem_ld16(tmem + lane_addr + BN + c0, uu);
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        if (c0 + j < ti.ntok) {
+                            const float h = swiglu(g[j], uu[j]);
+                            range_ok &= fabsf(h) <= 65504.0f;
+                            p.h16[static_cast<size_t>(ti.row0 + c0 + j) * F + orow] =
+                                __half_as_ushort(__float2half_rn(h));
+                        }
+                    }
+                } else {
+                    float v[16];
+                    tmem_ld16(tmem + lane_addr + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 16; j++)
+                        if (c0 + j < ti.ntok) p.y[static_cast<size_t>(ti.row0 + c0 + j) * D + orow] = v[j];
+                }
+            }
+            if (!range_ok) report(p.status, ST_RANGE);
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+            acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+    }
+}
+
+// The A operand as the producers write it, for tests: one 128-row x 64-column stage per CTA,
+// decoded by the same formats into a swizzled shared-memory tile, then un-swizzled into
+// dst16 [rows][cols] (fp16 bits).
+__global__ void __launch_bounds__(256) producer_dump_kernel(DeviceWeights w, const uint8_t *grid, int expert,
+                                                            int matrix, uint16_t *dst16) {
+    __shared__ __align__(1024) uint8_t tile[A_BYTES];
+    __shared__ uint2 table[256 * 16];
+    const int lane = threadIdx.x & 31;
+    const int u = threadIdx.x, r = u & 127, sel = u >> 7;
+    const bool down = matrix == DS4MOE_DOWN;
+    for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
+        const uint32_t e = static_cast<uint32_t>(i >> 4);
+        uint2 v;
+        if (!down) {
+            const uint8_t *g = grid + 8 * e;
+            v.x = mag_hibyte(g[0]) | (mag_hibyte(g[1]) << 8) | (mag_hibyte(g[2]) << 16) | (mag_hibyte(g[3]) << 24);
+            v.y = mag_hibyte(g[4]) | (mag_hibyte(g[5]) << 8) | (mag_hibyte(g[6]) << 16) | (mag_hibyte(g[7]) << 24);
+        } else {
+            uint32_t c[4];
+            for (int i2 = 0; i2 < 4; i2++) c[i2] = (e >> (2 * i2)) & 3u;
+            v.x = (2 * c[0]) | ((2 * c[0] + 1) << 4) | ((2 * c[1]) << 8) | ((2 * c[1] + 1) << 12);
+            v.y = (2 * c[2]) | ((2 * c[2] + 1) << 4) | ((2 * c[3]) << 8) | ((2 * c[3] + 1) << 12);
+        }
+        table[i] = v;
+    }
+    __syncthreads();
+    const int rows = down ? w.D : w.F, cols = down ? w.F : w.D;
+    const int m = blockIdx.x, kb = blockIdx.y;
+    const int wrow = m * BM + r;
+    const uint32_t t = smem_u32(tile);
+    const uint2 *tab = table + (lane & 15);
+    if (down) {
+        const size_t rowb = (static_cast<size_t>(expert) * w.D + wrow) * w.nbF;
+        Q2KFmt f{w.down_sq, w.down_dd, rowb, sel, tab};
+        f.emit(f.fetch(kb), t, r);
+    } else if (sel == 0) {
+        const size_t rowb = (static_cast<size_t>(expert) * w.F + wrow) * w.nbD;
+        IQ2Fmt f{matrix == DS4MOE_GATE ? w.gate_qs : w.up_qs, matrix == DS4MOE_GATE ? w.gate_d : w.up_d, rowb, tab};
+        f.emit(f.fetch(kb), t, r);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < BM * 8; i += blockDim.x) {  // 8 chunks of 16 bytes per row
+        const int rr = i >> 3, c = i & 7;
+        const uint4 v = *reinterpret_cast<const uint4 *>(tile + sw128_off(rr, c));
+        if (m * BM + rr < rows)
+            *reinterpret_cast<uint4 *>(dst16 + static_cast<size_t>(m * BM + rr) * cols + kb * BK + 8 * c) = v;
+    }
+}
+
+// x (bf16) -> x16 (fp16) for rows of tensor-core groups and of the shared expert.
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
+                                                     const int32_t *__restrict__ topk_idx,
+                                                     const int32_t *__restrict__ counts,
+                                                     const uint8_t *__restrict__ tc_ok, int gemm_min, int k, int D,
+                                                     int P, int T, int shared, uint16_t *__restrict__ x16,
+                                                     int *status) {
+    const int D8 = D / 8;
+    const size_t n = static_cast<size_t>(P + T) * D8;
+    bool range_ok = true;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int row = static_cast<int>(i / D8), c = static_cast<int>(i - static_cast<size_t>(row) * D8);
+        int tok;
+        if (row < P) {
+            const int pair = perm[row];
+            const int e = topk_idx[pair];
+            if (gemm_min <= 0 || counts[e] < gemm_min || !tc_ok[e]) continue;
+            tok = pair / k;
+        } else {
+            if (!shared) continue;
+            tok = row - P;
+        }
+        const uint4 v = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * D)[c];
+        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+        for (int j = 0; j < 8; j++) range_ok &= fabsf(f[j]) <= 65504.0f;
+        reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(row) * D)[c] =
+            make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+    }
+    if (!range_ok) report(status, ST_RANGE);
+}
+
+int sm_count_tc() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+template <int KIND>
+int launch_gemm(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) {
+    using C = Cfg<KIND>;
+    const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * (C::NA * A_BYTES + B_BYTES) + kTableBytes + 256;
+    static int seen[64];
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemm_kernel<KIND>), static_cast<int>(smem), seen);
+    if (err) return err;
+    gemm_kernel<KIND><<<sm_count_tc(), kThreads, smem, s>>>(maps, p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared) {
+    GemmParams p;
+    p.w = w;
+    p.offsets = ws.offsets;
+    p.gemm_list = ws.gemm_list;
+    p.tile_prefix = ws.tile_prefix;
+    p.meta = ws.meta;
+    p.grid = ws.grid;
+    p.h16 = ws.h16;
+    p.y = ws.y;
+    p.T = T;
+    p.P = T * k;
+    p.shared = shared ? 1 : 0;
+    p.status = ws.status;
+    return p;
+}
+
+}  // namespace
+
+int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, int gemm_min,
+                  bool shared, void *stream) {
+    const int P = T * k;
+    const size_t n = static_cast<size_t>(P + T) * (w.D / 8);
+    const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, static_cast<size_t>(sm_count_tc()) * 8));
+    gather_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, ws.perm, ws.topk_idx, ws.counts, w.tc_ok,
+                                                                         gemm_min, k, w.D, P, T, shared ? 1 : 0,
+                                                                         ws.x16, ws.status);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, uint16_t *dst16,
+                         void *stream) {
+    const bool down = matrix == DS4MOE_DOWN;
+    const int rows = down ? w.D : w.F, cols = down ? w.F : w.D;
+    dim3 g(rows / BM, cols / BK);
+    producer_dump_kernel<<<g, 256, 0, static_cast<cudaStream_t>(stream)>>>(w, grid, expert, matrix, dst16);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_gemm_up(const DeviceWeights &w, const Workspace &ws, const void *tmap_x16, int T, int k, bool shared,
+                   void *stream) {
+    return launch_gemm<UP>(*static_cast<const TokenMaps *>(tmap_x16), make_params(w, ws, T, k, shared),
+                           static_cast<cudaStream_t>(stream));
+}
+
+int launch_gemm_down(const DeviceWeights &w, const Workspace &ws, const void *tmap_h16, int T, int k, bool shared,
+                     void *stream) {
+    return launch_gemm<DOWN>(*static_cast<const TokenMaps *>(tmap_h16), make_params(w, ws, T, k, shared),
+                             static_cast<cudaStream_t>(stream));
+}
+
+// Tensor maps of an fp16 token operand [rows][cols] (row-major, SWIZZLE_128B): boxes of 64
+// columns and 16, 32, 64, 128, 256 rows, written to maps_out (kTokenBoxes maps of 128 bytes).
+int encode_token_maps(void *maps_out, void *base, int rows, int cols) {
+    for (int i = 0; i < kTokenBoxes; i++)
+        if (encode_token_map(static_cast<CUtensorMap *>(maps_out) + i, base, rows, cols, 16 << i)) return 1;
+    return 0;
+}
+
+// One tensor map: 64 x box_rows boxes.
+int encode_token_map(void *map_out, void *base, int rows, int cols, int box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return 1;
+        }
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(static_cast<CUtensorMap *>(map_out), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : 1;
+}
+
+}  // namespace ds4moe

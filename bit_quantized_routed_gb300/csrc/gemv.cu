@@ -391,27 +391,30 @@ int sm_count() {
     return n;
 }
 
+// CTAs per SM that fit the shared memory of one CTA (228 KB per SM, 1 KB reserved per CTA).
+int ctas_per_sm(size_t smem) {
+    const size_t per = smem + 1024;
+    const int n = static_cast<int>((228 * 1024) / per);
+    return n < 1 ? 1 : (n > 4 ? 4 : n);
+}
+
 template <int NT>
 int launch_up_nt(const UpParams &p, cudaStream_t s) {
+    static int seen[64];
     const size_t smem = 2048 + static_cast<size_t>(NT) * p.w.D * 2;
-    cudaError_t err = cudaFuncSetAttribute(gemv_up_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return static_cast<int>(err);
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_up_kernel<NT>, kThreads, smem);
-    gemv_up_kernel<NT><<<sm_count() * (per_sm > 0 ? per_sm : 1), kThreads, smem, s>>>(p);
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_up_kernel<NT>), static_cast<int>(smem), seen);
+    if (err) return err;
+    gemv_up_kernel<NT><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
 template <int NT>
 int launch_down_nt(const DownParams &p, cudaStream_t s) {
+    static int seen[64];
     const size_t smem = static_cast<size_t>(NT) * p.w.F * 4;
-    cudaError_t err = cudaFuncSetAttribute(gemv_down_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return static_cast<int>(err);
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_down_kernel<NT>, kThreads, smem);
-    gemv_down_kernel<NT><<<sm_count() * (per_sm > 0 ? per_sm : 1), kThreads, smem, s>>>(p);
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_down_kernel<NT>), static_cast<int>(smem), seen);
+    if (err) return err;
+    gemv_down_kernel<NT><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -303,6 +303,7 @@ namespace ds4moe {
 
 void host_grid(uint8_t out[2048]) { std::memcpy(out, grid().mag, 2048); }
 bool host_f16_finite(uint16_t h) { return f16_finite(h); }
+double host_f16_value(uint16_t h) { return f16_value(h); }
 
 }  // namespace ds4moe
 

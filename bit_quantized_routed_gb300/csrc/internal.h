@@ -8,8 +8,12 @@
 
 namespace ds4moe {
 
+constexpr int kGemmBN = 256;  // token rows per tensor-core tile
+constexpr int kTokenBoxes = 5; // TMA box heights 16, 32, 64, 128, 256 rows
+
 void host_grid(uint8_t out[2048]);
 bool host_f16_finite(uint16_t h);
+double host_f16_value(uint16_t h);
 
 // Device status bits, OR-ed by kernels into the handle's status word.
 enum : int {
@@ -32,14 +36,17 @@ struct DeviceWeights {
     uint16_t *sh_gate, *sh_up; // [F][D] bf16, or null
     uint16_t *sh_down;         // [D][F] bf16, or null
     uint16_t *sh_down_f16;     // [D][F] fp16 copy for the tensor-core path, or null
+    uint8_t *tc_ok;            // [E] 1 if every dequantised weight of the expert fits fp16
     bool has_shared;
+    bool shared_tc_ok;         // the shared expert's weights fit fp16
 };
 
 // Per-call grouping metadata written on the device by the grouping kernel.
 struct GroupMeta {
-    int n_gemv;  // experts with 0 < n_e < gemm_min, listed in gemv_list in expert order
-    int n_gemm;  // experts with n_e >= gemm_min, listed in gemm_list in expert order
-    int pad[2];
+    int n_gemv;    // experts with 0 < n_e < gemm_min (n_e > 1 when singles are split off), in gemv_list
+    int n_gemm;    // experts with n_e >= gemm_min, listed in gemm_list in expert order
+    int n_single;  // experts with exactly one token (when split off), listed in single_list
+    int pad;
 };
 
 struct Workspace {
@@ -52,6 +59,8 @@ struct Workspace {
     int32_t *inv;       // [P]
     int32_t *gemv_list; // [E]
     int32_t *gemm_list; // [E]
+    int32_t *single_list; // [E]
+    int32_t *tile_prefix; // [E+1] exclusive prefix of ceil(n_e / kGemmBN) over gemm_list
     GroupMeta *meta;
     uint8_t *grid;      // [256][8] IQ2-style grid
     float *h32;         // [P+T][F] fp32 intermediate of the GEMV path (rows P.. = shared expert)
@@ -74,6 +83,8 @@ struct ds4moe_weights {
     bool stage_ran[DS4MOE_N_STAGES];
     bool events_recorded;
     uint64_t calls, launches;
+    alignas(64) unsigned char tmap_x16[128 * ds4moe::kTokenBoxes];  // CUtensorMaps of x16 [rows][D]
+    alignas(64) unsigned char tmap_h16[128 * ds4moe::kTokenBoxes];  // CUtensorMaps of h16 [rows][F]
     void *allocs[64];
     int n_allocs;
 };
@@ -83,9 +94,23 @@ namespace ds4moe {
 // Launchers (return a cudaError_t as int; 0 = success).
 int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *idx, float *w,
                  void *stream);
-int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, int32_t *counts,
-                 int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list,
-                 int32_t *gemm_list, GroupMeta *meta, int *status, void *stream);
+int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok,
+                 int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list,
+                 int32_t *gemm_list, int32_t *single_list, int32_t *tile_prefix, GroupMeta *meta, int *status,
+                 void *stream);
+int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, int gemm_min,
+                  bool shared, void *stream);
+int launch_gemm_up(const DeviceWeights &w, const Workspace &ws, const void *tmap_x16, int T, int k, bool shared,
+                   void *stream);
+int launch_gemm_down(const DeviceWeights &w, const Workspace &ws, const void *tmap_h16, int T, int k, bool shared,
+                     void *stream);
+int encode_token_map(void *map_out, void *base, int rows, int cols, int box_rows);
+int encode_token_maps(void *maps_out, void *base, int rows, int cols);
+int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, uint16_t *dst16,
+                         void *stream);
+int launch_decode_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, bool shared,
+                     void *stream);
+int launch_decode_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared, void *stream);
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
                    bool shared_on_gemv, void *stream);
 int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv,

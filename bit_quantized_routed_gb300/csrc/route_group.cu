@@ -105,9 +105,10 @@ __device__ int block_exclusive_scan(int v, int *tmp, int *total) {
 // then each warp walks its range in order, ranking equal experts inside each batch of 32
 // with __match_any_sync, so positions follow (token, slot) order exactly.
 __global__ void __launch_bounds__(kGroupThreads, 1)
-    group_kernel(const int32_t *__restrict__ idx, int P, int E, int gemm_min, int32_t *__restrict__ counts,
-                 int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
-                 int32_t *__restrict__ gemv_list, int32_t *__restrict__ gemm_list, GroupMeta *meta,
+    group_kernel(const int32_t *__restrict__ idx, int P, int E, int gemm_min, const uint8_t *__restrict__ tc_ok,
+                 int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                 int32_t *__restrict__ inv, int32_t *__restrict__ gemv_list, int32_t *__restrict__ gemm_list,
+                 int32_t *__restrict__ single_list, int32_t *__restrict__ tile_prefix, GroupMeta *meta,
                  int *status) {
     extern __shared__ int sm[];
     int *hist = sm;                      // [kGroupWarps][E]: counts, then base positions
@@ -145,17 +146,25 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
         for (int w = 0; w < kGroupWarps; w++) hist[w * E + e] += off;
     }
     if (e == 0) offsets[E] = all;
-    // GEMV / tensor-core work lists, each in expert order
-    const bool big = e < E && tot > 0 && gemm_min > 0 && tot >= gemm_min;
-    const bool small = e < E && tot > 0 && !big;
-    int n_small = 0, n_big = 0;
+    // GEMV / tensor-core work lists, each in expert order; experts whose weights do not fit
+    // fp16 stay on the GEMV path
+    const bool big = e < E && tot > 0 && gemm_min > 0 && tot >= gemm_min && (!tc_ok || tc_ok[e]);
+    const bool single = single_list && e < E && tot == 1 && !big;  // one-token groups, own list
+    const bool small = e < E && tot > 0 && !big && !single;
+    int n_small = 0, n_big = 0, n_tiles = 0, n_single = 0;
+    const int psg = block_exclusive_scan(single ? 1 : 0, tmp, &n_single);
+    if (single) single_list[psg] = e;
     const int ps = block_exclusive_scan(small ? 1 : 0, tmp, &n_small);
     const int pb = block_exclusive_scan(big ? 1 : 0, tmp, &n_big);
+    const int pt = block_exclusive_scan(big ? (tot + kGemmBN - 1) / kGemmBN : 0, tmp, &n_tiles);
     if (small && gemv_list) gemv_list[ps] = e;
     if (big && gemm_list) gemm_list[pb] = e;
+    if (big && tile_prefix) tile_prefix[pb] = pt;
+    if (threadIdx.x == 0 && tile_prefix) tile_prefix[n_big] = n_tiles;
     if (threadIdx.x == 0 && meta) {
         meta->n_gemv = n_small;
         meta->n_gemm = n_big;
+        meta->n_single = n_single;
     }
     __syncthreads();
     // stable positions
@@ -203,16 +212,17 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
     return static_cast<int>(cudaGetLastError());
 }
 
-int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, int32_t *counts, int32_t *offsets,
-                 int32_t *perm, int32_t *inv, int32_t *gemv_list, int32_t *gemm_list, GroupMeta *meta,
-                 int *status, void *stream) {
+int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok, int32_t *counts,
+                 int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list, int32_t *gemm_list,
+                 int32_t *single_list, int32_t *tile_prefix, GroupMeta *meta, int *status, void *stream) {
     const int P = T * k;
     const size_t smem = (static_cast<size_t>(kGroupWarps) * E + 32) * sizeof(int);
-    cudaError_t err = cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return static_cast<int>(err);
+    static int seen[64];
+    const int err = ensure_smem(reinterpret_cast<const void *>(group_kernel), static_cast<int>(smem), seen);
+    if (err) return err;
     group_kernel<<<1, kGroupThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        idx, P, E, gemm_min, counts, offsets, perm, inv, gemv_list, gemm_list, meta, status);
+        idx, P, E, gemm_min, tc_ok, counts, offsets, perm, inv, gemv_list, gemm_list, single_list, tile_prefix, meta,
+        status);
     return static_cast<int>(cudaGetLastError());
 }
 

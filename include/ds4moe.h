@@ -60,10 +60,10 @@ enum ds4moe_matrix { DS4MOE_GATE = 0, DS4MOE_UP = 1, DS4MOE_DOWN = 2 };
 /* Options of a weights handle, for ds4moe_set_option(). */
 enum ds4moe_option {
     /* Expert groups with at least this many tokens run on the tcgen05 tensor-core path;
-     * smaller groups run on the fused dequant-GEMV path. 0 means never use tensor cores;
-     * 1 means always. Default 33. */
+     * smaller groups run on the fused dequant-GEMV kernels (one-token groups on the
+     * single-token kernels). 0 means never use tensor cores; 1 means always. Default 2. */
     DS4MOE_OPT_GEMM_MIN_TOKENS = 0,
-    /* Same threshold for the bf16 shared expert (by token count T). Default 33. */
+    /* Same threshold for the bf16 shared expert (by token count T). Default 2. */
     DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS = 1,
     /* 1: record CUDA events around each stage of ds4moe_expert_ffn on its stream, so that
      * ds4moe_get_stats() can report per-stage device times. Default 0. */
@@ -149,10 +149,10 @@ void ds4moe_weights_destroy(ds4moe_weights *w);
 
 int ds4moe_set_option(ds4moe_weights *w, int option, int value);
 
-/* Dequantise one resident expert matrix on the device, through the same device decode
- * the kernels use: fp32 values into dst_f32 (rows*cols floats, may be NULL) and the
- * fp16 operand values of the tensor-core path, RN-even of the fp32 value, into
- * dst_f16 (may be NULL). Asynchronous. */
+/* Dequantise one resident expert matrix on the device, through the device decode the
+ * kernels use: fp32 values (the GEMV path's weights) into dst_f32 (rows*cols floats, may be
+ * NULL), and into dst_f16 (may be NULL) the fp16 operand bytes exactly as the tensor-core
+ * producers write them, which are RN-even of the fp32 values. Asynchronous. */
 int ds4moe_weights_dequantize(const ds4moe_weights *w, int expert, int matrix, float *dst_f32,
                               uint16_t *dst_f16, ds4moe_stream_t stream);
 

@@ -153,3 +153,41 @@ def test_ffn_full_size_sampled(ds4, name, tokens):
     ref, _, _ = lay.oracle_delta(tokens=tokens)
     err = norm_max_err(got if tokens is None else got[tokens], ref)
     assert err <= FFN_TOL, err
+
+
+# ---------------------------------------------------------------- the tensor-core path
+
+@pytest.mark.parametrize("T,D,F,E,k,shared", [(4, 256, 256, 8, 2, True), (37, 512, 768, 8, 3, True),
+                                              (600, 256, 512, 4, 2, False), (300, 768, 256, 6, 4, True)])
+def test_ffn_tensor_core_path_forced(ds4, T, D, F, E, k, shared):
+    """Every group (and the shared expert) on tcgen05: several M tiles, N tiles and a ragged tail."""
+    wl = synth.Workload("tc", T=T, D=D, F=F, E=E, k=k, seed=T + F, bias=("zipf", 1.0), shared=shared)
+    err = _ffn_case(ds4, wl, gemm_min=1)
+    assert err <= FFN_TOL, err
+
+
+def test_ffn_mixed_gemv_and_tensor_core_groups(ds4):
+    wl = synth.Workload("mix", T=300, D=512, F=512, E=16, k=4, seed=17, bias=("zipf", 1.2))
+    L, _ = synth.draw_inputs(wl)
+    counts = np.bincount(oracle.route(L, wl.k)[0].reshape(-1), minlength=wl.E)
+    assert (counts >= 33).any() and ((counts > 0) & (counts < 33)).any()
+    err = _ffn_case(ds4, wl)   # default thresholds: both paths in one call
+    assert err <= FFN_TOL, err
+
+
+def test_ffn_tensor_core_reports_fp16_overflow(ds4):
+    import torch
+    wl = synth.Workload("ovf", T=40, D=256, F=256, E=2, k=1, seed=5)
+    lay = Layer(wl, quantized=False)
+    lay.x[3, 7] = synth.f32_to_bf16_bits(np.array([1e5], np.float32))[0]   # beyond fp16
+    W = lay.upload(ds4)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_MIN_TOKENS, 1)
+    x = torch.from_numpy(lay.x.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
+    ds4.ds4moe_expert_ffn(x, W, torch.from_numpy(lay.L).cuda(), wl.k, out)
+    assert ds4.ds4moe_last_status(W) == ds4.DS4MOE_ERANGE
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_MIN_TOKENS, 0)      # the fp32 GEMV path has no such limit
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS, 0)
+    ds4.ds4moe_expert_ffn(x, W, torch.from_numpy(lay.L).cuda(), wl.k, out)
+    assert ds4.ds4moe_last_status(W) == 0
+    W.close()
