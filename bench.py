@@ -170,7 +170,8 @@ def algorithmic(wl, counts):
     down_bytes = touched * Q2K_PER_EXPERT(D, F) + sh_down + rows * F * 4 + rows * D * 4
     flops_up = 2 * 2 * F * D * rows
     flops_down = 2 * D * F * rows
-    return {"touched": touched, "up_bytes": up_bytes, "down_bytes": down_bytes,
+    act_bytes = T * D * 2 + T * wl.E * 4 + 2 * T * D * 4 + 2 * rows * F * 4   # x, logits, out, h
+    return {"touched": touched, "up_bytes": up_bytes, "down_bytes": down_bytes, "act_bytes": act_bytes,
             "total_bytes": touched * (IQ2_PER_EXPERT(D, F) + Q2K_PER_EXPERT(D, F)) + sh_up + sh_down,
             "flops_up": flops_up, "flops_down": flops_down}
 
@@ -183,7 +184,8 @@ def src_sha(*names):
     return h.hexdigest()[:16]
 
 
-STAGE_KERNEL = {"up_gemv": ("gemv_up_kernel", "gemv.cu"), "down_gemv": ("gemv_down_kernel", "gemv.cu"),
+STAGE_KERNEL = {"step": ("decode_step_kernel", "decode_step.cu"),
+                "up_gemv": ("decode_up_kernel", "decode.cu"), "down_gemv": ("decode_down_kernel", "decode.cu"),
                 "combine": ("combine_kernel", "combine.cu"), "route": ("route_kernel", "route_group.cu"),
                 "group": ("group_kernel", "route_group.cu")}
 
@@ -343,8 +345,10 @@ def run_ours(args):
         raise RuntimeError(ds4.ds4moe_strerror(st))
 
     hbm, tflops, peak_src = load_peaks()
-    if dom in ("up_gemv", "down_gemv", "combine", "route", "group"):
+    if dom in ("step", "up_gemv", "down_gemv", "combine", "route", "group"):
         b = alg["up_bytes"] if dom == "up_gemv" else alg["down_bytes"] if dom == "down_gemv" else None
+        if dom == "step":  # the whole single-token call in one kernel
+            b = alg["total_bytes"] + alg["act_bytes"]
         if dom == "combine":
             b = (wl.T * wl.k + wl.T) * wl.D * 4 + 2 * wl.T * wl.D * 4
         achieved = (b / (dom_ms / 1e3) / 1e9) if b else None
@@ -355,7 +359,7 @@ def run_ours(args):
     else:
         f = alg["flops_up"] if dom == "up_gemm" else alg["flops_down"]
         achieved = f / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+        roof = {"bound": "tensor", "kernel": "gemm_kernel<UP>" if dom == "up_gemm" else "gemm_kernel<DOWN>", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
                 "frac": achieved / tflops, "traffic": None, "algorithmic_flops": f, "avg_launch_ms": dom_ms,
                 "peak_source": peak_src}
     roof["stage_ms"] = {n: round(v / K, 5) for n, v in stage_tot.items() if v > 0}

@@ -26,14 +26,16 @@ DS4MOE_GATE, DS4MOE_UP, DS4MOE_DOWN = 0, 1, 2
 DS4MOE_OPT_GEMM_MIN_TOKENS = 0
 DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS = 1
 DS4MOE_OPT_PROFILE = 2
-STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine"]
+DS4MOE_OPT_SINGLE_STEP = 3
+DS4MOE_OPT_TRACE = 4
+STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step"]
 
 EXPORTED = [
     "ds4moe_strerror", "ds4moe_q2k_bytes", "ds4moe_iq2_bytes", "ds4moe_iq2_grid",
     "ds4moe_quantize_q2k", "ds4moe_quantize_iq2", "ds4moe_dequantize_q2k", "ds4moe_dequantize_iq2",
     "ds4moe_weights_create", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
     "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
-    "ds4moe_expert_ffn_static",
+    "ds4moe_expert_ffn_static", "ds4moe_step_trace",
 ]
 
 
@@ -55,7 +57,7 @@ class _Desc(ctypes.Structure):
 
 
 class _Stats(ctypes.Structure):
-    _fields_ = [("calls", ctypes.c_uint64), ("launches", ctypes.c_uint64), ("stage_ms", ctypes.c_float * 8)]
+    _fields_ = [("calls", ctypes.c_uint64), ("launches", ctypes.c_uint64), ("stage_ms", ctypes.c_float * 9)]
 
 
 _lib = None
@@ -88,6 +90,7 @@ def lib():
             "ds4moe_get_stats": ([vp, ctypes.POINTER(_Stats)], i32),
             "ds4moe_last_status": ([vp, vp], i32),
             "ds4moe_expert_ffn_static": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
+            "ds4moe_step_trace": ([vp, vp, i32, ctypes.POINTER(i32)], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -290,6 +293,14 @@ def ds4moe_get_stats(weights):
     _check(lib().ds4moe_get_stats(weights.handle, ctypes.byref(st)), "ds4moe_get_stats")
     return {"calls": st.calls, "launches": st.launches,
             "stage_ms": {n: float(st.stage_ms[i]) for i, n in enumerate(STAGES)}}
+
+
+def ds4moe_step_trace(weights, max_ctas=1024):
+    """Per-CTA timestamps (ns) of the last single-token call: array [CTAs, 6]."""
+    out = np.zeros(max_ctas * 6, np.uint64)
+    n = ctypes.c_int(0)
+    _check(lib().ds4moe_step_trace(weights.handle, out.ctypes.data, out.size, ctypes.byref(n)), "ds4moe_step_trace")
+    return out[:n.value].reshape(-1, 6)
 
 
 def ds4moe_last_status(weights, stream=None):

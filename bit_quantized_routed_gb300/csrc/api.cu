@@ -157,6 +157,7 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     }
     h->gemm_min_tokens = 2;
     h->shared_gemm_min_tokens = 2;
+    h->single_step = 1;
     DeviceWeights &w = h->dw;
     w.D = D;
     w.F = F;
@@ -240,10 +241,17 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
         TRY(DS4MOE_ECUDA);
     TRY(dev_alloc(h, &ws.y, rows * D * 4));
     TRY(dev_alloc(h, &ws.status, 16));
+    TRY(dev_alloc(h, &ws.gbar, 16));
+    TRY(dev_alloc(h, &ws.hmax, 1024 * 8 * 4));
+    TRY(dev_alloc(h, &ws.trace, 1024 * 6 * 8));
+    if (cudaMemset(ws.gbar, 0, 16) != cudaSuccess) TRY(DS4MOE_ECUDA);
+    TRY(dev_alloc(h, &ws.grid_hi, 2048));
     {
-        uint8_t g[2048];
+        uint8_t g[2048], hb[2048];
         host_grid(g);
+        for (int i = 0; i < 2048; i++) hb[i] = g[i] == 1 ? 0x3C : g[i] == 3 ? 0x42 : g[i] == 5 ? 0x45 : 0x47;
         TRY(upload(ws.grid, g, 2048));
+        TRY(upload(ws.grid_hi, hb, 2048));
     }
     if (cudaMemset(ws.status, 0, 16) != cudaSuccess) TRY(DS4MOE_ECUDA);
     if (cudaDeviceSynchronize() != cudaSuccess) TRY(DS4MOE_ECUDA);
@@ -269,6 +277,8 @@ int ds4moe_set_option(ds4moe_weights *h, int option, int value) {
     switch (option) {
         case DS4MOE_OPT_GEMM_MIN_TOKENS: h->gemm_min_tokens = value; return DS4MOE_OK;
         case DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS: h->shared_gemm_min_tokens = value; return DS4MOE_OK;
+        case DS4MOE_OPT_SINGLE_STEP: h->single_step = value ? 1 : 0; return DS4MOE_OK;
+        case DS4MOE_OPT_TRACE: h->trace = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_PROFILE:
             if (value && !h->events[0]) {
                 for (auto &ev : h->events) {
@@ -322,6 +332,21 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     const DeviceWeights &w = h->dw;
     const Workspace &ws = h->ws;
     StageClock clk(h, stream);
+    if (T == 1 && h->single_step && decode_step_supported(w, k) &&
+        !(h->gemm_min_tokens == 1 || (w.has_shared && h->shared_gemm_min_tokens == 1))) {
+        // one token: routing, both expert phases and the combine in one cooperative kernel
+        int rc = clk.stage(DS4MOE_STAGE_STEP);
+        if (!rc) rc = launch_decode_step(w, ws, x, logits, k, gate_mode, out, h->trace ? ws.trace : nullptr, stream);
+        if (!rc) {
+            rc = clk.finish();
+            h->calls++;
+            return cuda_status(rc);
+        }
+        // the cooperative launch was refused (e.g. the SMs are shared): the separate kernels
+        cudaGetLastError();
+        h->stage_ran[DS4MOE_STAGE_STEP] = false;
+        h->launches--;
+    }
     // A group holds at most T tokens, so the tensor-core path can only be needed when
     // T reaches the threshold; the device decides per group after routing.
     const int gemm_min = (h->gemm_min_tokens > 0 && T >= h->gemm_min_tokens) ? h->gemm_min_tokens : 0;
@@ -393,6 +418,18 @@ int ds4moe_get_stats(ds4moe_weights *h, ds4moe_stats *out) {
         }
         out->stage_ms[i] = ms;
     }
+    return DS4MOE_OK;
+}
+
+int ds4moe_step_trace(ds4moe_weights *h, uint64_t *out, int max_values, int *n_values) {
+    if (!h || !out || !n_values || max_values < 0) return DS4MOE_EINVAL;
+    const int n = std::min(max_values, decode_step_ctas() * 6);
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(out, h->ws.trace, static_cast<size_t>(n) * 8, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ECUDA;
+    }
+    *n_values = n;
     return DS4MOE_OK;
 }
 

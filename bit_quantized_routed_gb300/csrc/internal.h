@@ -63,11 +63,15 @@ struct Workspace {
     int32_t *tile_prefix; // [E+1] exclusive prefix of ceil(n_e / kGemmBN) over gemm_list
     GroupMeta *meta;
     uint8_t *grid;      // [256][8] IQ2-style grid
+    uint8_t *grid_hi;   // [256][8] the grid's magnitudes as fp16 high bytes (1, 3, 5, 7 -> 3C, 42, 45, 47)
     float *h32;         // [P+T][F] fp32 intermediate of the GEMV path (rows P.. = shared expert)
     uint16_t *h16;      // [P+T][F] fp16 intermediate of the tensor-core path
     uint16_t *x16;      // [P+T][D] fp16 tokens gathered per group for the tensor-core path
     float *y;           // [P+T][D] per-pair expert outputs (rows P.. = shared expert)
     int *status;        // device status word
+    unsigned *gbar;     // grid barrier of the single-token kernel: count, generation
+    float *hmax;        // [1024][8] per-CTA maxima of the single-token kernel
+    uint64_t *trace;    // [1024][6] timestamps of the single-token kernel
 };
 
 }  // namespace ds4moe
@@ -79,6 +83,8 @@ struct ds4moe_weights {
     int gemm_min_tokens;
     int shared_gemm_min_tokens;
     int profile;
+    int single_step;  // T = 1 calls use the fused single-token kernel when it supports the shape
+    int trace;        // record the single-token kernel's per-CTA timestamps
     void *events[DS4MOE_N_STAGES + 1];  // cudaEvent_t: start of each stage, end of the call
     bool stage_ran[DS4MOE_N_STAGES];
     bool events_recorded;
@@ -111,6 +117,10 @@ int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert
 int launch_decode_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, bool shared,
                      void *stream);
 int launch_decode_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared, void *stream);
+bool decode_step_supported(const DeviceWeights &w, int k);
+int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, const float *logits, int k,
+                       int gate_mode, float *out, uint64_t *trace, void *stream);
+int decode_step_ctas();
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
                    bool shared_on_gemv, void *stream);
 int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv,

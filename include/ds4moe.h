@@ -67,7 +67,13 @@ enum ds4moe_option {
     DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS = 1,
     /* 1: record CUDA events around each stage of ds4moe_expert_ffn on its stream, so that
      * ds4moe_get_stats() can report per-stage device times. Default 0. */
-    DS4MOE_OPT_PROFILE = 2
+    DS4MOE_OPT_PROFILE = 2,
+    /* 1: a call with T = 1 runs as one cooperative kernel (routing, both expert phases and
+     * the combine; d_ff = 2048, k <= 8, d_model <= 8192); 0: as the separate kernels.
+     * Default 1. */
+    DS4MOE_OPT_SINGLE_STEP = 3,
+    /* 1: the single-token kernel records per-CTA timestamps, read by ds4moe_step_trace(). */
+    DS4MOE_OPT_TRACE = 4
 };
 
 /* Stages of ds4moe_expert_ffn, in launch order (indices into ds4moe_stats.stage_ms). */
@@ -80,7 +86,8 @@ enum ds4moe_stage {
     DS4MOE_STAGE_DOWN_GEMV = 5, /* dequant-GEMV down */
     DS4MOE_STAGE_DOWN_GEMM = 6, /* tensor-core down */
     DS4MOE_STAGE_COMBINE = 7,   /* gate-weighted combine into the residual */
-    DS4MOE_N_STAGES = 8
+    DS4MOE_STAGE_STEP = 8,      /* the single-token kernel: the whole call */
+    DS4MOE_N_STAGES = 9
 };
 
 typedef struct {
@@ -188,6 +195,12 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *w, const float *logits,
 /* Counters of the handle, and (when DS4MOE_OPT_PROFILE is on) the per-stage device times of
  * the last call, read from its CUDA events (waits for them). */
 int ds4moe_get_stats(ds4moe_weights *w, ds4moe_stats *out);
+
+/* Diagnostics of the single-token kernel (with DS4MOE_OPT_TRACE on): synchronises the device
+ * and copies up to max_values timestamps of the last call into out: per CTA six globaltimer
+ * values in ns -- start, prologue done, gate/up phase done, grid barrier passed, h staged,
+ * down phase done. *n_values receives the number copied (6 per CTA). */
+int ds4moe_step_trace(ds4moe_weights *w, uint64_t *out, int max_values, int *n_values);
 
 /* Synchronise the stream, then return and clear the handle's device status word
  * (DS4MOE_OK when no kernel reported an error since the last call). */

@@ -191,3 +191,26 @@ def test_ffn_tensor_core_reports_fp16_overflow(ds4):
     ds4.ds4moe_expert_ffn(x, W, torch.from_numpy(lay.L).cuda(), wl.k, out)
     assert ds4.ds4moe_last_status(W) == 0
     W.close()
+
+
+# ---------------------------------------------------------------- the single-token kernel
+
+@pytest.mark.parametrize("D,E,k,shared,mode", [(4096, 256, 8, True, 0), (7168, 64, 6, True, 1), (1024, 16, 8, False, 0)])
+def test_single_token_kernel_matches_oracle(ds4, D, E, k, shared, mode):
+    wl = synth.Workload("one", T=1, D=D, F=2048, E=E, k=k, seed=D + E, shared=shared)
+    err = _ffn_case(ds4, wl, quantized=False, mode=mode)
+    assert err <= FFN_TOL, err
+
+
+def test_single_token_kernel_equals_separate_kernels_and_is_deterministic(ds4):
+    import torch
+    wl = synth.WORKLOADS["decode_t1"]
+    lay = Layer(wl, quantized=False)
+    W = lay.upload(ds4)
+    a = lay.run(ds4, W)
+    b = lay.run(ds4, W)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SINGLE_STEP, 0)
+    c = lay.run(ds4, W)
+    W.close()
+    assert norm_max_err(a, c) <= FFN_TOL   # two valid paths, each within tolerance of the oracle
