@@ -167,32 +167,39 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     w.has_shared = n_shared == 3;
     const size_t nb_up = static_cast<size_t>(F) * w.nbD;    // blocks per gate/up matrix
     const size_t nb_down = static_cast<size_t>(D) * w.nbF;  // blocks per down matrix
-    TRY(dev_alloc(h, &w.gate_qs, E * nb_up * 64));
-    TRY(dev_alloc(h, &w.up_qs, E * nb_up * 64));
-    TRY(dev_alloc(h, &w.gate_d, E * nb_up * 2));
-    TRY(dev_alloc(h, &w.up_d, E * nb_up * 2));
-    TRY(dev_alloc(h, &w.down_sq, E * nb_down * 80));
-    TRY(dev_alloc(h, &w.down_dd, E * nb_down * 4));
+    const size_t up_bytes = nb_up * 132;       // gate + up of one expert, tiled (66 bytes per block each)
+    const size_t down_bytes = nb_down * 84;    // down of one expert, tiled
+    TRY(dev_alloc(h, &w.iq2, E * up_bytes));
+    TRY(dev_alloc(h, &w.q2k, E * down_bytes));
     TRY(dev_alloc(h, &w.tc_ok, E));
     {
-        std::vector<uint8_t> qs(nb_up * 64), sq(nb_down * 80), ok(E);
+        std::vector<uint8_t> qs(nb_up * 64), sq(nb_down * 80), ok(E), tiles(std::max(up_bytes, down_bytes));
         std::vector<uint16_t> dv(nb_up);
         std::vector<uint32_t> dd(nb_down);
+        DeviceWeights w0 = w;  // offsets of expert 0: the host staging buffer holds one expert
         for (int e = 0; e < E; e++) {
             const void *mats[2] = {desc->gate_iq2[e], desc->up_iq2[e]};
-            uint8_t *dqs[2] = {w.gate_qs, w.up_qs};
-            uint16_t *dds[2] = {w.gate_d, w.up_d};
             double amax = 0.0;
             for (int m = 0; m < 2; m++) {
                 if (!repack_iq2(static_cast<const uint8_t *>(mats[m]), nb_up, qs.data(), dv.data(), &amax))
                     TRY(DS4MOE_EBADDATA);
-                TRY(upload(dqs[m] + e * nb_up * 64, qs.data(), nb_up * 64));
-                TRY(upload(dds[m] + e * nb_up, dv.data(), nb_up * 2));
+                for (int r = 0; r < F; r++) {
+                    std::memcpy(tiles.data() + iq2_qs_offset(w0, m, 0, r), qs.data() + static_cast<size_t>(r) * w.nbD * 64,
+                                static_cast<size_t>(w.nbD) * 64);
+                    std::memcpy(tiles.data() + iq2_d_offset(w0, m, 0, r), dv.data() + static_cast<size_t>(r) * w.nbD,
+                                static_cast<size_t>(w.nbD) * 2);
+                }
             }
+            TRY(upload(w.iq2 + e * up_bytes, tiles.data(), up_bytes));
             if (!repack_q2k(static_cast<const uint8_t *>(desc->down_q2k[e]), nb_down, sq.data(), dd.data(), &amax))
                 TRY(DS4MOE_EBADDATA);
-            TRY(upload(w.down_sq + e * nb_down * 80, sq.data(), nb_down * 80));
-            TRY(upload(w.down_dd + e * nb_down, dd.data(), nb_down * 4));
+            for (int r = 0; r < D; r++) {
+                std::memcpy(tiles.data() + q2k_sq_offset(w0, 0, r), sq.data() + static_cast<size_t>(r) * w.nbF * 80,
+                            static_cast<size_t>(w.nbF) * 80);
+                std::memcpy(tiles.data() + q2k_dd_offset(w0, 0, r), dd.data() + static_cast<size_t>(r) * w.nbF,
+                            static_cast<size_t>(w.nbF) * 4);
+            }
+            TRY(upload(w.q2k + e * down_bytes, tiles.data(), down_bytes));
             ok[e] = amax <= kF16Max ? 1 : 0;  // otherwise the expert stays on the fp32 GEMV path
         }
         TRY(upload(w.tc_ok, ok.data(), E));

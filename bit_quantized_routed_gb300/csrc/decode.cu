@@ -145,11 +145,10 @@ __global__ void __launch_bounds__(kThreads) decode_up_kernel(DecParams p) {
                     float dg[kRW], du[kRW];
 #pragma unroll
                     for (int r = 0; r < kRW; r++) {
-                        const size_t rowb = (static_cast<size_t>(e) * F + r0 + r) * nbD + b;
-                        qg[r] = __ldg(reinterpret_cast<const uint4 *>(p.w.gate_qs + rowb * 64) + part);
-                        qu[r] = __ldg(reinterpret_cast<const uint4 *>(p.w.up_qs + rowb * 64) + part);
-                        dg[r] = f16_to_f32(__ldg(p.w.gate_d + rowb)) * xinv;
-                        du[r] = f16_to_f32(__ldg(p.w.up_d + rowb)) * xinv;
+                        qg[r] = __ldg(reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 0, e, r0 + r) + b * 64) + part);
+                        qu[r] = __ldg(reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 1, e, r0 + r) + b * 64) + part);
+                        dg[r] = f16_to_f32(__ldg(iq2_d_row(p.w, 0, e, r0 + r) + b)) * xinv;
+                        du[r] = f16_to_f32(__ldg(iq2_d_row(p.w, 1, e, r0 + r) + b)) * xinv;
                     }
 #pragma unroll
                     for (int r = 0; r < kRW; r++) {
@@ -288,11 +287,10 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(DecParams p) {
                     uint32_t scw[kRW], ddw[kRW];
 #pragma unroll
                     for (int r = 0; r < kRW; r++) {
-                        const size_t rowb = (static_cast<size_t>(e) * D + r0 + r) * nbF + b;
-                        const uint8_t *sq = p.w.down_sq + rowb * 80;
+                        const uint8_t *sq = q2k_sq_row(p.w, e, r0 + r) + b * 80;
                         qv[r] = __ldg(reinterpret_cast<const uint4 *>(sq + 16) + part);
                         scw[r] = __ldg(reinterpret_cast<const uint32_t *>(sq) + part);
-                        ddw[r] = __ldg(p.w.down_dd + rowb);
+                        ddw[r] = __ldg(q2k_dd_row(p.w, e, r0 + r) + b);
                     }
 #pragma unroll
                     for (int r = 0; r < kRW; r++) {

@@ -3,24 +3,38 @@
 //
 // "DwarfStar" README, "运行大于 RAM 的模型": every new token is routed through the experts
 // again, so each decode step streams the selected experts' packed rows once. At one token the
-// step is a pure stream of bytes, so the kernel is built to keep HBM busy:
+// step is a pure stream of bytes, so the kernel is built to keep HBM busy and to spend few
+// instructions and little shared-memory bandwidth per streamed weight:
+//   * one producer warp streams weight rows into a 4-stage shared-memory ring with 1-D TMA
+//     bulk copies; it starts at once on the bf16 shared expert's rows (they need no routing),
+//     so the ring fills while the first loads of x and the logits are still in flight
+//     and interleaves them with the routed experts' rows, which wait for the top-k; each
+//     warp reads its part of a stage into registers and frees the stage before the arithmetic;
 //   * every CTA (one per SM) routes the token itself -- top-k of the router logits, ties to the
 //     lower index -- so no launch or barrier separates routing from the experts;
-//   * one producer warp streams weight rows into a 3-stage shared-memory ring with 1-D TMA
-//     bulk copies (up to ~110 KB in flight per SM), sixteen compute warps decode from shared
-//     memory; the phase-2 (down) rows are fetched before the grid barrier that waits for h;
-//   * dot products of packed rows are exact integer sums: x (per 2048 columns) and h (per
-//     routed pair) are held as int16 with a power-of-two scale (2^14 over the absolute
-//     maximum: error ~2^-15 of that maximum), IQ2-style groups become signed int8 vectors
-//     (grid magnitudes, signs applied through a 128-entry table of byte masks) and Q2_K-style
-//     codes become int8 bytes through a 256-entry table; dp2a accumulates int16 x int8 pairs
-//     into int32 without rounding, and each 16- or 32-weight sub-block's integer sum is
-//     scaled into fp32 once; the bf16 shared expert runs in fp32;
-//   * the down phase owns whole output rows, so each row's 8 routed contributions and the
-//     shared one are summed in a fixed order and added to the residual once: deterministic.
-// Every wait is bounded (~2 s): a timeout sets DS4MOE_ETIMEOUT in the status word and the CTA
-// finishes without waiting further. The kernel is launched cooperatively, so all CTAs are
-// resident together when they meet at the grid barrier.
+//   * gate/up (phase 1): each compute warp owns one 1024-column quarter of x, 32 columns per
+//     lane held in registers as int16 with a power-of-two scale (2^14 over the quarter's absolute
+//     maximum), and the 16 rows of a unit are spread over the warps (4 rows per warp when x has
+//     four quarters). An IQ2-style group of 8 weights is one 32-bit codebook word of nibbles
+//     (m - 1, which is even; elements 0, 2, 4, 6 in the low nibbles, 1, 3, 5, 7 in the high ones)
+//     and one 32-bit sign word of nibbles, 0x9 (keep) or 0x7 (negate): their XOR is, per nibble,
+//     the signed weight plus 8 (m-1 ^ 9 = m + 8, m-1 ^ 7 = 8 - m, no carries). Two masks give
+//     the even weights as bytes and 16 x the odd ones; dp2a multiplies them (unsigned) by the
+//     int16 x pairs (signed) exactly, and 8 * sum(x) of the sub-block removes the offset. Each
+//     lookup is one 4-byte word per lane, so a warp's lookup is one shared-memory wavefront.
+//     Each 32-weight sub-block's integer sum is scaled once;
+//   * a routed unit is 16 rows of one expert's gate and up, i.e. exactly one 16-column
+//     sub-block of its down matrix, so the unit quantises its 16 h values to int16 with a scale
+//     of its own and keeps their fp32 sum (for the dmin term) -- stored in the order that lets
+//     the Q2_K-style bit pairs be used with one mask per four codes and no table;
+//   * down (phase 2): each thread keeps 32 columns of h (one expert) in registers for the whole
+//     phase; the bf16 shared expert runs in fp32 on fp32 h;
+//   * the cross-warp sums of each unit go through shared memory to a finisher warp, double-
+//     buffered and handed over with mbarriers, so compute warps never wait for one another; each
+//     output row is summed in a fixed order and added to the residual once: deterministic.
+// Every mbarrier wait is bounded (~2 s): a timeout sets DS4MOE_ETIMEOUT in the status word, and
+// the warps keep their barrier hand-shakes (without computing) so that the CTA always finishes.
+// The kernel is launched cooperatively, so all CTAs are resident together at the grid barrier.
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -32,17 +46,41 @@
 namespace ds4moe {
 namespace {
 
-constexpr int kCompute = 16;                   // compute warps
-constexpr int kThreads = (kCompute + 1) * 32;  // + one producer warp
-constexpr int kStages = 3;
+constexpr int kCompute = 16;             // compute warps
+constexpr int kProducer = kCompute;      // warp index of the weight streamer
+constexpr int kFinisher = kCompute + 1;  // warp index of the unit finisher
+constexpr int kThreads = (kCompute + 2) * 32;
+constexpr int kStages = 4;
 constexpr int kStageBytes = 38912;
-constexpr int kTabEntries = 256 * 16;  // lookup table replicated per half-warp lane
-constexpr int kSignEntries = 128 * 8;  // sign masks, replicated per quarter-warp lane (16-byte reads)
-constexpr int kActBytes = 44 * 1024;
-constexpr int kRows2 = 4;  // output rows per down-phase unit
+constexpr int kRows1 = 16;   // gate/up rows per routed unit: one 16-column sub-block of down
+constexpr int kRowsSh = 2;   // shared-expert gate/up rows per unit
+constexpr int kRows2 = 4;    // output rows per down unit
+static_assert(kRows1 == kIq2TileRows && kRows2 == kQ2kTileRows, "a unit is one weight tile per expert");
+constexpr int kLead = 4;     // shared-expert units streamed before the first routed one
+constexpr int kMaxD = 4096;
+// Shared memory: [ring: kStages x kStageBytes][table: 256 slots of 256 bytes][barriers, scratch].
+// Slot e holds codebook entry e in its first 128 bytes (one u32 replica per lane), and in its
+// second 128 bytes sign entry e (e < 128, one replica per lane) or, for e >= 128, four pairs of
+// fp32 x quads for the shared expert. A codebook byte offset is then lane * 4 | index << 8: one
+// byte_perm builds it, and the table's base folds into the load.
+constexpr int kTabOff = kStages * kStageBytes;
+constexpr int kTabBytes = 256 * 256;
+constexpr int kMiscOff = kTabOff + kTabBytes;
+constexpr int kSmemBytes = kMiscOff + 2048;
+static_assert(kTabOff % 256 == 0, "table slots are 256-byte aligned");
+static_assert(kMaxD / 8 <= 128 * 4, "x pairs fit the second halves of slots 128..255");
 
-// Swizzled 16-byte chunk index: lanes reading 64 or 128 contiguous bytes each hit distinct banks.
-__device__ __forceinline__ int swz(int q) { return q ^ ((q >> 3) & 7); }
+// Byte offset in the table of the fp32 x pair (columns 8q .. 8q+7) of the shared expert.
+__host__ __device__ constexpr int xpair_offset(int q) { return (128 + (q >> 2)) * 256 + 128 + (q & 3) * 32; }
+
+// Named barriers (0 is __syncthreads). The per-unit hand-off between the compute warps and the
+// finisher goes through mbarriers instead, so that no compute warp waits for another one.
+constexpr int kBarAll = 1;      // compute warps + finisher
+constexpr int kBarCompute = 2;  // compute warps
+constexpr int kNAll = (kCompute + 1) * 32;
+constexpr int kNCompute = kCompute * 32;
+
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 __device__ __forceinline__ uint64_t now_ns() {
     uint64_t t;
@@ -50,10 +88,14 @@ __device__ __forceinline__ uint64_t now_ns() {
     return t;
 }
 
-__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCompute * 32) : "memory"); }
+// v rounded to the nearest integer (ties to even), for |v| <= 2^22, as the low bits of the result:
+// adding 1.5 * 2^23 leaves the rounded integer in the mantissa (two full-rate operations).
+__device__ __forceinline__ uint32_t round_to_int_bits(float v) {
+    return static_cast<uint32_t>(__float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000);
+}
 
-// Barrier of the 4 warps that share output row r of a down-phase unit (ids 2..5).
-__device__ __forceinline__ void row_sync(int r) { asm volatile("bar.sync %0, 128;" ::"r"(2 + r) : "memory"); }
+// Exact int -> float for |v| < 2^22 with two full-rate operations (no conversion unit).
+__device__ __forceinline__ float small_int_to_float(int v) { return __int_as_float(0x4B400000 + v) - 12582912.0f; }
 
 struct StepParams {
     DeviceWeights w;
@@ -61,563 +103,756 @@ struct StepParams {
     const float *logits;   // [E]
     float *out;            // [D], += delta
     int k, mode;
-    const uint8_t *grid;   // grid magnitudes [256][8]
+    const uint8_t *grid;   // codebook magnitudes [256][8]
     int32_t *topk_idx;     // [k] (written by CTA 0)
     float *topk_w;         // [k]
-    float *h;              // [k+1][F] fp32, row k = shared expert
-    unsigned *bar;         // grid barrier: count, generation
-    float *hmax;           // [gridDim][8] per-CTA max |h| of each routed pair
+    int16_t *hq;           // [k][F] h as int16, each 16-row sub-block in dp2a order
+    float *hsc;            // [k][F/16] dequantisation factor of each sub-block
+    float *hsum;           // [k][F/16] fp32 sum of each sub-block's h
+    float *hsh;            // [F] shared expert's h (fp32)
+    unsigned long long *bar;  // grid barrier: arrivals since the workspace was made
     uint64_t *trace;       // null, or [gridDim][6] timestamps (ns)
     int *status;
-    int r1, rs;            // rows per phase-1 routed / shared unit
 };
 
-// Geometry of the units of one call, identical in every CTA.
-struct Units {
-    int per1;   // routed units per expert (F / r1)
-    int n1r;    // routed phase-1 units
-    int n1;     // all phase-1 units
-    int n2;     // phase-2 units (D / kRows2)
-};
-
-__device__ __forceinline__ Units units_of(const StepParams &p) {
-    Units u;
-    u.per1 = p.w.F / p.r1;
-    u.n1r = p.k * u.per1;
-    u.n1 = u.n1r + (p.w.has_shared ? p.w.F / p.rs : 0);
-    u.n2 = p.w.D / kRows2;
-    return u;
+__device__ __forceinline__ int count_of(int n) {
+    const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
+    return n > b ? (n - 1 - b) / g + 1 : 0;
 }
 
-// Issues the bulk copies of one unit into a stage (one thread).
-__device__ void issue_unit(const StepParams &p, const Units &U, const int *idx, int phase, int unit, uint32_t dst,
-                           uint32_t bar) {
+// Order of one CTA's gate/up units: kLead shared-expert units, then routed and shared
+// alternately, then what remains. Unit indices are blockIdx.x + i * gridDim.x within each kind.
+struct Seq1 {
+    int ts, tr, ns, nr;
+    __device__ bool next(bool &shared, int &unit) {
+        if (ts < ns && (tr >= nr || ts < kLead + tr)) {
+            shared = true;
+            unit = static_cast<int>(blockIdx.x) + ts++ * static_cast<int>(gridDim.x);
+            return true;
+        }
+        if (tr < nr) {
+            shared = false;
+            unit = static_cast<int>(blockIdx.x) + tr++ * static_cast<int>(gridDim.x);
+            return true;
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ Seq1 seq1_of(const StepParams &p) {
+    Seq1 s;
+    s.ts = s.tr = 0;
+    s.ns = p.w.has_shared ? count_of(p.w.F / kRowsSh) : 0;
+    s.nr = count_of(p.k * (p.w.F / kRows1));
+    return s;
+}
+
+// Bounded wait with the common case (phase already complete) inline.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status) {
+    return mbar_test(bar, parity) || mbar_wait(bar, parity, abort_flag, status);
+}
+
+// Sums two per-lane values over the warp; afterwards lane l holds the total of value (l >> 4) & 1.
+__device__ __forceinline__ float reduce2(float v0, float v1, int lane) {
+    const bool u16 = lane & 16;
+    float c = (u16 ? v1 : v0) + __shfl_xor_sync(0xffffffffu, u16 ? v0 : v1, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    return c;
+}
+
+// Sums four per-lane values over the warp; afterwards lane l holds the total of value (l >> 3) & 3.
+__device__ __forceinline__ float reduce4(float v0, float v1, float v2, float v3, int lane) {
+    const bool up16 = lane & 16, up8 = lane & 8;
+    float a = up16 ? v2 : v0, b = up16 ? v3 : v1;
+    const float sa = up16 ? v0 : v2, sb = up16 ? v1 : v3;
+    a += __shfl_xor_sync(0xffffffffu, sa, 16);
+    b += __shfl_xor_sync(0xffffffffu, sb, 16);
+    float c = up8 ? b : a;
+    const float sc = up8 ? a : b;
+    c += __shfl_xor_sync(0xffffffffu, sc, 8);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    return c;
+}
+
+// Issues the bulk copies of one gate/up unit into a stage (one thread).
+__device__ void issue1(const StepParams &p, const int *idx, bool shared, int unit, uint32_t dst, uint32_t bar) {
     const DeviceWeights &w = p.w;
-    if (phase == 1) {
-        if (unit < U.n1r) {
-            const int e = idx[unit / U.per1];
-            const int row0 = (unit % U.per1) * p.r1;
-            const size_t rb = (static_cast<size_t>(e) * w.F + row0) * w.nbD;  // first block
-            const uint32_t qs = static_cast<uint32_t>(p.r1 * w.nbD * 64), ds = static_cast<uint32_t>(p.r1 * w.nbD * 2);
-            mbar_expect_tx(bar, 2 * qs + 2 * ds);
-            bulk_load(dst, w.gate_qs + rb * 64, qs, bar);
-            bulk_load(dst + qs, w.up_qs + rb * 64, qs, bar);
-            bulk_load(dst + 2 * qs, w.gate_d + rb, ds, bar);
-            bulk_load(dst + 2 * qs + ds, w.up_d + rb, ds, bar);
-        } else {
-            const int row0 = (unit - U.n1r) * p.rs;
-            const uint32_t b = static_cast<uint32_t>(p.rs * w.D * 2);
-            mbar_expect_tx(bar, 2 * b);
-            bulk_load(dst, w.sh_gate + static_cast<size_t>(row0) * w.D, b, bar);
-            bulk_load(dst + b, w.sh_up + static_cast<size_t>(row0) * w.D, b, bar);
-        }
+    if (!shared) {
+        const int per = w.F / kRows1;
+        const int e = idx[unit / per];
+        const int row0 = (unit % per) * kRows1;
+        const uint32_t bytes = static_cast<uint32_t>(iq2_tile_bytes(w.nbD));  // gate and up rows, one tile
+        mbar_expect_tx(bar, bytes);
+        bulk_load(dst, w.iq2 + iq2_tile_offset(w, e, row0), bytes, bar);
     } else {
-        const int d0 = unit * kRows2;
-        const uint32_t sqb = static_cast<uint32_t>(kRows2 * w.nbF * 80), ddb = static_cast<uint32_t>(kRows2 * w.nbF * 4);
-        const uint32_t shb = w.has_shared ? static_cast<uint32_t>(kRows2 * w.F * 2) : 0u;
-        mbar_expect_tx(bar, p.k * (sqb + ddb) + shb);
-        for (int s = 0; s < p.k; s++) {
-            const size_t rb = (static_cast<size_t>(idx[s]) * w.D + d0) * w.nbF;
-            bulk_load(dst + s * sqb, w.down_sq + rb * 80, sqb, bar);
-            bulk_load(dst + p.k * sqb + s * ddb, w.down_dd + rb, ddb, bar);
-        }
-        if (w.has_shared) bulk_load(dst + p.k * (sqb + ddb), w.sh_down + static_cast<size_t>(d0) * w.F, shb, bar);
+        const int row0 = unit * kRowsSh;
+        const uint32_t b = static_cast<uint32_t>(kRowsSh * w.D * 2);
+        mbar_expect_tx(bar, 2 * b);
+        bulk_load(dst, w.sh_gate + static_cast<size_t>(row0) * w.D, b, bar);
+        bulk_load(dst + b, w.sh_up + static_cast<size_t>(row0) * w.D, b, bar);
     }
 }
 
-// One group of 8 IQ2-style weights dotted with 8 int16 x (4 registers of pairs), exactly:
-// grid magnitudes (int8 x 8) with the group's signs applied through the sign masks.
-__device__ __forceinline__ int iq2_group_idot(uint2 mag, uint4 sm, const uint32_t *xv, int acc) {
-    const int lo = static_cast<int>((mag.x ^ sm.x) + sm.z);
-    const int hi = static_cast<int>((mag.y ^ sm.y) + sm.w);
-    acc = __dp2a_lo(static_cast<int>(xv[0]), lo, acc);
-    acc = __dp2a_hi(static_cast<int>(xv[1]), lo, acc);
-    acc = __dp2a_lo(static_cast<int>(xv[2]), hi, acc);
-    acc = __dp2a_hi(static_cast<int>(xv[3]), hi, acc);
+// Issues the bulk copies of one down unit: kRows2 output rows of every routed expert and of
+// the shared one.
+__device__ void issue2(const StepParams &p, const int *idx, int unit, uint32_t dst, uint32_t bar) {
+    const DeviceWeights &w = p.w;
+    const int d0 = unit * kRows2;
+    const uint32_t tb = static_cast<uint32_t>(q2k_tile_bytes(w.nbF));  // kRows2 rows of one expert
+    const uint32_t shb = w.has_shared ? static_cast<uint32_t>(kRows2 * w.F * 2) : 0u;
+    mbar_expect_tx(bar, p.k * tb + shb);
+    for (int s = 0; s < p.k; s++) bulk_load(dst + s * tb, w.q2k + q2k_tile_offset(w, idx[s], d0), tb, bar);
+    if (w.has_shared) bulk_load(dst + p.k * tb, w.sh_down + static_cast<size_t>(d0) * w.F, shb, bar);
+}
+
+// Top-k of the logits by one warp (ties to the lower index, NaN orders as -inf) and the gate
+// weights of the selected experts (softmax over them, or normalised sigmoids).
+template <int NJ>
+__device__ void route_warp(const StepParams &p, int lane, int *sidx, float *sgw) {
+    const int E = p.w.E;
+    float key[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; j++) {
+        const int e = lane + 32 * j;
+        const float v = (e < E) ? __ldg(p.logits + e) : -INFINITY;
+        key[j] = (v != v) ? -INFINITY : v;
+    }
+    uint32_t taken = 0;
+    float my_v = -INFINITY;
+    int my_i = 0;
+    for (int r = 0; r < p.k; r++) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < NJ; j++) {
+            const int e = lane + 32 * j;
+            if (e < E && !((taken >> j) & 1u) && (key[j] > bv || (key[j] == bv && e < bi))) {
+                bv = key[j];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == r) {
+            my_v = bv;
+            my_i = bi;
+        }
+    }
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    float num = 0.0f;
+    if (lane < p.k) num = (p.mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+    const float den = warp_sum(num);
+    if (lane < p.k) {
+        sidx[lane] = my_i;
+        sgw[lane] = num / den;
+        if (blockIdx.x == 0) {
+            p.topk_idx[lane] = my_i;
+            p.topk_w[lane] = num / den;
+        }
+    }
+}
+
+// Order-preserving key of a logit: a larger float gives a larger unsigned key. NaN orders as
+// -inf and -0 as +0 (they compare equal as floats, so the lower expert index wins the tie).
+__device__ __forceinline__ uint32_t order_key(float v) {
+    if (v != v) v = -INFINITY;
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of at most 256 logits by one warp, the same selection as route_warp: each lane sorts its
+// eight (key, index) pairs once with a 19-comparator network (descending key, ascending index),
+// then every round takes the largest head key over the warp with one reduction and, among the
+// heads that hold it, the smallest expert index with a second; that lane drops its head.
+__device__ void route_sorted8(const StepParams &p, int lane, int *sidx, float *sgw) {
+    const int E = p.w.E;
+    uint32_t key[8];
+    int id[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const int e = lane + 32 * j;
+        key[j] = e < E ? order_key(__ldg(p.logits + e)) : 0u;  // 0: no expert (below every logit)
+        id[j] = e < E ? e : INT_MAX;
+    }
+    auto ce = [&](int a, int b) {  // position a takes the larger of (a, b)
+        const bool sw = key[b] > key[a] || (key[b] == key[a] && id[b] < id[a]);
+        const uint32_t ka = sw ? key[b] : key[a], kb = sw ? key[a] : key[b];
+        const int ia = sw ? id[b] : id[a], ib = sw ? id[a] : id[b];
+        key[a] = ka;
+        key[b] = kb;
+        id[a] = ia;
+        id[b] = ib;
+    };
+    ce(0, 2); ce(1, 3); ce(4, 6); ce(5, 7);
+    ce(0, 4); ce(1, 5); ce(2, 6); ce(3, 7);
+    ce(0, 1); ce(2, 3); ce(4, 5); ce(6, 7);
+    ce(2, 4); ce(3, 5);
+    ce(1, 4); ce(3, 6);
+    ce(1, 2); ce(3, 4); ce(5, 6);
+    float my_v = -INFINITY;
+    int my_i = 0;
+    for (int r = 0; r < p.k; r++) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == m ? static_cast<uint32_t>(id[0]) : 0xffffffffu);
+        if (lane == r) {
+            my_v = key_value(m);
+            my_i = static_cast<int>(win);
+        }
+        if (key[0] == m && static_cast<uint32_t>(id[0]) == win) {
+#pragma unroll
+            for (int i = 0; i < 7; i++) {
+                key[i] = key[i + 1];
+                id[i] = id[i + 1];
+            }
+            key[7] = 0u;
+            id[7] = INT_MAX;
+        }
+    }
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    float num = 0.0f;
+    if (lane < p.k) num = (p.mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+    const float den = warp_sum(num);
+    if (lane < p.k) {
+        sidx[lane] = my_i;
+        sgw[lane] = num / den;
+        if (blockIdx.x == 0) {
+            p.topk_idx[lane] = my_i;
+            p.topk_w[lane] = num / den;
+        }
+    }
+}
+
+// d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) or with bytes 2, 3 (hi): signed 16-bit a,
+// unsigned bytes b.
+__device__ __forceinline__ int dp2a_lo_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// One IQ2-style 32-weight sub-block of a row dotted with the lane's 32 x values: xr holds per
+// group g the int16 pairs (x0,x2), (x4,x6), (x1,x3), (x5,x7) of its 8 columns, x8 = 8 * the sum
+// of the 32 values; q = the sub-block's 4 codebook indices and its sign/scale word, ds = the
+// block's d times the x factor / 16; tab = the table, lane4 = 4 * lane.
+__device__ __forceinline__ float iq2_sub(uint2 q, float ds, const uint32_t *xr, int x8, const uint8_t *tab,
+                                         uint32_t lane4) {
+    int ce = -x8, co = 0;  // even and odd elements; the offset of 8 per weight removed up front
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+        // codebook entry q.x byte g: offset lane4 | index << 8; sign entry (7 bits at 7g of q.y):
+        // offset lane4 | 128 | signs << 8
+        const uint32_t og = __byte_perm(lane4, q.x, 0x1140u + 0x10u * g);
+        const uint32_t f = g == 0 ? (q.y << 8) : g == 1 ? (q.y << 1) : (q.y >> (7 * g - 8));
+        const uint32_t os = (f & 0x7F00u) | lane4 | 128u;
+        const uint32_t gv = *reinterpret_cast<const uint32_t *>(tab + og);
+        const uint32_t sv = *reinterpret_cast<const uint32_t *>(tab + os);
+        const uint32_t ev = (gv ^ sv) & 0x0F0F0F0Fu;  // weights 0, 2, 4, 6 plus 8, as bytes
+        const uint32_t od = (gv ^ sv) & 0xF0F0F0F0u;  // 16 x (weights 1, 3, 5, 7 plus 8)
+        const uint32_t *xv = xr + 4 * g;
+        ce = dp2a_hi_su(xv[1], ev, dp2a_lo_su(xv[0], ev, ce));
+        co = dp2a_hi_su(xv[3], od, dp2a_lo_su(xv[2], od, co));
+    }
+    // the odd sum is a multiple of 16: the shift is exact
+    const int tot = ce + (co >> 4);
+    const float s1 = small_int_to_float(static_cast<int>((q.y >> 28) + 1u));  // sub-block scale s + 1
+    return ds * s1 * small_int_to_float(tot);
+}
+
+// Sixteen Q2_K-style 2-bit codes (one u32: byte b holds weights 4b..4b+3) dotted with 16 int16 h
+// stored as hp[2j] = (h_j, h_4+j), hp[2j+1] = (h_8+j, h_12+j).
+__device__ __forceinline__ int q2k_idot(uint32_t qw, const uint32_t *hp) {
+    int a[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int c = static_cast<int>((qw >> (2 * j)) & 0x03030303u);  // weights j, 4+j, 8+j, 12+j
+        a[j] = __dp2a_hi(static_cast<int>(hp[2 * j + 1]), c, __dp2a_lo(static_cast<int>(hp[2 * j]), c, 0));
+    }
+    return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
+__device__ __forceinline__ float dot8_bf16(uint4 w, float4 xa, float4 xb, float acc) {
+    acc = fmaf(bf16_lo(w.x), xa.x, acc);
+    acc = fmaf(bf16_hi(w.x), xa.y, acc);
+    acc = fmaf(bf16_lo(w.y), xa.z, acc);
+    acc = fmaf(bf16_hi(w.y), xa.w, acc);
+    acc = fmaf(bf16_lo(w.z), xb.x, acc);
+    acc = fmaf(bf16_hi(w.z), xb.y, acc);
+    acc = fmaf(bf16_lo(w.w), xb.z, acc);
+    acc = fmaf(bf16_hi(w.w), xb.w, acc);
     return acc;
 }
 
-// Bounded grid barrier, one thread per CTA. Generation counting: the barrier words never need
-// resetting between calls.
-__device__ bool grid_barrier(unsigned *bar, int *status) {
-    volatile unsigned *gen = bar + 1;
-    const unsigned g = *gen;
-    __threadfence();
-    const unsigned ticket = atomicAdd(bar, 1u);
-    if (ticket == gridDim.x - 1) {
-        atomicExch(bar, 0u);
-        __threadfence();
-        atomicAdd(bar + 1, 1u);
-        return true;
-    }
+// Bounded grid barrier, one thread per CTA, on a 64-bit arrival counter that only grows: the
+// CTAs of one call take tickets n*G .. n*G+G-1 and wait until the counter reaches (n+1)*G, so
+// the counter never needs resetting. The add releases this CTA's writes (observed by this
+// thread through the CTA barrier before it) at GPU scope; the polling load acquires the others'.
+__device__ bool grid_barrier(unsigned long long *count, int *status) {
+    const unsigned long long G = gridDim.x;
+    unsigned long long ticket;
+    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(ticket) : "l"(count) : "memory");
+    const unsigned long long target = (ticket / G + 1ull) * G;
     const long long t0 = clock64();
-    while (*gen == g) {
+    while (true) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(count) : "memory");
+        if (v >= target) return true;
         if (clock64() - t0 > kWaitCycles) {
             report(status, ST_TIMEOUT);
             return false;
         }
-        __nanosleep(64);
+        __nanosleep(20);
     }
-    __threadfence();
-    return true;
 }
 
+// NQ: 1024-column quarters of x (1, 2 or 4); each compute warp holds one of them in registers.
+template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    // align by an integer offset so that every pointer below stays a shared-memory pointer
-    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    uint8_t *ring = smem;                                                     // kStages x kStageBytes
-    uint2 *tab = reinterpret_cast<uint2 *>(smem + kStages * kStageBytes);    // [256][16]
-    uint4 *stab = reinterpret_cast<uint4 *>(smem + kStages * kStageBytes + kTabEntries * 8);  // [128][8]
-    uint8_t *act = smem + kStages * kStageBytes + kTabEntries * 8 + kSignEntries * 16;        // kActBytes
-    uint64_t *bars = reinterpret_cast<uint64_t *>(act + kActBytes);          // full[S], empty[S]
-    int *sidx = reinterpret_cast<int *>(bars + 2 * kStages);                 // [8]
+    constexpr int RG = kCompute / NQ;  // row groups
+    constexpr int RPW = kRows1 / RG;   // rows of a unit per warp (NQ)
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // fixed offsets from the symbol, so that the table's base folds into its loads
+    uint8_t *smem = smem_raw;
+    uint8_t *ring = smem;                                                    // kStages x kStageBytes
+    uint8_t *tab = smem + kTabOff;
+    // mbarriers: full[S], empty[S], route, rfull[2], rempty[2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kMiscOff);
+    int *sidx = reinterpret_cast<int *>(bars + 2 * kStages + 6);             // [8]
     float *sgw = reinterpret_cast<float *>(sidx + 8);                         // [8]
-    float *scal = sgw + 8;                                                    // [8] x scales / [9] h scales
-    float *red = scal + 16;                                                   // [8 warps][16]
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + kCompute * 16);
-    unsigned *hmax_cta = reinterpret_cast<unsigned *>(red + kCompute * 16 + 4);  // [8] max |h| per pair, this CTA
+    float *red = sgw + 8;                                                     // [2][128]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 256);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+    const uint32_t route_bar = smem_u32(bars + 2 * kStages);
+    // rfull[b]: the 16 compute warps have written a unit's partial sums into red[b];
+    // rempty[b]: the finisher has read them
+    const uint32_t rfull = smem_u32(bars + 2 * kStages + 1), rempty = smem_u32(bars + 2 * kStages + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DeviceWeights &w = p.w;
     const int D = w.D, F = w.F, nbD = w.nbD, nbF = w.nbF;
-    const Units U = units_of(p);
-    const int nph = (D + 2047) / 2048;  // x phases of 2048 columns
+    const int n2 = D / kRows2;
     uint64_t *tr = (p.trace && threadIdx.x == 0) ? p.trace + 6 * static_cast<size_t>(blockIdx.x) : nullptr;
     if (tr) tr[0] = now_ns();
 
-    // ---------------------------------------------------------------- prologue
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == kProducer * 32) {
         for (int s = 0; s < kStages; s++) {
-            mbar_init(smem_u32(bars + s), 1);
-            mbar_init(smem_u32(bars + kStages + s), kCompute);
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kCompute);
+        }
+        mbar_init(route_bar, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(rfull + 8 * b, kCompute);
+            mbar_init(rempty + 8 * b, 1);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {  // route: top-k of the logits, ties to the lower expert index
-        const int E = w.E;
-        float key[32];  // lane holds experts lane, lane+32, ... (E <= 1024)
-#pragma unroll
-        for (int j = 0; j < 32; j++) {
-            const int e = lane + 32 * j;
-            float v = (e < E) ? __ldg(p.logits + e) : -INFINITY;
-            key[j] = (v != v) ? -INFINITY : v;
-        }
-        uint32_t taken = 0;
-        float my_v = -INFINITY;
-        int my_i = 0;
-        for (int r = 0; r < p.k; r++) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
-#pragma unroll
-            for (int j = 0; j < 32; j++) {
-                const int e = lane + 32 * j;
-                if (e < E && !((taken >> j) & 1u) && (key[j] > bv || (key[j] == bv && e < bi))) {
-                    bv = key[j];
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == r) {
-                my_v = bv;
-                my_i = bi;
-            }
-        }
-        const float top = __shfl_sync(0xffffffffu, my_v, 0);
-        float num = 0.0f;
-        if (lane < p.k) num = (p.mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
-        const float den = warp_sum(num);
-        if (lane < p.k) {
-            sidx[lane] = my_i;
-            sgw[lane] = num / den;
-            if (blockIdx.x == 0) {
-                p.topk_idx[lane] = my_i;
-                p.topk_w[lane] = num / den;
-            }
-        }
-    }
-    // x: per 2048-column phase, a power-of-two scale and the fp16 values (swizzled chunks)
-    if (warp < kCompute) {
-        uint16_t *x16 = reinterpret_cast<uint16_t *>(act);
-        unsigned *xmax = reinterpret_cast<unsigned *>(scal);
-        if (threadIdx.x < 16) xmax[threadIdx.x] = 0u;
-        if (threadIdx.x < 8) hmax_cta[threadIdx.x] = 0u;
-        named_sync();
-        constexpr int kXq = 2;  // 16-byte chunks of x per thread (D <= 8192)
-        uint4 xr[kXq];
-#pragma unroll
-        for (int j = 0; j < kXq; j++) {
-            const int q = threadIdx.x + j * kCompute * 32;
-            xr[j] = q < D / 8 ? __ldg(reinterpret_cast<const uint4 *>(p.x) + q) : make_uint4(0, 0, 0, 0);
-            const uint32_t u4[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
-            float m = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 4; i++) m = fmaxf(m, fmaxf(fabsf(bf16_lo(u4[i])), fabsf(bf16_hi(u4[i]))));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));  // a warp's 32 chunks share one phase
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            if (lane == 0 && q < D / 8) atomicMax(xmax + q / 256, __float_as_uint(m));
-        }
-        named_sync();
-        if (threadIdx.x < nph) {
-            const float m = __uint_as_float(xmax[threadIdx.x]);
-            int e = 0;
-            frexpf(m, &e);
-            e = m > 0.0f ? e : 0;
-            scal[threadIdx.x] = ldexpf(1.0f, e);  // 1/scale, multiplies results back
-        }
-        named_sync();
-#pragma unroll
-        for (int j = 0; j < kXq; j++) {  // 16-byte chunks -> int16 with the phase's scale 2^(14-e)
-            const int q = threadIdx.x + j * kCompute * 32;
-            if (q >= D / 8) continue;
-            const float sc = 16384.0f / scal[q / 256];
-            const uint32_t u4[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-                o[i] = (static_cast<uint32_t>(__float2int_rn(bf16_lo(u4[i]) * sc)) & 0xffffu) |
-                       (static_cast<uint32_t>(__float2int_rn(bf16_hi(u4[i]) * sc)) << 16);
-            reinterpret_cast<uint4 *>(x16)[swz(q)] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        for (int i = threadIdx.x; i < kTabEntries; i += kCompute * 32)  // grid magnitudes (int8)
-            tab[i] = __ldg(reinterpret_cast<const uint2 *>(p.grid) + (i >> 4));
-        for (int i = threadIdx.x; i < kSignEntries; i += kCompute * 32) {
-            // 7 stored signs + parity -> byte masks M (0xFF where negative) and B = M & 0x01:
-            // (magnitudes ^ M) + B negates the marked bytes (no carry: magnitudes are <= 7)
-            const uint32_t s7 = static_cast<uint32_t>(i >> 3);
-            const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
-            uint32_t m[2];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; h2++) {
-                uint32_t v = 0;
-#pragma unroll
-                for (int b = 0; b < 4; b++) v |= ((s8 >> (4 * h2 + b)) & 1u) ? (0xFFu << (8 * b)) : 0u;
-                m[h2] = v;
-            }
-            stab[i] = make_uint4(m[0], m[1], m[0] & 0x01010101u, m[1] & 0x01010101u);
-        }
-    }
     __syncthreads();
-    if (tr) tr[1] = now_ns();
 
-    if (warp == kCompute) {
-        // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------------- producer
+    if (warp == kProducer) {
         if (lane == 0) {
             int stage = 0, issued_parity[kStages];
             uint32_t phase = 0;
             for (int s = 0; s < kStages; s++) issued_parity[s] = -1;
-            bool ok = true;
-            for (int ph = 1; ph <= 2 && ok; ph++) {
-                const int n = ph == 1 ? U.n1 : U.n2;
-                for (int u = blockIdx.x; u < n; u += gridDim.x) {
-                    if (!mbar_wait(smem_u32(bars + kStages + stage), phase ^ 1u, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    issue_unit(p, U, sidx, ph, u, smem_u32(ring + stage * kStageBytes), smem_u32(bars + stage));
-                    issued_parity[stage] = static_cast<int>(phase);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            bool ok = true, routed = false;
+            auto acquire = [&](bool needs_route) -> bool {
+                if (needs_route && !routed) {
+                    if (!mbar_wait(route_bar, 0u, abort_flag, p.status)) return false;
+                    routed = true;
                 }
+                return mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status);
+            };
+            auto advance = [&]() {
+                issued_parity[stage] = static_cast<int>(phase);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
+            Seq1 q = seq1_of(p);
+            bool shared;
+            int unit;
+            while (ok && q.next(shared, unit)) {
+                if (!acquire(!shared)) {
+                    ok = false;
+                    break;
+                }
+                issue1(p, sidx, shared, unit, smem_u32(ring + stage * kStageBytes), full0 + 8 * stage);
+                advance();
+            }
+            for (int u = blockIdx.x; ok && u < n2; u += gridDim.x) {
+                if (!acquire(true)) {
+                    ok = false;
+                    break;
+                }
+                issue2(p, sidx, u, smem_u32(ring + stage * kStageBytes), full0 + 8 * stage);
+                advance();
             }
             if (!ok)
                 for (int s = 0; s < kStages; s++)
-                    if (issued_parity[s] >= 0) mbar_drain(smem_u32(bars + s), static_cast<uint32_t>(issued_parity[s]));
+                    if (issued_parity[s] >= 0) mbar_drain(full0 + 8 * s, static_cast<uint32_t>(issued_parity[s]));
         }
-        return;  // the producer takes no part in the compute warps' barriers
+        return;  // the producer takes no part in the named barriers
     }
 
-    // -------------------------------------------------------------------- compute warps
-    const uint2 *gt = tab + (lane & 15);
-    const uint4 *st8 = stab + (lane & 7);
-    const uint4 *x16v = reinterpret_cast<const uint4 *>(act);
-    int stage = 0;
-    uint32_t sphase = 0;
+    const Seq1 seq0 = seq1_of(p);
+
+    // ---------------------------------------------------------------- finisher
+    if (warp == kFinisher) {
+        // route first: the producer's routed units and the down phase wait for it
+        if (w.E <= 256)
+            route_sorted8(p, lane, sidx, sgw);
+        else
+            route_warp<32>(p, lane, sidx, sgw);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(route_bar);
+        int it = 0;
+        Seq1 q = seq0;
+        bool shared;
+        int unit;
+        while (q.next(shared, unit)) {
+            const int buf = it & 1;
+            const float *rb = red + buf * 128;
+            wait_phase(rfull + 8 * buf, static_cast<uint32_t>(it >> 1) & 1u, abort_flag, p.status);
+            if (shared) {
+                if (lane < kRowsSh) {
+                    float g = 0.0f, u = 0.0f;
+#pragma unroll
+                    for (int ww = 0; ww < kCompute; ww++) {
+                        g += rb[ww * 4 + 2 * lane];
+                        u += rb[ww * 4 + 2 * lane + 1];
+                    }
+                    p.hsh[unit * kRowsSh + lane] = swiglu(g, u);
+                }
+            } else {
+                // lane r < 16: row r of the unit = column r of one down sub-block
+                const int per = F / kRows1, slot = unit / per, row0 = (unit % per) * kRows1;
+                float hv = 0.0f;
+                if (lane < kRows1) {
+                    float g = 0.0f, u = 0.0f;
+#pragma unroll
+                    for (int qx = 0; qx < NQ; qx++) {
+                        g += rb[(lane * NQ + qx) * 2];
+                        u += rb[(lane * NQ + qx) * 2 + 1];
+                    }
+                    hv = swiglu(g, u);
+                }
+                float m = fabsf(hv), sum = hv;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) {
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                }
+                int e = 0;
+                frexpf(m, &e);
+                e = m > 0.0f ? e : 0;
+                if (lane < kRows1) {
+                    const int pos = 4 * (lane & 3) + (lane >> 2);
+                    p.hq[static_cast<size_t>(slot) * F + row0 + pos] =
+                        static_cast<int16_t>(__float2int_rn(hv * ldexpf(1.0f, 14 - e)));
+                }
+                if (lane == 0) {
+                    p.hsc[static_cast<size_t>(slot) * (F / 16) + row0 / 16] = ldexpf(1.0f, e - 14);
+                    p.hsum[static_cast<size_t>(slot) * (F / 16) + row0 / 16] = sum;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rempty + 8 * buf);
+            it++;
+        }
+        bar_sync(kBarAll, kNAll);  // this CTA's h is written
+        for (int u = blockIdx.x; u < n2; u += gridDim.x, it++) {
+            const int buf = it & 1;
+            const float *rb = red + buf * 128;
+            wait_phase(rfull + 8 * buf, static_cast<uint32_t>(it >> 1) & 1u, abort_flag, p.status);
+            if (lane < kRows2) {
+                float s = 0.0f;
+#pragma unroll
+                for (int ww = 0; ww < kCompute; ww++) s += rb[ww * 4 + lane];
+                p.out[u * kRows2 + lane] += s;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rempty + 8 * buf);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- compute warps: prologue
+    const int tid = threadIdx.x;  // 0 .. kNCompute-1
+    // all global loads of the prologue first, so that their latencies overlap
+    const int qx = warp % NQ, rg = warp / NQ;
+    const int c = qx * 32 + lane;  // this lane's 32-column sub-block of x
+    const bool cval = c < D / 32;
+    uint4 raw[4];  // this lane's 32 columns of x
+#pragma unroll
+    for (int j = 0; j < 4; j++)
+        raw[j] = cval ? __ldg(reinterpret_cast<const uint4 *>(p.x) + 4 * c + j) : make_uint4(0, 0, 0, 0);
+    uint2 graw[16];  // codebook entry warp + 16 * j, replica lane: one broadcast load per warp
+#pragma unroll
+    for (int j = 0; j < 16; j++) graw[j] = __ldg(reinterpret_cast<const uint2 *>(p.grid) + warp + 16 * j);
+    const bool xfq = tid < D / 8;
+    const uint4 xv = xfq ? __ldg(reinterpret_cast<const uint4 *>(p.x) + tid) : make_uint4(0, 0, 0, 0);
+    // fp32 x for the bf16 shared expert (D <= 8 * kNCompute)
+    if (xfq) {
+        float4 *xp = reinterpret_cast<float4 *>(tab + xpair_offset(tid));
+        xp[0] = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
+        xp[1] = make_float4(bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w));
+    }
+#pragma unroll
+    for (int j = 0; j < 16; j++) {  // codebook: nibbles m - 1, elements 2b in byte b's low nibble, 2b+1 in its high
+        const uint32_t lo = graw[j].x - 0x01010101u, hi = graw[j].y - 0x01010101u;  // bytes m - 1
+        // bytes (e0, e1, e2, e3), (e4, e5, e6, e7) -> bytes (e0 | e1 << 4, e2 | e3 << 4, ...)
+        const uint32_t ev = __byte_perm(lo, hi, 0x6420), od = __byte_perm(lo, hi, 0x7531);
+        *reinterpret_cast<uint32_t *>(tab + (warp + 16 * j) * 256 + lane * 4) = ev | (od << 4);
+    }
+    // int16 x in registers with the quarter's power-of-two scale, per group the pairs
+    // (x0,x2), (x4,x6), (x1,x3), (x5,x7); x8 = 8 * their sum
+    uint32_t xr[16];
+    float xinv;
+    int x8 = 0;
+    {
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const uint32_t u4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) m = fmaxf(m, fmaxf(fabsf(bf16_lo(u4[i])), fabsf(bf16_hi(u4[i]))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        int e = 0;
+        frexpf(m, &e);
+        e = m > 0.0f ? e : 0;
+        const float sc = ldexpf(1.0f, 14 - e);
+        xinv = ldexpf(1.0f, e - 14) * 0.0625f;  // also carries the sub-block scale's 1/16
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const uint32_t u4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+            uint32_t q[8];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                q[2 * i] = round_to_int_bits(bf16_lo(u4[i]) * sc);
+                q[2 * i + 1] = round_to_int_bits(bf16_hi(u4[i]) * sc);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i++) x8 += static_cast<int>(static_cast<int16_t>(q[i] & 0xffffu));
+            xr[4 * j] = __byte_perm(q[0], q[2], 0x5410);
+            xr[4 * j + 1] = __byte_perm(q[4], q[6], 0x5410);
+            xr[4 * j + 2] = __byte_perm(q[1], q[3], 0x5410);
+            xr[4 * j + 3] = __byte_perm(q[5], q[7], 0x5410);
+        }
+        x8 *= 8;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        // 7 stored signs + their parity -> per element a nibble, 0x7 (negate) or 0x9 (keep), in
+        // the codebook word's order (element 2b in byte b's low nibble, 2b+1 in its high nibble)
+        const uint32_t s7 = static_cast<uint32_t>(warp + 16 * j);
+        const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
+        uint32_t v = 0;
+#pragma unroll
+        for (int el = 0; el < 8; el++) v |= (((s8 >> el) & 1u) ? 0x7u : 0x9u) << (8 * (el >> 1) + 4 * (el & 1));
+        *reinterpret_cast<uint32_t *>(tab + s7 * 256 + 128 + lane * 4) = v;
+    }
+    bar_sync(kBarCompute, kNCompute);
+    if (tr) tr[1] = now_ns();
+
+    // ring position rc: stage rc % kStages, parity (rc / kStages) & 1
     bool ok = true;
-    auto next_stage = [&]() -> const uint8_t * {
-        if (!ok || !mbar_wait(smem_u32(bars + stage), sphase, abort_flag, p.status)) {
+    auto wait_stage = [&](int rc) -> const uint8_t * {
+        if (!ok || !wait_phase(full0 + 8 * (rc % kStages), static_cast<uint32_t>(rc / kStages) & 1u, abort_flag, p.status)) {
             ok = false;
             return nullptr;
         }
-        return ring + stage * kStageBytes;
+        return ring + (rc % kStages) * kStageBytes;
     };
-    auto release_stage = [&]() {
+    auto release_stage = [&](int rc) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(bars + kStages + stage));
-        if (++stage == kStages) {
-            stage = 0;
-            sphase ^= 1u;
-        }
+        if (lane == 0) mbar_arrive(empty0 + 8 * (rc % kStages));
     };
 
-    // ---------------------------------------------------------------- phase 1: gate/up, SwiGLU
-    const int nchunk = nbD * 4;  // 64-column chunks per row
-    for (int u = blockIdx.x; u < U.n1 && ok; u += gridDim.x) {
-        const uint8_t *st = next_stage();
-        if (!st) break;
-        if (u < U.n1r) {
-            const int slot = u / U.per1, row0 = (u % U.per1) * p.r1;
-            const int wpr = kCompute / p.r1;                      // warps per row (1 or 2)
-            const int rl = warp % p.r1, psub = warp / p.r1;       // local row, phase subset
-            const uint8_t *gq = st, *uq = st + p.r1 * nbD * 64;
-            const uint16_t *gd = reinterpret_cast<const uint16_t *>(st + 2 * p.r1 * nbD * 64);
-            const uint16_t *ud = gd + p.r1 * nbD;
-            float ag = 0.0f, au = 0.0f;
-            for (int ph = psub; ph < nph; ph += wpr) {
-                const int c = ph * 32 + lane;
-                if (c >= nchunk) continue;
-                uint32_t xh[32];
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const uint4 v = x16v[swz(8 * c + j)];
-                    xh[4 * j] = v.x;
-                    xh[4 * j + 1] = v.y;
-                    xh[4 * j + 2] = v.z;
-                    xh[4 * j + 3] = v.w;
-                }
-                const float xinv = scal[ph] * (1.0f / 16384.0f);
-                const uint4 qg = *reinterpret_cast<const uint4 *>(gq + (rl * nbD * 4 + c) * 16);
-                const uint4 qu = *reinterpret_cast<const uint4 *>(uq + (rl * nbD * 4 + c) * 16);
-                const float dg = f16_to_f32(gd[rl * nbD + (c >> 2)]) * xinv;
-                const float du = f16_to_f32(ud[rl * nbD + (c >> 2)]) * xinv;
-#pragma unroll
-                for (int sb = 0; sb < 2; sb++) {
-                    const uint32_t igw = sb ? qg.z : qg.x, sgw2 = sb ? qg.w : qg.y;
-                    const uint32_t iuw = sb ? qu.z : qu.x, suw = sb ? qu.w : qu.y;
-                    int g0 = 0, g1 = 0, u0 = 0, u1 = 0;  // two accumulators per matrix: shorter chains
-#pragma unroll
-                    for (int g = 0; g < 4; g += 2) {
-                        const uint32_t *xv0 = xh + 16 * sb + 4 * g, *xv1 = xv0 + 4;
-                        g0 = iq2_group_idot(gt[((igw >> (8 * g)) & 255u) << 4], st8[((sgw2 >> (7 * g)) & 127u) << 3], xv0, g0);
-                        u0 = iq2_group_idot(gt[((iuw >> (8 * g)) & 255u) << 4], st8[((suw >> (7 * g)) & 127u) << 3], xv0, u0);
-                        g1 = iq2_group_idot(gt[((igw >> (8 * g + 8)) & 255u) << 4], st8[((sgw2 >> (7 * g + 7)) & 127u) << 3], xv1, g1);
-                        u1 = iq2_group_idot(gt[((iuw >> (8 * g + 8)) & 255u) << 4], st8[((suw >> (7 * g + 7)) & 127u) << 3], xv1, u1);
+    // ---------------------------------------------------------------- phase 1: gate/up
+    const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
+    int rc = 0;
+    {
+        Seq1 q = seq0;
+        bool shared;
+        int unit;
+        while (q.next(shared, unit)) {
+            const int it = rc++;
+            const int buf = it & 1;
+            float *rb = red + buf * 128;
+            const uint8_t *st = wait_stage(it);
+            if (shared) {
+                // two bf16 rows of gate and up; thread tid takes columns 8*tid .. +7 (D <= 8 * kNCompute).
+                // The stage is read into registers and released before the arithmetic.
+                float g0 = 0.0f, u0 = 0.0f, g1 = 0.0f, u1 = 0.0f;
+                if (st) {
+                    const int nq = D / 8;
+                    const bool qv = tid < nq;
+                    const uint4 *sgw8 = reinterpret_cast<const uint4 *>(st);
+                    const uint4 *suw8 = sgw8 + kRowsSh * nq;
+                    uint4 wv[4];
+                    if (qv) {
+                        wv[0] = sgw8[tid];
+                        wv[1] = sgw8[nq + tid];
+                        wv[2] = suw8[tid];
+                        wv[3] = suw8[nq + tid];
                     }
-                    ag = fmaf(iq2_scale(dg, sgw2), static_cast<float>(g0 + g1), ag);
-                    au = fmaf(iq2_scale(du, suw), static_cast<float>(u0 + u1), au);
-                }
-            }
-            float g = warp_sum(ag), uu = warp_sum(au);
-            release_stage();
-            if (wpr > 1) {  // the second warp of a row hands its partial sums over
-                if (lane == 0 && psub > 0) {
-                    red[warp * 16] = g;
-                    red[warp * 16 + 1] = uu;
-                }
-                named_sync();
-                if (psub == 0)
-                    for (int o = 1; o < wpr; o++) {
-                        g += red[(warp + o * p.r1) * 16];
-                        uu += red[(warp + o * p.r1) * 16 + 1];
+                    release_stage(it);
+                    if (qv) {
+                        const float4 *xp = reinterpret_cast<const float4 *>(tab + xpair_offset(tid));
+                        const float4 xa = xp[0], xb = xp[1];
+                        g0 = dot8_bf16(wv[0], xa, xb, g0);
+                        g1 = dot8_bf16(wv[1], xa, xb, g1);
+                        u0 = dot8_bf16(wv[2], xa, xb, u0);
+                        u1 = dot8_bf16(wv[3], xa, xb, u1);
                     }
-                named_sync();
-            }
-            if (lane == 0 && psub == 0) {
-                const float hv = swiglu(g, uu);
-                p.h[static_cast<size_t>(slot) * F + row0 + rl] = hv;
-                atomicMax(hmax_cta + slot, __float_as_uint(fabsf(hv)));
-            }
-        } else {
-            // shared expert: rs bf16 rows of gate and up; threads split the 16-byte chunks
-            const int row0 = (u - U.n1r) * p.rs;
-            const uint4 *sg = reinterpret_cast<const uint4 *>(st);
-            const uint4 *su = reinterpret_cast<const uint4 *>(st + p.rs * D * 2);
-            const int tid = warp * 32 + lane, nq = D / 8;
-            float pg[8], pu[8];
-#pragma unroll
-            for (int r = 0; r < 8; r++) pg[r] = pu[r] = 0.0f;
-            for (int q = tid; q < nq; q += kCompute * 32) {
-                const uint4 xv = x16v[swz(q)];
-                const float xi = scal[q / 256] * (1.0f / 16384.0f);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                float xf[8];
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    xf[2 * i] = static_cast<float>(static_cast<int16_t>(xw[i] & 0xffffu)) * xi;
-                    xf[2 * i + 1] = static_cast<float>(static_cast<int16_t>(xw[i] >> 16)) * xi;
                 }
-#pragma unroll
-                for (int r = 0; r < 8; r++) {
-                    if (r < p.rs) {
-                        const uint4 gv = sg[r * nq + q], uv = su[r * nq + q];
-                        const uint32_t g4[4] = {gv.x, gv.y, gv.z, gv.w}, u4[4] = {uv.x, uv.y, uv.z, uv.w};
-#pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            pg[r] = fmaf(bf16_lo(g4[i]), xf[2 * i], pg[r]);
-                            pg[r] = fmaf(bf16_hi(g4[i]), xf[2 * i + 1], pg[r]);
-                            pu[r] = fmaf(bf16_lo(u4[i]), xf[2 * i], pu[r]);
-                            pu[r] = fmaf(bf16_hi(u4[i]), xf[2 * i + 1], pu[r]);
+                const float v = reduce4(g0, u0, g1, u1, lane);
+                if (it >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((it >> 1) - 1) & 1u, abort_flag, p.status);
+                if ((lane & 7) == 0) rb[warp * 4 + (lane >> 3)] = v;
+            } else {
+                // rows rg + i * RG of the unit, i < RPW, one at a time (a short loop body keeps the
+                // hot code small): the row's gate and up sub-block c, summed over the warp into
+                // red; the stage is released after the last row
+                if (it >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((it >> 1) - 1) & 1u, abort_flag, p.status);
+                if (st) {
+                    const uint8_t *gq = st, *uq = st + kRows1 * nbD * 64;
+                    const uint16_t *gd = reinterpret_cast<const uint16_t *>(st + 2 * kRows1 * nbD * 64);
+                    const uint16_t *ud = gd + kRows1 * nbD;
+#pragma unroll 1
+                    for (int i = 0; i < RPW; i++) {
+                        const int rl = rg + i * RG;
+                        float pg = 0.0f, pu = 0.0f;
+                        if (cval) {
+                            const uint2 qg = *reinterpret_cast<const uint2 *>(gq + (rl * nbD * 8 + c) * 8);
+                            const uint2 qu = *reinterpret_cast<const uint2 *>(uq + (rl * nbD * 8 + c) * 8);
+                            const float dg = f16_to_f32(gd[rl * nbD + (c >> 3)]) * xinv;
+                            const float du = f16_to_f32(ud[rl * nbD + (c >> 3)]) * xinv;
+                            pg = iq2_sub(qg, dg, xr, x8, tab, lane4);
+                            pu = iq2_sub(qu, du, xr, x8, tab, lane4);
                         }
+                        const float v = reduce2(pg, pu, lane);  // lane 0: gate, lane 16: up
+                        if ((lane & 15) == 0) rb[(rl * NQ + qx) * 2 + (lane >> 4)] = v;
                     }
+                    release_stage(it);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < 8; r++) {
-                if (r < p.rs) {
-                    const float g = warp_sum(pg[r]), uu = warp_sum(pu[r]);
-                    if (lane == 0) {
-                        red[warp * 16 + 2 * r] = g;
-                        red[warp * 16 + 2 * r + 1] = uu;
-                    }
-                }
-            }
-            release_stage();
-            named_sync();
-            if (warp == 0 && lane < p.rs) {
-                float g = 0.0f, uu = 0.0f;
-                for (int ww = 0; ww < kCompute; ww++) {
-                    g += red[ww * 16 + 2 * lane];
-                    uu += red[ww * 16 + 2 * lane + 1];
-                }
-                p.h[static_cast<size_t>(p.k) * F + row0 + lane] = swiglu(g, uu);
-            }
-            named_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rfull + 8 * buf);
         }
     }
 
     // ---------------------------------------------------------------- grid barrier: all h written
-    named_sync();
+    bar_sync(kBarAll, kNAll);
     if (tr) tr[2] = now_ns();
-    uint32_t *ctab = reinterpret_cast<uint32_t *>(tab);  // code byte -> its four codes as int8 [256][16]
-    for (int i = threadIdx.x; i < kTabEntries; i += kCompute * 32) {
-        const uint32_t b = static_cast<uint32_t>(i >> 4);
-        ctab[i] = (b & 3u) | (((b >> 2) & 3u) << 8) | (((b >> 4) & 3u) << 16) | (((b >> 6) & 3u) << 24);
-    }
-    if (threadIdx.x < p.k) p.hmax[static_cast<size_t>(blockIdx.x) * 8 + threadIdx.x] = __uint_as_float(hmax_cta[threadIdx.x]);
-    named_sync();
     if (threadIdx.x == 0 && !grid_barrier(p.bar, p.status)) *abort_flag = 1;
-    named_sync();
+    bar_sync(kBarCompute, kNCompute);
     if (tr) tr[3] = now_ns();
 
-    // h for the down phase: per routed pair a power-of-two scale (from the CTAs' maxima), fp16
-    // values (swizzled chunks) and the fp32 sums of its 16-column sub-blocks; the shared
-    // expert's h stays fp32
-    uint16_t *h16 = reinterpret_cast<uint16_t *>(act);           // [k][F]
-    float *hsum = reinterpret_cast<float *>(act + p.k * F * 2);  // [k][F/16]
-    float *hsh = hsum + p.k * (F / 16);                          // [F]
-    {
-        const int tid = threadIdx.x;
-        if (warp < p.k) {  // warp s reduces pair s over the CTAs
-            float m = 0.0f;
-            for (int c = lane; c < static_cast<int>(gridDim.x); c += 32)
-                m = fmaxf(m, __ldcg(p.hmax + static_cast<size_t>(c) * 8 + warp));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            int e = 0;
-            frexpf(m, &e);
-            e = m > 0.0f ? e : 0;
-            if (lane == 0) scal[warp] = ldexpf(1.0f, e);
+    // this thread's down columns: expert slot s2, columns 32*j2 .. +31 (two sub-blocks)
+    const int s2 = tid >> 6, j2 = tid & 63;
+    const bool sval = s2 < p.k;
+    uint32_t hp[16];
+    float gh0 = 0.0f, gh1 = 0.0f, gs0 = 0.0f, gs1 = 0.0f;
+    float4 hs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < 16; i++) hp[i] = 0u;
+    if (sval) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.hq + static_cast<size_t>(s2) * F + 32 * j2);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint4 v = __ldcg(src + i);
+            hp[4 * i] = v.x;
+            hp[4 * i + 1] = v.y;
+            hp[4 * i + 2] = v.z;
+            hp[4 * i + 3] = v.w;
         }
-        named_sync();
-        for (int sb = tid; sb < p.k * F / 16; sb += kCompute * 32) {  // one 16-column sub-block
-            const float sc = 16384.0f / scal[sb / (F / 16)];
-            const float4 *src = reinterpret_cast<const float4 *>(p.h) + 4 * sb;
-            const float4 a = __ldcg(src), b = __ldcg(src + 1), c = __ldcg(src + 2), d = __ldcg(src + 3);
-            auto pk = [sc](float x0, float x1) {
-                return (static_cast<uint32_t>(__float2int_rn(x0 * sc)) & 0xffffu) |
-                       (static_cast<uint32_t>(__float2int_rn(x1 * sc)) << 16);
-            };
-            uint4 o0, o1;
-            o0.x = pk(a.x, a.y);
-            o0.y = pk(a.z, a.w);
-            o0.z = pk(b.x, b.y);
-            o0.w = pk(b.z, b.w);
-            o1.x = pk(c.x, c.y);
-            o1.y = pk(c.z, c.w);
-            o1.z = pk(d.x, d.y);
-            o1.w = pk(d.z, d.w);
-            reinterpret_cast<uint4 *>(h16)[swz(2 * sb)] = o0;
-            reinterpret_cast<uint4 *>(h16)[swz(2 * sb + 1)] = o1;
-            hsum[sb] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w)) + ((c.x + c.y) + (c.z + c.w)) +
-                       ((d.x + d.y) + (d.z + d.w));
-        }
-        if (w.has_shared)
-            for (int q = tid; q < F / 4; q += kCompute * 32)
-                reinterpret_cast<float4 *>(hsh)[q] = __ldcg(reinterpret_cast<const float4 *>(p.h + static_cast<size_t>(p.k) * F) + q);
-        named_sync();
+        const float2 sc2 = __ldcg(reinterpret_cast<const float2 *>(p.hsc + static_cast<size_t>(s2) * (F / 16)) + j2);
+        const float2 sm2 = __ldcg(reinterpret_cast<const float2 *>(p.hsum + static_cast<size_t>(s2) * (F / 16)) + j2);
+        const float gw = sgw[s2];
+        gh0 = gw * sc2.x;
+        gh1 = gw * sc2.y;
+        gs0 = gw * sm2.x;
+        gs1 = gw * sm2.y;
     }
+    if (w.has_shared) hs = __ldcg(reinterpret_cast<const float4 *>(p.hsh) + tid);
     if (tr) tr[4] = now_ns();
 
     // ---------------------------------------------------------------- phase 2: down + combine
-    const uint4 *h16v = reinterpret_cast<const uint4 *>(h16);
-    const int rl2 = warp >> 2;              // local output row of this warp
-    const int qt = warp & 3;                // which quarter of F
-    const int col = qt * (F / 4) + lane * 16;  // this lane's 16 columns: one sub-block
-    const int b2 = col >> 8, part64 = (col >> 6) & 3, sub = (col >> 4) & 3;
-    for (int u = blockIdx.x; u < U.n2 && ok; u += gridDim.x) {
-        const uint8_t *st = next_stage();
-        if (!st) break;
-        const int sqb = kRows2 * nbF * 80, ddb = kRows2 * nbF * 4;
-        float acc = 0.0f;
-        for (int s = 0; s < p.k; s++) {
-            const uint8_t *blk = st + s * sqb + (rl2 * nbF + b2) * 80;
-            const uint32_t qw = *reinterpret_cast<const uint32_t *>(blk + 16 + 16 * part64 + 4 * sub);
-            const uint32_t scb = blk[4 * part64 + sub];
-            const uint32_t ddw = *reinterpret_cast<const uint32_t *>(st + p.k * sqb + s * ddb + (rl2 * nbF + b2) * 4);
-            const uint4 h0 = h16v[swz((s * F + col) / 8)], h1 = h16v[swz((s * F + col) / 8 + 1)];
-            const uint32_t hh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-            const uint32_t *ct = reinterpret_cast<const uint32_t *>(tab) + (lane & 15);
-            int a0 = 0, a1 = 0;
+    // stage: per routed slot one down tile ([sq: kRows2 x nbF x 80][dd: kRows2 x nbF x 4]), then
+    // the shared expert's kRows2 bf16 rows
+    const int tb = kRows2 * nbF * 84;
+    const int blk_off = s2 * tb + (j2 >> 3) * 80, dd_off = s2 * tb + kRows2 * nbF * 80 + (j2 >> 3) * 4;
+    const int sh_off = p.k * tb + 8 * tid;
+    for (int u = blockIdx.x; u < n2; u += gridDim.x) {
+        const int r0 = rc++;  // ring position = hand-off counter (units of both phases)
+        const int buf = r0 & 1;
+        float *rb = red + buf * 128;
+        const uint8_t *st = wait_stage(r0);
+        float acc[kRows2] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (st) {
+            uint2 qw[kRows2], bw[kRows2];
+            uint32_t scw[kRows2], dd[kRows2];
 #pragma unroll
-            for (int bb = 0; bb < 4; bb += 2) {
-                const int c0 = static_cast<int>(ct[((qw >> (8 * bb)) & 255u) << 4]);
-                const int c1 = static_cast<int>(ct[((qw >> (8 * bb + 8)) & 255u) << 4]);
-                a0 = __dp2a_lo(static_cast<int>(hh[2 * bb]), c0, a0);
-                a1 = __dp2a_lo(static_cast<int>(hh[2 * bb + 2]), c1, a1);
-                a0 = __dp2a_hi(static_cast<int>(hh[2 * bb + 1]), c0, a0);
-                a1 = __dp2a_hi(static_cast<int>(hh[2 * bb + 3]), c1, a1);
+            for (int r = 0; r < kRows2; r++) {
+                if (sval) {
+                    const uint8_t *blk = st + blk_off + r * nbF * 80;
+                    qw[r] = *reinterpret_cast<const uint2 *>(blk + 16 + 8 * (j2 & 7));
+                    scw[r] = *reinterpret_cast<const uint16_t *>(blk + 2 * (j2 & 7));
+                    dd[r] = *reinterpret_cast<const uint32_t *>(st + dd_off + r * nbF * 4);
+                }
+                if (w.has_shared) bw[r] = *reinterpret_cast<const uint2 *>(st + sh_off + r * F * 2);
             }
-            const float d = f16_to_f32(static_cast<uint16_t>(ddw & 0xffffu));
-            const float dmin = f16_to_f32(static_cast<uint16_t>(ddw >> 16));
-            float part = d * static_cast<float>(scb & 15u) * (scal[s] * (1.0f / 16384.0f)) * static_cast<float>(a0 + a1);
-            part = fmaf(-dmin * static_cast<float>(scb >> 4), hsum[s * (F / 16) + (col >> 4)], part);
-            acc = fmaf(sgw[s], part, acc);
-        }
-        if (w.has_shared) {  // this quarter of the row: lanes take interleaved 16-byte chunks
-            const uint4 *row = reinterpret_cast<const uint4 *>(st + p.k * (sqb + ddb) + rl2 * F * 2);
-            const float4 *hv = reinterpret_cast<const float4 *>(hsh);
-            for (int q = qt * (F / 32) + lane; q < (qt + 1) * (F / 32); q += 32) {
-                const uint4 v = row[q];
-                const float4 x0 = hv[2 * q], x1 = hv[2 * q + 1];
-                acc = fmaf(bf16_lo(v.x), x0.x, acc);
-                acc = fmaf(bf16_hi(v.x), x0.y, acc);
-                acc = fmaf(bf16_lo(v.y), x0.z, acc);
-                acc = fmaf(bf16_hi(v.y), x0.w, acc);
-                acc = fmaf(bf16_lo(v.z), x1.x, acc);
-                acc = fmaf(bf16_hi(v.z), x1.y, acc);
-                acc = fmaf(bf16_lo(v.w), x1.z, acc);
-                acc = fmaf(bf16_hi(v.w), x1.w, acc);
+            release_stage(r0);
+#pragma unroll
+            for (int r = 0; r < kRows2; r++) {
+                if (sval) {
+                    const int a0 = q2k_idot(qw[r].x, hp), a1 = q2k_idot(qw[r].y, hp + 8);
+                    const float d = f16_to_f32(static_cast<uint16_t>(dd[r] & 0xffffu));
+                    const float dmin = f16_to_f32(static_cast<uint16_t>(dd[r] >> 16));
+                    const uint32_t sc = scw[r];
+                    const float t = fmaf(gh0 * small_int_to_float(static_cast<int>(sc & 15u)), small_int_to_float(a0),
+                                         gh1 * small_int_to_float(static_cast<int>((sc >> 8) & 15u)) *
+                                             small_int_to_float(a1));
+                    const float mt = fmaf(gs0, small_int_to_float(static_cast<int>((sc >> 4) & 15u)),
+                                          gs1 * small_int_to_float(static_cast<int>(sc >> 12)));
+                    acc[r] = fmaf(d, t, -dmin * mt);
+                }
+                if (w.has_shared) {
+                    acc[r] = fmaf(bf16_lo(bw[r].x), hs.x, acc[r]);
+                    acc[r] = fmaf(bf16_hi(bw[r].x), hs.y, acc[r]);
+                    acc[r] = fmaf(bf16_lo(bw[r].y), hs.z, acc[r]);
+                    acc[r] = fmaf(bf16_hi(bw[r].y), hs.w, acc[r]);
+                }
             }
         }
-        acc = warp_sum(acc);
-        // the four warps of this output row meet on the row's own barrier; parity-alternating
-        // slots let the next unit's partials be written while this one is still read
-        float *slot = red + ((u / gridDim.x) & 1) * 64;
-        if (lane == 0) slot[warp * 4] = acc;
-        release_stage();
-        row_sync(rl2);
-        if (qt == 0 && lane == 0) {
-            const int d = u * kRows2 + rl2;
-            p.out[d] += (slot[(4 * rl2) * 4] + slot[(4 * rl2 + 1) * 4]) + (slot[(4 * rl2 + 2) * 4] + slot[(4 * rl2 + 3) * 4]);
-        }
+        const float v = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
+        if (r0 >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((r0 >> 1) - 1) & 1u, abort_flag, p.status);
+        if ((lane & 7) == 0) rb[warp * 4 + (lane >> 3)] = v;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rfull + 8 * buf);
     }
     if (tr) tr[5] = now_ns();
 }
@@ -635,27 +870,25 @@ int n_sms() {
 
 }  // namespace
 
-// Whether the fused single-token kernel covers this shape.
 int decode_step_ctas() { return n_sms(); }
 
+// Whether the fused single-token kernel covers this shape.
 bool decode_step_supported(const DeviceWeights &w, int k) {
-    if (k < 1 || k > 8 || w.F != 2048 || w.D > 8192) return false;
-    const int r1 = (static_cast<size_t>(16) * w.nbD * 132 <= kStageBytes) ? 16 : 8;
-    if (static_cast<size_t>(r1) * w.nbD * 132 > kStageBytes) return false;
-    if (w.has_shared && static_cast<size_t>(4) * w.D > kStageBytes) return false;
+    if (k < 1 || k > 8 || w.F != 2048 || w.D % 256 != 0 || w.D > kMaxD || w.E > 1024) return false;
+    if (static_cast<size_t>(kRows1) * w.nbD * 132 > kStageBytes) return false;
+    if (w.has_shared && static_cast<size_t>(kRowsSh) * 2 * w.D * 2 > kStageBytes) return false;
     const size_t down = static_cast<size_t>(k) * kRows2 * w.nbF * 84 + (w.has_shared ? kRows2 * w.F * 2 : 0);
-    if (down > kStageBytes) return false;
-    const size_t act1 = static_cast<size_t>(w.D) * 2;
-    const size_t act2 = static_cast<size_t>(k) * w.F * 2 + static_cast<size_t>(k) * (w.F / 16) * 4 + w.F * 4;
-    return act1 <= kActBytes && act2 <= kActBytes;
+    return down <= kStageBytes;
 }
 
 int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, const float *logits, int k,
                        int gate_mode, float *out, uint64_t *trace, void *stream) {
-    static int seen[64];
-    const size_t smem =
-        128 + static_cast<size_t>(kStages) * kStageBytes + kTabEntries * 8 + kSignEntries * 16 + kActBytes + 2048;
-    int err = ensure_smem(reinterpret_cast<const void *>(decode_step_kernel), static_cast<int>(smem), seen);
+    static int seen[3][64];
+    const int nq = w.D <= 1024 ? 1 : w.D <= 2048 ? 2 : 4;  // 1024-column quarters of x
+    const void *kern = nq == 1   ? reinterpret_cast<const void *>(decode_step_kernel<1>)
+                       : nq == 2 ? reinterpret_cast<const void *>(decode_step_kernel<2>)
+                                 : reinterpret_cast<const void *>(decode_step_kernel<4>);
+    int err = ensure_smem(kern, kSmemBytes, seen[nq == 1 ? 0 : nq == 2 ? 1 : 2]);
     if (err) return err;
     StepParams p;
     p.w = w;
@@ -667,17 +900,17 @@ int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16
     p.grid = ws.grid;
     p.topk_idx = ws.topk_idx;
     p.topk_w = ws.topk_w;
-    p.h = ws.h32;
-    p.bar = ws.gbar;
-    p.hmax = ws.hmax;
+    // h32 holds at least (k + 1) * F floats: int16 h, the sub-block factors and sums, shared h
+    uint8_t *hb = reinterpret_cast<uint8_t *>(ws.h32);
+    p.hq = reinterpret_cast<int16_t *>(hb);
+    p.hsc = reinterpret_cast<float *>(hb + static_cast<size_t>(k) * w.F * 2);
+    p.hsum = p.hsc + static_cast<size_t>(k) * (w.F / 16);
+    p.hsh = p.hsum + static_cast<size_t>(k) * (w.F / 16);
+    p.bar = reinterpret_cast<unsigned long long *>(ws.gbar);
     p.trace = trace;
     p.status = ws.status;
-    p.r1 = (static_cast<size_t>(16) * w.nbD * 132 <= kStageBytes) ? 16 : 8;
-    p.rs = 1;
-    while (p.rs < 8 && static_cast<size_t>(p.rs * 2) * w.D * 4 <= kStageBytes && w.F % (p.rs * 2) == 0) p.rs *= 2;
     void *args[] = {&p};
-    return static_cast<int>(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(decode_step_kernel),
-                                                        dim3(n_sms()), dim3(kThreads), args, smem,
+    return static_cast<int>(cudaLaunchCooperativeKernel(kern, dim3(n_sms()), dim3(kThreads), args, kSmemBytes,
                                                         static_cast<cudaStream_t>(stream)));
 }
 

@@ -166,15 +166,14 @@ struct IQ2Fmt {
         uint4 q;
         uint32_t d;
     };
-    const uint8_t *qs;
-    const uint16_t *dp;
-    size_t rowb;
+    const uint8_t *qs;   // this row's code blocks
+    const uint16_t *dp;  // this row's block scales
     const uint2 *gt;  // grid as fp16 high bytes, this lane's replica
     __device__ __forceinline__ Data fetch(int kb) const {
         const int b = kb >> 2, part = kb & 3;
         Data v;
-        v.q = __ldg(reinterpret_cast<const uint4 *>(qs + (rowb + b) * 64) + part);
-        v.d = __ldg(dp + rowb + b);
+        v.q = __ldg(reinterpret_cast<const uint4 *>(qs + b * 64) + part);
+        v.d = __ldg(dp + b);
         return v;
     }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
@@ -211,18 +210,17 @@ struct Q2KFmt {
         uint32_t sc;
         uint32_t dd;
     };
-    const uint8_t *sq;
-    const uint32_t *ddp;
-    size_t rowb;
+    const uint8_t *sq;    // this row's blocks (scales, codes)
+    const uint32_t *ddp;  // this row's d | dmin words
     int half;
     const uint2 *st;  // code byte -> two byte_perm selectors, this lane's replica
     __device__ __forceinline__ Data fetch(int kb) const {
         const int b = kb >> 2, part = kb & 3;
-        const uint8_t *blk = sq + (rowb + b) * 80;
+        const uint8_t *blk = sq + b * 80;
         Data v;
         v.q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 16 * part + 8 * half));
         v.sc = __ldg(reinterpret_cast<const uint16_t *>(blk + 4 * part + 2 * half));
-        v.dd = __ldg(ddp + rowb + b);
+        v.dd = __ldg(ddp + b);
         return v;
     }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
@@ -512,8 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else {
-                    const size_t rowb = (static_cast<size_t>(ti.e) * F + wrow) * p.w.nbD;
-                    IQ2Fmt f{sel ? p.w.up_qs : p.w.gate_qs, sel ? p.w.up_d : p.w.gate_d, rowb, tab};
+                    IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 }
             } else {
@@ -521,8 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, sel};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
                 } else {
-                    const size_t rowb = (static_cast<size_t>(ti.e) * D + wrow) * p.w.nbF;
-                    Q2KFmt f{p.w.down_sq, p.w.down_dd, rowb, sel, tab};
+                    Q2KFmt f{q2k_sq_row(p.w, ti.e, wrow), q2k_dd_row(p.w, ti.e, wrow), sel, tab};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
                 }
             }
@@ -604,12 +600,11 @@ __global__ void __launch_bounds__(256) producer_dump_kernel(DeviceWeights w, con
     const uint32_t t = smem_u32(tile);
     const uint2 *tab = table + (lane & 15);
     if (down) {
-        const size_t rowb = (static_cast<size_t>(expert) * w.D + wrow) * w.nbF;
-        Q2KFmt f{w.down_sq, w.down_dd, rowb, sel, tab};
+        Q2KFmt f{q2k_sq_row(w, expert, wrow), q2k_dd_row(w, expert, wrow), sel, tab};
         f.emit(f.fetch(kb), t, r);
     } else if (sel == 0) {
-        const size_t rowb = (static_cast<size_t>(expert) * w.F + wrow) * w.nbD;
-        IQ2Fmt f{matrix == DS4MOE_GATE ? w.gate_qs : w.up_qs, matrix == DS4MOE_GATE ? w.gate_d : w.up_d, rowb, tab};
+        const int m = matrix == DS4MOE_GATE ? 0 : 1;
+        IQ2Fmt f{iq2_qs_row(w, m, expert, wrow), iq2_d_row(w, m, expert, wrow), tab};
         f.emit(f.fetch(kb), t, r);
     }
     __syncthreads();

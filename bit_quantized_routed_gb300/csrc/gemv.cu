@@ -127,11 +127,10 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
 #pragma unroll 1
                 for (int rr = 0; rr < kUpRows / kWarps; rr++) {
                     const int r = r0 + warp + rr * kWarps;
-                    const size_t rowb = (static_cast<size_t>(e) * F + r) * nbD;
-                    const uint4 *qg = reinterpret_cast<const uint4 *>(p.w.gate_qs + rowb * 64);
-                    const uint4 *qu = reinterpret_cast<const uint4 *>(p.w.up_qs + rowb * 64);
-                    const uint16_t *dg = p.w.gate_d + rowb;
-                    const uint16_t *du = p.w.up_d + rowb;
+                    const uint4 *qg = reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 0, e, r));
+                    const uint4 *qu = reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 1, e, r));
+                    const uint16_t *dg = iq2_d_row(p.w, 0, e, r);
+                    const uint16_t *du = iq2_d_row(p.w, 1, e, r);
                     float ag[NT], au[NT];
 #pragma unroll
                     for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
@@ -258,9 +257,8 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
 #pragma unroll 1
                 for (int rr = 0; rr < kDownRows / kWarps; rr++) {
                     const int r = r0 + warp + rr * kWarps;
-                    const size_t rowb = (static_cast<size_t>(e) * D + r) * nbF;
-                    const uint8_t *sq = p.w.down_sq + rowb * 80;
-                    const uint32_t *dd = p.w.down_dd + rowb;
+                    const uint8_t *sq = q2k_sq_row(p.w, e, r);
+                    const uint32_t *dd = q2k_dd_row(p.w, e, r);
                     float acc[NT];
 #pragma unroll
                     for (int j = 0; j < NT; j++) acc[j] = 0.0f;
@@ -342,12 +340,11 @@ __global__ void dequant_kernel(DeviceWeights w, int expert, int matrix, const ui
         const int c = static_cast<int>(ci - r * (cols / 64));
         float v[64];
         if (matrix == DS4MOE_DOWN) {
-            const size_t rowb = (static_cast<size_t>(expert) * D + r) * w.nbF;
-            const uint8_t *sq = w.down_sq + rowb * 80;
+            const uint8_t *sq = q2k_sq_row(w, expert, static_cast<int>(r));
             const int b = c >> 2, part = c & 3;
             const uint4 qv = *(reinterpret_cast<const uint4 *>(sq + b * 80 + 16) + part);
             const uint32_t scw = *(reinterpret_cast<const uint32_t *>(sq + b * 80) + part);
-            const uint32_t ddw = w.down_dd[rowb + b];
+            const uint32_t ddw = q2k_dd_row(w, expert, static_cast<int>(r))[b];
             const float d = f16_to_f32(static_cast<uint16_t>(ddw & 0xffffu));
             const float dmin = f16_to_f32(static_cast<uint16_t>(ddw >> 16));
             for (int sub = 0; sub < 4; sub++) {
@@ -358,9 +355,9 @@ __global__ void dequant_kernel(DeviceWeights w, int expert, int matrix, const ui
                 for (int i = 0; i < 16; i++) v[16 * sub + i] = q2k_weight(ds, dm, (qw >> (2 * i)) & 3u);
             }
         } else {
-            const size_t rowb = (static_cast<size_t>(expert) * F + r) * w.nbD;
-            const uint8_t *qs = (matrix == DS4MOE_GATE ? w.gate_qs : w.up_qs) + rowb * 64;
-            const uint16_t *dp = (matrix == DS4MOE_GATE ? w.gate_d : w.up_d) + rowb;
+            const int m = matrix == DS4MOE_GATE ? 0 : 1;
+            const uint8_t *qs = iq2_qs_row(w, m, expert, static_cast<int>(r));
+            const uint16_t *dp = iq2_d_row(w, m, expert, static_cast<int>(r));
             const uint4 q = *(reinterpret_cast<const uint4 *>(qs) + c);
             const float d = f16_to_f32(dp[c >> 2]);
             for (int sb = 0; sb < 2; sb++) {

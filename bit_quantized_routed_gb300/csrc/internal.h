@@ -29,10 +29,8 @@ enum : int {
 struct DeviceWeights {
     int D, F, E;
     int nbD, nbF;           // blocks per row of gate/up (D/256) and of down (F/256)
-    uint8_t *gate_qs, *up_qs;  // [E][F][nbD][64]
-    uint16_t *gate_d, *up_d;   // [E][F][nbD]
-    uint8_t *down_sq;          // [E][D][nbF][80]
-    uint32_t *down_dd;         // [E][D][nbF]  (d | dmin << 16)
+    uint8_t *iq2;              // gate and up, tiled: see iq2_qs_row
+    uint8_t *q2k;              // down, tiled: see q2k_sq_row
     uint16_t *sh_gate, *sh_up; // [F][D] bf16, or null
     uint16_t *sh_down;         // [D][F] bf16, or null
     uint16_t *sh_down_f16;     // [D][F] fp16 copy for the tensor-core path, or null
@@ -40,6 +38,59 @@ struct DeviceWeights {
     bool has_shared;
     bool shared_tc_ok;         // the shared expert's weights fit fp16
 };
+
+// Tiled device layout of the routed experts' packed weights: the rows that one single-token
+// step streams together are one contiguous range, so each is fetched with one bulk copy.
+//   gate/up: expert e, rows 16t .. 16t+15 form one tile of 16 * nbD * 132 bytes:
+//            [gate qs: 16 x nbD x 64][up qs: 16 x nbD x 64][gate d: 16 x nbD fp16][up d: 16 x nbD fp16]
+//   down:    expert e, rows 4t .. 4t+3 form one tile of 4 * nbF * 84 bytes:
+//            [sq: 4 x nbF x 80 (scales, codes)][dd: 4 x nbF x u32 (d | dmin << 16)]
+// Within a tile each row's blocks stay contiguous, so kernels index a row pointer by block.
+#ifdef __CUDACC__
+#define DS4MOE_HD __host__ __device__
+#else
+#define DS4MOE_HD
+#endif
+
+constexpr int kIq2TileRows = 16;
+constexpr int kQ2kTileRows = 4;
+
+DS4MOE_HD inline size_t iq2_tile_bytes(int nbD) { return static_cast<size_t>(kIq2TileRows) * nbD * 132; }
+DS4MOE_HD inline size_t q2k_tile_bytes(int nbF) { return static_cast<size_t>(kQ2kTileRows) * nbF * 84; }
+DS4MOE_HD inline size_t iq2_tile_offset(const DeviceWeights &w, int e, int r) {
+    return (static_cast<size_t>(e) * (w.F / kIq2TileRows) + r / kIq2TileRows) * iq2_tile_bytes(w.nbD);
+}
+DS4MOE_HD inline size_t q2k_tile_offset(const DeviceWeights &w, int e, int d) {
+    return (static_cast<size_t>(e) * (w.D / kQ2kTileRows) + d / kQ2kTileRows) * q2k_tile_bytes(w.nbF);
+}
+// Row r of gate (m = 0) or up (m = 1) of expert e: nbD blocks of 64 code bytes, and their nbD scales d.
+DS4MOE_HD inline size_t iq2_qs_offset(const DeviceWeights &w, int m, int e, int r) {
+    return iq2_tile_offset(w, e, r) + static_cast<size_t>(m * kIq2TileRows + r % kIq2TileRows) * w.nbD * 64;
+}
+DS4MOE_HD inline size_t iq2_d_offset(const DeviceWeights &w, int m, int e, int r) {
+    return iq2_tile_offset(w, e, r) + static_cast<size_t>(2 * kIq2TileRows) * w.nbD * 64 +
+           static_cast<size_t>(m * kIq2TileRows + r % kIq2TileRows) * w.nbD * 2;
+}
+// Row d of down of expert e: nbF blocks of 80 bytes (scales, codes), and their nbF d | dmin words.
+DS4MOE_HD inline size_t q2k_sq_offset(const DeviceWeights &w, int e, int d) {
+    return q2k_tile_offset(w, e, d) + static_cast<size_t>(d % kQ2kTileRows) * w.nbF * 80;
+}
+DS4MOE_HD inline size_t q2k_dd_offset(const DeviceWeights &w, int e, int d) {
+    return q2k_tile_offset(w, e, d) + static_cast<size_t>(kQ2kTileRows) * w.nbF * 80 +
+           static_cast<size_t>(d % kQ2kTileRows) * w.nbF * 4;
+}
+DS4MOE_HD inline const uint8_t *iq2_qs_row(const DeviceWeights &w, int m, int e, int r) {
+    return w.iq2 + iq2_qs_offset(w, m, e, r);
+}
+DS4MOE_HD inline const uint16_t *iq2_d_row(const DeviceWeights &w, int m, int e, int r) {
+    return reinterpret_cast<const uint16_t *>(w.iq2 + iq2_d_offset(w, m, e, r));
+}
+DS4MOE_HD inline const uint8_t *q2k_sq_row(const DeviceWeights &w, int e, int d) {
+    return w.q2k + q2k_sq_offset(w, e, d);
+}
+DS4MOE_HD inline const uint32_t *q2k_dd_row(const DeviceWeights &w, int e, int d) {
+    return reinterpret_cast<const uint32_t *>(w.q2k + q2k_dd_offset(w, e, d));
+}
 
 // Per-call grouping metadata written on the device by the grouping kernel.
 struct GroupMeta {

@@ -38,13 +38,27 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_test, but a thread whose phase is not complete may sleep up to ~hint_ns in the
+// instruction (it wakes when the phase completes): waiting warps then issue almost nothing.
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase of the given parity to complete. Gives up (false) when the CTA's
 // abort flag is raised or after kWaitCycles, raising the flag and the status bit itself.
 static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_test(bar, parity)) return true;
+        if (mbar_test_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitCycles) {
             *abort_flag = 1;

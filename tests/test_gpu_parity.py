@@ -195,11 +195,39 @@ def test_ffn_tensor_core_reports_fp16_overflow(ds4):
 
 # ---------------------------------------------------------------- the single-token kernel
 
-@pytest.mark.parametrize("D,E,k,shared,mode", [(4096, 256, 8, True, 0), (7168, 64, 6, True, 1), (1024, 16, 8, False, 0)])
-def test_single_token_kernel_matches_oracle(ds4, D, E, k, shared, mode):
+# (D, E, k, shared, mode, fused): the fused kernel covers F == 2048, D <= 4096; D = 7168 takes
+# the separate single-token kernels. D = 3072 leaves half of the second x half empty.
+@pytest.mark.parametrize("D,E,k,shared,mode,fused", [
+    (4096, 256, 8, True, 0, True), (2048, 64, 6, True, 1, True), (1024, 16, 8, False, 0, True),
+    (3072, 32, 4, True, 1, True), (4096, 300, 1, False, 1, True), (7168, 64, 6, True, 1, False)])
+def test_single_token_kernel_matches_oracle(ds4, D, E, k, shared, mode, fused):
     wl = synth.Workload("one", T=1, D=D, F=2048, E=E, k=k, seed=D + E, shared=shared)
-    err = _ffn_case(ds4, wl, quantized=False, mode=mode)
+    lay = Layer(wl, quantized=False)
+    W = lay.upload(ds4)
+    before = ds4.ds4moe_get_stats(W)
+    got = lay.run(ds4, W, mode=mode)
+    after = ds4.ds4moe_get_stats(W)
+    W.close()
+    assert (after["launches"] - before["launches"] == 1) == fused
+    ref, _, _ = lay.oracle_delta(mode=mode)
+    err = norm_max_err(got, ref)
     assert err <= FFN_TOL, err
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_single_token_kernel_breaks_ties_like_the_oracle(ds4, mode):
+    # many equal logits (and -0 next to +0): the selection must take the lower expert index
+    wl = synth.Workload("ties", T=1, D=1024, F=2048, E=64, k=8, seed=77, shared=False)
+    lay = Layer(wl, quantized=False)
+    vals = np.array([-1.0, 0.0, -0.0, 0.5, 2.0], np.float32)
+    lay.L = vals[np.random.default_rng(5).integers(0, len(vals), size=(1, wl.E))]
+    W = lay.upload(ds4)
+    before = ds4.ds4moe_get_stats(W)["launches"]
+    got = lay.run(ds4, W, mode=mode)
+    assert ds4.ds4moe_get_stats(W)["launches"] - before == 1  # the fused kernel ran
+    W.close()
+    ref, _, _ = lay.oracle_delta(mode=mode)
+    assert norm_max_err(got, ref) <= FFN_TOL
 
 
 def test_single_token_kernel_equals_separate_kernels_and_is_deterministic(ds4):
