@@ -28,6 +28,7 @@ DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS = 1
 DS4MOE_OPT_PROFILE = 2
 DS4MOE_OPT_SINGLE_STEP = 3
 DS4MOE_OPT_TRACE = 4
+DS4MOE_OPT_SMALL_GROUPS = 5
 STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step"]
 
 EXPORTED = [

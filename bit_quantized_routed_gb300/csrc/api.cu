@@ -155,9 +155,10 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
         delete h;
         return DS4MOE_ECUDA;
     }
-    h->gemm_min_tokens = 2;
+    h->gemm_min_tokens = -1;
     h->shared_gemm_min_tokens = 2;
     h->single_step = 1;
+    h->small_groups = 1;
     DeviceWeights &w = h->dw;
     w.D = D;
     w.F = F;
@@ -184,8 +185,10 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
                 if (!repack_iq2(static_cast<const uint8_t *>(mats[m]), nb_up, qs.data(), dv.data(), &amax))
                     TRY(DS4MOE_EBADDATA);
                 for (int r = 0; r < F; r++) {
-                    std::memcpy(tiles.data() + iq2_qs_offset(w0, m, 0, r), qs.data() + static_cast<size_t>(r) * w.nbD * 64,
-                                static_cast<size_t>(w.nbD) * 64);
+                    const int swz = iq2_swz(w0, r);
+                    for (int q = 0; q < 4 * w.nbD; q++)  // 16-byte chunks, permuted within the row
+                        std::memcpy(tiles.data() + iq2_qs_offset(w0, m, 0, r) + static_cast<size_t>(q ^ swz) * 16,
+                                    qs.data() + static_cast<size_t>(r) * w.nbD * 64 + static_cast<size_t>(q) * 16, 16);
                     std::memcpy(tiles.data() + iq2_d_offset(w0, m, 0, r), dv.data() + static_cast<size_t>(r) * w.nbD,
                                 static_cast<size_t>(w.nbD) * 2);
                 }
@@ -251,6 +254,10 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     TRY(dev_alloc(h, &ws.gbar, 16));
     TRY(dev_alloc(h, &ws.hmax, 1024 * 8 * 4));
     TRY(dev_alloc(h, &ws.trace, 1024 * 6 * 8));
+    TRY(dev_alloc(h, &ws.small_pos, P * 4));
+    TRY(dev_alloc(h, &ws.xq, static_cast<size_t>(desc->max_tokens) * D * 2));
+    TRY(dev_alloc(h, &ws.x8, static_cast<size_t>(desc->max_tokens) * (D / 32) * 4));
+    TRY(dev_alloc(h, &ws.xsc, static_cast<size_t>(desc->max_tokens) * 16));
     if (cudaMemset(ws.gbar, 0, 16) != cudaSuccess) TRY(DS4MOE_ECUDA);
     TRY(dev_alloc(h, &ws.grid_hi, 2048));
     {
@@ -280,11 +287,12 @@ void ds4moe_weights_destroy(ds4moe_weights *h) {
 }
 
 int ds4moe_set_option(ds4moe_weights *h, int option, int value) {
-    if (!h || value < 0) return DS4MOE_EINVAL;
+    if (!h || (value < 0 && !(option == DS4MOE_OPT_GEMM_MIN_TOKENS && value == -1))) return DS4MOE_EINVAL;
     switch (option) {
         case DS4MOE_OPT_GEMM_MIN_TOKENS: h->gemm_min_tokens = value; return DS4MOE_OK;
         case DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS: h->shared_gemm_min_tokens = value; return DS4MOE_OK;
         case DS4MOE_OPT_SINGLE_STEP: h->single_step = value ? 1 : 0; return DS4MOE_OK;
+        case DS4MOE_OPT_SMALL_GROUPS: h->small_groups = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_TRACE: h->trace = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_PROFILE:
             if (value && !h->events[0]) {
@@ -326,7 +334,7 @@ int ds4moe_group(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, 
     if (static_cast<int64_t>(T) * k > (int64_t(1) << 30)) return DS4MOE_EINVAL;
     if (!counts || !offsets || (T > 0 && (!topk_idx || !perm || !inv))) return DS4MOE_EINVAL;
     return cuda_status(launch_group(topk_idx, T, k, E, 0, nullptr, counts, offsets, perm, inv, nullptr, nullptr,
-                                    nullptr, nullptr, nullptr, nullptr, stream));
+                                    nullptr, nullptr, nullptr, nullptr, nullptr, stream));
 }
 
 int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits, int T, int k, int gate_mode,
@@ -356,28 +364,44 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     }
     // A group holds at most T tokens, so the tensor-core path can only be needed when
     // T reaches the threshold; the device decides per group after routing.
-    const int gemm_min = (h->gemm_min_tokens > 0 && T >= h->gemm_min_tokens) ? h->gemm_min_tokens : 0;
+    const bool sg_fits = h->small_groups && small_groups_supported(w);
+    const int gm = h->gemm_min_tokens >= 0 ? h->gemm_min_tokens : sg_fits ? (T <= 64 ? 0 : 7) : 2;
+    const int gemm_min = (gm > 0 && T >= gm) ? gm : 0;
     const bool shared_tc = w.has_shared && w.shared_tc_ok && h->shared_gemm_min_tokens > 0 &&
                            T >= h->shared_gemm_min_tokens;
     const bool any_tc = gemm_min > 0 || shared_tc;
+    // The small-group kernels take every routed group below the threshold; the shared expert
+    // must then be on the tensor cores, or (T = 1) on the single-token decode kernels.
+    const bool sg = sg_fits && (!w.has_shared || shared_tc || T == 1);
     int rc = clk.stage(DS4MOE_STAGE_ROUTE);
     if (!rc) rc = launch_route(logits, T, w.E, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
     if (!rc) rc = clk.stage(DS4MOE_STAGE_GROUP);
     if (!rc)
         rc = launch_group(ws.topk_idx, T, k, w.E, gemm_min, w.tc_ok, ws.counts, ws.offsets, ws.perm, ws.inv,
-                          ws.gemv_list, ws.gemm_list, ws.single_list, ws.tile_prefix, ws.meta, ws.status, stream);
+                          ws.gemv_list, ws.gemm_list, sg ? nullptr : ws.single_list, ws.tile_prefix,
+                          sg ? ws.small_pos : nullptr, ws.meta, ws.status, stream);
     if (any_tc) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_GATHER);
         if (!rc) rc = launch_gather(w, ws, x, T, k, gemm_min, shared_tc, stream);
     }
-    // one-token groups (every group at T = 1) run on the decode kernels; groups of 2 ..
-    // gemm_min-1 tokens on the multi-token GEMV kernels, which are launched only when such
-    // groups can exist; larger groups on the tensor cores
-    const bool multi_gemv = gemm_min == 0 ? T > 1 : gemm_min > 2;
+    // Without the small-group kernels: one-token groups (every group at T = 1) run on the
+    // decode kernels; groups of 2 .. gemm_min-1 tokens on the multi-token GEMV kernels, which
+    // are launched only when such groups can exist; larger groups on the tensor cores.
+    const bool multi_gemv = !sg && (gemm_min == 0 ? T > 1 : gemm_min > 2);
     const bool shared_single = w.has_shared && !shared_tc && T == 1;
     const bool shared_multi = w.has_shared && !shared_tc && T > 1;
     if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMV);
-    if (!rc) rc = launch_decode_up(w, ws, x, T, k, shared_single, stream);
+    if (sg) {
+        if (!rc) rc = launch_prep_x(ws, x, T, w.D, stream);
+        if (!rc) rc = launch_small_up(w, ws, T, k, stream);
+        h->launches++;
+        if (shared_single) {  // T = 1: the decode kernels take the shared expert alone (no single list)
+            if (!rc) rc = launch_decode_up(w, ws, x, T, k, true, stream);
+            h->launches++;
+        }
+    } else {
+        if (!rc) rc = launch_decode_up(w, ws, x, T, k, shared_single, stream);
+    }
     if (multi_gemv || shared_multi) {
         if (!rc) rc = launch_gemv_up(w, ws, x, T, k, shared_multi, stream);
         h->launches++;
@@ -387,7 +411,15 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         if (!rc) rc = launch_gemm_up(w, ws, h->tmap_x16, T, k, shared_tc, stream);
     }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMV);
-    if (!rc) rc = launch_decode_down(w, ws, T, k, shared_single, stream);
+    if (sg) {
+        if (!rc) rc = launch_small_down(w, ws, T, k, stream);
+        if (shared_single) {
+            if (!rc) rc = launch_decode_down(w, ws, T, k, true, stream);
+            h->launches++;
+        }
+    } else {
+        if (!rc) rc = launch_decode_down(w, ws, T, k, shared_single, stream);
+    }
     if (multi_gemv || shared_multi) {
         if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_multi, stream);
         h->launches++;

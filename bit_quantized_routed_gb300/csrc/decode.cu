@@ -140,13 +140,14 @@ __global__ void __launch_bounds__(kThreads) decode_up_kernel(DecParams p) {
                     xh[4 * j + 3] = h2u(__floats2half2_rn(bf16_lo(xr[j].w) * xs, bf16_hi(xr[j].w) * xs));
                 }
                 if (live) {
-                    const int b = c >> 2, part = c & 3;
+                    const int b = c >> 2;
                     uint4 qg[kRW], qu[kRW];
                     float dg[kRW], du[kRW];
 #pragma unroll
                     for (int r = 0; r < kRW; r++) {
-                        qg[r] = __ldg(reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 0, e, r0 + r) + b * 64) + part);
-                        qu[r] = __ldg(reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 1, e, r0 + r) + b * 64) + part);
+                        const int cs = c ^ iq2_swz(p.w, r0 + r);  // chunk c = 4 * b + part
+                        qg[r] = __ldg(reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 0, e, r0 + r)) + cs);
+                        qu[r] = __ldg(reinterpret_cast<const uint4 *>(iq2_qs_row(p.w, 1, e, r0 + r)) + cs);
                         dg[r] = f16_to_f32(__ldg(iq2_d_row(p.w, 0, e, r0 + r) + b)) * xinv;
                         du[r] = f16_to_f32(__ldg(iq2_d_row(p.w, 1, e, r0 + r) + b)) * xinv;
                     }

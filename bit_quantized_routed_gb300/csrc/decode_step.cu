@@ -40,8 +40,7 @@
 #include <cfloat>
 #include <climits>
 
-#include "common.cuh"
-#include "ptx.cuh"
+#include "step_common.cuh"
 
 namespace ds4moe {
 namespace {
@@ -80,22 +79,11 @@ constexpr int kBarCompute = 2;  // compute warps
 constexpr int kNAll = (kCompute + 1) * 32;
 constexpr int kNCompute = kCompute * 32;
 
-__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-
 __device__ __forceinline__ uint64_t now_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
-
-// v rounded to the nearest integer (ties to even), for |v| <= 2^22, as the low bits of the result:
-// adding 1.5 * 2^23 leaves the rounded integer in the mantissa (two full-rate operations).
-__device__ __forceinline__ uint32_t round_to_int_bits(float v) {
-    return static_cast<uint32_t>(__float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000);
-}
-
-// Exact int -> float for |v| < 2^22 with two full-rate operations (no conversion unit).
-__device__ __forceinline__ float small_int_to_float(int v) { return __int_as_float(0x4B400000 + v) - 12582912.0f; }
 
 struct StepParams {
     DeviceWeights w;
@@ -145,11 +133,6 @@ __device__ __forceinline__ Seq1 seq1_of(const StepParams &p) {
     s.ns = p.w.has_shared ? count_of(p.w.F / kRowsSh) : 0;
     s.nr = count_of(p.k * (p.w.F / kRows1));
     return s;
-}
-
-// Bounded wait with the common case (phase already complete) inline.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status) {
-    return mbar_test(bar, parity) || mbar_wait(bar, parity, abort_flag, status);
 }
 
 // Sums two per-lane values over the warp; afterwards lane l holds the total of value (l >> 4) & 1.
@@ -337,19 +320,6 @@ __device__ void route_sorted8(const StepParams &p, int lane, int *sidx, float *s
     }
 }
 
-// d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) or with bytes 2, 3 (hi): signed 16-bit a,
-// unsigned bytes b.
-__device__ __forceinline__ int dp2a_lo_su(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ int dp2a_hi_su(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 // One IQ2-style 32-weight sub-block of a row dotted with the lane's 32 x values: xr holds per
 // group g the int16 pairs (x0,x2), (x4,x6), (x1,x3), (x5,x7) of its 8 columns, x8 = 8 * the sum
 // of the 32 values; q = the sub-block's 4 codebook indices and its sign/scale word, ds = the
@@ -361,9 +331,7 @@ __device__ __forceinline__ float iq2_sub(uint2 q, float ds, const uint32_t *xr, 
     for (int g = 0; g < 4; g++) {
         // codebook entry q.x byte g: offset lane4 | index << 8; sign entry (7 bits at 7g of q.y):
         // offset lane4 | 128 | signs << 8
-        const uint32_t og = __byte_perm(lane4, q.x, 0x1140u + 0x10u * g);
-        const uint32_t f = g == 0 ? (q.y << 8) : g == 1 ? (q.y << 1) : (q.y >> (7 * g - 8));
-        const uint32_t os = (f & 0x7F00u) | lane4 | 128u;
+        const uint32_t og = iq2_cb_off(q.x, g, lane4), os = iq2_sg_off(q.y, g, lane4);
         const uint32_t gv = *reinterpret_cast<const uint32_t *>(tab + og);
         const uint32_t sv = *reinterpret_cast<const uint32_t *>(tab + os);
         const uint32_t ev = (gv ^ sv) & 0x0F0F0F0Fu;  // weights 0, 2, 4, 6 plus 8, as bytes
@@ -376,18 +344,6 @@ __device__ __forceinline__ float iq2_sub(uint2 q, float ds, const uint32_t *xr, 
     const int tot = ce + (co >> 4);
     const float s1 = small_int_to_float(static_cast<int>((q.y >> 28) + 1u));  // sub-block scale s + 1
     return ds * s1 * small_int_to_float(tot);
-}
-
-// Sixteen Q2_K-style 2-bit codes (one u32: byte b holds weights 4b..4b+3) dotted with 16 int16 h
-// stored as hp[2j] = (h_j, h_4+j), hp[2j+1] = (h_8+j, h_12+j).
-__device__ __forceinline__ int q2k_idot(uint32_t qw, const uint32_t *hp) {
-    int a[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const int c = static_cast<int>((qw >> (2 * j)) & 0x03030303u);  // weights j, 4+j, 8+j, 12+j
-        a[j] = __dp2a_hi(static_cast<int>(hp[2 * j + 1]), c, __dp2a_lo(static_cast<int>(hp[2 * j]), c, 0));
-    }
-    return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
 __device__ __forceinline__ float dot8_bf16(uint4 w, float4 xa, float4 xb, float acc) {
@@ -567,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
                 frexpf(m, &e);
                 e = m > 0.0f ? e : 0;
                 if (lane < kRows1) {
-                    const int pos = 4 * (lane & 3) + (lane >> 2);
+                    const int pos = q2k_h_pos(lane);
                     p.hq[static_cast<size_t>(slot) * F + row0 + pos] =
                         static_cast<int16_t>(__float2int_rn(hv * ldexpf(1.0f, 14 - e)));
                 }
@@ -618,13 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
         xp[0] = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
         xp[1] = make_float4(bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w));
     }
-#pragma unroll
-    for (int j = 0; j < 16; j++) {  // codebook: nibbles m - 1, elements 2b in byte b's low nibble, 2b+1 in its high
-        const uint32_t lo = graw[j].x - 0x01010101u, hi = graw[j].y - 0x01010101u;  // bytes m - 1
-        // bytes (e0, e1, e2, e3), (e4, e5, e6, e7) -> bytes (e0 | e1 << 4, e2 | e3 << 4, ...)
-        const uint32_t ev = __byte_perm(lo, hi, 0x6420), od = __byte_perm(lo, hi, 0x7531);
-        *reinterpret_cast<uint32_t *>(tab + (warp + 16 * j) * 256 + lane * 4) = ev | (od << 4);
-    }
     // int16 x in registers with the quarter's power-of-two scale, per group the pairs
     // (x0,x2), (x4,x6), (x1,x3), (x5,x7); x8 = 8 * their sum
     uint32_t xr[16];
@@ -663,17 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
         }
         x8 *= 8;
     }
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-        // 7 stored signs + their parity -> per element a nibble, 0x7 (negate) or 0x9 (keep), in
-        // the codebook word's order (element 2b in byte b's low nibble, 2b+1 in its high nibble)
-        const uint32_t s7 = static_cast<uint32_t>(warp + 16 * j);
-        const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
-        uint32_t v = 0;
-#pragma unroll
-        for (int el = 0; el < 8; el++) v |= (((s8 >> el) & 1u) ? 0x7u : 0x9u) << (8 * (el >> 1) + 4 * (el & 1));
-        *reinterpret_cast<uint32_t *>(tab + s7 * 256 + 128 + lane * 4) = v;
-    }
+    iq2_table_store(tab, graw, warp, lane);  // codebook and sign words, one replica per lane
     bar_sync(kBarCompute, kNCompute);
     if (tr) tr[1] = now_ns();
 
@@ -693,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
 
     // ---------------------------------------------------------------- phase 1: gate/up
     const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
+    const int swm = iq2_swz(w, 15);  // chunk permutation mask of the tiles' rows (iq2_swz)
     int rc = 0;
     {
         Seq1 q = seq0;
@@ -746,8 +686,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
                         const int rl = rg + i * RG;
                         float pg = 0.0f, pu = 0.0f;
                         if (cval) {
-                            const uint2 qg = *reinterpret_cast<const uint2 *>(gq + (rl * nbD * 8 + c) * 8);
-                            const uint2 qu = *reinterpret_cast<const uint2 *>(uq + (rl * nbD * 8 + c) * 8);
+                            // sub-block c is half c & 1 of the row's chunk c >> 1, stored at (c >> 1) ^ swizzle
+                            const int cb = rl * nbD * 64 + (((c >> 1) ^ (rl & swm)) << 4) + ((c & 1) << 3);
+                            const uint2 qg = *reinterpret_cast<const uint2 *>(gq + cb);
+                            const uint2 qu = *reinterpret_cast<const uint2 *>(uq + cb);
                             const float dg = f16_to_f32(gd[rl * nbD + (c >> 3)]) * xinv;
                             const float du = f16_to_f32(ud[rl * nbD + (c >> 3)]) * xinv;
                             pg = iq2_sub(qg, dg, xr, x8, tab, lane4);

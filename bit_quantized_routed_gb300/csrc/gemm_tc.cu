@@ -169,11 +169,11 @@ struct IQ2Fmt {
     const uint8_t *qs;   // this row's code blocks
     const uint16_t *dp;  // this row's block scales
     const uint2 *gt;  // grid as fp16 high bytes, this lane's replica
+    int swz;          // the row's chunk permutation (iq2_swz)
     __device__ __forceinline__ Data fetch(int kb) const {
-        const int b = kb >> 2, part = kb & 3;
         Data v;
-        v.q = __ldg(reinterpret_cast<const uint4 *>(qs + b * 64) + part);
-        v.d = __ldg(dp + b);
+        v.q = __ldg(reinterpret_cast<const uint4 *>(qs) + (kb ^ swz));  // chunk kb = 4 * block + part
+        v.d = __ldg(dp + (kb >> 2));
         return v;
     }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else {
-                    IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab};
+                    IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab, iq2_swz(p.w, wrow)};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 }
             } else {
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(256) producer_dump_kernel(DeviceWeights w, con
         f.emit(f.fetch(kb), t, r);
     } else if (sel == 0) {
         const int m = matrix == DS4MOE_GATE ? 0 : 1;
-        IQ2Fmt f{iq2_qs_row(w, m, expert, wrow), iq2_d_row(w, m, expert, wrow), tab};
+        IQ2Fmt f{iq2_qs_row(w, m, expert, wrow), iq2_d_row(w, m, expert, wrow), tab, iq2_swz(w, wrow)};
         f.emit(f.fetch(kb), t, r);
     }
     __syncthreads();

@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
 #pragma unroll
                     for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
                     for (int c = lane; c < nbD * 4; c += 32) {
-                        const uint4 vg = __ldg(qg + c), vu = __ldg(qu + c);
+                        const int cs = c ^ iq2_swz(p.w, r);
+                        const uint4 vg = __ldg(qg + cs), vu = __ldg(qu + cs);
                         const float sdg = f16_to_f32(__ldg(dg + (c >> 2)));
                         const float sdu = f16_to_f32(__ldg(du + (c >> 2)));
 #pragma unroll
@@ -358,7 +359,7 @@ __global__ void dequant_kernel(DeviceWeights w, int expert, int matrix, const ui
             const int m = matrix == DS4MOE_GATE ? 0 : 1;
             const uint8_t *qs = iq2_qs_row(w, m, expert, static_cast<int>(r));
             const uint16_t *dp = iq2_d_row(w, m, expert, static_cast<int>(r));
-            const uint4 q = *(reinterpret_cast<const uint4 *>(qs) + c);
+            const uint4 q = *(reinterpret_cast<const uint4 *>(qs) + (c ^ iq2_swz(w, static_cast<int>(r))));
             const float d = f16_to_f32(dp[c >> 2]);
             for (int sb = 0; sb < 2; sb++) {
                 const uint32_t iw = sb ? q.z : q.x, sw = sb ? q.w : q.y;

@@ -45,7 +45,8 @@ struct DeviceWeights {
 //            [gate qs: 16 x nbD x 64][up qs: 16 x nbD x 64][gate d: 16 x nbD fp16][up d: 16 x nbD fp16]
 //   down:    expert e, rows 4t .. 4t+3 form one tile of 4 * nbF * 84 bytes:
 //            [sq: 4 x nbF x 80 (scales, codes)][dd: 4 x nbF x u32 (d | dmin << 16)]
-// Within a tile each row's blocks stay contiguous, so kernels index a row pointer by block.
+// Within a tile each row's blocks stay together, so kernels index a row pointer by block; the
+// 16-byte chunks of a row's codes are permuted by iq2_swz (below).
 #ifdef __CUDACC__
 #define DS4MOE_HD __host__ __device__
 #else
@@ -79,6 +80,12 @@ DS4MOE_HD inline size_t q2k_dd_offset(const DeviceWeights &w, int e, int d) {
     return q2k_tile_offset(w, e, d) + static_cast<size_t>(kQ2kTileRows) * w.nbF * 80 +
            static_cast<size_t>(d % kQ2kTileRows) * w.nbF * 4;
 }
+// Within a row, the 16-byte chunks of codes (two 32-weight sub-blocks each) are stored permuted:
+// chunk q at position q ^ iq2_swz(w, r). The rows of a tile are 64 * nbD bytes apart (a multiple of
+// 128 when nbD is even), so without it the 16 rows of a tile read at one chunk index would all hit
+// the same shared-memory banks; with it, eight consecutive rows cover all eight 16-byte bank groups,
+// and a row read chunk by chunk still covers each aligned group of eight chunks once.
+DS4MOE_HD inline int iq2_swz(const DeviceWeights &w, int r) { return r & ((w.nbD & 1) ? 3 : 7); }
 DS4MOE_HD inline const uint8_t *iq2_qs_row(const DeviceWeights &w, int m, int e, int r) {
     return w.iq2 + iq2_qs_offset(w, m, e, r);
 }
@@ -97,7 +104,7 @@ struct GroupMeta {
     int n_gemv;    // experts with 0 < n_e < gemm_min (n_e > 1 when singles are split off), in gemv_list
     int n_gemm;    // experts with n_e >= gemm_min, listed in gemm_list in expert order
     int n_single;  // experts with exactly one token (when split off), listed in single_list
-    int pad;
+    int n_small_pairs;  // pairs of the gemv_list experts (positions listed in small_pos when requested)
 };
 
 struct Workspace {
@@ -123,6 +130,10 @@ struct Workspace {
     unsigned *gbar;     // grid barrier of the single-token kernel: count, generation
     float *hmax;        // [1024][8] per-CTA maxima of the single-token kernel
     uint64_t *trace;    // [1024][6] timestamps of the single-token kernel
+    int32_t *small_pos; // [P] positions of the small-group pairs (expert order)
+    uint32_t *xq;       // [T][D/8][4] tokens as int16 pairs for the small-group kernels (dp2a order)
+    int32_t *x8;        // [T][D/32] 8 x the sum of each 32-column sub-block of xq
+    float *xsc;         // [T][4] dequantisation factor of xq (element 0; the rest pad to 16 bytes)
 };
 
 }  // namespace ds4moe
@@ -136,6 +147,7 @@ struct ds4moe_weights {
     int profile;
     int single_step;  // T = 1 calls use the fused single-token kernel when it supports the shape
     int trace;        // record the single-token kernel's per-CTA timestamps
+    int small_groups; // groups below the tensor-core threshold run on the small-group kernels
     void *events[DS4MOE_N_STAGES + 1];  // cudaEvent_t: start of each stage, end of the call
     bool stage_ran[DS4MOE_N_STAGES];
     bool events_recorded;
@@ -153,8 +165,12 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
                  void *stream);
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok,
                  int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list,
-                 int32_t *gemm_list, int32_t *single_list, int32_t *tile_prefix, GroupMeta *meta, int *status,
-                 void *stream);
+                 int32_t *gemm_list, int32_t *single_list, int32_t *tile_prefix, int32_t *small_pos, GroupMeta *meta,
+                 int *status, void *stream);
+bool small_groups_supported(const DeviceWeights &w);
+int launch_prep_x(const Workspace &ws, const uint16_t *x, int T, int D, void *stream);
+int launch_small_up(const DeviceWeights &w, const Workspace &ws, int T, int k, void *stream);
+int launch_small_down(const DeviceWeights &w, const Workspace &ws, int T, int k, void *stream);
 int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, int gemm_min,
                   bool shared, void *stream);
 int launch_gemm_up(const DeviceWeights &w, const Workspace &ws, const void *tmap_x16, int T, int k, bool shared,

@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     group_kernel(const int32_t *__restrict__ idx, int P, int E, int gemm_min, const uint8_t *__restrict__ tc_ok,
                  int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                  int32_t *__restrict__ inv, int32_t *__restrict__ gemv_list, int32_t *__restrict__ gemm_list,
-                 int32_t *__restrict__ single_list, int32_t *__restrict__ tile_prefix, GroupMeta *meta,
-                 int *status) {
+                 int32_t *__restrict__ single_list, int32_t *__restrict__ tile_prefix, int32_t *__restrict__ small_pos,
+                 GroupMeta *meta, int *status) {
     extern __shared__ int sm[];
     int *hist = sm;                      // [kGroupWarps][E]: counts, then base positions
     int *tmp = sm + kGroupWarps * E;     // [32]
@@ -158,6 +158,11 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     const int pb = block_exclusive_scan(big ? 1 : 0, tmp, &n_big);
     const int pt = block_exclusive_scan(big ? (tot + kGemmBN - 1) / kGemmBN : 0, tmp, &n_tiles);
     if (small && gemv_list) gemv_list[ps] = e;
+    // positions of the small groups' pairs, in expert order (the small-group down kernel's slots)
+    int n_small_pairs = 0;
+    const int pp = block_exclusive_scan(small ? tot : 0, tmp, &n_small_pairs);
+    if (small && small_pos)
+        for (int r = 0; r < tot; r++) small_pos[pp + r] = off + r;
     if (big && gemm_list) gemm_list[pb] = e;
     if (big && tile_prefix) tile_prefix[pb] = pt;
     if (threadIdx.x == 0 && tile_prefix) tile_prefix[n_big] = n_tiles;
@@ -165,6 +170,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
         meta->n_gemv = n_small;
         meta->n_gemm = n_big;
         meta->n_single = n_single;
+        meta->n_small_pairs = n_small_pairs;
     }
     __syncthreads();
     // stable positions
@@ -214,15 +220,16 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
 
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok, int32_t *counts,
                  int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list, int32_t *gemm_list,
-                 int32_t *single_list, int32_t *tile_prefix, GroupMeta *meta, int *status, void *stream) {
+                 int32_t *single_list, int32_t *tile_prefix, int32_t *small_pos, GroupMeta *meta, int *status,
+                 void *stream) {
     const int P = T * k;
     const size_t smem = (static_cast<size_t>(kGroupWarps) * E + 32) * sizeof(int);
     static int seen[64];
     const int err = ensure_smem(reinterpret_cast<const void *>(group_kernel), static_cast<int>(smem), seen);
     if (err) return err;
     group_kernel<<<1, kGroupThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        idx, P, E, gemm_min, tc_ok, counts, offsets, perm, inv, gemv_list, gemm_list, single_list, tile_prefix, meta,
-        status);
+        idx, P, E, gemm_min, tc_ok, counts, offsets, perm, inv, gemv_list, gemm_list, single_list, tile_prefix,
+        small_pos, meta, status);
     return static_cast<int>(cudaGetLastError());
 }
 

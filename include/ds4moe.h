@@ -60,8 +60,10 @@ enum ds4moe_matrix { DS4MOE_GATE = 0, DS4MOE_UP = 1, DS4MOE_DOWN = 2 };
 /* Options of a weights handle, for ds4moe_set_option(). */
 enum ds4moe_option {
     /* Expert groups with at least this many tokens run on the tcgen05 tensor-core path;
-     * smaller groups run on the fused dequant-GEMV kernels (one-token groups on the
-     * single-token kernels). 0 means never use tensor cores; 1 means always. Default 2. */
+     * smaller groups run on the small-group kernels (DS4MOE_OPT_SMALL_GROUPS) or on the fused
+     * dequant-GEMV kernels. 0 means never use tensor cores; 1 means always; -1 (the default)
+     * chooses: with the small-group kernels, no tensor cores for calls of at most 64 tokens
+     * and 7 above that; without them, 2. */
     DS4MOE_OPT_GEMM_MIN_TOKENS = 0,
     /* Same threshold for the bf16 shared expert (by token count T). Default 2. */
     DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS = 1,
@@ -73,7 +75,13 @@ enum ds4moe_option {
      * Default 1. */
     DS4MOE_OPT_SINGLE_STEP = 3,
     /* 1: the single-token kernel records per-CTA timestamps, read by ds4moe_step_trace(). */
-    DS4MOE_OPT_TRACE = 4
+    DS4MOE_OPT_TRACE = 4,
+    /* 1: expert groups below the tensor-core threshold run on the small-group kernels, which
+     * decode each 2-bit weight group once for all the tokens of its group (up to 6 at a time)
+     * and take the down projection pair by pair; used when d_model <= 4096 and d_ff <= 2048
+     * and the bf16 shared expert, if any, is on the tensor cores (or T = 1). 0: the fused
+     * dequant-GEMV kernels. Default 1. */
+    DS4MOE_OPT_SMALL_GROUPS = 5
 };
 
 /* Stages of ds4moe_expert_ffn, in launch order (indices into ds4moe_stats.stage_ms). */

@@ -69,9 +69,10 @@ def test_group_one_expert_takes_all(ds4):
 
 # ---------------------------------------------------------------- device dequantisation
 
-def test_device_dequant_bitexact(ds4):
+@pytest.mark.parametrize("D,F", [(512, 768), (768, 512)])   # even and odd blocks per row (chunk permutation)
+def test_device_dequant_bitexact(ds4, D, F):
     import torch
-    wl = synth.Workload("dq", T=1, D=512, F=768, E=3, k=1, seed=11)
+    wl = synth.Workload("dq", T=1, D=D, F=F, E=3, k=1, seed=11)
     lay = Layer(wl, quantized=False, experts=range(3))
     lay.gate[1] = oracle.quantize_iq2(synth.expert_weight(5, 1, synth.GATE, wl.F, wl.D))
     lay.down[1] = oracle.quantize_q2k(synth.expert_weight(5, 1, synth.DOWN, wl.D, wl.F))
@@ -191,6 +192,55 @@ def test_ffn_tensor_core_reports_fp16_overflow(ds4):
     ds4.ds4moe_expert_ffn(x, W, torch.from_numpy(lay.L).cuda(), wl.k, out)
     assert ds4.ds4moe_last_status(W) == 0
     W.close()
+
+
+# ---------------------------------------------------------------- the small-group kernels
+
+# (T, D, F, E, k, shared, small_groups, tokens): groups of up to ~30 tokens (chunks of 6), odd
+# block counts (D = 2304: 9 blocks per row, F = 1280: 80 gate/up tiles), the bf16 shared expert on
+# tcgen05 beside them, and the same layer on the fused GEMV kernels for comparison.
+@pytest.mark.parametrize("T,D,F,E,k,shared,sg,tokens", [
+    (4, 256, 256, 8, 2, False, 1, None),
+    (45, 1024, 512, 6, 4, True, 1, None),
+    (45, 1024, 512, 6, 4, True, 0, None),
+    (13, 2304, 1280, 16, 5, False, 1, None),
+    (48, 4096, 2048, 24, 6, True, 1, [0, 17, 47]),
+])
+def test_small_group_kernels_match_oracle(ds4, T, D, F, E, k, shared, sg, tokens):
+    wl = synth.Workload("sg", T=T, D=D, F=F, E=E, k=k, seed=T + D + F, bias=("normal", 0.5), shared=shared)
+    lay = Layer(wl, quantized=D * F <= 1024 * 512)
+    W = lay.upload(ds4)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SMALL_GROUPS, sg)
+    got = lay.run(ds4, W)
+    again = lay.run(ds4, W)
+    W.close()
+    assert np.array_equal(got.view(np.uint32), again.view(np.uint32))   # deterministic
+    ref, _, _ = lay.oracle_delta(tokens=tokens)
+    err = norm_max_err(got if tokens is None else got[tokens], ref)
+    assert err <= FFN_TOL, err
+
+
+def test_small_groups_beside_tensor_core_groups(ds4):
+    # more than 64 tokens: groups of at least 7 tokens on tcgen05, the rest on the small-group kernels
+    wl = synth.Workload("sgmix", T=200, D=1024, F=512, E=32, k=4, seed=23, bias=("zipf", 1.0))
+    L, _ = synth.draw_inputs(wl)
+    counts = np.bincount(oracle.route(L, wl.k)[0].reshape(-1), minlength=wl.E)
+    assert (counts >= 7).any() and ((counts > 0) & (counts < 7)).any()
+    err = _ffn_case(ds4, wl, quantized=False)
+    assert err <= FFN_TOL, err
+
+
+def test_small_groups_at_one_token_without_the_fused_kernel(ds4):
+    # T = 1 on the separate kernels: the routed experts on the small-group kernels, the shared
+    # expert on the single-token decode kernels
+    wl = synth.Workload("sg1", T=1, D=2048, F=2048, E=64, k=6, seed=31, shared=True)
+    lay = Layer(wl, quantized=False)
+    W = lay.upload(ds4)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SINGLE_STEP, 0)
+    got = lay.run(ds4, W)
+    W.close()
+    ref, _, _ = lay.oracle_delta()
+    assert norm_max_err(got, ref) <= FFN_TOL
 
 
 # ---------------------------------------------------------------- the single-token kernel
