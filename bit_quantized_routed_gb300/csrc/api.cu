@@ -373,6 +373,12 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     // The small-group kernels take every routed group below the threshold; the shared expert
     // must then be on the tensor cores, or (T = 1) on the single-token decode kernels.
     const bool sg = sg_fits && (!w.has_shared || shared_tc || T == 1);
+    // With few tokens the shared expert's gate/up runs on its own warp-MMA kernel (one CTA per 16
+    // rows) and only its down projection on the tensor-core kernel.
+    // (Not when the caller forces everything onto the tensor cores with a threshold of 1.)
+    const bool shared_up_small = sg && shared_tc && T <= shared_small_max_tokens() && h->gemm_min_tokens != 1 &&
+                                 h->shared_gemm_min_tokens != 1;
+    const bool up_tc = gemm_min > 0 || (shared_tc && !shared_up_small);
     int rc = clk.stage(DS4MOE_STAGE_ROUTE);
     if (!rc) rc = launch_route(logits, T, w.E, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
     if (!rc) rc = clk.stage(DS4MOE_STAGE_GROUP);
@@ -380,9 +386,9 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         rc = launch_group(ws.topk_idx, T, k, w.E, gemm_min, w.tc_ok, ws.counts, ws.offsets, ws.perm, ws.inv,
                           ws.gemv_list, ws.gemm_list, sg ? nullptr : ws.single_list, ws.tile_prefix,
                           sg ? ws.small_pos : nullptr, ws.meta, ws.status, stream);
-    if (any_tc) {
+    if (up_tc) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_GATHER);
-        if (!rc) rc = launch_gather(w, ws, x, T, k, gemm_min, shared_tc, stream);
+        if (!rc) rc = launch_gather(w, ws, x, T, k, gemm_min, shared_tc && !shared_up_small, stream);
     }
     // Without the small-group kernels: one-token groups (every group at T = 1) run on the
     // decode kernels; groups of 2 .. gemm_min-1 tokens on the multi-token GEMV kernels, which
@@ -406,9 +412,14 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         if (!rc) rc = launch_gemv_up(w, ws, x, T, k, shared_multi, stream);
         h->launches++;
     }
-    if (any_tc) {
+    if (shared_up_small) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMM);
-        if (!rc) rc = launch_gemm_up(w, ws, h->tmap_x16, T, k, shared_tc, stream);
+        if (!rc) rc = launch_shared_up_small(w, ws, x, T, k, stream);
+    }
+    if (up_tc) {
+        if (!rc && !shared_up_small) rc = clk.stage(DS4MOE_STAGE_UP_GEMM);
+        else h->launches++;
+        if (!rc) rc = launch_gemm_up(w, ws, h->tmap_x16, T, k, shared_tc && !shared_up_small, stream);
     }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMV);
     if (sg) {

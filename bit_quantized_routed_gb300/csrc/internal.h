@@ -171,6 +171,9 @@ bool small_groups_supported(const DeviceWeights &w);
 int launch_prep_x(const Workspace &ws, const uint16_t *x, int T, int D, void *stream);
 int launch_small_up(const DeviceWeights &w, const Workspace &ws, int T, int k, void *stream);
 int launch_small_down(const DeviceWeights &w, const Workspace &ws, int T, int k, void *stream);
+int shared_small_max_tokens();
+int launch_shared_up_small(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
+                           void *stream);
 int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, int gemm_min,
                   bool shared, void *stream);
 int launch_gemm_up(const DeviceWeights &w, const Workspace &ws, const void *tmap_x16, int T, int k, bool shared,

@@ -201,6 +201,7 @@ def test_ffn_tensor_core_reports_fp16_overflow(ds4):
 # tcgen05 beside them, and the same layer on the fused GEMV kernels for comparison.
 @pytest.mark.parametrize("T,D,F,E,k,shared,sg,tokens", [
     (4, 256, 256, 8, 2, False, 1, None),
+    (9, 512, 256, 4, 2, True, 1, None),
     (45, 1024, 512, 6, 4, True, 1, None),
     (45, 1024, 512, 6, 4, True, 0, None),
     (13, 2304, 1280, 16, 5, False, 1, None),
