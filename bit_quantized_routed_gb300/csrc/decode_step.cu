@@ -12,10 +12,11 @@
 //     warp reads its part of a stage into registers and frees the stage before the arithmetic;
 //   * every CTA (one per SM) routes the token itself -- top-k of the router logits, ties to the
 //     lower index -- so no launch or barrier separates routing from the experts;
-//   * gate/up (phase 1): each compute warp owns one 1024-column quarter of x, 32 columns per
-//     lane held in registers as int16 with a power-of-two scale (2^14 over the quarter's absolute
-//     maximum), and the 16 rows of a unit are spread over the warps (4 rows per warp when x has
-//     four quarters). An IQ2-style group of 8 weights is one 32-bit codebook word of nibbles
+//   * gate/up (phase 1): x is held in the table as int16 with a power-of-two scale per 1024-column
+//     quarter (2^14 over the quarter's absolute maximum), as the pairs dp2a reads; lane l of every
+//     compute warp owns row l & 15 of a unit's gate and up and a strided set of its 16-byte chunks,
+//     so a unit ends with one shuffle and one store per lane (the finisher sums the warps).
+//     An IQ2-style group of 8 weights is one 32-bit codebook word of nibbles
 //     (m - 1, which is even; elements 0, 2, 4, 6 in the low nibbles, 1, 3, 5, 7 in the high ones)
 //     and one 32-bit sign word of nibbles, 0x9 (keep) or 0x7 (negate): their XOR is, per nibble,
 //     the signed weight plus 8 (m-1 ^ 9 = m + 8, m-1 ^ 7 = 8 - m, no carries). Two masks give
@@ -37,6 +38,7 @@
 // The kernel is launched cooperatively, so all CTAs are resident together at the grid barrier.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -59,18 +61,25 @@ constexpr int kLead = 4;     // shared-expert units streamed before the first ro
 constexpr int kMaxD = 4096;
 // Shared memory: [ring: kStages x kStageBytes][table: 256 slots of 256 bytes][barriers, scratch].
 // Slot e holds codebook entry e in its first 128 bytes (one u32 replica per lane), and in its
-// second 128 bytes sign entry e (e < 128, one replica per lane) or, for e >= 128, four pairs of
-// fp32 x quads for the shared expert. A codebook byte offset is then lane * 4 | index << 8: one
-// byte_perm builds it, and the table's base folds into the load.
+// second 128 bytes: sign entry e (e < 128, one replica per lane); for 128 <= e < 192, x as int16
+// dp2a pairs, 16 bytes per 8-column group, the 8 groups of 16-byte weight chunk q = e - 128 (two
+// 32-column sub-blocks); for e >= 192, x in bf16 for the shared expert, 8-column group g in slot
+// 192 + g / 8. A codebook byte offset is then lane * 4 | index << 8: one byte_perm builds it, and
+// the table's base folds into the load.
 constexpr int kTabOff = kStages * kStageBytes;
 constexpr int kTabBytes = 256 * 256;
 constexpr int kMiscOff = kTabOff + kTabBytes;
-constexpr int kSmemBytes = kMiscOff + 2048;
+constexpr int kRedBuf = kCompute * 32;  // floats of one unit's partial sums (routed: one per lane and warp)
+constexpr int kMaxSharedUnits = 16;     // shared-expert units of one CTA (their partial sums wait in smem)
+// misc: mbarriers (14 slots), sidx[8], sgw[8], quarter scales of x[4], x8[128], red[2][kRedBuf],
+// shared-unit partials [kMaxSharedUnits][kCompute][4], abort flag
+constexpr int kSmemBytes = kMiscOff + 112 + 32 + 32 + 16 + 512 + 2 * kRedBuf * 4 + kMaxSharedUnits * kCompute * 16 + 64;
 static_assert(kTabOff % 256 == 0, "table slots are 256-byte aligned");
-static_assert(kMaxD / 8 <= 128 * 4, "x pairs fit the second halves of slots 128..255");
+static_assert(kMaxD / 8 <= 64 * 8, "x (int16 and bf16) fits the second halves of slots 128..255");
 
-// Byte offset in the table of the fp32 x pair (columns 8q .. 8q+7) of the shared expert.
-__host__ __device__ constexpr int xpair_offset(int q) { return (128 + (q >> 2)) * 256 + 128 + (q & 3) * 32; }
+// Byte offsets in the table of 8-column group g of x: int16 dp2a pairs, and bf16.
+__host__ __device__ constexpr int xq_offset(int g) { return (128 + (g >> 3)) * 256 + 128 + (g & 7) * 16; }
+__host__ __device__ constexpr int xb_offset(int g) { return (192 + (g >> 3)) * 256 + 128 + (g & 7) * 16; }
 
 // Named barriers (0 is __syncthreads). The per-unit hand-off between the compute warps and the
 // finisher goes through mbarriers instead, so that no compute warp waits for another one.
@@ -108,14 +117,31 @@ __device__ __forceinline__ int count_of(int n) {
     return n > b ? (n - 1 - b) / g + 1 : 0;
 }
 
+// A routed unit costs about kRoutedCost shared units of compute. The shared units are split into
+// contiguous ranges in proportion to what each CTA's routed units (blockIdx.x + i * gridDim.x, so
+// the first nr % G CTAs have one more) leave of an even share of the total; in closed form, so
+// every thread computes its CTA's range [s0, s1) at once.
+constexpr int kRoutedCost = 3;
+// 32-bit arithmetic: the host admits a shape only if ns * G * (kRoutedCost * nr + ns) < 2^31.
+__host__ __device__ inline unsigned shared_capacity_before(unsigned c, unsigned G, unsigned ns, unsigned nr) {
+    const unsigned A = kRoutedCost * nr + ns, q = nr / G, rem = nr % G;
+    return c * A - kRoutedCost * G * (c * q + (c < rem ? c : rem));
+}
+__host__ __device__ inline void shared_range(unsigned b, unsigned G, unsigned ns, unsigned nr, int *s0, int *s1) {
+    const unsigned all = G * ns;  // shared_capacity_before(G)
+    *s0 = all > 0 ? static_cast<int>(ns * shared_capacity_before(b, G, ns, nr) / all) : 0;
+    *s1 = all > 0 ? static_cast<int>(ns * shared_capacity_before(b + 1, G, ns, nr) / all) : 0;
+}
+
 // Order of one CTA's gate/up units: kLead shared-expert units, then routed and shared
-// alternately, then what remains. Unit indices are blockIdx.x + i * gridDim.x within each kind.
+// alternately, then what remains. Routed units are blockIdx.x + i * gridDim.x; the CTA's shared
+// units are the contiguous range s0 .. s0+ns-1 (shared_range).
 struct Seq1 {
-    int ts, tr, ns, nr;
+    int ts, tr, ns, nr, s0;
     __device__ bool next(bool &shared, int &unit) {
         if (ts < ns && (tr >= nr || ts < kLead + tr)) {
             shared = true;
-            unit = static_cast<int>(blockIdx.x) + ts++ * static_cast<int>(gridDim.x);
+            unit = s0 + ts++;
             return true;
         }
         if (tr < nr) {
@@ -130,19 +156,15 @@ struct Seq1 {
 __device__ __forceinline__ Seq1 seq1_of(const StepParams &p) {
     Seq1 s;
     s.ts = s.tr = 0;
-    s.ns = p.w.has_shared ? count_of(p.w.F / kRowsSh) : 0;
-    s.nr = count_of(p.k * (p.w.F / kRows1));
+    const int nr = p.k * (p.w.F / kRows1);
+    int s0 = 0, s1 = 0;
+    shared_range(blockIdx.x, gridDim.x, p.w.has_shared ? p.w.F / kRowsSh : 0, nr, &s0, &s1);
+    s.s0 = s0;
+    s.ns = s1 - s0;
+    s.nr = count_of(nr);
     return s;
 }
 
-// Sums two per-lane values over the warp; afterwards lane l holds the total of value (l >> 4) & 1.
-__device__ __forceinline__ float reduce2(float v0, float v1, int lane) {
-    const bool u16 = lane & 16;
-    float c = (u16 ? v1 : v0) + __shfl_xor_sync(0xffffffffu, u16 ? v0 : v1, 16);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    return c;
-}
 
 // Sums four per-lane values over the warp; afterwards lane l holds the total of value (l >> 3) & 3.
 __device__ __forceinline__ float reduce4(float v0, float v1, float v2, float v3, int lane) {
@@ -320,30 +342,30 @@ __device__ void route_sorted8(const StepParams &p, int lane, int *sidx, float *s
     }
 }
 
-// One IQ2-style 32-weight sub-block of a row dotted with the lane's 32 x values: xr holds per
-// group g the int16 pairs (x0,x2), (x4,x6), (x1,x3), (x5,x7) of its 8 columns, x8 = 8 * the sum
-// of the 32 values; q = the sub-block's 4 codebook indices and its sign/scale word, ds = the
-// block's d times the x factor / 16; tab = the table, lane4 = 4 * lane.
-__device__ __forceinline__ float iq2_sub(uint2 q, float ds, const uint32_t *xr, int x8, const uint8_t *tab,
-                                         uint32_t lane4) {
-    int ce = -x8, co = 0;  // even and odd elements; the offset of 8 per weight removed up front
+// One IQ2-style 32-weight sub-block of a gate row and of an up row dotted with x: xb holds the
+// sub-block's four 8-column groups as int16 pairs (x0,x2), (x4,x6), (x1,x3), (x5,x7), 16 bytes each,
+// x8 = 8 * the sum of its 32 values; qg/qu = the rows' 4 codebook indices and sign/scale words;
+// dg/du = the blocks' d times the x factor / 16; tab = the table, lane4 = 4 * lane.
+__device__ __forceinline__ void iq2_sub2(uint2 qg, uint2 qu, float dg, float du, const uint8_t *xb, int x8,
+                                         const uint8_t *tab, uint32_t lane4, float &pg, float &pu) {
+    int ceg = -x8, cog = 0, ceu = -x8, cou = 0;  // even and odd elements; the offset of 8 removed up front
 #pragma unroll
     for (int g = 0; g < 4; g++) {
-        // codebook entry q.x byte g: offset lane4 | index << 8; sign entry (7 bits at 7g of q.y):
-        // offset lane4 | 128 | signs << 8
-        const uint32_t og = iq2_cb_off(q.x, g, lane4), os = iq2_sg_off(q.y, g, lane4);
-        const uint32_t gv = *reinterpret_cast<const uint32_t *>(tab + og);
-        const uint32_t sv = *reinterpret_cast<const uint32_t *>(tab + os);
-        const uint32_t ev = (gv ^ sv) & 0x0F0F0F0Fu;  // weights 0, 2, 4, 6 plus 8, as bytes
-        const uint32_t od = (gv ^ sv) & 0xF0F0F0F0u;  // 16 x (weights 1, 3, 5, 7 plus 8)
-        const uint32_t *xv = xr + 4 * g;
-        ce = dp2a_hi_su(xv[1], ev, dp2a_lo_su(xv[0], ev, ce));
-        co = dp2a_hi_su(xv[3], od, dp2a_lo_su(xv[2], od, co));
+        const uint32_t gvg = *reinterpret_cast<const uint32_t *>(tab + iq2_cb_off(qg.x, g, lane4));
+        const uint32_t svg = *reinterpret_cast<const uint32_t *>(tab + iq2_sg_off(qg.y, g, lane4));
+        const uint32_t gvu = *reinterpret_cast<const uint32_t *>(tab + iq2_cb_off(qu.x, g, lane4));
+        const uint32_t svu = *reinterpret_cast<const uint32_t *>(tab + iq2_sg_off(qu.y, g, lane4));
+        const uint32_t evg = (gvg ^ svg) & 0x0F0F0F0Fu, odg = (gvg ^ svg) & 0xF0F0F0F0u;
+        const uint32_t evu = (gvu ^ svu) & 0x0F0F0F0Fu, odu = (gvu ^ svu) & 0xF0F0F0F0u;
+        const uint4 xv = *reinterpret_cast<const uint4 *>(xb + 16 * g);
+        ceg = dp2a_hi_su(xv.y, evg, dp2a_lo_su(xv.x, evg, ceg));
+        cog = dp2a_hi_su(xv.w, odg, dp2a_lo_su(xv.z, odg, cog));
+        ceu = dp2a_hi_su(xv.y, evu, dp2a_lo_su(xv.x, evu, ceu));
+        cou = dp2a_hi_su(xv.w, odu, dp2a_lo_su(xv.z, odu, cou));
     }
-    // the odd sum is a multiple of 16: the shift is exact
-    const int tot = ce + (co >> 4);
-    const float s1 = small_int_to_float(static_cast<int>((q.y >> 28) + 1u));  // sub-block scale s + 1
-    return ds * s1 * small_int_to_float(tot);
+    // the odd sums are multiples of 16: the shifts are exact; (s + 1) is each row's sub-block scale
+    pg = fmaf(dg * small_int_to_float(static_cast<int>((qg.y >> 28) + 1u)), small_int_to_float(ceg + (cog >> 4)), pg);
+    pu = fmaf(du * small_int_to_float(static_cast<int>((qu.y >> 28) + 1u)), small_int_to_float(ceu + (cou >> 4)), pu);
 }
 
 __device__ __forceinline__ float dot8_bf16(uint4 w, float4 xa, float4 xb, float acc) {
@@ -383,8 +405,6 @@ __device__ bool grid_barrier(unsigned long long *count, int *status) {
 // NQ: 1024-column quarters of x (1, 2 or 4); each compute warp holds one of them in registers.
 template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) {
-    constexpr int RG = kCompute / NQ;  // row groups
-    constexpr int RPW = kRows1 / RG;   // rows of a unit per warp (NQ)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // fixed offsets from the symbol, so that the table's base folds into its loads
     uint8_t *smem = smem_raw;
@@ -394,8 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kMiscOff);
     int *sidx = reinterpret_cast<int *>(bars + 2 * kStages + 6);             // [8]
     float *sgw = reinterpret_cast<float *>(sidx + 8);                         // [8]
-    float *red = sgw + 8;                                                     // [2][128]
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 256);
+    float *xsc = sgw + 8;                                                     // [4] x factor of each quarter
+    int *x8s = reinterpret_cast<int *>(xsc + 4);                              // [kMaxD / 32]
+    float *red = reinterpret_cast<float *>(x8s + kMaxD / 32);                 // [2][kRedBuf]
+    float *sacc = red + 2 * kRedBuf;                                          // [kMaxSharedUnits][kCompute][4]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sacc + kMaxSharedUnits * kCompute * 4);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t route_bar = smem_u32(bars + 2 * kStages);
     // rfull[b]: the 16 compute warps have written a unit's partial sums into red[b];
@@ -487,32 +510,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
         bool shared;
         int unit;
         while (q.next(shared, unit)) {
+            if (shared) continue;  // the compute warps finish the shared units themselves
             const int buf = it & 1;
-            const float *rb = red + buf * 128;
+            const float *rb = red + buf * kRedBuf;
             wait_phase(rfull + 8 * buf, static_cast<uint32_t>(it >> 1) & 1u, abort_flag, p.status);
-            if (shared) {
-                if (lane < kRowsSh) {
-                    float g = 0.0f, u = 0.0f;
-#pragma unroll
-                    for (int ww = 0; ww < kCompute; ww++) {
-                        g += rb[ww * 4 + 2 * lane];
-                        u += rb[ww * 4 + 2 * lane + 1];
-                    }
-                    p.hsh[unit * kRowsSh + lane] = swiglu(g, u);
-                }
-            } else {
-                // lane r < 16: row r of the unit = column r of one down sub-block
+            {
+                // lane r < 16: row r of the unit = column r of one down sub-block; the warps wrote
+                // gate row r in lane r and up row r in lane 16 + r
                 const int per = F / kRows1, slot = unit / per, row0 = (unit % per) * kRows1;
-                float hv = 0.0f;
-                if (lane < kRows1) {
-                    float g = 0.0f, u = 0.0f;
+                float v = 0.0f;
 #pragma unroll
-                    for (int qx = 0; qx < NQ; qx++) {
-                        g += rb[(lane * NQ + qx) * 2];
-                        u += rb[(lane * NQ + qx) * 2 + 1];
-                    }
-                    hv = swiglu(g, u);
-                }
+                for (int ww = 0; ww < kCompute; ww++) v += rb[ww * 32 + lane];
+                const float u = __shfl_down_sync(0xffffffffu, v, 16);
+                const float hv = lane < kRows1 ? swiglu(v, u) : 0.0f;
                 float m = fabsf(hv), sum = hv;
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) {
@@ -539,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
         bar_sync(kBarAll, kNAll);  // this CTA's h is written
         for (int u = blockIdx.x; u < n2; u += gridDim.x, it++) {
             const int buf = it & 1;
-            const float *rb = red + buf * 128;
+            const float *rb = red + buf * kRedBuf;
             wait_phase(rfull + 8 * buf, static_cast<uint32_t>(it >> 1) & 1u, abort_flag, p.status);
             if (lane < kRows2) {
                 float s = 0.0f;
@@ -568,14 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
     for (int j = 0; j < 16; j++) graw[j] = __ldg(reinterpret_cast<const uint2 *>(p.grid) + warp + 16 * j);
     const bool xfq = tid < D / 8;
     const uint4 xv = xfq ? __ldg(reinterpret_cast<const uint4 *>(p.x) + tid) : make_uint4(0, 0, 0, 0);
-    // fp32 x for the bf16 shared expert (D <= 8 * kNCompute)
-    if (xfq) {
-        float4 *xp = reinterpret_cast<float4 *>(tab + xpair_offset(tid));
-        xp[0] = make_float4(bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y));
-        xp[1] = make_float4(bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w));
-    }
-    // int16 x in registers with the quarter's power-of-two scale, per group the pairs
-    // (x0,x2), (x4,x6), (x1,x3), (x5,x7); x8 = 8 * their sum
+    // bf16 x for the shared expert: thread tid stores group tid (D <= 8 * kNCompute)
+    if (xfq) *reinterpret_cast<uint4 *>(tab + xb_offset(tid)) = xv;
+    // int16 x with the quarter's power-of-two scale, per group the pairs (x0,x2), (x4,x6), (x1,x3),
+    // (x5,x7); x8 = 8 * their sum. The warps of the first row group store it for the routed units.
     uint32_t xr[16];
     float xinv;
     int x8 = 0;
@@ -612,6 +618,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
         }
         x8 *= 8;
     }
+    if (rg == 0 && cval) {  // lane: sub-block c = 4 groups of int16 x, their sum, the quarter's factor
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            *reinterpret_cast<uint4 *>(tab + xq_offset(4 * c + j)) = make_uint4(xr[4 * j], xr[4 * j + 1], xr[4 * j + 2], xr[4 * j + 3]);
+        x8s[c] = x8;
+        if (lane == 0) xsc[qx] = xinv;
+    }
     iq2_table_store(tab, graw, warp, lane);  // codebook and sign words, one replica per lane
     bar_sync(kBarCompute, kNCompute);
     if (tr) tr[1] = now_ns();
@@ -633,15 +646,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
     // ---------------------------------------------------------------- phase 1: gate/up
     const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
     const int swm = iq2_swz(w, 15);  // chunk permutation mask of the tiles' rows (iq2_swz)
-    int rc = 0;
+    int rc = 0;  // ring position: units of both phases
+    int hc = 0;  // hand-offs to the finisher: routed units, then down units
     {
         Seq1 q = seq0;
         bool shared;
         int unit;
         while (q.next(shared, unit)) {
             const int it = rc++;
-            const int buf = it & 1;
-            float *rb = red + buf * 128;
             const uint8_t *st = wait_stage(it);
             if (shared) {
                 // two bf16 rows of gate and up; thread tid takes columns 8*tid .. +7 (D <= 8 * kNCompute).
@@ -661,48 +673,66 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
                     }
                     release_stage(it);
                     if (qv) {
-                        const float4 *xp = reinterpret_cast<const float4 *>(tab + xpair_offset(tid));
-                        const float4 xa = xp[0], xb = xp[1];
+                        const uint4 xw = *reinterpret_cast<const uint4 *>(tab + xb_offset(tid));
+                        const float4 xa = make_float4(bf16_lo(xw.x), bf16_hi(xw.x), bf16_lo(xw.y), bf16_hi(xw.y));
+                        const float4 xb = make_float4(bf16_lo(xw.z), bf16_hi(xw.z), bf16_lo(xw.w), bf16_hi(xw.w));
                         g0 = dot8_bf16(wv[0], xa, xb, g0);
                         g1 = dot8_bf16(wv[1], xa, xb, g1);
                         u0 = dot8_bf16(wv[2], xa, xb, u0);
                         u1 = dot8_bf16(wv[3], xa, xb, u1);
                     }
                 }
+                // no hand-off: the warp's sums wait in shared memory until the end of the phase
                 const float v = reduce4(g0, u0, g1, u1, lane);
-                if (it >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((it >> 1) - 1) & 1u, abort_flag, p.status);
-                if ((lane & 7) == 0) rb[warp * 4 + (lane >> 3)] = v;
+                if ((lane & 7) == 0) sacc[((q.ts - 1) * kCompute + warp) * 4 + (lane >> 3)] = v;
             } else {
-                // rows rg + i * RG of the unit, i < RPW, one at a time (a short loop body keeps the
-                // hot code small): the row's gate and up sub-block c, summed over the warp into
-                // red; the stage is released after the last row
-                if (it >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((it >> 1) - 1) & 1u, abort_flag, p.status);
+                const int buf = hc & 1;
+                float *rb = red + buf * kRedBuf;
+                // lane l owns row l & 15 of the unit's gate and up and, of each row, the 16-byte chunks
+                // q = 2 * warp + (l >> 4) + 32 i (two 32-weight sub-blocks each): it decodes whole
+                // groups of its rows with x read from the table (half-warp broadcasts), so a unit
+                // needs one shuffle and one store per lane instead of a reduction per row
+                if (hc >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((hc >> 1) - 1) & 1u, abort_flag, p.status);
+                float pg = 0.0f, pu = 0.0f;
                 if (st) {
-                    const uint8_t *gq = st, *uq = st + kRows1 * nbD * 64;
-                    const uint16_t *gd = reinterpret_cast<const uint16_t *>(st + 2 * kRows1 * nbD * 64);
-                    const uint16_t *ud = gd + kRows1 * nbD;
+                    const int r = lane & 15, rowb = nbD * 64, sw = r & swm;
+                    const uint8_t *rgp = st + r * rowb, *rup = st + (kRows1 + r) * rowb;
+                    const uint16_t *dgp = reinterpret_cast<const uint16_t *>(st + 2 * kRows1 * rowb) + r * nbD;
+                    const uint16_t *dup = dgp + kRows1 * nbD;
 #pragma unroll 1
-                    for (int i = 0; i < RPW; i++) {
-                        const int rl = rg + i * RG;
-                        float pg = 0.0f, pu = 0.0f;
-                        if (cval) {
-                            // sub-block c is half c & 1 of the row's chunk c >> 1, stored at (c >> 1) ^ swizzle
-                            const int cb = rl * nbD * 64 + (((c >> 1) ^ (rl & swm)) << 4) + ((c & 1) << 3);
-                            const uint2 qg = *reinterpret_cast<const uint2 *>(gq + cb);
-                            const uint2 qu = *reinterpret_cast<const uint2 *>(uq + cb);
-                            const float dg = f16_to_f32(gd[rl * nbD + (c >> 3)]) * xinv;
-                            const float du = f16_to_f32(ud[rl * nbD + (c >> 3)]) * xinv;
-                            pg = iq2_sub(qg, dg, xr, x8, tab, lane4);
-                            pu = iq2_sub(qu, du, xr, x8, tab, lane4);
-                        }
-                        const float v = reduce2(pg, pu, lane);  // lane 0: gate, lane 16: up
-                        if ((lane & 15) == 0) rb[(rl * NQ + qx) * 2 + (lane >> 4)] = v;
+                    for (int q = 2 * warp + (lane >> 4); q < 4 * nbD; q += 2 * kCompute) {
+                        const uint4 qg4 = *reinterpret_cast<const uint4 *>(rgp + ((q ^ sw) << 4));
+                        const uint4 qu4 = *reinterpret_cast<const uint4 *>(rup + ((q ^ sw) << 4));
+                        const float xf = xsc[q >> 4];  // the quarter's x factor (1024 columns = 16 chunks)
+                        const float dg = f16_to_f32(dgp[q >> 2]) * xf, du = f16_to_f32(dup[q >> 2]) * xf;
+                        const uint8_t *xb = tab + xq_offset(8 * q);  // groups 8q .. 8q+7, 128 contiguous bytes
+                        iq2_sub2(make_uint2(qg4.x, qg4.y), make_uint2(qu4.x, qu4.y), dg, du, xb, x8s[2 * q], tab,
+                                 lane4, pg, pu);
+                        iq2_sub2(make_uint2(qg4.z, qg4.w), make_uint2(qu4.z, qu4.w), dg, du, xb + 64, x8s[2 * q + 1],
+                                 tab, lane4, pg, pu);
                     }
                     release_stage(it);
                 }
+                pg += __shfl_xor_sync(0xffffffffu, pg, 16);  // the row's two column halves
+                pu += __shfl_xor_sync(0xffffffffu, pu, 16);
+                rb[warp * 32 + lane] = (lane & 16) ? pu : pg;  // lanes 0-15 gate, 16-31 up
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rfull + 8 * buf);
+                hc++;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(rfull + 8 * buf);
+        }
+        // the CTA's shared-expert units: per row, the 16 warps' gate and up sums, then SwiGLU
+        bar_sync(kBarCompute, kNCompute);
+        const int nsu = q.ns;
+        for (int i = tid; i < nsu * kRowsSh; i += kNCompute) {
+            const int j = i / kRowsSh, r = i % kRowsSh;
+            float g = 0.0f, u = 0.0f;
+#pragma unroll
+            for (int ww = 0; ww < kCompute; ww++) {
+                g += sacc[(j * kCompute + ww) * 4 + 2 * r];
+                u += sacc[(j * kCompute + ww) * 4 + 2 * r + 1];
+            }
+            p.hsh[(q.s0 + j) * kRowsSh + r] = swiglu(g, u);
         }
     }
 
@@ -749,9 +779,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
     const int blk_off = s2 * tb + (j2 >> 3) * 80, dd_off = s2 * tb + kRows2 * nbF * 80 + (j2 >> 3) * 4;
     const int sh_off = p.k * tb + 8 * tid;
     for (int u = blockIdx.x; u < n2; u += gridDim.x) {
-        const int r0 = rc++;  // ring position = hand-off counter (units of both phases)
-        const int buf = r0 & 1;
-        float *rb = red + buf * 128;
+        const int r0 = rc++;   // ring position
+        const int hcur = hc++;  // hand-off to the finisher
+        const int buf = hcur & 1;
+        float *rb = red + buf * kRedBuf;
         const uint8_t *st = wait_stage(r0);
         float acc[kRows2] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (st) {
@@ -791,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
             }
         }
         const float v = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
-        if (r0 >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((r0 >> 1) - 1) & 1u, abort_flag, p.status);
+        if (hcur >= 2) wait_phase(rempty + 8 * buf, static_cast<uint32_t>((hcur >> 1) - 1) & 1u, abort_flag, p.status);
         if ((lane & 7) == 0) rb[warp * 4 + (lane >> 3)] = v;
         __syncwarp();
         if (lane == 0) mbar_arrive(rfull + 8 * buf);
@@ -820,7 +851,18 @@ bool decode_step_supported(const DeviceWeights &w, int k) {
     if (static_cast<size_t>(kRows1) * w.nbD * 132 > kStageBytes) return false;
     if (w.has_shared && static_cast<size_t>(kRowsSh) * 2 * w.D * 2 > kStageBytes) return false;
     const size_t down = static_cast<size_t>(k) * kRows2 * w.nbF * 84 + (w.has_shared ? kRows2 * w.F * 2 : 0);
-    return down <= kStageBytes;
+    if (down > kStageBytes) return false;
+    // every CTA's share of shared-expert units is non-negative and fits the partials area
+    const unsigned G = n_sms();
+    const unsigned ns = w.has_shared ? w.F / kRowsSh : 0, nr = k * (w.F / kRows1);
+    if (static_cast<unsigned long long>(ns) * G * (kRoutedCost * nr + ns) >= (1ull << 31)) return false;
+    if (ns > 0 && kRoutedCost * G * (nr / G + 1) > kRoutedCost * nr + ns) return false;  // every share >= 0
+    for (unsigned c = 0; c < G; c++) {
+        int s0 = 0, s1 = 0;
+        shared_range(c, G, ns, nr, &s0, &s1);
+        if (s1 - s0 > kMaxSharedUnits) return false;
+    }
+    return true;
 }
 
 int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, const float *logits, int k,
