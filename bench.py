@@ -161,6 +161,12 @@ def make_weights(ds4, wl, experts, mode):
     return gate, up, down
 
 
+def small_path(wl):
+    """Whether a multi-token call runs its small groups on the small-group kernels (the library's
+    default for d_model <= 4096 and d_ff <= 2048)."""
+    return wl.T > 1 and wl.D <= 4096 and wl.F <= 2048
+
+
 def algorithmic(wl, counts):
     """Bytes and FLOPs the method must move / compute for one call, per stage."""
     D, F, T, k = wl.D, wl.F, wl.T, wl.k
@@ -171,6 +177,14 @@ def algorithmic(wl, counts):
     rows = P + (T if wl.shared else 0)
     up_bytes = touched * IQ2_PER_EXPERT(D, F) + sh_up + T * D * 2 + rows * F * 4
     down_bytes = touched * Q2K_PER_EXPERT(D, F) + sh_down + rows * F * 4 + rows * D * 4
+    if small_path(wl):
+        # the small-group kernels' stages: routed groups below the tensor-core threshold only (the
+        # shared expert and larger groups run in the tensor-core stages)
+        gm = 0 if T <= 64 else 7
+        sel = (counts > 0) & ((counts < gm) if gm else True)
+        n_small, p_small = int(np.count_nonzero(sel)), int(counts[sel].sum())
+        up_bytes = n_small * IQ2_PER_EXPERT(D, F) + T * D * 2 + p_small * F * 4
+        down_bytes = n_small * Q2K_PER_EXPERT(D, F) + p_small * F * 4 + p_small * D * 4
     flops_up = 2 * 2 * F * D * rows
     flops_down = 2 * D * F * rows
     act_bytes = T * D * 2 + T * wl.E * 4 + 2 * T * D * 4 + 2 * rows * F * 4   # x, logits, out, h
@@ -193,13 +207,23 @@ STAGE_KERNEL = {"step": ("decode_step_kernel", "decode_step.cu"),
                 "group": ("group_kernel", "route_group.cu")}
 
 
+SMALL_STAGE_KERNEL = {"up_gemv": ("small_up_kernel", "small_groups.cu"),
+                      "down_gemv": ("small_down_kernel", "small_groups.cu")}
+
+
+def stage_kernel(stage, wl):
+    if small_path(wl) and stage in SMALL_STAGE_KERNEL:
+        return SMALL_STAGE_KERNEL[stage]
+    return STAGE_KERNEL.get(stage, (stage, None))
+
+
 def ncu_traffic(stage, workload):
     """dram read+write bytes per launch from the committed ncu summary, if the kernel
     source is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if stage not in STAGE_KERNEL or not os.path.exists(path):
+    kern, src = stage_kernel(stage, synth.WORKLOADS[workload])
+    if src is None or not os.path.exists(path):
         return None
-    kern, src = STAGE_KERNEL[stage]
     rec = json.load(open(path)).get("%s@%s" % (kern, workload))
     if not rec or rec.get("src_sha") != src_sha(src):
         return None
@@ -370,7 +394,7 @@ def run_ours(args):
         if dom == "combine":
             b = (wl.T * wl.k + wl.T) * wl.D * 4 + 2 * wl.T * wl.D * 4
         achieved = (b / (dom_ms / 1e3) / 1e9) if b else None
-        roof = {"bound": "hbm", "kernel": STAGE_KERNEL.get(dom, (dom,))[0], "achieved": achieved, "peak": hbm,
+        roof = {"bound": "hbm", "kernel": stage_kernel(dom, wl)[0], "achieved": achieved, "peak": hbm,
                 "unit": "GB/s", "frac": (achieved / hbm) if achieved else None,
                 "traffic": ncu_traffic(dom, wl.name), "algorithmic_bytes": b, "avg_launch_ms": dom_ms,
                 "peak_source": peak_src}
