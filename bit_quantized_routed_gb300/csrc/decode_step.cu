@@ -24,12 +24,14 @@
 //     int16 x pairs (signed) exactly, and 8 * sum(x) of the sub-block removes the offset. Each
 //     lookup is one 4-byte word per lane, so a warp's lookup is one shared-memory wavefront.
 //     Each 32-weight sub-block's integer sum is scaled once;
-//   * a routed unit is 16 rows of one expert's gate and up, i.e. exactly one 16-column
-//     sub-block of its down matrix, so the unit quantises its 16 h values to int16 with a scale
-//     of its own and keeps their fp32 sum (for the dmin term) -- stored in the order that lets
-//     the Q2_K-style bit pairs be used with one mask per four codes and no table;
+//   * a routed unit is 16 rows of one expert's gate and up, i.e. exactly one 16-column sub-block
+//     of its down matrix, so the finisher quantises its 16 h values to int16 with a power-of-two
+//     scale of their own, stored in the order q2k_idot reads them;
 //   * down (phase 2): each thread keeps 32 columns of h (one expert) in registers for the whole
-//     phase; the bf16 shared expert runs in fp32 on fp32 h;
+//     phase, its two sub-blocks brought to one power-of-two scale by an integer shift, in the order
+//     that lets the Q2_K-style bit pairs be used with one mask per four codes and no table; a row's two
+//     sub-blocks combine their scales and mins in integers, so only two conversions and the two
+//     block factors remain in floating point; the bf16 shared expert runs in fp32 on fp32 h;
 //   * the cross-warp sums of each unit go through shared memory to a finisher warp, double-
 //     buffered and handed over with mbarriers, so compute warps never wait for one another; each
 //     output row is summed in a fixed order and added to the residual once: deterministic.
@@ -103,9 +105,8 @@ struct StepParams {
     const uint8_t *grid;   // codebook magnitudes [256][8]
     int32_t *topk_idx;     // [k] (written by CTA 0)
     float *topk_w;         // [k]
-    int16_t *hq;           // [k][F] h as int16, each 16-row sub-block in dp2a order
-    float *hsc;            // [k][F/16] dequantisation factor of each sub-block
-    float *hsum;           // [k][F/16] fp32 sum of each sub-block's h
+    int16_t *hq;           // [k][F] the routed experts' h as int16, each 16-row sub-block in dp2a order
+    int *hexp;             // [k][F/16] its power-of-two exponent: h = hq * 2^(hexp - 14)
     float *hsh;            // [F] shared expert's h (fp32)
     unsigned long long *bar;  // grid barrier: arrivals since the workspace was made
     uint64_t *trace;       // null, or [gridDim][6] timestamps (ns)
@@ -523,24 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
                 for (int ww = 0; ww < kCompute; ww++) v += rb[ww * 32 + lane];
                 const float u = __shfl_down_sync(0xffffffffu, v, 16);
                 const float hv = lane < kRows1 ? swiglu(v, u) : 0.0f;
-                float m = fabsf(hv), sum = hv;
+                // int16 with the 16 values' power-of-two scale (2^14 over their absolute maximum)
+                float m = fabsf(hv);
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) {
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                }
+                for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
                 int e = 0;
                 frexpf(m, &e);
                 e = m > 0.0f ? e : 0;
-                if (lane < kRows1) {
-                    const int pos = q2k_h_pos(lane);
-                    p.hq[static_cast<size_t>(slot) * F + row0 + pos] =
+                if (lane < kRows1)
+                    p.hq[static_cast<size_t>(slot) * F + row0 + q2k_h_pos(lane)] =
                         static_cast<int16_t>(__float2int_rn(hv * ldexpf(1.0f, 14 - e)));
-                }
-                if (lane == 0) {
-                    p.hsc[static_cast<size_t>(slot) * (F / 16) + row0 / 16] = ldexpf(1.0f, e - 14);
-                    p.hsum[static_cast<size_t>(slot) * (F / 16) + row0 / 16] = sum;
-                }
+                if (lane == 0) p.hexp[static_cast<size_t>(slot) * (F / 16) + row0 / 16] = e;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(rempty + 8 * buf);
@@ -746,8 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
     // this thread's down columns: expert slot s2, columns 32*j2 .. +31 (two sub-blocks)
     const int s2 = tid >> 6, j2 = tid & 63;
     const bool sval = s2 < p.k;
+    // the thread's 32 int16 h values (two sub-blocks, each with its own exponent) brought to one
+    // power-of-two scale: the sub-block with the smaller exponent is shifted right (rounded) by
+    // the difference; hp keeps q2k_idot's order, hs0/hs1 = the sub-blocks' integer sums
     uint32_t hp[16];
-    float gh0 = 0.0f, gh1 = 0.0f, gs0 = 0.0f, gs1 = 0.0f;
+    int hs0 = 0, hs1 = 0;
+    float gh = 0.0f;  // gate weight x the dequantisation factor
     float4 hs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < 16; i++) hp[i] = 0u;
@@ -761,13 +759,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
             hp[4 * i + 2] = v.z;
             hp[4 * i + 3] = v.w;
         }
-        const float2 sc2 = __ldcg(reinterpret_cast<const float2 *>(p.hsc + static_cast<size_t>(s2) * (F / 16)) + j2);
-        const float2 sm2 = __ldcg(reinterpret_cast<const float2 *>(p.hsum + static_cast<size_t>(s2) * (F / 16)) + j2);
-        const float gw = sgw[s2];
-        gh0 = gw * sc2.x;
-        gh1 = gw * sc2.y;
-        gs0 = gw * sm2.x;
-        gs1 = gw * sm2.y;
+        const int2 ex = __ldcg(reinterpret_cast<const int2 *>(p.hexp + static_cast<size_t>(s2) * (F / 16)) + j2);
+        const int et = max(ex.x, ex.y);
+#pragma unroll
+        for (int sb = 0; sb < 2; sb++) {
+            const int sh = min(et - (sb ? ex.y : ex.x), 16);
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                int lo = static_cast<int>(static_cast<int16_t>(hp[8 * sb + i] & 0xffffu));
+                int hi = static_cast<int>(hp[8 * sb + i]) >> 16;
+                if (sh > 0) {
+                    lo = (lo + (1 << (sh - 1))) >> sh;
+                    hi = (hi + (1 << (sh - 1))) >> sh;
+                }
+                hp[8 * sb + i] = (static_cast<uint32_t>(lo) & 0xffffu) | (static_cast<uint32_t>(hi) << 16);
+                sum += lo + hi;
+            }
+            if (sb) hs1 = sum; else hs0 = sum;
+        }
+        gh = sgw[s2] * ldexpf(1.0f, et - 14);
     }
     if (w.has_shared) hs = __ldcg(reinterpret_cast<const float4 *>(p.hsh) + tid);
     if (tr) tr[4] = now_ns();
@@ -802,16 +813,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
 #pragma unroll
             for (int r = 0; r < kRows2; r++) {
                 if (sval) {
+                    // sum_sb d sc_sb (q . h)_sb - dmin m_sb sum(h)_sb, in integers up to the two block factors
                     const int a0 = q2k_idot(qw[r].x, hp), a1 = q2k_idot(qw[r].y, hp + 8);
+                    const uint32_t sc = scw[r];
+                    const int i1 = static_cast<int>(sc & 15u) * a0 + static_cast<int>((sc >> 8) & 15u) * a1;
+                    const int i2 = static_cast<int>((sc >> 4) & 15u) * hs0 + static_cast<int>(sc >> 12) * hs1;
                     const float d = f16_to_f32(static_cast<uint16_t>(dd[r] & 0xffffu));
                     const float dmin = f16_to_f32(static_cast<uint16_t>(dd[r] >> 16));
-                    const uint32_t sc = scw[r];
-                    const float t = fmaf(gh0 * small_int_to_float(static_cast<int>(sc & 15u)), small_int_to_float(a0),
-                                         gh1 * small_int_to_float(static_cast<int>((sc >> 8) & 15u)) *
-                                             small_int_to_float(a1));
-                    const float mt = fmaf(gs0, small_int_to_float(static_cast<int>((sc >> 4) & 15u)),
-                                          gs1 * small_int_to_float(static_cast<int>(sc >> 12)));
-                    acc[r] = fmaf(d, t, -dmin * mt);
+                    acc[r] = gh * fmaf(d, int_to_float(i1), -dmin * int_to_float(i2));
                 }
                 if (w.has_shared) {
                     acc[r] = fmaf(bf16_lo(bw[r].x), hs.x, acc[r]);
@@ -884,12 +893,11 @@ int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16
     p.grid = ws.grid;
     p.topk_idx = ws.topk_idx;
     p.topk_w = ws.topk_w;
-    // h32 holds at least (k + 1) * F floats: int16 h, the sub-block factors and sums, shared h
+    // h32 holds at least (k + 1) * F floats: int16 h and exponents of the routed experts, the shared h
     uint8_t *hb = reinterpret_cast<uint8_t *>(ws.h32);
     p.hq = reinterpret_cast<int16_t *>(hb);
-    p.hsc = reinterpret_cast<float *>(hb + static_cast<size_t>(k) * w.F * 2);
-    p.hsum = p.hsc + static_cast<size_t>(k) * (w.F / 16);
-    p.hsh = p.hsum + static_cast<size_t>(k) * (w.F / 16);
+    p.hexp = reinterpret_cast<int *>(hb + static_cast<size_t>(k) * w.F * 2);
+    p.hsh = reinterpret_cast<float *>(p.hexp + static_cast<size_t>(k) * (w.F / 16));
     p.bar = reinterpret_cast<unsigned long long *>(ws.gbar);
     p.trace = trace;
     p.status = ws.status;
