@@ -46,6 +46,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--router", action="store_true",
+                    help="a step also computes the router logits on the device (bf16 router, fp32 bias) in "
+                         "front of routing, instead of taking the workload's logits")
     ap.add_argument("--calls", type=int, default=0,
                     help="run the workload's call this many times (no timing, no JSON line) and exit: "
                          "a fixed launch sequence for profilers")
@@ -269,17 +272,26 @@ def run_ours(args):
         wl = wl.replace(seed=wl.seed + 1000 * rank)   # each replica its own batch
     mode = args.weights or ("quantized" if wl.T <= 32 else "random")
     L, x = synth.draw_inputs(wl)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    if args.router:
+        # a seeded bf16 router and fp32 bias with the workload's routing mix; the logits the step
+        # routes on are computed on the device from x
+        wr, br = synth.router_weights(wl)
+        wrd = torch.from_numpy(wr.view(np.int16)).cuda().view(torch.bfloat16)
+        brd = torch.from_numpy(br).cuda()
+        L = ds4.ds4moe_router_logits(xd, wrd, brd).cpu().numpy()
     experts = touched_experts(ds4, wl, L)
     gate, up, down = make_weights(ds4, wl, experts, mode)
     shared = synth.shared_weights(wl.seed, wl.D, wl.F) if wl.shared else None
     W = ds4.ds4moe_weights_create(gate, up, down, wl.D, wl.F, shared=shared, max_tokens=wl.T, max_k=wl.k)
     del gate, up, down
-    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     Ld = torch.from_numpy(L).cuda()
     out = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     counts, _, _, _ = ds4.ds4moe_group(ds4.ds4moe_route(Ld, wl.k)[0], wl.E)
     alg = algorithmic(wl, counts.cpu().numpy())
+    if args.router:
+        alg["total_bytes"] += wl.E * wl.D * 2 + wl.E * 4   # the router's weights and bias
     flush = alg["total_bytes"] < 4 * L2_BYTES
     if flush:
         fw = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
@@ -290,6 +302,8 @@ def run_ours(args):
         fr.sum()             # ... then read more than L2, so no dirty line is left behind
 
     def step():
+        if args.router:
+            ds4.ds4moe_router_logits(xd, wrd, brd, logits=Ld)
         ds4.ds4moe_expert_ffn(xd, W, Ld, wl.k, out)
 
     if args.calls:
@@ -312,7 +326,7 @@ def run_ours(args):
         raise RuntimeError(ds4.ds4moe_strerror(st))
     before = ds4.ds4moe_get_stats(W)["launches"]
     step()
-    launches_per_call = ds4.ds4moe_get_stats(W)["launches"] - before
+    launches_per_call = ds4.ds4moe_get_stats(W)["launches"] - before + (1 if args.router else 0)
 
     # The call is replayed as a CUDA graph, so the device time of a step is not
     # stretched by host-side launch latency.
@@ -373,14 +387,15 @@ def run_ours(args):
             l2_flush()
         e2e_ev[i][0].record(stream)
         xd.copy_(xh, non_blocking=True)
-        Ld.copy_(Lh, non_blocking=True)
+        if not args.router:
+            Ld.copy_(Lh, non_blocking=True)
         out.copy_(out_in, non_blocking=True)
-        ds4.ds4moe_expert_ffn(xd, W, Ld, wl.k, out)
+        step()
         out_h.copy_(out, non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, "cuda")
-    h2d = wl.T * wl.D * 2 + wl.T * wl.E * 4 + wl.T * wl.D * 4
+    h2d = wl.T * wl.D * 2 + (0 if args.router else wl.T * wl.E * 4) + wl.T * wl.D * 4
     d2h = wl.T * wl.D * 4
     st = ds4.ds4moe_last_status(W)
     if st:
@@ -417,7 +432,9 @@ def run_ours(args):
                                          ("host-quantised N(0,0.02)" if mode == "quantized" else "random valid blocks"),
                        "experts_touched": alg["touched"],
                        "l2": "flushed between steps (write then read 256 MB)" if flush else "working set > 4x L2",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       **({"router": "bf16 [E x D] + fp32 bias, logits computed on the device in front of routing"}
+                          if args.router else {})},
             "gpu_launches": int(launches),
             "e2e": {"value": whole_job_rate(K * wl.T, world, e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -35,7 +35,7 @@ EXPORTED = [
     "ds4moe_strerror", "ds4moe_q2k_bytes", "ds4moe_iq2_bytes", "ds4moe_iq2_grid",
     "ds4moe_quantize_q2k", "ds4moe_quantize_iq2", "ds4moe_dequantize_q2k", "ds4moe_dequantize_iq2",
     "ds4moe_weights_create", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
-    "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
+    "ds4moe_router_logits", "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
     "ds4moe_expert_ffn_static", "ds4moe_step_trace",
 ]
 
@@ -85,6 +85,7 @@ def lib():
             "ds4moe_weights_destroy": ([vp], None),
             "ds4moe_set_option": ([vp, i32, i32], i32),
             "ds4moe_weights_dequantize": ([vp, i32, i32, vp, vp, vp], i32),
+            "ds4moe_router_logits": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
             "ds4moe_route": ([vp, i32, i32, i32, i32, vp, vp, vp], i32),
             "ds4moe_group": ([vp, i32, i32, i32, vp, vp, vp, vp, vp], i32),
             "ds4moe_expert_ffn": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
@@ -246,6 +247,23 @@ def ds4moe_weights_dequantize(weights, expert, matrix, dst_f32=None, dst_f16=Non
                                            _ptr(dst_f32, torch.float32, "dst_f32"),
                                            _ptr(dst_f16, torch.float16, "dst_f16"), _stream(stream)),
            "ds4moe_weights_dequantize")
+
+
+def ds4moe_router_logits(x, w_router, bias=None, logits=None, stream=None):
+    """Router logits on the device in the library's fixed fp32 order. x: bf16 CUDA [T, D];
+    w_router: bf16 CUDA [E, D]; bias: fp32 CUDA [E] or None. Returns fp32 [T, E]."""
+    import torch
+    T, D = x.shape
+    E = w_router.shape[0]
+    if w_router.shape[1] != D:
+        raise ValueError("w_router must be [E, D]")
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    _check(lib().ds4moe_router_logits(_ptr(x, torch.bfloat16, "x"), _ptr(w_router, torch.bfloat16, "w_router"),
+                                      _ptr(bias, torch.float32, "bias") if bias is not None else None, T, D, E,
+                                      _ptr(logits, torch.float32, "logits"), _stream(stream)),
+           "ds4moe_router_logits")
+    return logits
 
 
 def ds4moe_route(logits, k, gate_mode=DS4MOE_GATE_SOFTMAX, topk_idx=None, topk_w=None, stream=None):

@@ -319,6 +319,16 @@ int ds4moe_weights_dequantize(const ds4moe_weights *h, int expert, int matrix, f
     return cuda_status(rc);
 }
 
+int ds4moe_router_logits(const void *x, const void *w_router, const float *bias, int T, int D, int E,
+                         float *logits, ds4moe_stream_t stream) {
+    if (T < 0 || D <= 0 || D % 256 || D > 8192 || E < 8 || E % 8 || E > 1024) return DS4MOE_EINVAL;
+    if (T == 0) return DS4MOE_OK;
+    if (!x || !w_router || !logits || !aligned16(x) || !aligned16(w_router)) return DS4MOE_EINVAL;
+    if (reinterpret_cast<uintptr_t>(logits) % 4 || (bias && reinterpret_cast<uintptr_t>(bias) % 4)) return DS4MOE_EINVAL;
+    return cuda_status(launch_router(static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(w_router), bias, T,
+                                     D, E, logits, stream));
+}
+
 int ds4moe_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *topk_idx, float *topk_w,
                  ds4moe_stream_t stream) {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return DS4MOE_EINVAL;

@@ -161,6 +161,8 @@ struct ds4moe_weights {
 namespace ds4moe {
 
 // Launchers (return a cudaError_t as int; 0 = success).
+int launch_router(const uint16_t *x, const uint16_t *w, const float *bias, int T, int D, int E, float *logits,
+                  void *stream);
 int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *idx, float *w,
                  void *stream);
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok,

@@ -91,6 +91,25 @@ def draw_inputs(wl):
     return L, x
 
 
+def router_weights(wl):
+    """A seeded router for the workload: bf16 bits [E, D] drawn N(0, 1/sqrt(D)), so that with
+    x ~ N(0, 1) the logits spread like the drawn ones (unit variance), and an fp32 bias [E] of the
+    workload's per-expert kind (Zipf -s log(rank) over a random expert order, N(0, p), or zero),
+    so that routing on the computed logits has the workload's group-size mix."""
+    rng = np.random.default_rng(wl.seed + 7919)
+    w = f32_to_bf16_bits((rng.standard_normal((wl.E, wl.D)) / np.sqrt(wl.D)).astype(np.float32))
+    b = np.zeros(wl.E, np.float32)
+    if wl.bias:
+        kind, p = wl.bias
+        if kind == "normal":
+            b = rng.normal(0.0, p, wl.E).astype(np.float32)
+        elif kind == "zipf":
+            b = (-p * np.log(rng.permutation(wl.E) + 1)).astype(np.float32)
+        else:
+            raise ValueError(kind)
+    return w, b
+
+
 def _gen(seed, a, b):
     return np.random.Generator(np.random.Philox(key=[int(seed), (int(a) << 8) | int(b)]))
 

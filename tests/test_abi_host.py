@@ -101,6 +101,14 @@ def test_device_entry_points_reject_bad_arguments_on_host(ds4):
     assert L.ds4moe_route(None, 4, 8, 2, 7, None, None, None) == ds4.DS4MOE_EINVAL
     assert L.ds4moe_route(None, 4, 8, 2, 0, None, None, None) == ds4.DS4MOE_EINVAL  # null pointers
     assert L.ds4moe_route(None, 0, 8, 2, 0, None, None, None) == ds4.DS4MOE_OK      # T = 0: no-op
+    # router logits: D a multiple of 256 (<= 8192), E a multiple of 8 in [8, 1024], pointers checked before any launch
+    assert L.ds4moe_router_logits(None, None, None, 1, 300, 8, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_router_logits(None, None, None, 1, 256, 12, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_router_logits(None, None, None, 1, 256, 2048, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_router_logits(None, None, None, 1, 8448, 8, None, None) == ds4.DS4MOE_EINVAL  # D > 8192
+    assert L.ds4moe_router_logits(None, None, None, -1, 256, 8, None, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_router_logits(None, None, None, 1, 256, 8, None, None) == ds4.DS4MOE_EINVAL  # null pointers
+    assert L.ds4moe_router_logits(None, None, None, 0, 256, 8, None, None) == ds4.DS4MOE_OK      # T = 0: no-op
     assert L.ds4moe_group(None, 4, 2, 8, None, None, None, None, None) == ds4.DS4MOE_EINVAL
     assert L.ds4moe_expert_ffn(None, None, None, 1, 1, 0, None, None) == ds4.DS4MOE_EINVAL
     assert L.ds4moe_set_option(None, 0, 1) == ds4.DS4MOE_EINVAL

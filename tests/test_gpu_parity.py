@@ -293,3 +293,50 @@ def test_single_token_kernel_equals_separate_kernels_and_is_deterministic(ds4):
     c = lay.run(ds4, W)
     W.close()
     assert norm_max_err(a, c) <= FFN_TOL   # two valid paths, each within tolerance of the oracle
+
+
+# ---------------------------------------------------------------- router logits in front of routing
+
+@pytest.mark.parametrize("T,D,E,bias", [(1, 4096, 256, True), (37, 512, 64, False), (4, 256, 8, True),
+                                        (130, 1024, 128, True), (3, 7168, 256, False)])
+def test_router_logits_bitexact_and_the_selection_from_them(ds4, T, D, E, bias):
+    import torch
+    from oracle.router import router_logits
+    rng = np.random.default_rng(T + D + E)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((T, D)).astype(np.float32))
+    w = synth.f32_to_bf16_bits((0.02 * rng.standard_normal((E, D))).astype(np.float32))
+    b = (0.1 * rng.standard_normal(E)).astype(np.float32) if bias else None
+    ref = router_logits(x, w, b)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    wd = torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16)
+    bd = torch.from_numpy(b).cuda() if bias else None
+    got = ds4.ds4moe_router_logits(xd, wd, bd)
+    assert np.array_equal(got.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    k = min(8, E)
+    idx, _ = ds4.ds4moe_route(got, k)
+    ref_idx, _ = oracle.route(ref, k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+
+
+def test_layer_from_hidden_states(ds4):
+    # router in front: the logits come from the router on the device, the oracle takes its own
+    import torch
+    from oracle.router import router_logits
+    wl = synth.Workload("hid", T=1, D=4096, F=2048, E=256, k=8, seed=41, shared=True)
+    rng = np.random.default_rng(41)
+    lay = Layer(wl, quantized=False)
+    w = synth.f32_to_bf16_bits((0.02 * rng.standard_normal((wl.E, wl.D))).astype(np.float32))
+    b = (0.1 * rng.standard_normal(wl.E)).astype(np.float32)
+    lay.L = router_logits(lay.x, w, b)
+    # the layer's random blobs were made for the experts of the drawn logits: cover these too
+    lay.gate, lay.up, lay.down = synth.random_expert_blobs(wl, np.unique(oracle.route(lay.L, wl.k)[0]))
+    W = lay.upload(ds4)
+    x = torch.from_numpy(lay.x.view(np.int16)).cuda().view(torch.bfloat16)
+    logits = ds4.ds4moe_router_logits(x, torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16),
+                                      torch.from_numpy(b).cuda())
+    out = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
+    ds4.ds4moe_expert_ffn(x, W, logits, wl.k, out)
+    assert ds4.ds4moe_last_status(W) == 0
+    W.close()
+    ref, _, _ = lay.oracle_delta()
+    assert norm_max_err(out.cpu().numpy(), ref) <= FFN_TOL
