@@ -567,9 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
 #pragma unroll
     for (int j = 0; j < 4; j++)
         raw[j] = cval ? __ldg(reinterpret_cast<const uint4 *>(p.x) + 4 * c + j) : make_uint4(0, 0, 0, 0);
-    uint2 graw[16];  // codebook entry warp + 16 * j, replica lane: one broadcast load per warp
-#pragma unroll
-    for (int j = 0; j < 16; j++) graw[j] = __ldg(reinterpret_cast<const uint2 *>(p.grid) + warp + 16 * j);
+    const uint2 gown = __ldg(reinterpret_cast<const uint2 *>(p.grid) + warp + 16 * (lane & 15));  // for iq2_table_store
     const bool xfq = tid < D / 8;
     const uint4 xv = xfq ? __ldg(reinterpret_cast<const uint4 *>(p.x) + tid) : make_uint4(0, 0, 0, 0);
     // bf16 x for the shared expert: thread tid stores group tid (D <= 8 * kNCompute)
@@ -619,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
         x8s[c] = x8;
         if (lane == 0) xsc[qx] = xinv;
     }
-    iq2_table_store(tab, graw, warp, lane);  // codebook and sign words, one replica per lane
+    iq2_table_store(tab, gown, warp, lane);  // codebook and sign words, one replica per lane
     bar_sync(kBarCompute, kNCompute);
     if (tr) tr[1] = now_ns();
 

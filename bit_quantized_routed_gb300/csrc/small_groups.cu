@@ -346,10 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_up_kernel(UpParams p) {
             info[3] = u1 - u0;
         }
     } else if (warp < kCompute) {
-        uint2 graw[16];  // codebook entry warp + 16 j
-#pragma unroll
-        for (int j = 0; j < 16; j++) graw[j] = __ldg(reinterpret_cast<const uint2 *>(p.grid) + warp + 16 * j);
-        iq2_table_store(tab, graw, warp, lane);
+        const uint2 gown = __ldg(reinterpret_cast<const uint2 *>(p.grid) + warp + 16 * (lane & 15));
+        iq2_table_store(tab, gown, warp, lane);
     }
     __syncthreads();
     Walker wk;

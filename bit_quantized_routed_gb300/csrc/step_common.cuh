@@ -51,28 +51,30 @@ __device__ __forceinline__ uint32_t iq2_nibble_word(uint2 g) {
     return ev | (od << 4);
 }
 
-// The sign word of a 7-bit stored sign pattern (the 8th sign is the parity of the 7).
+// The sign word of a 7-bit stored sign pattern (the 8th sign is the parity of the 7): the 8 sign
+// bits spread to one per nibble (bit e at 4 e), then 0x9 ^ 0xE = 0x7 where a sign is set.
 __device__ __forceinline__ uint32_t iq2_sign_word(uint32_t s7) {
-    const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
-    uint32_t v = 0;
-#pragma unroll
-    for (int el = 0; el < 8; el++) v |= (((s8 >> el) & 1u) ? 0x7u : 0x9u) << (8 * (el >> 1) + 4 * (el & 1));
-    return v;
+    uint32_t v = s7 | ((__popc(s7) & 1u) << 7);
+    v = (v | (v << 12)) & 0x000F000Fu;  // signs 0-3 at bits 0-3, 4-7 at bits 16-19
+    v = (v | (v << 6)) & 0x03030303u;   // two per byte
+    v = (v | (v << 3)) & 0x11111111u;   // one per nibble
+    return 0x99999999u ^ (v * 0xEu);
 }
 
 // The lookup table: 256 slots of 256 bytes. Slot e holds codebook word e in its first 128 bytes and
 // sign word e (e < 128) in its second 128 bytes, one u32 replica per lane, so any index a lane
-// looks up sits in that lane's own bank. Built by 16 warps (warp16 = 0..15) in two parts so the
-// caller can issue the grid loads early: graw[j] = grid entry warp16 + 16 * j.
-__device__ __forceinline__ void iq2_table_store(uint8_t *tab, const uint2 graw[16], int warp16, int lane) {
+// looks up sits in that lane's own bank. Built by 16 warps (warp16 = 0..15): each word is computed
+// once per warp (lane l < 16: codebook word of entry warp16 + 16 l, from its grid entry gown that
+// the caller loaded early; lane 16 + j: sign word of pattern warp16 + 16 j) and handed to every lane
+// by a shuffle.
+__device__ __forceinline__ void iq2_table_store(uint8_t *tab, uint2 gown, int warp16, int lane) {
+    const uint32_t mine = lane < 16 ? iq2_nibble_word(gown) : iq2_sign_word(static_cast<uint32_t>(warp16 + 16 * (lane & 7)));
 #pragma unroll
     for (int j = 0; j < 16; j++)
-        *reinterpret_cast<uint32_t *>(tab + (warp16 + 16 * j) * 256 + lane * 4) = iq2_nibble_word(graw[j]);
+        *reinterpret_cast<uint32_t *>(tab + (warp16 + 16 * j) * 256 + lane * 4) = __shfl_sync(0xffffffffu, mine, j);
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const uint32_t s7 = static_cast<uint32_t>(warp16 + 16 * j);
-        *reinterpret_cast<uint32_t *>(tab + s7 * 256 + 128 + lane * 4) = iq2_sign_word(s7);
-    }
+    for (int j = 0; j < 8; j++)
+        *reinterpret_cast<uint32_t *>(tab + (warp16 + 16 * j) * 256 + 128 + lane * 4) = __shfl_sync(0xffffffffu, mine, 16 + j);
 }
 
 // Byte offsets in the table of group g's codebook and sign words of a sub-block whose index word
