@@ -32,8 +32,8 @@ namespace {
 constexpr int BM = 128;   // weight rows per tile (MMA M)
 constexpr int BN = kGemmBN;  // token rows per tile (MMA N at most)
 constexpr int BK = 64;    // K elements per stage: one 128-byte swizzle atom
-constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA (+ TMEM alloc), warps 2..9 producers/epilogue
-constexpr int kProducers = 256;
+constexpr int kThreads = 576;  // warp 0 TMA, warp 1 MMA (+ TMEM alloc), warps 2..17 producers/epilogue
+constexpr int kProducers = 512;
 constexpr int kTableBytes = 256 * 16 * 8;  // replicated lookup table (grid or code selectors)
 
 enum { UP = 0, DOWN = 1 };
@@ -145,11 +145,12 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_ti
 
 // ------------------------------------------------------------------ producers
 //
-// Each of the 256 producer threads owns one tile row of one matrix (first GEMM: gate or up,
-// 64 columns per stage) or one half row (down GEMM, 32 columns per stage). A format fetches
-// the packed data of a stage into registers (a ring of PF stages in flight hides the HBM
-// latency) and emits it as fp16 into the swizzled A tile. Every fp16 value is RN-even of
-// the weight's exact fp32 value.
+// Each of the 512 producer threads owns one slice of one tile row per stage: first GEMM, one
+// 32-column half of a row of gate or up (thread u: row (u >> 1) & 127, matrix u >> 8, half u & 1,
+// so two neighbouring lanes read the two halves of one 16-byte chunk); down GEMM, one 16-column
+// quarter of a row (row (u >> 2) & 127, quarter u & 3). A format fetches the packed data of a
+// stage into registers (a ring of PF stages in flight hides the HBM latency) and emits it as fp16
+// into the swizzled A tile. Every fp16 value is RN-even of the weight's exact fp32 value.
 
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -159,124 +160,92 @@ __device__ __forceinline__ uint32_t mag_hibyte(uint32_t m) {
     return m == 1u ? 0x3Cu : m == 3u ? 0x42u : m == 5u ? 0x45u : 0x47u;
 }
 
-// IQ2-style rows: 64 weights = 2 sub-blocks = 8 groups per stage.
+// IQ2-style rows: one 32-weight sub-block (4 groups of 8) per stage.
 struct IQ2Fmt {
     static constexpr int PF = 4;
     struct Data {
-        uint4 q;
+        uint2 q;  // index word, sign/scale word
         uint32_t d;
     };
     const uint8_t *qs;   // this row's code blocks
     const uint16_t *dp;  // this row's block scales
     const uint2 *gt;  // grid as fp16 high bytes, this lane's replica
     int swz;          // the row's chunk permutation (iq2_swz)
+    int sb;           // which sub-block of the stage's 16-byte chunk
     __device__ __forceinline__ Data fetch(int kb) const {
         Data v;
-        v.q = __ldg(reinterpret_cast<const uint4 *>(qs) + (kb ^ swz));  // chunk kb = 4 * block + part
+        v.q = __ldg(reinterpret_cast<const uint2 *>(qs) + 2 * (kb ^ swz) + sb);  // chunk kb = 4 * block + part
         v.d = __ldg(dp + (kb >> 2));
         return v;
     }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
         const __half2 dh = u2h(v.d | (v.d << 16));
+        const uint32_t iw = v.q.x, sw = v.q.y;
+        // (s+1)/16, exact in fp16; G*(s+1)/16 is then exact and one multiply by d rounds once
+        const __half2 c16 = __float2half2_rn(static_cast<float>((sw >> 28) + 1u) * 0.0625f);
 #pragma unroll
-        for (int sb = 0; sb < 2; sb++) {
-            const uint32_t iw = sb ? v.q.z : v.q.x, sw = sb ? v.q.w : v.q.y;
-            // (s+1)/16, exact in fp16; G*(s+1)/16 is then exact and one multiply by d rounds once
-            const __half2 c16 = __float2half2_rn(static_cast<float>((sw >> 28) + 1u) * 0.0625f);
-#pragma unroll
-            for (int g = 0; g < 4; g++) {
-                const uint2 ent = gt[((iw >> (8 * g)) & 255u) << 4];
-                const uint32_t s7 = (sw >> (7 * g)) & 127u;
-                const uint32_t lo = ent.x ^ ((s7 * 0x10204080u) & 0x80808080u);
-                const uint32_t hi = ent.y ^ ((s7 * 0x01020408u + (__popc(s7) << 31)) & 0x80808080u);
-                uint4 o;
-                o.x = h2u(__hmul2(__hmul2(u2h(__byte_perm(lo, 0u, 0x1404)), c16), dh));
-                o.y = h2u(__hmul2(__hmul2(u2h(__byte_perm(lo, 0u, 0x3424)), c16), dh));
-                o.z = h2u(__hmul2(__hmul2(u2h(__byte_perm(hi, 0u, 0x1404)), c16), dh));
-                o.w = h2u(__hmul2(__hmul2(u2h(__byte_perm(hi, 0u, 0x3424)), c16), dh));
-                st_shared16(tile + sw128_off(r, sb * 4 + g), o);
-            }
+        for (int g = 0; g < 4; g++) {
+            const uint2 ent = gt[((iw >> (8 * g)) & 255u) << 4];
+            const uint32_t s7 = (sw >> (7 * g)) & 127u;
+            const uint32_t lo = ent.x ^ ((s7 * 0x10204080u) & 0x80808080u);
+            const uint32_t hi = ent.y ^ ((s7 * 0x01020408u + (__popc(s7) << 31)) & 0x80808080u);
+            uint4 o;
+            o.x = h2u(__hmul2(__hmul2(u2h(__byte_perm(lo, 0u, 0x1404)), c16), dh));
+            o.y = h2u(__hmul2(__hmul2(u2h(__byte_perm(lo, 0u, 0x3424)), c16), dh));
+            o.z = h2u(__hmul2(__hmul2(u2h(__byte_perm(hi, 0u, 0x1404)), c16), dh));
+            o.w = h2u(__hmul2(__hmul2(u2h(__byte_perm(hi, 0u, 0x3424)), c16), dh));
+            st_shared16(tile + sw128_off(r, sb * 4 + g), o);
         }
     }
 };
 
-// Q2_K-style rows, half row: 32 weights = 2 sub-blocks per stage. The 4 possible values of a
-// sub-block, RN-even(fp32(d*sc*q - dmin*m)) for q = 0..3, are formed once; each code byte
-// then selects its four values with two byte permutations (selectors from a table).
+// Q2_K-style rows, quarter row: one 16-weight sub-block per stage. The 4 possible values of the
+// sub-block, RN-even(fp32(d*sc*q - dmin*m)) for q = 0..3, are formed once; each code byte then
+// selects its four values with two byte permutations (selectors from a table).
 struct Q2KFmt {
     static constexpr int PF = 4;
     struct Data {
-        uint2 q;
-        uint32_t sc;
+        uint32_t q;   // 16 codes
+        uint32_t sc;  // scale byte (low 4 bits sc, high 4 bits m)
         uint32_t dd;
     };
     const uint8_t *sq;    // this row's blocks (scales, codes)
     const uint32_t *ddp;  // this row's d | dmin words
-    int half;
+    int qp;               // which quarter of the stage's 64 columns
     const uint2 *st;  // code byte -> two byte_perm selectors, this lane's replica
     __device__ __forceinline__ Data fetch(int kb) const {
         const int b = kb >> 2, part = kb & 3;
         const uint8_t *blk = sq + b * 80;
         Data v;
-        v.q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 16 * part + 8 * half));
-        v.sc = __ldg(reinterpret_cast<const uint16_t *>(blk + 4 * part + 2 * half));
+        v.q = __ldg(reinterpret_cast<const uint32_t *>(blk + 16 + 16 * part + 4 * qp));
+        v.sc = __ldg(blk + 4 * part + qp);
         v.dd = __ldg(ddp + b);
         return v;
     }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
         const float d = f16_to_f32(static_cast<uint16_t>(v.dd & 0xffffu));
         const float dmin = f16_to_f32(static_cast<uint16_t>(v.dd >> 16));
+        const float ds = __fmul_rn(d, static_cast<float>(v.sc & 15u));
+        const float dm = __fmul_rn(dmin, static_cast<float>((v.sc >> 4) & 15u));
+        const uint32_t p01 = pack_h2(q2k_weight(ds, dm, 0u), q2k_weight(ds, dm, 1u));
+        const uint32_t p23 = pack_h2(q2k_weight(ds, dm, 2u), q2k_weight(ds, dm, 3u));
 #pragma unroll
-        for (int j = 0; j < 2; j++) {
-            const uint32_t sc = (v.sc >> (8 * j)) & 15u, mn = (v.sc >> (8 * j + 4)) & 15u;
-            const float ds = __fmul_rn(d, static_cast<float>(sc));
-            const float dm = __fmul_rn(dmin, static_cast<float>(mn));
-            const uint32_t p01 = pack_h2(q2k_weight(ds, dm, 0u), q2k_weight(ds, dm, 1u));
-            const uint32_t p23 = pack_h2(q2k_weight(ds, dm, 2u), q2k_weight(ds, dm, 3u));
-            const uint32_t qw = j ? v.q.y : v.q.x;
-#pragma unroll
-            for (int hh = 0; hh < 2; hh++) {
-                const uint2 s0 = st[((qw >> (16 * hh)) & 255u) << 4];
-                const uint2 s1 = st[((qw >> (16 * hh + 8)) & 255u) << 4];
-                uint4 o;
-                o.x = __byte_perm(p01, p23, s0.x);
-                o.y = __byte_perm(p01, p23, s0.y);
-                o.z = __byte_perm(p01, p23, s1.x);
-                o.w = __byte_perm(p01, p23, s1.y);
-                st_shared16(tile + sw128_off(r, 4 * half + 2 * j + hh), o);
-            }
+        for (int hh = 0; hh < 2; hh++) {
+            const uint2 s0 = st[((v.q >> (16 * hh)) & 255u) << 4];
+            const uint2 s1 = st[((v.q >> (16 * hh + 8)) & 255u) << 4];
+            uint4 o;
+            o.x = __byte_perm(p01, p23, s0.x);
+            o.y = __byte_perm(p01, p23, s0.y);
+            o.z = __byte_perm(p01, p23, s1.x);
+            o.w = __byte_perm(p01, p23, s1.y);
+            st_shared16(tile + sw128_off(r, 2 * qp + hh), o);
         }
     }
 };
 
-// bf16 rows (shared gate/up), 64 columns per stage -> fp16.
+// bf16 rows (shared gate/up), half row: 32 columns per stage -> fp16.
 struct BF16Fmt {
-    static constexpr int PF = 2;
-    struct Data {
-        uint4 v[8];
-    };
-    const uint16_t *row;
-    __device__ __forceinline__ Data fetch(int kb) const {
-        Data d;
-        const uint4 *src = reinterpret_cast<const uint4 *>(row + kb * BK);
-#pragma unroll
-        for (int c = 0; c < 8; c++) d.v[c] = __ldg(src + c);
-        return d;
-    }
-    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
-#pragma unroll
-        for (int c = 0; c < 8; c++) {
-            const uint4 v = d.v[c];
-            st_shared16(tile + sw128_off(r, c),
-                        make_uint4(pack_h2(bf16_lo(v.x), bf16_hi(v.x)), pack_h2(bf16_lo(v.y), bf16_hi(v.y)),
-                                   pack_h2(bf16_lo(v.z), bf16_hi(v.z)), pack_h2(bf16_lo(v.w), bf16_hi(v.w))));
-        }
-    }
-};
-
-// fp16 rows (shared down), half row: 32 columns per stage -> copied.
-struct F16Fmt {
-    static constexpr int PF = 4;
+    static constexpr int PF = 1;
     struct Data {
         uint4 v[4];
     };
@@ -291,7 +260,33 @@ struct F16Fmt {
     }
     __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
 #pragma unroll
-        for (int c = 0; c < 4; c++) st_shared16(tile + sw128_off(r, 4 * half + c), d.v[c]);
+        for (int c = 0; c < 4; c++) {
+            const uint4 v = d.v[c];
+            st_shared16(tile + sw128_off(r, 4 * half + c),
+                        make_uint4(pack_h2(bf16_lo(v.x), bf16_hi(v.x)), pack_h2(bf16_lo(v.y), bf16_hi(v.y)),
+                                   pack_h2(bf16_lo(v.z), bf16_hi(v.z)), pack_h2(bf16_lo(v.w), bf16_hi(v.w))));
+        }
+    }
+};
+
+// fp16 rows (shared down), quarter row: 16 columns per stage -> copied.
+struct F16Fmt {
+    static constexpr int PF = 2;
+    struct Data {
+        uint4 v[2];
+    };
+    const uint16_t *row;
+    int qp;
+    __device__ __forceinline__ Data fetch(int kb) const {
+        Data d;
+        const uint4 *src = reinterpret_cast<const uint4 *>(row + kb * BK + 16 * qp);
+#pragma unroll
+        for (int c = 0; c < 2; c++) d.v[c] = __ldg(src + c);
+        return d;
+    }
+    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
+#pragma unroll
+        for (int c = 0; c < 2; c++) st_shared16(tile + sw128_off(r, 2 * qp + c), d.v[c]);
     }
 };
 
@@ -311,10 +306,12 @@ __device__ __forceinline__ bool produce_tile(const Fmt &f, int num_kb, uint8_t *
     constexpr int PF = Fmt::PF;
     typename Fmt::Data ring[PF];
 #pragma unroll
-    for (int i = 0; i < PF; i++) ring[i] = f.fetch(i);  // num_kb >= 4 >= PF
+    for (int i = 0; i < PF; i++)
+        if (i < num_kb) ring[i] = f.fetch(i);
     for (int kb0 = 0; kb0 < num_kb; kb0 += PF) {
 #pragma unroll
         for (int i = 0; i < PF; i++) {
+            if (kb0 + i >= num_kb) break;
             const typename Fmt::Data cur = ring[i];
             if (kb0 + i + PF < num_kb) ring[i] = f.fetch(kb0 + i + PF);
             if (!mbar_wait(smem_u32(pp.bars + 2 * pp.S + pp.stage), pp.phase ^ 1u, pp.abort_flag, pp.status))
@@ -492,11 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
     } else {
         // ---------------------------------------------------------- producers, then epilogue
-        const int u = (warp - 2) * 32 + lane;  // 0..255
-        const int r = u & 127;                 // tile row == TMEM lane
-        const int sel = u >> 7;                // first GEMM: matrix (gate/up); down GEMM: half row
+        const int u = (warp - 2) * 32 + lane;  // 0..511
+        // first GEMM: row (u >> 1) & 127 of matrix u >> 8 (gate/up), half u & 1; down GEMM: row
+        // (u >> 2) & 127, quarter u & 3
+        const int r = KIND == UP ? (u >> 1) & 127 : (u >> 2) & 127;  // tile row
+        const int sel = KIND == UP ? u >> 8 : 0;
+        const int part = KIND == UP ? u & 1 : u & 3;
         const int q = warp & 3;                // TMEM lane quarter this warp may access
-        const int colhalf = (warp - 2) >> 2;   // epilogue: which 16-column chunks
+        const int colq = (warp - 2) >> 2;      // epilogue: which 16-column chunks (one of four)
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint2 *tab = table + (lane & 15);
         Pipe pp{bars, S, 0, 0u, abort_flag, p.status};
@@ -507,23 +507,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int wrow = ti.m * BM + r;
             if (KIND == UP) {
                 if (ti.shared) {
-                    BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D};
+                    BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D, part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else {
-                    IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab, iq2_swz(p.w, wrow)};
+                    IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab, iq2_swz(p.w, wrow), part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 }
             } else {
                 if (ti.shared) {
-                    F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, sel};
+                    F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
                 } else {
-                    Q2KFmt f{q2k_sq_row(p.w, ti.e, wrow), q2k_dd_row(p.w, ti.e, wrow), sel, tab};
+                    Q2KFmt f{q2k_sq_row(p.w, ti.e, wrow), q2k_dd_row(p.w, ti.e, wrow), part, tab};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
                 }
             }
             if (!ok) break;
-            // epilogue: accumulators -> registers -> global; two warps per TMEM lane quarter
+            // epilogue: accumulators -> registers -> global; four warps per TMEM lane quarter
             if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) {
                 ok = false;
                 break;
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_after();
             const int orow = ti.m * BM + q * 32 + lane;
             bool range_ok = true;
-            for (int c0 = 16 * colhalf; c0 < ti.ntok; c0 += 32) {
+            for (int c0 = 16 * colq; c0 < ti.ntok; c0 += 64) {
                 if (KIND == UP) {
                     float g[16], uu[16];
                     tmem_ld16(tmem + lane_addr + c0, g);
@@ -571,13 +571,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // The A operand as the producers write it, for tests: one 128-row x 64-column stage per CTA,
 // decoded by the same formats into a swizzled shared-memory tile, then un-swizzled into
 // dst16 [rows][cols] (fp16 bits).
-__global__ void __launch_bounds__(256) producer_dump_kernel(DeviceWeights w, const uint8_t *grid, int expert,
+__global__ void __launch_bounds__(kProducers) producer_dump_kernel(DeviceWeights w, const uint8_t *grid, int expert,
                                                             int matrix, uint16_t *dst16) {
     __shared__ __align__(1024) uint8_t tile[A_BYTES];
     __shared__ uint2 table[256 * 16];
     const int lane = threadIdx.x & 31;
-    const int u = threadIdx.x, r = u & 127, sel = u >> 7;
+    // the GEMM producers' slices: down, row (u >> 2) & 127, quarter u & 3; gate/up (one matrix),
+    // row (u >> 1) & 127, half u & 1 for u < 256
+    const int u = threadIdx.x;
     const bool down = matrix == DS4MOE_DOWN;
+    const int r = down ? (u >> 2) & 127 : (u >> 1) & 127;
     for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
         const uint32_t e = static_cast<uint32_t>(i >> 4);
         uint2 v;
@@ -600,11 +603,11 @@ __global__ void __launch_bounds__(256) producer_dump_kernel(DeviceWeights w, con
     const uint32_t t = smem_u32(tile);
     const uint2 *tab = table + (lane & 15);
     if (down) {
-        Q2KFmt f{q2k_sq_row(w, expert, wrow), q2k_dd_row(w, expert, wrow), sel, tab};
+        Q2KFmt f{q2k_sq_row(w, expert, wrow), q2k_dd_row(w, expert, wrow), u & 3, tab};
         f.emit(f.fetch(kb), t, r);
-    } else if (sel == 0) {
+    } else if (u < 256) {
         const int m = matrix == DS4MOE_GATE ? 0 : 1;
-        IQ2Fmt f{iq2_qs_row(w, m, expert, wrow), iq2_d_row(w, m, expert, wrow), tab, iq2_swz(w, wrow)};
+        IQ2Fmt f{iq2_qs_row(w, m, expert, wrow), iq2_d_row(w, m, expert, wrow), tab, iq2_swz(w, wrow), u & 1};
         f.emit(f.fetch(kb), t, r);
     }
     __syncthreads();
@@ -707,7 +710,7 @@ int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert
     const bool down = matrix == DS4MOE_DOWN;
     const int rows = down ? w.D : w.F, cols = down ? w.F : w.D;
     dim3 g(rows / BM, cols / BK);
-    producer_dump_kernel<<<g, 256, 0, static_cast<cudaStream_t>(stream)>>>(w, grid, expert, matrix, dst16);
+    producer_dump_kernel<<<g, kProducers, 0, static_cast<cudaStream_t>(stream)>>>(w, grid, expert, matrix, dst16);
     return static_cast<int>(cudaGetLastError());
 }
 
