@@ -240,6 +240,7 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     TRY(dev_alloc(h, &ws.gemm_list, E * 4));
     TRY(dev_alloc(h, &ws.single_list, E * 4));
     TRY(dev_alloc(h, &ws.tile_prefix, (E + 1) * 4));
+    TRY(dev_alloc(h, &ws.tile_desc, (E + P / kGemmBN + 1) * 16));
     TRY(dev_alloc(h, &ws.meta, sizeof(GroupMeta)));
     TRY(dev_alloc(h, &ws.grid, 2048));
     TRY(dev_alloc(h, &ws.h32, rows * F * 4));
@@ -344,7 +345,7 @@ int ds4moe_group(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, 
     if (static_cast<int64_t>(T) * k > (int64_t(1) << 30)) return DS4MOE_EINVAL;
     if (!counts || !offsets || (T > 0 && (!topk_idx || !perm || !inv))) return DS4MOE_EINVAL;
     return cuda_status(launch_group(topk_idx, T, k, E, 0, nullptr, counts, offsets, perm, inv, nullptr, nullptr,
-                                    nullptr, nullptr, nullptr, nullptr, nullptr, stream));
+                                    nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, stream));
 }
 
 int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits, int T, int k, int gate_mode,
@@ -394,7 +395,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     if (!rc) rc = clk.stage(DS4MOE_STAGE_GROUP);
     if (!rc)
         rc = launch_group(ws.topk_idx, T, k, w.E, gemm_min, w.tc_ok, ws.counts, ws.offsets, ws.perm, ws.inv,
-                          ws.gemv_list, ws.gemm_list, sg ? nullptr : ws.single_list, ws.tile_prefix,
+                          ws.gemv_list, ws.gemm_list, sg ? nullptr : ws.single_list, ws.tile_prefix, ws.tile_desc,
                           sg ? ws.small_pos : nullptr, ws.meta, ws.status, stream);
     if (up_tc) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_GATHER);

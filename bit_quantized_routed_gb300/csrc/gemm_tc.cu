@@ -87,7 +87,7 @@ __device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
 
 struct GemmParams {
     DeviceWeights w;
-    const int32_t *offsets, *gemm_list, *tile_prefix;
+    const int4 *tile_desc;
     const GroupMeta *meta;
     const uint8_t *grid;
     uint16_t *h16;  // UP output, [rows][F]
@@ -104,35 +104,23 @@ struct Tile {
     int m;       // weight-row tile
 };
 
-__device__ __forceinline__ int n_tiles_total(const GemmParams &p, int m_tiles) {
-    const int n_gemm = p.meta->n_gemm;
-    const int routed = p.tile_prefix[n_gemm];
+// Tiles t = nt * m_tiles + m: token tile nt (the routed experts' tiles first, in the order of
+// tile_desc, then the shared expert's), weight-row tile m. routed = meta->n_tiles.
+__device__ __forceinline__ int n_tiles_total(const GemmParams &p, int m_tiles, int routed) {
     const int sh = p.shared ? (p.T + BN - 1) / BN : 0;
     return (routed + sh) * m_tiles;
 }
 
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_tiles) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_tiles, int routed) {
     Tile ti;
     ti.m = t % m_tiles;
     const int nt = t / m_tiles;
-    const int n_gemm = p.meta->n_gemm;
-    const int routed = p.tile_prefix[n_gemm];
     if (nt < routed) {
-        int lo = 0, hi = n_gemm - 1;  // largest gi with tile_prefix[gi] <= nt
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.tile_prefix[mid] <= nt)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const int e = p.gemm_list[lo];
-        const int off = p.offsets[e], n = p.offsets[e + 1] - off;
-        const int lt = nt - p.tile_prefix[lo];
+        const int4 d = __ldg(p.tile_desc + nt);  // expert, first row, tokens
         ti.shared = 0;
-        ti.e = e;
-        ti.row0 = off + lt * BN;
-        ti.ntok = min(BN, n - lt * BN);
+        ti.e = d.x;
+        ti.row0 = d.y;
+        ti.ntok = d.z;
     } else {
         const int lt = nt - routed;
         ti.shared = 1;
@@ -153,6 +141,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_ti
 // into the swizzled A tile. Every fp16 value is RN-even of the weight's exact fp32 value.
 
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+__device__ __forceinline__ void prefetch_l2(const void *a) { asm volatile("prefetch.global.L2 [%0];" ::"l"(a)); }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
 // fp16 high byte of magnitude m in {1, 3, 5, 7}: their low bytes are zero.
@@ -163,6 +152,8 @@ __device__ __forceinline__ uint32_t mag_hibyte(uint32_t m) {
 // IQ2-style rows: one 32-weight sub-block (4 groups of 8) per stage.
 struct IQ2Fmt {
     static constexpr int PF = 4;
+    static constexpr int PD = 16;  // L2 prefetch distance (stages), every 8 stages (one 128-byte line of chunks)
+    static constexpr int PE = 8;
     struct Data {
         uint2 q;  // index word, sign/scale word
         uint32_t d;
@@ -178,6 +169,7 @@ struct IQ2Fmt {
         v.d = __ldg(dp + (kb >> 2));
         return v;
     }
+    __device__ __forceinline__ void prefetch(int kb) const { prefetch_l2(qs + 16 * (kb ^ swz)); }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
         const __half2 dh = u2h(v.d | (v.d << 16));
         const uint32_t iw = v.q.x, sw = v.q.y;
@@ -204,6 +196,8 @@ struct IQ2Fmt {
 // selects its four values with two byte permutations (selectors from a table).
 struct Q2KFmt {
     static constexpr int PF = 4;
+    static constexpr int PD = 8;  // L2 prefetch distance (stages), every 4 stages (one 80-byte block)
+    static constexpr int PE = 4;
     struct Data {
         uint32_t q;   // 16 codes
         uint32_t sc;  // scale byte (low 4 bits sc, high 4 bits m)
@@ -221,6 +215,11 @@ struct Q2KFmt {
         v.sc = __ldg(blk + 4 * part + qp);
         v.dd = __ldg(ddp + b);
         return v;
+    }
+    __device__ __forceinline__ void prefetch(int kb) const {
+        const uint8_t *blk = sq + (kb >> 2) * 80;
+        prefetch_l2(blk);
+        prefetch_l2(blk + 79);
     }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
         const float d = f16_to_f32(static_cast<uint16_t>(v.dd & 0xffffu));
@@ -246,6 +245,8 @@ struct Q2KFmt {
 // bf16 rows (shared gate/up), half row: 32 columns per stage -> fp16.
 struct BF16Fmt {
     static constexpr int PF = 1;
+    static constexpr int PD = 0;  // no L2 prefetch
+    static constexpr int PE = 1;
     struct Data {
         uint4 v[4];
     };
@@ -258,6 +259,7 @@ struct BF16Fmt {
         for (int c = 0; c < 4; c++) d.v[c] = __ldg(src + c);
         return d;
     }
+    __device__ __forceinline__ void prefetch(int) const {}
     __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
 #pragma unroll
         for (int c = 0; c < 4; c++) {
@@ -272,6 +274,8 @@ struct BF16Fmt {
 // fp16 rows (shared down), quarter row: 16 columns per stage -> copied.
 struct F16Fmt {
     static constexpr int PF = 2;
+    static constexpr int PD = 0;
+    static constexpr int PE = 1;
     struct Data {
         uint4 v[2];
     };
@@ -284,6 +288,7 @@ struct F16Fmt {
         for (int c = 0; c < 2; c++) d.v[c] = __ldg(src + c);
         return d;
     }
+    __device__ __forceinline__ void prefetch(int) const {}
     __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
 #pragma unroll
         for (int c = 0; c < 2; c++) st_shared16(tile + sw128_off(r, 2 * qp + c), d.v[c]);
@@ -314,6 +319,7 @@ __device__ __forceinline__ bool produce_tile(const Fmt &f, int num_kb, uint8_t *
             if (kb0 + i >= num_kb) break;
             const typename Fmt::Data cur = ring[i];
             if (kb0 + i + PF < num_kb) ring[i] = f.fetch(kb0 + i + PF);
+            if (Fmt::PD > 0 && (kb0 + i) % Fmt::PE == 0 && kb0 + i + Fmt::PD < num_kb) f.prefetch(kb0 + i + Fmt::PD);
             if (!mbar_wait(smem_u32(pp.bars + 2 * pp.S + pp.stage), pp.phase ^ 1u, pp.abort_flag, pp.status))
                 return false;
             f.emit(cur, smem_u32(smem + pp.stage * stage_bytes + a_off), r);
@@ -359,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = p.w.D, F = p.w.F;
     const int m_tiles = (KIND == UP ? F : D) / BM;
-    const int total = n_tiles_total(p, m_tiles);
+    const int routed = p.meta->n_tiles;
+    const int total = n_tiles_total(p, m_tiles, routed);
     if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA, before any allocation
     const int num_kb = (KIND == UP ? D : F) / BK;
 
@@ -421,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int s = 0; s < S; s++) issued_parity[s] = -1;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = decode_tile(p, t, m_tiles);
+                const Tile ti = decode_tile(p, t, m_tiles, routed);
                 const int bi = box_index(ti.ntok);
                 const CUtensorMap *map = &maps.m[bi];
                 const uint32_t bytes = static_cast<uint32_t>(16 << bi) * BK * 2;
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = decode_tile(p, t, m_tiles);
+                const Tile ti = decode_tile(p, t, m_tiles, routed);
                 if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -503,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile ti = decode_tile(p, t, m_tiles);
+            const Tile ti = decode_tile(p, t, m_tiles, routed);
             const int wrow = ti.m * BM + r;
             if (KIND == UP) {
                 if (ti.shared) {
@@ -678,9 +685,7 @@ int launch_gemm(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) {
 GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared) {
     GemmParams p;
     p.w = w;
-    p.offsets = ws.offsets;
-    p.gemm_list = ws.gemm_list;
-    p.tile_prefix = ws.tile_prefix;
+    p.tile_desc = reinterpret_cast<const int4 *>(ws.tile_desc);
     p.meta = ws.meta;
     p.grid = ws.grid;
     p.h16 = ws.h16;

@@ -105,6 +105,7 @@ struct GroupMeta {
     int n_gemm;    // experts with n_e >= gemm_min, listed in gemm_list in expert order
     int n_single;  // experts with exactly one token (when split off), listed in single_list
     int n_small_pairs;  // pairs of the gemv_list experts (positions listed in small_pos when requested)
+    int n_tiles;   // tensor-core token tiles of the gemm_list experts (ceil(n_e / kGemmBN) each)
 };
 
 struct Workspace {
@@ -119,6 +120,7 @@ struct Workspace {
     int32_t *gemm_list; // [E]
     int32_t *single_list; // [E]
     int32_t *tile_prefix; // [E+1] exclusive prefix of ceil(n_e / kGemmBN) over gemm_list
+    int32_t *tile_desc;   // [E + P/kGemmBN][4] per tensor-core token tile: expert, first row, tokens, 0
     GroupMeta *meta;
     uint8_t *grid;      // [256][8] IQ2-style grid
     uint8_t *grid_hi;   // [256][8] the grid's magnitudes as fp16 high bytes (1, 3, 5, 7 -> 3C, 42, 45, 47)
@@ -167,7 +169,7 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
                  void *stream);
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok,
                  int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list,
-                 int32_t *gemm_list, int32_t *single_list, int32_t *tile_prefix, int32_t *small_pos, GroupMeta *meta,
+                 int32_t *gemm_list, int32_t *single_list, int32_t *tile_prefix, int32_t *tile_desc, int32_t *small_pos, GroupMeta *meta,
                  int *status, void *stream);
 bool small_groups_supported(const DeviceWeights &w);
 int launch_prep_x(const Workspace &ws, const uint16_t *x, int T, int D, void *stream);

@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     group_kernel(const int32_t *__restrict__ idx, int P, int E, int gemm_min, const uint8_t *__restrict__ tc_ok,
                  int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                  int32_t *__restrict__ inv, int32_t *__restrict__ gemv_list, int32_t *__restrict__ gemm_list,
-                 int32_t *__restrict__ single_list, int32_t *__restrict__ tile_prefix, int32_t *__restrict__ small_pos,
-                 GroupMeta *meta, int *status) {
+                 int32_t *__restrict__ single_list, int32_t *__restrict__ tile_prefix, int32_t *__restrict__ tile_desc,
+                 int32_t *__restrict__ small_pos, GroupMeta *meta, int *status) {
     extern __shared__ int sm[];
     int *hist = sm;                      // [kGroupWarps][E]: counts, then base positions
     int *tmp = sm + kGroupWarps * E;     // [32]
@@ -166,11 +166,16 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     if (big && gemm_list) gemm_list[pb] = e;
     if (big && tile_prefix) tile_prefix[pb] = pt;
     if (threadIdx.x == 0 && tile_prefix) tile_prefix[n_big] = n_tiles;
+    // one descriptor per tensor-core token tile (expert, first row, tokens), in tile order
+    if (big && tile_desc)
+        for (int lt = 0; lt * kGemmBN < tot; lt++)
+            reinterpret_cast<int4 *>(tile_desc)[pt + lt] = make_int4(e, off + lt * kGemmBN, min(kGemmBN, tot - lt * kGemmBN), 0);
     if (threadIdx.x == 0 && meta) {
         meta->n_gemv = n_small;
         meta->n_gemm = n_big;
         meta->n_single = n_single;
         meta->n_small_pairs = n_small_pairs;
+        meta->n_tiles = n_tiles;
     }
     __syncthreads();
     // stable positions
@@ -220,7 +225,7 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
 
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok, int32_t *counts,
                  int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list, int32_t *gemm_list,
-                 int32_t *single_list, int32_t *tile_prefix, int32_t *small_pos, GroupMeta *meta, int *status,
+                 int32_t *single_list, int32_t *tile_prefix, int32_t *tile_desc, int32_t *small_pos, GroupMeta *meta, int *status,
                  void *stream) {
     const int P = T * k;
     const size_t smem = (static_cast<size_t>(kGroupWarps) * E + 32) * sizeof(int);
@@ -229,7 +234,7 @@ int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const ui
     if (err) return err;
     group_kernel<<<1, kGroupThreads, smem, static_cast<cudaStream_t>(stream)>>>(
         idx, P, E, gemm_min, tc_ok, counts, offsets, perm, inv, gemv_list, gemm_list, single_list, tile_prefix,
-        small_pos, meta, status);
+        tile_desc, small_pos, meta, status);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -64,6 +64,7 @@ size_t carve(unsigned char *base, int T, int k, int E, int D, int F, Workspace *
     ws->h32 = reinterpret_cast<float *>(take(rows * F * 4));
     ws->y = reinterpret_cast<float *>(take(rows * D * 4));
     ws->tile_prefix = nullptr;
+    ws->tile_desc = nullptr;
     ws->single_list = nullptr;
     ws->h16 = nullptr;
     ws->x16 = nullptr;
@@ -100,7 +101,7 @@ extern "C" int ds4moe_expert_ffn_static(const uint16_t *x, const ds4moe_weights 
     int rc = launch_route(logits, T, w.E, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
     if (!rc)
         rc = launch_group(ws.topk_idx, T, k, w.E, 0, nullptr, ws.counts, ws.offsets, ws.perm, ws.inv, ws.gemv_list,
-                          ws.gemm_list, nullptr, nullptr, nullptr, ws.meta, ws.status, stream);
+                          ws.gemm_list, nullptr, nullptr, nullptr, nullptr, ws.meta, ws.status, stream);
     if (!rc) rc = launch_gemv_up(w, ws, x, T, k, true, stream);
     if (!rc) rc = launch_gemv_down(w, ws, T, k, true, stream);
     if (!rc) rc = launch_combine(w, ws, T, k, out, stream);
