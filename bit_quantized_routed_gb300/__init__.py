@@ -19,6 +19,7 @@ DS4MOE_EBADDATA = 4
 DS4MOE_ETIMEOUT = 5
 DS4MOE_EUNSUPPORTED = 6
 DS4MOE_ERANGE = 7
+DS4MOE_ECAPACITY = 8
 
 DS4MOE_GATE_SOFTMAX = 0
 DS4MOE_GATE_SIGMOID = 1
@@ -29,12 +30,12 @@ DS4MOE_OPT_PROFILE = 2
 DS4MOE_OPT_SINGLE_STEP = 3
 DS4MOE_OPT_TRACE = 4
 DS4MOE_OPT_SMALL_GROUPS = 5
-STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step"]
+STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step", "pool"]
 
 EXPORTED = [
     "ds4moe_strerror", "ds4moe_q2k_bytes", "ds4moe_iq2_bytes", "ds4moe_iq2_grid",
     "ds4moe_quantize_q2k", "ds4moe_quantize_iq2", "ds4moe_dequantize_q2k", "ds4moe_dequantize_iq2",
-    "ds4moe_weights_create", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
+    "ds4moe_weights_create", "ds4moe_weights_create_pooled", "ds4moe_pool_info", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
     "ds4moe_router_logits", "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
     "ds4moe_expert_ffn_static", "ds4moe_step_trace",
 ]
@@ -58,7 +59,7 @@ class _Desc(ctypes.Structure):
 
 
 class _Stats(ctypes.Structure):
-    _fields_ = [("calls", ctypes.c_uint64), ("launches", ctypes.c_uint64), ("stage_ms", ctypes.c_float * 9)]
+    _fields_ = [("calls", ctypes.c_uint64), ("launches", ctypes.c_uint64), ("stage_ms", ctypes.c_float * 10)]
 
 
 _lib = None
@@ -82,6 +83,9 @@ def lib():
             "ds4moe_dequantize_q2k": ([vp, i64, i64, vp], i32),
             "ds4moe_dequantize_iq2": ([vp, i64, i64, vp], i32),
             "ds4moe_weights_create": ([ctypes.POINTER(_Desc), ctypes.POINTER(vp)], i32),
+            "ds4moe_weights_create_pooled": ([ctypes.POINTER(_Desc), i32, ctypes.POINTER(vp)], i32),
+            "ds4moe_pool_info": ([vp, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_uint64),
+                                  ctypes.POINTER(ctypes.c_uint64), vp], i32),
             "ds4moe_weights_destroy": ([vp], None),
             "ds4moe_set_option": ([vp, i32, i32], i32),
             "ds4moe_weights_dequantize": ([vp, i32, i32, vp, vp, vp], i32),
@@ -202,9 +206,12 @@ class Weights:
             pass
 
 
-def ds4moe_weights_create(gate_iq2, up_iq2, down_q2k, d_model, d_ff, shared=None, max_tokens=1, max_k=8):
+def ds4moe_weights_create(gate_iq2, up_iq2, down_q2k, d_model, d_ff, shared=None, max_tokens=1, max_k=8,
+                          n_slots=None):
     """Upload per-expert packed blobs (lists of uint8 arrays) and an optional bf16 shared
-    expert (gate, up, down as uint16 arrays of bf16 bits) to the current CUDA device."""
+    expert (gate, up, down as uint16 arrays of bf16 bits) to the current CUDA device. With
+    n_slots, a pooled handle (ds4moe_weights_create_pooled): the experts stay in pinned host
+    memory and stream into n_slots device slots as calls touch them."""
     E = len(gate_iq2)
     keep = []
 
@@ -229,8 +236,23 @@ def ds4moe_weights_create(gate_iq2, up_iq2, down_q2k, d_model, d_ff, shared=None
         keep.extend(sh)
         desc.shared_gate_bf16, desc.shared_up_bf16, desc.shared_down_bf16 = (s.ctypes.data for s in sh)
     h = ctypes.c_void_p()
-    _check(lib().ds4moe_weights_create(ctypes.byref(desc), ctypes.byref(h)), "ds4moe_weights_create")
+    if n_slots is None:
+        _check(lib().ds4moe_weights_create(ctypes.byref(desc), ctypes.byref(h)), "ds4moe_weights_create")
+    else:
+        _check(lib().ds4moe_weights_create_pooled(ctypes.byref(desc), int(n_slots), ctypes.byref(h)),
+               "ds4moe_weights_create_pooled")
     return Weights(h, d_model, d_ff, E, max_tokens, max_k, shared is not None)
+
+
+def ds4moe_pool_info(weights):
+    """(n_slots, hits, misses, slot_expert int32 [n_slots]) of a pooled handle."""
+    n = ctypes.c_int(0)
+    _check(lib().ds4moe_pool_info(weights.handle, ctypes.byref(n), None, None, None), "ds4moe_pool_info")
+    hits, misses = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    slots = np.zeros(n.value, np.int32)
+    _check(lib().ds4moe_pool_info(weights.handle, None, ctypes.byref(hits), ctypes.byref(misses), slots.ctypes.data),
+           "ds4moe_pool_info")
+    return n.value, hits.value, misses.value, slots
 
 
 def ds4moe_weights_destroy(weights):

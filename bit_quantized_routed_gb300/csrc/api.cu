@@ -34,6 +34,28 @@ int dev_alloc(ds4moe_weights *h, T **p, size_t bytes) {
 void free_all(ds4moe_weights *h) {
     for (int i = 0; i < h->n_allocs; i++) cudaFree(h->allocs[i]);
     h->n_allocs = 0;
+    for (int i = 0; i < h->n_host_allocs; i++) cudaFreeHost(h->host_allocs[i]);
+    h->n_host_allocs = 0;
+}
+
+// Pinned host memory that the device can read (device-mapped); *dev receives its device address.
+template <class T>
+int host_alloc(ds4moe_weights *h, T **p, const uint8_t **dev, size_t bytes) {
+    *p = nullptr;
+    if (h->n_host_allocs >= static_cast<int>(sizeof(h->host_allocs) / sizeof(h->host_allocs[0]))) return DS4MOE_ENOMEM;
+    void *q = nullptr, *d = nullptr;
+    if (cudaHostAlloc(&q, bytes ? bytes : 16, cudaHostAllocMapped) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ENOMEM;
+    }
+    h->host_allocs[h->n_host_allocs++] = q;
+    if (cudaHostGetDevicePointer(&d, q, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ECUDA;
+    }
+    *p = static_cast<T *>(q);
+    *dev = static_cast<const uint8_t *>(d);
+    return DS4MOE_OK;
 }
 
 int cuda_status(int err) {
@@ -115,9 +137,11 @@ struct StageClock {
     StageClock(ds4moe_weights *h_, ds4moe_stream_t s_) : h(h_), s(s_) {
         for (bool &r : h->stage_ran) r = false;
         h->events_recorded = false;
+        h->n_stage_order = 0;
     }
     int stage(int i) {
         h->stage_ran[i] = true;
+        h->stage_order[h->n_stage_order++] = i;
         h->launches++;
         if (!h->profile) return 0;
         return static_cast<int>(cudaEventRecord(static_cast<cudaEvent_t>(h->events[i]), s));
@@ -133,12 +157,16 @@ struct StageClock {
 
 extern "C" {
 
-int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out) {
+// n_slots = 0: every expert resident in device memory; otherwise a pooled handle (see
+// ds4moe_weights_create_pooled) whose device weights are n_slots expert slots.
+static int create_impl(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weights **out) {
     if (!desc || !out) return DS4MOE_EINVAL;
     *out = nullptr;
     const int D = desc->d_model, F = desc->d_ff, E = desc->n_experts;
     if (D <= 0 || F <= 0 || D % 256 || F % 256 || E < 1 || E > 1024) return DS4MOE_EINVAL;
     if (desc->max_tokens < 1 || desc->max_k < 1 || desc->max_k > 32 || desc->max_k > E) return DS4MOE_EINVAL;
+    if (n_slots < 0 || (n_slots > 0 && (n_slots > E || n_slots < desc->max_k))) return DS4MOE_EINVAL;
+    const int S = n_slots ? n_slots : E;  // experts held in device memory
     if (!desc->gate_iq2 || !desc->up_iq2 || !desc->down_q2k) return DS4MOE_EINVAL;
     for (int e = 0; e < E; e++)
         if (!desc->gate_iq2[e] || !desc->up_iq2[e] || !desc->down_q2k[e]) return DS4MOE_EINVAL;
@@ -162,7 +190,7 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     DeviceWeights &w = h->dw;
     w.D = D;
     w.F = F;
-    w.E = E;
+    w.E = S;
     w.nbD = D / 256;
     w.nbF = F / 256;
     w.has_shared = n_shared == 3;
@@ -170,9 +198,31 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     const size_t nb_down = static_cast<size_t>(D) * w.nbF;  // blocks per down matrix
     const size_t up_bytes = nb_up * 132;       // gate + up of one expert, tiled (66 bytes per block each)
     const size_t down_bytes = nb_down * 84;    // down of one expert, tiled
-    TRY(dev_alloc(h, &w.iq2, E * up_bytes));
-    TRY(dev_alloc(h, &w.q2k, E * down_bytes));
-    TRY(dev_alloc(h, &w.tc_ok, E));
+    TRY(dev_alloc(h, &w.iq2, S * up_bytes));
+    TRY(dev_alloc(h, &w.q2k, S * down_bytes));
+    TRY(dev_alloc(h, &w.tc_ok, S));
+    SlotPool &sp = h->pool;
+    uint8_t *store_iq2 = nullptr, *store_q2k = nullptr, *store_ok = nullptr;  // pooled: host views of the store
+    if (n_slots) {
+        sp.S = S;
+        sp.E = E;
+        sp.up_bytes = up_bytes;
+        sp.down_bytes = down_bytes;
+        TRY(host_alloc(h, &store_iq2, &sp.host_iq2, E * up_bytes));
+        TRY(host_alloc(h, &store_q2k, &sp.host_q2k, E * down_bytes));
+        TRY(host_alloc(h, &store_ok, &sp.host_tc_ok, E));
+        TRY(dev_alloc(h, &sp.slot_of, E * 4));
+        TRY(dev_alloc(h, &sp.expert_of, S * 4));
+        TRY(dev_alloc(h, &sp.stamp, S * 4));
+        TRY(dev_alloc(h, &sp.ctr, 4 * 8));
+        TRY(dev_alloc(h, &sp.miss, S * 8));
+        // no expert resident yet; empty slots hold zero blocks (every weight 0)
+        if (cudaMemset(sp.slot_of, 0xff, E * 4) != cudaSuccess || cudaMemset(sp.expert_of, 0xff, S * 4) != cudaSuccess ||
+            cudaMemset(sp.stamp, 0, S * 4) != cudaSuccess || cudaMemset(sp.ctr, 0, 32) != cudaSuccess ||
+            cudaMemset(sp.miss, 0, S * 8) != cudaSuccess || cudaMemset(w.iq2, 0, S * up_bytes) != cudaSuccess ||
+            cudaMemset(w.q2k, 0, S * down_bytes) != cudaSuccess || cudaMemset(w.tc_ok, 0, S) != cudaSuccess)
+            TRY(DS4MOE_ECUDA);
+    }
     {
         std::vector<uint8_t> qs(nb_up * 64), sq(nb_down * 80), ok(E), tiles(std::max(up_bytes, down_bytes));
         std::vector<uint16_t> dv(nb_up);
@@ -193,7 +243,10 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
                                 static_cast<size_t>(w.nbD) * 2);
                 }
             }
-            TRY(upload(w.iq2 + e * up_bytes, tiles.data(), up_bytes));
+            if (n_slots)
+                std::memcpy(store_iq2 + e * up_bytes, tiles.data(), up_bytes);
+            else
+                TRY(upload(w.iq2 + e * up_bytes, tiles.data(), up_bytes));
             if (!repack_q2k(static_cast<const uint8_t *>(desc->down_q2k[e]), nb_down, sq.data(), dd.data(), &amax))
                 TRY(DS4MOE_EBADDATA);
             for (int r = 0; r < D; r++) {
@@ -202,10 +255,16 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
                 std::memcpy(tiles.data() + q2k_dd_offset(w0, 0, r), dd.data() + static_cast<size_t>(r) * w.nbF,
                             static_cast<size_t>(w.nbF) * 4);
             }
-            TRY(upload(w.q2k + e * down_bytes, tiles.data(), down_bytes));
+            if (n_slots)
+                std::memcpy(store_q2k + e * down_bytes, tiles.data(), down_bytes);
+            else
+                TRY(upload(w.q2k + e * down_bytes, tiles.data(), down_bytes));
             ok[e] = amax <= kF16Max ? 1 : 0;  // otherwise the expert stays on the fp32 GEMV path
         }
-        TRY(upload(w.tc_ok, ok.data(), E));
+        if (n_slots)
+            std::memcpy(store_ok, ok.data(), E);
+        else
+            TRY(upload(w.tc_ok, ok.data(), E));
     }
     if (w.has_shared) {
         const size_t n = static_cast<size_t>(F) * D;
@@ -274,6 +333,31 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
     return DS4MOE_OK;
 }
 
+int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out) { return create_impl(desc, 0, out); }
+
+int ds4moe_weights_create_pooled(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weights **out) {
+    if (n_slots < 1) {
+        if (out) *out = nullptr;
+        return DS4MOE_EINVAL;
+    }
+    return create_impl(desc, n_slots, out);
+}
+
+int ds4moe_pool_info(ds4moe_weights *h, int *n_slots, uint64_t *hits, uint64_t *misses, int32_t *slot_expert) {
+    if (!h || !h->pool.S) return DS4MOE_EINVAL;
+    unsigned long long c[4] = {0, 0, 0, 0};
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(c, h->pool.ctr, sizeof c, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        (slot_expert && cudaMemcpy(slot_expert, h->pool.expert_of, static_cast<size_t>(h->pool.S) * 4,
+                                   cudaMemcpyDeviceToHost) != cudaSuccess)) {
+        cudaGetLastError();
+        return DS4MOE_ECUDA;
+    }
+    if (n_slots) *n_slots = h->pool.S;
+    if (hits) *hits = c[1];
+    if (misses) *misses = c[2];
+    return DS4MOE_OK;
+}
+
 void ds4moe_weights_destroy(ds4moe_weights *h) {
     if (!h) return;
     int cur = 0;
@@ -313,6 +397,7 @@ int ds4moe_weights_dequantize(const ds4moe_weights *h, int expert, int matrix, f
                               ds4moe_stream_t stream) {
     if (!h || expert < 0 || expert >= h->dw.E || matrix < 0 || matrix > 2 || (!dst_f32 && !dst_f16))
         return DS4MOE_EINVAL;
+    if (h->pool.S) return DS4MOE_EUNSUPPORTED;  // a pooled handle's slots change from call to call
     int rc = 0;
     if (dst_f32) rc = launch_dequant(h->dw, h->ws.grid, expert, matrix, dst_f32, nullptr, stream);
     // the fp16 values are the tensor-core path's own operand bytes, from its producers
@@ -358,11 +443,27 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     const DeviceWeights &w = h->dw;
     const Workspace &ws = h->ws;
     StageClock clk(h, stream);
+    const bool pooled = h->pool.S > 0;
+    const int E_route = pooled ? h->pool.E : w.E;  // the experts the logits route over
+    int rc = 0;
+    if (pooled) {
+        // a pooled handle routes first: slots for the touched experts, the missing ones copied
+        // in, the top-k indices rewritten to slots (the fused kernel maps its own top-k)
+        rc = clk.stage(DS4MOE_STAGE_ROUTE);
+        if (!rc) rc = launch_route(logits, T, E_route, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
+        if (!rc) rc = clk.stage(DS4MOE_STAGE_POOL);
+        if (!rc) rc = launch_pool_assign(h->pool, ws.topk_idx, T * k, ws.status, stream);
+        if (!rc) rc = launch_pool_fill(h->pool, w, decode_step_ctas(), stream);
+        h->launches++;
+        if (rc) return cuda_status(rc);
+    }
     if (T == 1 && h->single_step && decode_step_supported(w, k) &&
         !(h->gemm_min_tokens == 1 || (w.has_shared && h->shared_gemm_min_tokens == 1))) {
         // one token: routing, both expert phases and the combine in one cooperative kernel
-        int rc = clk.stage(DS4MOE_STAGE_STEP);
-        if (!rc) rc = launch_decode_step(w, ws, x, logits, k, gate_mode, out, h->trace ? ws.trace : nullptr, stream);
+        rc = clk.stage(DS4MOE_STAGE_STEP);
+        if (!rc)
+            rc = launch_decode_step(w, ws, x, logits, k, gate_mode, out, h->trace ? ws.trace : nullptr, E_route,
+                                    pooled ? h->pool.slot_of : nullptr, stream);
         if (!rc) {
             rc = clk.finish();
             h->calls++;
@@ -372,6 +473,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         cudaGetLastError();
         h->stage_ran[DS4MOE_STAGE_STEP] = false;
         h->launches--;
+        rc = 0;
     }
     // A group holds at most T tokens, so the tensor-core path can only be needed when
     // T reaches the threshold; the device decides per group after routing.
@@ -390,8 +492,10 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     const bool shared_up_small = sg && shared_tc && T <= shared_small_max_tokens() && h->gemm_min_tokens != 1 &&
                                  h->shared_gemm_min_tokens != 1;
     const bool up_tc = gemm_min > 0 || (shared_tc && !shared_up_small);
-    int rc = clk.stage(DS4MOE_STAGE_ROUTE);
-    if (!rc) rc = launch_route(logits, T, w.E, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
+    if (!pooled) {  // (a pooled handle has routed already)
+        rc = clk.stage(DS4MOE_STAGE_ROUTE);
+        if (!rc) rc = launch_route(logits, T, w.E, k, gate_mode, ws.topk_idx, ws.topk_w, stream);
+    }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_GROUP);
     if (!rc)
         rc = launch_group(ws.topk_idx, T, k, w.E, gemm_min, w.tc_ok, ws.counts, ws.offsets, ws.perm, ws.inv,
@@ -467,10 +571,16 @@ int ds4moe_get_stats(ds4moe_weights *h, ds4moe_stats *out) {
         cudaGetLastError();
         return DS4MOE_ECUDA;
     }
-    for (int i = 0; i < DS4MOE_N_STAGES; i++) {
-        if (!h->stage_ran[i]) continue;
-        int j = i + 1;  // the next recorded event ends this stage
-        while (j < DS4MOE_N_STAGES && !h->stage_ran[j]) j++;
+    for (int n = 0; n < h->n_stage_order; n++) {
+        const int i = h->stage_order[n];
+        if (!h->stage_ran[i]) continue;  // a stage taken back (the fused kernel's refused launch)
+        // the next stage recorded in this call ends this one, the call's end event the last
+        int j = DS4MOE_N_STAGES;
+        for (int m = n + 1; m < h->n_stage_order; m++)
+            if (h->stage_ran[h->stage_order[m]]) {
+                j = h->stage_order[m];
+                break;
+            }
         float ms = 0.0f;
         if (cudaEventElapsedTime(&ms, static_cast<cudaEvent_t>(h->events[i]),
                                  static_cast<cudaEvent_t>(h->events[j])) != cudaSuccess) {
@@ -506,6 +616,7 @@ int ds4moe_last_status(ds4moe_weights *h, ds4moe_stream_t stream) {
     if (st & ST_RANGE) return DS4MOE_ERANGE;
     if (st & ST_TIMEOUT) return DS4MOE_ETIMEOUT;
     if (st & ST_BADIDX) return DS4MOE_EINVAL;
+    if (st & ST_CAPACITY) return DS4MOE_ECAPACITY;
     return DS4MOE_OK;
 }
 

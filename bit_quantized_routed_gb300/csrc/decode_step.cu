@@ -100,6 +100,8 @@ struct StepParams {
     DeviceWeights w;
     const uint16_t *x;     // bf16 [D]
     const float *logits;   // [E]
+    int E;                 // experts the logits route over (a pooled handle: its store's)
+    const int32_t *slot_of;  // null, or a pooled handle's expert -> slot map
     float *out;            // [D], += delta
     int k, mode;
     const uint8_t *grid;   // codebook magnitudes [256][8]
@@ -218,7 +220,7 @@ __device__ void issue2(const StepParams &p, const int *idx, int unit, uint32_t d
 // weights of the selected experts (softmax over them, or normalised sigmoids).
 template <int NJ>
 __device__ void route_warp(const StepParams &p, int lane, int *sidx, float *sgw) {
-    const int E = p.w.E;
+    const int E = p.E;
     float key[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; j++) {
@@ -260,7 +262,7 @@ __device__ void route_warp(const StepParams &p, int lane, int *sidx, float *sgw)
     if (lane < p.k) num = (p.mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
     const float den = warp_sum(num);
     if (lane < p.k) {
-        sidx[lane] = my_i;
+        sidx[lane] = p.slot_of ? p.slot_of[my_i] : my_i;  // a pooled handle's experts sit in slots
         sgw[lane] = num / den;
         if (blockIdx.x == 0) {
             p.topk_idx[lane] = my_i;
@@ -286,7 +288,7 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // then every round takes the largest head key over the warp with one reduction and, among the
 // heads that hold it, the smallest expert index with a second; that lane drops its head.
 __device__ void route_sorted8(const StepParams &p, int lane, int *sidx, float *sgw) {
-    const int E = p.w.E;
+    const int E = p.E;
     uint32_t key[8];
     int id[8];
 #pragma unroll
@@ -334,7 +336,7 @@ __device__ void route_sorted8(const StepParams &p, int lane, int *sidx, float *s
     if (lane < p.k) num = (p.mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
     const float den = warp_sum(num);
     if (lane < p.k) {
-        sidx[lane] = my_i;
+        sidx[lane] = p.slot_of ? p.slot_of[my_i] : my_i;  // a pooled handle's experts sit in slots
         sgw[lane] = num / den;
         if (blockIdx.x == 0) {
             p.topk_idx[lane] = my_i;
@@ -500,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
     // ---------------------------------------------------------------- finisher
     if (warp == kFinisher) {
         // route first: the producer's routed units and the down phase wait for it
-        if (w.E <= 256)
+        if (p.E <= 256)
             route_sorted8(p, lane, sidx, sgw);
         else
             route_warp<32>(p, lane, sidx, sgw);
@@ -873,7 +875,7 @@ bool decode_step_supported(const DeviceWeights &w, int k) {
 }
 
 int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, const float *logits, int k,
-                       int gate_mode, float *out, uint64_t *trace, void *stream) {
+                       int gate_mode, float *out, uint64_t *trace, int E_route, const int32_t *slot_of, void *stream) {
     static int seen[3][64];
     const int nq = w.D <= 1024 ? 1 : w.D <= 2048 ? 2 : 4;  // 1024-column quarters of x
     const void *kern = nq == 1   ? reinterpret_cast<const void *>(decode_step_kernel<1>)
@@ -885,6 +887,8 @@ int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16
     p.w = w;
     p.x = x;
     p.logits = logits;
+    p.E = E_route;
+    p.slot_of = slot_of;
     p.out = out;
     p.k = k;
     p.mode = gate_mode;

@@ -321,6 +321,7 @@ const char *ds4moe_strerror(int status) {
         case DS4MOE_ETIMEOUT: return "device-side wait timed out";
         case DS4MOE_EUNSUPPORTED: return "unsupported shape or device";
         case DS4MOE_ERANGE: return "value outside the fp16 range of the tensor-core path";
+        case DS4MOE_ECAPACITY: return "a call touched more experts than the handle's slots";
         default: return "unknown status";
     }
 }

@@ -20,6 +20,7 @@ enum : int {
     ST_RANGE = 1,    // a value overflowed fp16 on the tensor-core path
     ST_TIMEOUT = 2,  // a bounded wait gave up
     ST_BADIDX = 4,   // an expert index outside [0, E) reached the grouping kernel
+    ST_CAPACITY = 8, // a call touched more experts than a pooled handle's slots
 };
 
 // Resident, repacked expert weights. Each IQ2-style row keeps its 64-byte block payloads
@@ -108,6 +109,23 @@ struct GroupMeta {
     int n_tiles;   // tensor-core token tiles of the gemm_list experts (ceil(n_e / kGemmBN) each)
 };
 
+// Streamed experts (pooled handles): the host store and the slot state. The store holds every
+// expert in the device layout (gate/up tiles, then down tiles); the device pool (DeviceWeights
+// with E = S) holds S of them.
+struct SlotPool {
+    int S;                       // slots, 0 for a resident handle
+    int E;                       // experts in the store
+    size_t up_bytes, down_bytes; // one expert's gate/up and down ranges
+    const uint8_t *host_iq2;     // [E][up_bytes]   device-mapped pinned host memory
+    const uint8_t *host_q2k;     // [E][down_bytes]
+    const uint8_t *host_tc_ok;   // [E]
+    int32_t *slot_of;            // [E] slot of each expert, -1 if not resident
+    int32_t *expert_of;          // [S] expert of each slot, -1 if empty
+    uint32_t *stamp;             // [S] number of the last call that used the slot, 0 if none
+    unsigned long long *ctr;     // [4] calls, hits, misses, misses of the last call
+    int32_t *miss;               // [S][2] the last call's misses: expert, slot
+};
+
 struct Workspace {
     int max_T, max_k;
     int32_t *topk_idx;  // [T*k]
@@ -156,6 +174,11 @@ struct ds4moe_weights {
     uint64_t calls, launches;
     alignas(64) unsigned char tmap_x16[128 * ds4moe::kTokenBoxes];  // CUtensorMaps of x16 [rows][D]
     alignas(64) unsigned char tmap_h16[128 * ds4moe::kTokenBoxes];  // CUtensorMaps of h16 [rows][F]
+    int stage_order[DS4MOE_N_STAGES];  // stages in the order the last call recorded them
+    int n_stage_order;
+    ds4moe::SlotPool pool;            // pool.S > 0: a pooled handle
+    void *host_allocs[4];             // pinned host memory of the pool's store
+    int n_host_allocs;
     void *allocs[64];
     int n_allocs;
 };
@@ -167,6 +190,8 @@ int launch_router(const uint16_t *x, const uint16_t *w, const float *bias, int T
                   void *stream);
 int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *idx, float *w,
                  void *stream);
+int launch_pool_assign(const SlotPool &sp, int32_t *idx, int P, int *status, void *stream);
+int launch_pool_fill(const SlotPool &sp, const DeviceWeights &w, int n_sms, void *stream);
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok,
                  int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list,
                  int32_t *gemm_list, int32_t *single_list, int32_t *tile_prefix, int32_t *tile_desc, int32_t *small_pos, GroupMeta *meta,
@@ -192,8 +217,9 @@ int launch_decode_up(const DeviceWeights &w, const Workspace &ws, const uint16_t
                      void *stream);
 int launch_decode_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared, void *stream);
 bool decode_step_supported(const DeviceWeights &w, int k);
+// E_route: experts the logits route over; slot_of: null, or a pooled handle's expert -> slot map
 int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, const float *logits, int k,
-                       int gate_mode, float *out, uint64_t *trace, void *stream);
+                       int gate_mode, float *out, uint64_t *trace, int E_route, const int32_t *slot_of, void *stream);
 int decode_step_ctas();
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
                    bool shared_on_gemv, void *stream);

@@ -46,7 +46,8 @@ enum ds4moe_status {
     DS4MOE_EBADDATA = 4,     /* input data rejected (non-finite weights, bad packed scale) */
     DS4MOE_ETIMEOUT = 5,     /* a bounded device-side wait gave up */
     DS4MOE_EUNSUPPORTED = 6, /* shape or device not supported by this build */
-    DS4MOE_ERANGE = 7        /* a value overflowed the fp16 operand range of the tensor-core path */
+    DS4MOE_ERANGE = 7,       /* a value overflowed the fp16 operand range of the tensor-core path */
+    DS4MOE_ECAPACITY = 8     /* a call touched more experts than a pooled handle's slots */
 };
 
 enum ds4moe_gate_mode {
@@ -95,7 +96,8 @@ enum ds4moe_stage {
     DS4MOE_STAGE_DOWN_GEMM = 6, /* tensor-core down */
     DS4MOE_STAGE_COMBINE = 7,   /* gate-weighted combine into the residual */
     DS4MOE_STAGE_STEP = 8,      /* the single-token kernel: the whole call */
-    DS4MOE_N_STAGES = 9
+    DS4MOE_STAGE_POOL = 9,      /* pooled handles: slot assignment and the copies of missing experts */
+    DS4MOE_N_STAGES = 10
 };
 
 typedef struct {
@@ -158,6 +160,28 @@ typedef struct {
  * repacks them into the device layout, uploads them and allocates the workspace for
  * max_tokens x max_k pairs. Synchronous. EBADDATA names a non-finite fp16 scale. */
 int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out);
+
+/* A handle whose routed experts stream from host memory into a pool of n_slots expert slots
+ * in device memory ("DwarfStar" README, "运行大于 RAM 的模型": a model larger than memory
+ * keeps its routed experts outside and loads the ones each token routes to). The packed
+ * experts are kept in pinned, device-mapped host memory in the device layout, which the GPU
+ * reads directly (over NVLink-C2C on Grace systems). Each call, after routing and in stream
+ * order (no host synchronisation):
+ *   - every expert the call touches gets a slot: a resident expert keeps its slot (a hit);
+ *     each missing expert, in increasing expert order, takes the slot not used by this call
+ *     that was used least recently (empty slots first, then the oldest last use, ties to the
+ *     lower slot), evicting its expert, and is copied in (a miss);
+ *   - the experts then run on the same kernels as a resident handle's (not the fused
+ *     single-token kernel), with results identical bit for bit to a resident handle's.
+ * A call that touches more than n_slots experts records DS4MOE_ECAPACITY in the status word
+ * (ds4moe_last_status), changes no slot and leaves out unspecified.
+ * max_k <= n_slots <= n_experts. Other arguments and errors as ds4moe_weights_create. */
+int ds4moe_weights_create_pooled(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weights **out);
+
+/* Pool state of a pooled handle (synchronises the device): its slot count, the hits and
+ * misses since creation, and (slot_expert: n_slots ints, may be NULL) the expert held by each
+ * slot or -1. Any output pointer may be NULL. EINVAL for a handle that is not pooled. */
+int ds4moe_pool_info(ds4moe_weights *w, int *n_slots, uint64_t *hits, uint64_t *misses, int32_t *slot_expert);
 
 /* Free a handle (NULL is allowed). Synchronises the device first. */
 void ds4moe_weights_destroy(ds4moe_weights *w);

@@ -41,6 +41,8 @@ class Workload:
     bias: tuple = ()        # () | ("normal", sigma) | ("zipf", s)
     tie_frac: float = 0.0   # fraction of tokens with forced exact logit ties
     shared: bool = True     # one always-on bf16 shared expert of the same shape
+    slots: int = 0          # > 0: experts stream from host memory into this many device slots
+    ring: int = 1           # distinct inputs cycled through, one per step (seeds seed .. seed+ring-1)
 
     def replace(self, **kw):
         d = dict(self.__dict__)
@@ -56,6 +58,9 @@ WORKLOADS = {
         Workload("prefill_t2048", T=2048, D=4096, F=2048, E=256, k=8, seed=3, bias=("zipf", 1.0)),
         Workload("prefill_t8192_d7168", T=8192, D=7168, F=2048, E=256, k=8, seed=4,
                  bias=("zipf", 1.2), tie_frac=0.05),
+        # decode with cold experts: 64 of the 256 experts fit in device memory, and each step is
+        # a different token, so most of its experts must be copied in from host memory
+        Workload("decode_t1_cold", T=1, D=4096, F=2048, E=256, k=8, seed=11, slots=64, ring=64),
     ]
 }
 

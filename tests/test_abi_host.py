@@ -114,3 +114,7 @@ def test_device_entry_points_reject_bad_arguments_on_host(ds4):
     assert L.ds4moe_set_option(None, 0, 1) == ds4.DS4MOE_EINVAL
     assert L.ds4moe_weights_dequantize(None, 0, 0, None, None, None) == ds4.DS4MOE_EINVAL
     assert L.ds4moe_weights_create(None, None) == ds4.DS4MOE_EINVAL
+    # pooled handles: at least one slot, a descriptor; pool state only of a pooled handle
+    assert L.ds4moe_weights_create_pooled(None, 4, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_weights_create_pooled(None, 0, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_pool_info(None, None, None, None, None) == ds4.DS4MOE_EINVAL
