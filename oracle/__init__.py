@@ -11,7 +11,8 @@ Sources (page titles and sections):
     IQ2_XXS and down to Q2_K; shared expert, projections and router stay unquantised.
   * "DwarfStar 深度解析", §2.1 (routed MoE: the experts a token uses are chosen per token)
     and §3.4.3 (the quantisation split; the router stays at full precision).
-  * The byte layouts, the grid and the quantisers are readings fixed in FORMAT.md.
+  * The byte layouts, the grid and the quantisers are readings fixed in FORMAT.md, including
+    the Q4_K-style block of the 4-bit variant ("DwarfStar" README, "模型权重": the q4 build).
 
 Parity pins: every function here is checked in ``tests/test_oracle_*.py`` against something
 other than itself (numpy's float16 rounding, a published splitmix64 output, hand-built
@@ -64,6 +65,9 @@ def lib():
         L.or_iq2_quantize.argtypes = [f32p, i64, i64, u8p, u8p]
         L.or_iq2_quantize.restype = ctypes.c_int
         L.or_q2k_dequant.argtypes = [u8p, i64, i64, f32p]
+        L.or_q4k_quantize.argtypes = [f32p, i64, i64, u8p]
+        L.or_q4k_quantize.restype = ctypes.c_int
+        L.or_q4k_dequant.argtypes = [u8p, i64, i64, f32p]
         L.or_iq2_dequant.argtypes = [u8p, i64, i64, u8p, f32p]
         L.or_route.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, f64p]
         L.or_permute.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, i32p, i32p, i32p]
@@ -76,6 +80,7 @@ def _p(a, ctype):
 
 
 Q2K_BLOCK_BYTES = 84
+Q4K_BLOCK_BYTES = 144
 IQ2_BLOCK_BYTES = 66
 
 
@@ -112,6 +117,25 @@ def quantize_q2k(w):
     out = np.zeros(rows * cols // 256 * Q2K_BLOCK_BYTES, np.uint8)
     if lib().or_q2k_quantize(_p(w, ctypes.c_float), rows, cols, _p(out, ctypes.c_uint8)) != 0:
         raise ValueError("q2k quantisation rejected the input (non-finite or fp16 overflow)")
+    return out
+
+
+def quantize_q4k(w):
+    """FORMAT.md's Q4_K-style quantiser (the 4-bit variant) of fp32 [rows, cols]."""
+    w = np.ascontiguousarray(w, np.float32)
+    rows, cols = w.shape
+    assert cols % 256 == 0
+    out = np.zeros(rows * cols // 256 * Q4K_BLOCK_BYTES, np.uint8)
+    if lib().or_q4k_quantize(_p(w, ctypes.c_float), rows, cols, _p(out, ctypes.c_uint8)) != 0:
+        raise ValueError("q4k quantisation rejected the input (non-finite or fp16 overflow)")
+    return out
+
+
+def dequant_q4k(blob, rows, cols):
+    blob = np.ascontiguousarray(blob, np.uint8)
+    assert blob.size == rows * cols // 256 * Q4K_BLOCK_BYTES
+    out = np.empty((rows, cols), np.float32)
+    lib().or_q4k_dequant(_p(blob, ctypes.c_uint8), rows, cols, _p(out, ctypes.c_float))
     return out
 
 

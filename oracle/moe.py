@@ -17,7 +17,7 @@ pages do not spell the activation out.
 """
 import numpy as np
 
-from . import dequant_iq2, dequant_q2k, permute, route
+from . import dequant_iq2, dequant_q2k, dequant_q4k, permute, route
 
 
 def bf16_to_f64(bits):
@@ -41,12 +41,13 @@ def expert_ffn_dense(x, w_gate, w_up, w_down):
 
 
 def moe_ffn(x_bf16, logits, k, gate_blobs, up_blobs, down_blobs, d_model, d_ff,
-            shared=None, mode=0, tokens=None):
+            shared=None, mode=0, tokens=None, fmt="q2"):
     """Delta added to the residual by one routed-MoE expert FFN.
 
     x_bf16      uint16 [T, D] (bf16 bits);  logits float32 [T, E]
     gate_blobs, up_blobs: per expert, IQ2-style blobs of [d_ff, d_model]
     down_blobs: per expert, Q2_K-style blob of [d_model, d_ff]
+    fmt:        "q2" (the above) or "q4": all three per-expert blobs Q4_K-style
     shared:     None, or (gate, up, down) bf16 bits of shapes [F, D], [F, D], [D, F]
     tokens:     None for all tokens, or the token ids to evaluate (others are not computed)
 
@@ -66,9 +67,14 @@ def moe_ffn(x_bf16, logits, k, gate_blobs, up_blobs, down_blobs, d_model, d_ff,
         pairs = [int(p) for p in pairs if int(p) // k in pos_of]
         if not pairs:
             continue
-        wg = dequant_iq2(gate_blobs[e], F, D).astype(np.float64)
-        wu = dequant_iq2(up_blobs[e], F, D).astype(np.float64)
-        wd = dequant_q2k(down_blobs[e], D, F).astype(np.float64)
+        if fmt == "q4":
+            wg = dequant_q4k(gate_blobs[e], F, D).astype(np.float64)
+            wu = dequant_q4k(up_blobs[e], F, D).astype(np.float64)
+            wd = dequant_q4k(down_blobs[e], D, F).astype(np.float64)
+        else:
+            wg = dequant_iq2(gate_blobs[e], F, D).astype(np.float64)
+            wu = dequant_iq2(up_blobs[e], F, D).astype(np.float64)
+            wd = dequant_q2k(down_blobs[e], D, F).astype(np.float64)
         rows = np.array([pos_of[p // k] for p in pairs])
         slots = np.array([p % k for p in pairs])
         y[rows, slots] = expert_ffn_dense(x[tok[rows]], wg, wu, wd)

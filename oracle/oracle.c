@@ -153,6 +153,73 @@ void or_q2k_dequant_block(const uint8_t *in, float *out) {
     }
 }
 
+/* ------------------------------------------------------------------ Q4_K-style block */
+
+/* The 6-bit scale and min of sub-block j of a 144-byte block. */
+static void q4k_scale_min(const uint8_t *blk, int j, int *sc, int *m) {
+    int lo = blk[4 + j], hi = (blk[12 + j / 2] >> (4 * (j % 2))) & 15;
+    *sc = (lo & 15) | ((hi & 3) << 4);
+    *m = (lo >> 4) | ((hi >> 2) << 4);
+}
+
+/* Quantise 256 weights into one 144-byte block (FORMAT.md, Q4_K-style). Returns 0, or -1 on
+ * non-finite input or an fp16 overflow of d/dmin. */
+int or_q4k_quantize_block(const float *w, uint8_t *out) {
+    double a[8], b[8];
+    for (int i = 0; i < 256; i++)
+        if (!isfinite(w[i])) return -1;
+    double amax_a = 0.0, amax_b = 0.0;
+    for (int j = 0; j < 8; j++) {
+        double mn = w[32 * j], mx = w[32 * j];
+        for (int i = 1; i < 32; i++) {
+            double v = w[32 * j + i];
+            if (v < mn) mn = v;
+            if (v > mx) mx = v;
+        }
+        double lo = mn < 0.0 ? mn : 0.0;
+        double hi = mx > lo ? mx : lo;
+        a[j] = (hi - lo) / 15.0;
+        b[j] = 0.0 - lo;
+        if (a[j] > amax_a) amax_a = a[j];
+        if (b[j] > amax_b) amax_b = b[j];
+    }
+    uint16_t dh = or_double_to_half(amax_a / 63.0);
+    uint16_t mh = or_double_to_half(amax_b / 63.0);
+    if (((dh >> 10) & 31) == 31 || ((mh >> 10) & 31) == 31) return -1;
+    double d = or_half_to_double(dh), dmin = or_half_to_double(mh);
+    memset(out, 0, 144);
+    out[0] = (uint8_t)(dh & 0xff);
+    out[1] = (uint8_t)(dh >> 8);
+    out[2] = (uint8_t)(mh & 0xff);
+    out[3] = (uint8_t)(mh >> 8);
+    for (int j = 0; j < 8; j++) {
+        int sc = d > 0.0 ? (int)clampd(nearbyint(a[j] / d), 0.0, 63.0) : 0;
+        int m = dmin > 0.0 ? (int)clampd(nearbyint(b[j] / dmin), 0.0, 63.0) : 0;
+        out[4 + j] = (uint8_t)((sc & 15) | ((m & 15) << 4));
+        out[12 + j / 2] |= (uint8_t)(((sc >> 4) | ((m >> 4) << 2)) << (4 * (j % 2)));
+        double den = d * (double)sc;
+        double off = dmin * (double)m;
+        for (int i = 0; i < 32; i++) {
+            int k = 32 * j + i;
+            int q = den > 0.0 ? (int)clampd(nearbyint(((double)w[k] + off) / den), 0.0, 15.0) : 0;
+            out[16 + k / 2] |= (uint8_t)(q << (4 * (k % 2)));
+        }
+    }
+    return 0;
+}
+
+/* One block back to 256 fp32 values: w = d*sc*q - dmin*m, rounded once to fp32. */
+void or_q4k_dequant_block(const uint8_t *in, float *out) {
+    double d = or_half_to_double((uint16_t)(in[0] | (in[1] << 8)));
+    double dmin = or_half_to_double((uint16_t)(in[2] | (in[3] << 8)));
+    for (int k = 0; k < 256; k++) {
+        int sc, m;
+        q4k_scale_min(in, k / 32, &sc, &m);
+        int q = (in[16 + k / 2] >> (4 * (k % 2))) & 15;
+        out[k] = (float)(d * (double)sc * (double)q - dmin * (double)m);
+    }
+}
+
 /* ------------------------------------------------------------------ IQ2-style block */
 
 int or_iq2_quantize_block(const float *w, const uint8_t *grid, uint8_t *out) {
@@ -279,6 +346,20 @@ int or_iq2_quantize(const float *w, int64_t rows, int64_t cols, const uint8_t *g
             if (or_iq2_quantize_block(w + r * cols + 256 * b, grid, dst + (r * nb + b) * 66))
                 return -1;
     return 0;
+}
+
+int or_q4k_quantize(const float *w, int64_t rows, int64_t cols, uint8_t *dst) {
+    int64_t nb = cols / 256;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < nb; b++)
+            if (or_q4k_quantize_block(w + r * cols + 256 * b, dst + (r * nb + b) * 144)) return -1;
+    return 0;
+}
+
+void or_q4k_dequant(const uint8_t *src, int64_t rows, int64_t cols, float *dst) {
+    int64_t nb = cols / 256;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < nb; b++) or_q4k_dequant_block(src + (r * nb + b) * 144, dst + r * cols + 256 * b);
 }
 
 void or_q2k_dequant(const uint8_t *src, int64_t rows, int64_t cols, float *dst) {

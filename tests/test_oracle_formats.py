@@ -169,6 +169,97 @@ def test_q2k_rejects_non_finite():
         oracle.quantize_q2k(w)
 
 
+# ---------------------------------------------------------------- Q4_K-style blocks
+
+def test_q4k_dequant_hand_built_block():
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = np.array([_half_bits(0.5)], np.uint16).view(np.uint8)    # d = 0.5
+    blk[2:4] = np.array([_half_bits(0.25)], np.uint16).view(np.uint8)   # dmin = 0.25
+    # sub-block 0: sc = 5 (0b000101), m = 18 (0b010010): low nibbles 5 and 2, high bits 0 and 1
+    blk[4] = 0x25
+    blk[12] = 0b0100          # j = 0 in bits 0-3: sc high bits 00, m high bits 01
+    # sub-block 3: sc = 63 (0b111111), m = 0: low nibble 15, high bits 11 in byte 12 + 1, bits 4-7
+    blk[7] = 0x0F
+    blk[13] = 0b0011 << 4
+    blk[16] = 0x21            # weights 0, 1: q = 1, 2
+    blk[17] = 0xF0            # weights 2, 3: q = 0, 15
+    blk[16 + 48] = 0x07       # weight 96 (sub-block 3): q = 7, weight 97: q = 0
+    w = oracle.dequant_q4k(blk, 1, 256)[0]
+    # w = d*sc*q - dmin*m: sub-block 0: 2.5 q - 4.5; sub-block 3: 31.5 q
+    assert list(w[:5]) == [-2.0, 0.5, -4.5, 33.0, -4.5]
+    assert list(w[96:98]) == [220.5, 0.0]
+    assert np.all(w[32:96] == 0.0) and np.all(w[128:] == 0.0)
+
+
+def _exact_q4k_block(rng):
+    """A block whose fp32 values are exact and which the quantiser must reproduce."""
+    while True:
+        d = np.float16(rng.uniform(2 ** -9, 2 ** -7))
+        dmin = np.float16(rng.uniform(2 ** -9, 2 ** -7))
+        sc = rng.integers(1, 64, 8)
+        m = rng.integers(0, 64, 8)
+        sc[rng.integers(8)] = 63
+        m[rng.integers(8)] = 63
+        q = rng.integers(0, 16, 256)
+        for j in range(8):
+            a, b = rng.choice(32, 2, replace=False)
+            q[32 * j + a], q[32 * j + b] = 0, 15
+        blk = np.zeros(144, np.uint8)
+        blk[0:2] = np.array([d], np.float16).view(np.uint8)
+        blk[2:4] = np.array([dmin], np.float16).view(np.uint8)
+        for j in range(8):
+            blk[4 + j] = (sc[j] & 15) | ((m[j] & 15) << 4)
+            blk[12 + j // 2] |= ((sc[j] >> 4) | ((m[j] >> 4) << 2)) << (4 * (j % 2))
+        for k in range(256):
+            blk[16 + k // 2] |= q[k] << (4 * (k % 2))
+        exact = np.array([float(d) * sc[k // 32] * q[k] - float(dmin) * m[k // 32] for k in range(256)])
+        if np.all(np.abs(exact) < 60000) and np.array_equal(exact.astype(np.float32).astype(np.float64), exact):
+            return blk, exact
+
+
+def test_q4k_round_trip_fixed_point():
+    rng = np.random.default_rng(13)
+    for _ in range(40):
+        blk, exact = _exact_q4k_block(rng)
+        w = oracle.dequant_q4k(blk, 1, 256)[0]
+        assert np.array_equal(w.astype(np.float64), exact)
+        assert np.array_equal(oracle.quantize_q4k(w[None, :]), blk)
+
+
+def test_q4k_zero_and_constant_blocks():
+    assert np.all(oracle.quantize_q4k(np.zeros((1, 256), np.float32)) == 0)
+    # constants on the code grid: 945 * 2^-12 = d*sc*q with d = 2^-12, sc = 63, q = 15;
+    # -63 * 2^-12 = -dmin*m with dmin = 2^-12, m = 63 (and d = 0)
+    for v in (945 / 4096, -63 / 4096):
+        c = np.full((1, 256), v, np.float32)
+        assert np.array_equal(oracle.dequant_q4k(oracle.quantize_q4k(c), 1, 256), c)
+
+
+def test_q4k_error_bound_on_gaussian_blocks():
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((64, 256)) * 0.02).astype(np.float32)
+    blob = oracle.quantize_q4k(w).reshape(64, 144)
+    wh = oracle.dequant_q4k(blob, 64, 256)
+    for r in range(64):
+        d = float(blob[r, 0:2].view(np.float16)[0])
+        dmin = float(blob[r, 2:4].view(np.float16)[0])
+        for j in range(8):
+            sc = (blob[r, 4 + j] & 15) | (((blob[r, 12 + j // 2] >> (4 * (j % 2))) & 3) << 4)
+            # rounding the affine grid (step a_j = d*sc +- d/2 over 15 steps, offset +- dmin/2)
+            bound = 0.5 * d * sc + 7.5 * d + 0.5 * dmin + 1e-6
+            assert np.max(np.abs(w[r, 32 * j:32 * j + 32] - wh[r, 32 * j:32 * j + 32])) <= bound
+    # and the 4-bit codes are finer than the 2-bit ones on the same weights
+    e2 = np.abs(oracle.dequant_q2k(oracle.quantize_q2k(w), 64, 256) - w).mean()
+    assert np.abs(wh - w).mean() < 0.3 * e2
+
+
+def test_q4k_rejects_non_finite():
+    w = np.zeros((1, 256), np.float32)
+    w[0, 7] = np.inf
+    with pytest.raises(ValueError):
+        oracle.quantize_q4k(w)
+
+
 # ---------------------------------------------------------------- IQ2-style blocks
 
 def test_iq2_dequant_hand_built_block():
