@@ -33,9 +33,10 @@ DS4MOE_OPT_SMALL_GROUPS = 5
 STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step", "pool"]
 
 EXPORTED = [
-    "ds4moe_strerror", "ds4moe_q2k_bytes", "ds4moe_iq2_bytes", "ds4moe_iq2_grid",
-    "ds4moe_quantize_q2k", "ds4moe_quantize_iq2", "ds4moe_dequantize_q2k", "ds4moe_dequantize_iq2",
-    "ds4moe_weights_create", "ds4moe_weights_create_pooled", "ds4moe_pool_info", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
+    "ds4moe_strerror", "ds4moe_q2k_bytes", "ds4moe_iq2_bytes", "ds4moe_q4k_bytes", "ds4moe_iq2_grid",
+    "ds4moe_quantize_q2k", "ds4moe_quantize_iq2", "ds4moe_quantize_q4k", "ds4moe_dequantize_q2k",
+    "ds4moe_dequantize_iq2", "ds4moe_dequantize_q4k",
+    "ds4moe_weights_create", "ds4moe_weights_create_q4", "ds4moe_weights_create_pooled", "ds4moe_pool_info", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
     "ds4moe_router_logits", "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
     "ds4moe_expert_ffn_static", "ds4moe_step_trace",
 ]
@@ -77,6 +78,10 @@ def lib():
             "ds4moe_strerror": ([i32], ctypes.c_char_p),
             "ds4moe_q2k_bytes": ([i64, i64], sz),
             "ds4moe_iq2_bytes": ([i64, i64], sz),
+            "ds4moe_q4k_bytes": ([i64, i64], sz),
+            "ds4moe_quantize_q4k": ([vp, i64, i64, vp, sz], i32),
+            "ds4moe_dequantize_q4k": ([vp, i64, i64, vp], i32),
+            "ds4moe_weights_create_q4": ([ctypes.POINTER(_Desc), ctypes.POINTER(vp)], i32),
             "ds4moe_iq2_grid": ([vp], i32),
             "ds4moe_quantize_q2k": ([vp, i64, i64, vp, sz], i32),
             "ds4moe_quantize_iq2": ([vp, i64, i64, vp, sz], i32),
@@ -123,6 +128,10 @@ def ds4moe_iq2_bytes(rows, cols):
     return lib().ds4moe_iq2_bytes(rows, cols)
 
 
+def ds4moe_q4k_bytes(rows, cols):
+    return lib().ds4moe_q4k_bytes(rows, cols)
+
+
 def ds4moe_iq2_grid():
     g = np.zeros(2048, np.uint8)
     _check(lib().ds4moe_iq2_grid(g.ctypes.data), "ds4moe_iq2_grid")
@@ -161,6 +170,15 @@ def _dequantize(fn, nbytes, blob, rows, cols):
 
 def ds4moe_dequantize_q2k(blob, rows, cols):
     return _dequantize(lib().ds4moe_dequantize_q2k, ds4moe_q2k_bytes, blob, rows, cols)
+
+
+def ds4moe_quantize_q4k(w):
+    """Host quantisation of fp32 [rows, cols] to the 4-bit variant's Q4_K-style blocks."""
+    return _quantize(lib().ds4moe_quantize_q4k, ds4moe_q4k_bytes, w)
+
+
+def ds4moe_dequantize_q4k(blob, rows, cols):
+    return _dequantize(lib().ds4moe_dequantize_q4k, ds4moe_q4k_bytes, blob, rows, cols)
 
 
 def ds4moe_dequantize_iq2(blob, rows, cols):
@@ -207,11 +225,12 @@ class Weights:
 
 
 def ds4moe_weights_create(gate_iq2, up_iq2, down_q2k, d_model, d_ff, shared=None, max_tokens=1, max_k=8,
-                          n_slots=None):
+                          n_slots=None, fmt="q2"):
     """Upload per-expert packed blobs (lists of uint8 arrays) and an optional bf16 shared
     expert (gate, up, down as uint16 arrays of bf16 bits) to the current CUDA device. With
     n_slots, a pooled handle (ds4moe_weights_create_pooled): the experts stay in pinned host
-    memory and stream into n_slots device slots as calls touch them."""
+    memory and stream into n_slots device slots as calls touch them. fmt="q4": the 4-bit variant,
+    all three per-expert blobs Q4_K-style (ds4moe_weights_create_q4)."""
     E = len(gate_iq2)
     keep = []
 
@@ -225,9 +244,14 @@ def ds4moe_weights_create(gate_iq2, up_iq2, down_q2k, d_model, d_ff, shared=None
             arr[e] = b.ctypes.data
         return arr
 
-    gi = ptrs(gate_iq2, ds4moe_iq2_bytes(d_ff, d_model))
-    ui = ptrs(up_iq2, ds4moe_iq2_bytes(d_ff, d_model))
-    dq = ptrs(down_q2k, ds4moe_q2k_bytes(d_model, d_ff))
+    if fmt == "q4":
+        gi = ptrs(gate_iq2, ds4moe_q4k_bytes(d_ff, d_model))
+        ui = ptrs(up_iq2, ds4moe_q4k_bytes(d_ff, d_model))
+        dq = ptrs(down_q2k, ds4moe_q4k_bytes(d_model, d_ff))
+    else:
+        gi = ptrs(gate_iq2, ds4moe_iq2_bytes(d_ff, d_model))
+        ui = ptrs(up_iq2, ds4moe_iq2_bytes(d_ff, d_model))
+        dq = ptrs(down_q2k, ds4moe_q2k_bytes(d_model, d_ff))
     desc = _Desc(d_model, d_ff, E, gi, ui, dq, None, None, None, max_tokens, max_k)
     if shared is not None:
         sh = [np.ascontiguousarray(s, np.uint16).reshape(-1) for s in shared]
@@ -236,7 +260,11 @@ def ds4moe_weights_create(gate_iq2, up_iq2, down_q2k, d_model, d_ff, shared=None
         keep.extend(sh)
         desc.shared_gate_bf16, desc.shared_up_bf16, desc.shared_down_bf16 = (s.ctypes.data for s in sh)
     h = ctypes.c_void_p()
-    if n_slots is None:
+    if fmt == "q4":
+        if n_slots is not None:
+            raise ValueError("the 4-bit variant has no pooled handle")
+        _check(lib().ds4moe_weights_create_q4(ctypes.byref(desc), ctypes.byref(h)), "ds4moe_weights_create_q4")
+    elif n_slots is None:
         _check(lib().ds4moe_weights_create(ctypes.byref(desc), ctypes.byref(h)), "ds4moe_weights_create")
     else:
         _check(lib().ds4moe_weights_create_pooled(ctypes.byref(desc), int(n_slots), ctypes.byref(h)),

@@ -158,14 +158,16 @@ struct StageClock {
 extern "C" {
 
 // n_slots = 0: every expert resident in device memory; otherwise a pooled handle (see
-// ds4moe_weights_create_pooled) whose device weights are n_slots expert slots.
-static int create_impl(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weights **out) {
+// ds4moe_weights_create_pooled) whose device weights are n_slots expert slots. fmt 1: the 4-bit
+// variant (Q4_K-style blobs for all three projections, resident).
+static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds4moe_weights **out) {
     if (!desc || !out) return DS4MOE_EINVAL;
     *out = nullptr;
     const int D = desc->d_model, F = desc->d_ff, E = desc->n_experts;
     if (D <= 0 || F <= 0 || D % 256 || F % 256 || E < 1 || E > 1024) return DS4MOE_EINVAL;
     if (desc->max_tokens < 1 || desc->max_k < 1 || desc->max_k > 32 || desc->max_k > E) return DS4MOE_EINVAL;
     if (n_slots < 0 || (n_slots > 0 && (n_slots > E || n_slots < desc->max_k))) return DS4MOE_EINVAL;
+    if (fmt == 1 && n_slots) return DS4MOE_EUNSUPPORTED;  // the 4-bit variant is resident only
     const int S = n_slots ? n_slots : E;  // experts held in device memory
     if (!desc->gate_iq2 || !desc->up_iq2 || !desc->down_q2k) return DS4MOE_EINVAL;
     for (int e = 0; e < E; e++)
@@ -198,9 +200,40 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weig
     const size_t nb_down = static_cast<size_t>(D) * w.nbF;  // blocks per down matrix
     const size_t up_bytes = nb_up * 132;       // gate + up of one expert, tiled (66 bytes per block each)
     const size_t down_bytes = nb_down * 84;    // down of one expert, tiled
-    TRY(dev_alloc(h, &w.iq2, S * up_bytes));
-    TRY(dev_alloc(h, &w.q2k, S * down_bytes));
-    TRY(dev_alloc(h, &w.tc_ok, S));
+    w.fmt = fmt;
+    if (fmt == 1) {
+        // the 4-bit variant: each expert's gate, up and down blocks as given, validated (finite
+        // fp16 d and dmin in every block), in row order; never on the tensor-core path
+        const size_t q4b = q4_expert_bytes(w);
+        TRY(dev_alloc(h, &w.q4, E * q4b));
+        TRY(dev_alloc(h, &w.iq2, 16));
+        TRY(dev_alloc(h, &w.q2k, 16));
+        TRY(dev_alloc(h, &w.tc_ok, E));
+        if (cudaMemset(w.tc_ok, 0, E) != cudaSuccess) TRY(DS4MOE_ECUDA);
+        const size_t gb = nb_up * 144, db = nb_down * 144;
+        for (int e = 0; e < E; e++) {
+            const uint8_t *mats[3] = {static_cast<const uint8_t *>(desc->gate_iq2[e]),
+                                      static_cast<const uint8_t *>(desc->up_iq2[e]),
+                                      static_cast<const uint8_t *>(desc->down_q2k[e])};
+            for (int m = 0; m < 3; m++) {
+                const size_t nbk = m < 2 ? nb_up : nb_down;
+                for (size_t b = 0; b < nbk; b++) {
+                    const uint8_t *blk = mats[m] + b * 144;
+                    if (!host_f16_finite(static_cast<uint16_t>(blk[0] | (blk[1] << 8))) ||
+                        !host_f16_finite(static_cast<uint16_t>(blk[2] | (blk[3] << 8))))
+                        TRY(DS4MOE_EBADDATA);
+                }
+            }
+            TRY(upload(w.q4 + e * q4b, mats[0], gb));
+            TRY(upload(w.q4 + e * q4b + gb, mats[1], gb));
+            TRY(upload(w.q4 + e * q4b + 2 * gb, mats[2], db));
+        }
+    }
+    if (fmt == 0) {
+        TRY(dev_alloc(h, &w.iq2, S * up_bytes));
+        TRY(dev_alloc(h, &w.q2k, S * down_bytes));
+        TRY(dev_alloc(h, &w.tc_ok, S));
+    }
     SlotPool &sp = h->pool;
     uint8_t *store_iq2 = nullptr, *store_q2k = nullptr, *store_ok = nullptr;  // pooled: host views of the store
     if (n_slots) {
@@ -223,7 +256,7 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weig
             cudaMemset(w.q2k, 0, S * down_bytes) != cudaSuccess || cudaMemset(w.tc_ok, 0, S) != cudaSuccess)
             TRY(DS4MOE_ECUDA);
     }
-    {
+    if (fmt == 0) {
         std::vector<uint8_t> qs(nb_up * 64), sq(nb_down * 80), ok(E), tiles(std::max(up_bytes, down_bytes));
         std::vector<uint16_t> dv(nb_up);
         std::vector<uint32_t> dd(nb_down);
@@ -333,14 +366,16 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weig
     return DS4MOE_OK;
 }
 
-int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out) { return create_impl(desc, 0, out); }
+int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out) { return create_impl(desc, 0, 0, out); }
+
+int ds4moe_weights_create_q4(const ds4moe_weights_desc *desc, ds4moe_weights **out) { return create_impl(desc, 0, 1, out); }
 
 int ds4moe_weights_create_pooled(const ds4moe_weights_desc *desc, int n_slots, ds4moe_weights **out) {
     if (n_slots < 1) {
         if (out) *out = nullptr;
         return DS4MOE_EINVAL;
     }
-    return create_impl(desc, n_slots, out);
+    return create_impl(desc, n_slots, 0, out);
 }
 
 int ds4moe_pool_info(ds4moe_weights *h, int *n_slots, uint64_t *hits, uint64_t *misses, int32_t *slot_expert) {
@@ -398,6 +433,7 @@ int ds4moe_weights_dequantize(const ds4moe_weights *h, int expert, int matrix, f
     if (!h || expert < 0 || expert >= h->dw.E || matrix < 0 || matrix > 2 || (!dst_f32 && !dst_f16))
         return DS4MOE_EINVAL;
     if (h->pool.S) return DS4MOE_EUNSUPPORTED;  // a pooled handle's slots change from call to call
+    if (h->dw.fmt == 1 && dst_f16) return DS4MOE_EUNSUPPORTED;  // the 4-bit variant has no fp16 operand path
     int rc = 0;
     if (dst_f32) rc = launch_dequant(h->dw, h->ws.grid, expert, matrix, dst_f32, nullptr, stream);
     // the fp16 values are the tensor-core path's own operand bytes, from its producers
@@ -477,8 +513,9 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     }
     // A group holds at most T tokens, so the tensor-core path can only be needed when
     // T reaches the threshold; the device decides per group after routing.
-    const bool sg_fits = h->small_groups && small_groups_supported(w);
-    const int gm = h->gemm_min_tokens >= 0 ? h->gemm_min_tokens : sg_fits ? (T <= 64 ? 0 : 7) : 2;
+    const bool q4 = w.fmt == 1;  // the 4-bit variant: every routed group on the dequant-GEMV kernels
+    const bool sg_fits = !q4 && h->small_groups && small_groups_supported(w);
+    const int gm = q4 ? 0 : h->gemm_min_tokens >= 0 ? h->gemm_min_tokens : sg_fits ? (T <= 64 ? 0 : 7) : 2;
     const int gemm_min = (gm > 0 && T >= gm) ? gm : 0;
     const bool shared_tc = w.has_shared && w.shared_tc_ok && h->shared_gemm_min_tokens > 0 &&
                            T >= h->shared_gemm_min_tokens;
@@ -499,7 +536,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     if (!rc) rc = clk.stage(DS4MOE_STAGE_GROUP);
     if (!rc)
         rc = launch_group(ws.topk_idx, T, k, w.E, gemm_min, w.tc_ok, ws.counts, ws.offsets, ws.perm, ws.inv,
-                          ws.gemv_list, ws.gemm_list, sg ? nullptr : ws.single_list, ws.tile_prefix, ws.tile_desc,
+                          ws.gemv_list, ws.gemm_list, (sg || q4) ? nullptr : ws.single_list, ws.tile_prefix, ws.tile_desc,
                           sg ? ws.small_pos : nullptr, ws.meta, ws.status, stream);
     if (up_tc) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_GATHER);
@@ -508,7 +545,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     // Without the small-group kernels: one-token groups (every group at T = 1) run on the
     // decode kernels; groups of 2 .. gemm_min-1 tokens on the multi-token GEMV kernels, which
     // are launched only when such groups can exist; larger groups on the tensor cores.
-    const bool multi_gemv = !sg && (gemm_min == 0 ? T > 1 : gemm_min > 2);
+    const bool multi_gemv = q4 || (!sg && (gemm_min == 0 ? T > 1 : gemm_min > 2));
     const bool shared_single = w.has_shared && !shared_tc && T == 1;
     const bool shared_multi = w.has_shared && !shared_tc && T > 1;
     if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMV);
@@ -520,8 +557,10 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
             if (!rc) rc = launch_decode_up(w, ws, x, T, k, true, stream);
             h->launches++;
         }
-    } else {
+    } else if (!q4 || shared_single) {  // (the 4-bit variant: only the shared expert at T = 1)
         if (!rc) rc = launch_decode_up(w, ws, x, T, k, shared_single, stream);
+    } else {
+        h->launches--;  // the stage's kernel is the GEMV below, counted there
     }
     if (multi_gemv || shared_multi) {
         if (!rc) rc = launch_gemv_up(w, ws, x, T, k, shared_multi, stream);
@@ -543,8 +582,10 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
             if (!rc) rc = launch_decode_down(w, ws, T, k, true, stream);
             h->launches++;
         }
-    } else {
+    } else if (!q4 || shared_single) {
         if (!rc) rc = launch_decode_down(w, ws, T, k, shared_single, stream);
+    } else {
+        h->launches--;
     }
     if (multi_gemv || shared_multi) {
         if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_multi, stream);

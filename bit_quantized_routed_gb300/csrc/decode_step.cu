@@ -856,6 +856,7 @@ int decode_step_ctas() { return n_sms(); }
 
 // Whether the fused single-token kernel covers this shape.
 bool decode_step_supported(const DeviceWeights &w, int k) {
+    if (w.fmt != 0) return false;  // the 2-bit formats only
     if (k < 1 || k > 8 || w.F != 2048 || w.D % 256 != 0 || w.D > kMaxD || w.E > 1024) return false;
     if (static_cast<size_t>(kRows1) * w.nbD * 132 > kStageBytes) return false;
     if (w.has_shared && static_cast<size_t>(kRowsSh) * 2 * w.D * 2 > kStageBytes) return false;

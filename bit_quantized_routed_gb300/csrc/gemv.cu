@@ -65,6 +65,23 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     return fmaf(a.w, b.w, acc);
 }
 
+// The 4-bit variant: sub-block j (32 weights) of a Q4_K-style block whose first 16 bytes are
+// hdr: its scale d * sc_j and offset dmin * m_j, both exact in fp32.
+__device__ __forceinline__ void q4_sub_scale(uint4 hdr, int j, float &ds, float &dm) {
+    const float d = f16_to_f32(static_cast<uint16_t>(hdr.x & 0xffffu));
+    const float dmin = f16_to_f32(static_cast<uint16_t>(hdr.x >> 16));
+    const uint32_t low = ((j < 4 ? hdr.y : hdr.z) >> (8 * (j & 3))) & 0xffu;
+    const uint32_t high = (hdr.w >> (8 * (j >> 1) + 4 * (j & 1))) & 15u;
+    ds = __fmul_rn(d, static_cast<float>((low & 15u) | ((high & 3u) << 4)));
+    dm = __fmul_rn(dmin, static_cast<float>((low >> 4) | ((high >> 2) << 4)));
+}
+
+// Eight 4-bit codes of one u32 (weight i in bits 4i..4i+3) as weights d sc q - dmin m, rounded once.
+__device__ __forceinline__ void q4_group(uint32_t word, float ds, float dm, float w[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) w[i] = q2k_weight(ds, dm, (word >> (4 * i)) & 15u);
+}
+
 struct UpParams {
     DeviceWeights w;
     const uint16_t *x;  // bf16 [T][D]
@@ -77,7 +94,7 @@ struct UpParams {
 };
 
 // Phase 1: h[pos][r] = silu(gate_r . x) * (up_r . x) for the group's tokens.
-template <int NT>
+template <int NT, bool Q4>
 __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint2 *grid_s = reinterpret_cast<uint2 *>(smem);              // 256 x 8 B
@@ -123,7 +140,48 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
                 staged_key = key;
                 staged_tok0 = tok0;
             }
-            if (is_routed) {
+            if (is_routed && Q4) {
+#pragma unroll 1
+                for (int rr = 0; rr < kUpRows / kWarps; rr++) {
+                    const int r = r0 + warp + rr * kWarps;
+                    const uint8_t *rg = q4_row(p.w, 0, e, r), *ru = q4_row(p.w, 1, e, r);
+                    float ag[NT], au[NT];
+#pragma unroll
+                    for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
+                    for (int c = lane; c < nbD * 8; c += 32) {  // 32-weight sub-block c of the row
+                        const int b = c >> 3, sub = c & 7;
+                        const uint4 hg = __ldg(reinterpret_cast<const uint4 *>(rg + b * 144));
+                        const uint4 hu = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144));
+                        const uint4 vg = __ldg(reinterpret_cast<const uint4 *>(rg + b * 144 + 16) + sub);
+                        const uint4 vu = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144 + 16) + sub);
+                        float dsg, dmg, dsu, dmu;
+                        q4_sub_scale(hg, sub, dsg, dmg);
+                        q4_sub_scale(hu, sub, dsu, dmu);
+#pragma unroll
+                        for (int g = 0; g < 4; g++) {
+                            float wg[8], wu[8];
+                            q4_group(g == 0 ? vg.x : g == 1 ? vg.y : g == 2 ? vg.z : vg.w, dsg, dmg, wg);
+                            q4_group(g == 0 ? vu.x : g == 1 ? vu.y : g == 2 ? vu.z : vu.w, dsu, dmu, wu);
+                            const int xc = swz8(4 * c + g);
+#pragma unroll
+                            for (int j = 0; j < NT; j++) {
+                                if (j < nt) {
+                                    const uint4 xv = xs[j * D8 + xc];
+                                    dot8_bf16(wg, xv, ag[j]);
+                                    dot8_bf16(wu, xv, au[j]);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; j++) {
+                        if (j < nt) {
+                            const float g = warp_sum(ag[j]), u = warp_sum(au[j]);
+                            if (lane == 0) p.h[static_cast<size_t>(off + tok0 + j) * F + r] = swiglu(g, u);
+                        }
+                    }
+                }
+            } else if (is_routed) {
 #pragma unroll 1
                 for (int rr = 0; rr < kUpRows / kWarps; rr++) {
                     const int r = r0 + warp + rr * kWarps;
@@ -213,7 +271,7 @@ struct DownParams {
 };
 
 // Phase 2: y[pos][r] = down_r . h[pos] for the group's tokens.
-template <int NT>
+template <int NT, bool Q4>
 __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     float4 *hs = reinterpret_cast<float4 *>(smem);  // [NT][F/4] swizzled
@@ -254,7 +312,43 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
                 staged_key = key;
                 staged_tok0 = tok0;
             }
-            if (is_routed) {
+            if (is_routed && Q4) {
+#pragma unroll 1
+                for (int rr = 0; rr < kDownRows / kWarps; rr++) {
+                    const int r = r0 + warp + rr * kWarps;
+                    const uint8_t *rd = q4_row(p.w, 2, e, r);
+                    float acc[NT];
+#pragma unroll
+                    for (int j = 0; j < NT; j++) acc[j] = 0.0f;
+                    for (int c = lane; c < nbF * 8; c += 32) {  // 32-weight sub-block c of the row
+                        const int b = c >> 3, sub = c & 7;
+                        const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(rd + b * 144));
+                        const uint4 vd = __ldg(reinterpret_cast<const uint4 *>(rd + b * 144 + 16) + sub);
+                        float ds, dm;
+                        q4_sub_scale(hd, sub, ds, dm);
+#pragma unroll
+                        for (int g = 0; g < 4; g++) {
+                            float wv[8];
+                            q4_group(g == 0 ? vd.x : g == 1 ? vd.y : g == 2 ? vd.z : vd.w, ds, dm, wv);
+#pragma unroll
+                            for (int j = 0; j < NT; j++) {
+                                if (j < nt) {
+                                    const float4 h0 = hs[j * F4 + swz16(8 * c + 2 * g)], h1 = hs[j * F4 + swz16(8 * c + 2 * g + 1)];
+                                    acc[j] = dot4(make_float4(wv[0], wv[1], wv[2], wv[3]), h0, acc[j]);
+                                    acc[j] = dot4(make_float4(wv[4], wv[5], wv[6], wv[7]), h1, acc[j]);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; j++) {
+                        if (j < nt) {
+                            const float v = warp_sum(acc[j]);
+                            if (lane == 0) p.y[static_cast<size_t>(off + tok0 + j) * D + r] = v;
+                        }
+                    }
+                }
+            } else if (is_routed) {
 #pragma unroll 1
                 for (int rr = 0; rr < kDownRows / kWarps; rr++) {
                     const int r = r0 + warp + rr * kWarps;
@@ -340,7 +434,22 @@ __global__ void dequant_kernel(DeviceWeights w, int expert, int matrix, const ui
         const size_t r = ci / (cols / 64);
         const int c = static_cast<int>(ci - r * (cols / 64));
         float v[64];
-        if (matrix == DS4MOE_DOWN) {
+        if (w.fmt == 1) {  // the 4-bit variant: chunk c = sub-blocks 2c, 2c+1
+            const int m = matrix == DS4MOE_DOWN ? 2 : matrix == DS4MOE_GATE ? 0 : 1;
+            const uint8_t *row = q4_row(w, m, expert, static_cast<int>(r));
+            const int b = c >> 2;
+            const uint4 hdr = *reinterpret_cast<const uint4 *>(row + b * 144);
+            for (int half = 0; half < 2; half++) {
+                const int sub = 2 * (c & 3) + half;
+                float ds, dm;
+                q4_sub_scale(hdr, sub, ds, dm);
+                const uint4 q = *(reinterpret_cast<const uint4 *>(row + b * 144 + 16) + sub);
+                q4_group(q.x, ds, dm, v + 32 * half);
+                q4_group(q.y, ds, dm, v + 32 * half + 8);
+                q4_group(q.z, ds, dm, v + 32 * half + 16);
+                q4_group(q.w, ds, dm, v + 32 * half + 24);
+            }
+        } else if (matrix == DS4MOE_DOWN) {
             const uint8_t *sq = q2k_sq_row(w, expert, static_cast<int>(r));
             const int b = c >> 2, part = c & 3;
             const uint4 qv = *(reinterpret_cast<const uint4 *>(sq + b * 80 + 16) + part);
@@ -396,23 +505,23 @@ int ctas_per_sm(size_t smem) {
     return n < 1 ? 1 : (n > 4 ? 4 : n);
 }
 
-template <int NT>
+template <int NT, bool Q4>
 int launch_up_nt(const UpParams &p, cudaStream_t s) {
     static int seen[64];
     const size_t smem = 2048 + static_cast<size_t>(NT) * p.w.D * 2;
-    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_up_kernel<NT>), static_cast<int>(smem), seen);
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_up_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
-    gemv_up_kernel<NT><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
+    gemv_up_kernel<NT, Q4><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
-template <int NT>
+template <int NT, bool Q4>
 int launch_down_nt(const DownParams &p, cudaStream_t s) {
     static int seen[64];
     const size_t smem = static_cast<size_t>(NT) * p.w.F * 4;
-    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_down_kernel<NT>), static_cast<int>(smem), seen);
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_down_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
-    gemv_down_kernel<NT><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
+    gemv_down_kernel<NT, Q4><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -434,7 +543,8 @@ int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *
     p.P = T * k;
     p.shared = shared_on_gemv && w.has_shared;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return T == 1 ? launch_up_nt<1>(p, s) : launch_up_nt<8>(p, s);
+    if (w.fmt == 1) return T == 1 ? launch_up_nt<1, true>(p, s) : launch_up_nt<8, true>(p, s);
+    return T == 1 ? launch_up_nt<1, false>(p, s) : launch_up_nt<8, false>(p, s);
 }
 
 int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream) {
@@ -449,7 +559,8 @@ int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, 
     p.P = T * k;
     p.shared = shared_on_gemv && w.has_shared;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return T == 1 ? launch_down_nt<1>(p, s) : launch_down_nt<8>(p, s);
+    if (w.fmt == 1) return T == 1 ? launch_down_nt<1, true>(p, s) : launch_down_nt<8, true>(p, s);
+    return T == 1 ? launch_down_nt<1, false>(p, s) : launch_down_nt<8, false>(p, s);
 }
 
 int launch_dequant(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, float *dst32,

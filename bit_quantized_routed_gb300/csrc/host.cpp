@@ -181,6 +181,68 @@ void q2k_block_values(const uint8_t *blk, float *w) {
     }
 }
 
+// ------------------------------------------------------------------ Q4_K-style (the 4-bit variant)
+
+// Sub-block j's 6-bit scale and min: low nibbles at byte 4 + j, the two high bits of each at
+// byte 12 + j/2, nibble j % 2 (scale bits 0-1, min bits 2-3).
+inline void q4k_sm(const uint8_t *blk, int j, int *sc, int *mn) {
+    const int low = blk[4 + j], high = (blk[12 + j / 2] >> (4 * (j & 1))) & 15;
+    *sc = (low & 15) | ((high & 3) << 4);
+    *mn = (low >> 4) | ((high >> 2) << 4);
+}
+
+bool q4k_block(const float *w, uint8_t *blk) {
+    double step[8], off[8];
+    double top_step = 0.0, top_off = 0.0;
+    for (int j = 0; j < 8; j++) {
+        double lo = w[32 * j], hi = w[32 * j];
+        for (int i = 0; i < 32; i++) {
+            const double v = w[32 * j + i];
+            if (!std::isfinite(v)) return false;
+            lo = v < lo ? v : lo;
+            hi = v > hi ? v : hi;
+        }
+        lo = lo < 0.0 ? lo : 0.0;
+        hi = hi > lo ? hi : lo;
+        step[j] = (hi - lo) / 15.0;
+        off[j] = 0.0 - lo;
+        top_step = step[j] > top_step ? step[j] : top_step;
+        top_off = off[j] > top_off ? off[j] : top_off;
+    }
+    const uint16_t dbits = f16_round(top_step / 63.0);
+    const uint16_t mbits = f16_round(top_off / 63.0);
+    if (!f16_finite(dbits) || !f16_finite(mbits)) return false;
+    const double d = f16_value(dbits), dmin = f16_value(mbits);
+    std::memset(blk, 0, 144);
+    wr16(blk, dbits);
+    wr16(blk + 2, mbits);
+    for (int j = 0; j < 8; j++) {
+        const int sc = d > 0.0 ? static_cast<int>(clip(rne(step[j] / d), 0.0, 63.0)) : 0;
+        const int mn = dmin > 0.0 ? static_cast<int>(clip(rne(off[j] / dmin), 0.0, 63.0)) : 0;
+        blk[4 + j] = static_cast<uint8_t>((sc & 15) | ((mn & 15) << 4));
+        blk[12 + j / 2] |= static_cast<uint8_t>(((sc >> 4) | ((mn >> 4) << 2)) << (4 * (j & 1)));
+        const double den = d * sc;
+        const double shift = dmin * mn;
+        for (int i = 0; i < 32; i++) {
+            const int n = 32 * j + i;
+            int q = 0;
+            if (den > 0.0) q = static_cast<int>(clip(rne((static_cast<double>(w[n]) + shift) / den), 0.0, 15.0));
+            blk[16 + n / 2] |= static_cast<uint8_t>(q << (4 * (n & 1)));
+        }
+    }
+    return true;
+}
+
+void q4k_block_values(const uint8_t *blk, float *w) {
+    const double d = f16_value(rd16(blk)), dmin = f16_value(rd16(blk + 2));
+    for (int n = 0; n < 256; n++) {
+        int sc = 0, mn = 0;
+        q4k_sm(blk, n / 32, &sc, &mn);
+        const int q = (blk[16 + n / 2] >> (4 * (n & 1))) & 15;
+        w[n] = static_cast<float>(d * sc * q - dmin * mn);  // both products exact, one rounding
+    }
+}
+
 // ------------------------------------------------------------------ IQ2-style
 
 bool iq2_block(const float *w, uint8_t *blk) {
@@ -328,6 +390,33 @@ const char *ds4moe_strerror(int status) {
 
 size_t ds4moe_q2k_bytes(int64_t rows, int64_t cols) {
     return shape_ok(rows, cols) ? static_cast<size_t>(rows) * static_cast<size_t>(cols / 256) * 84u : 0u;
+}
+
+size_t ds4moe_q4k_bytes(int64_t rows, int64_t cols) {
+    return shape_ok(rows, cols) ? static_cast<size_t>(rows) * static_cast<size_t>(cols / 256) * 144u : 0u;
+}
+
+int ds4moe_quantize_q4k(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes) {
+    if (!w || !dst || !shape_ok(rows, cols) || dst_bytes < ds4moe_q4k_bytes(rows, cols)) return DS4MOE_EINVAL;
+    const int64_t nb = cols / 256;
+    uint8_t *out = static_cast<uint8_t *>(dst);
+    const bool ok = for_rows(rows, [&](int64_t r) {
+        for (int64_t b = 0; b < nb; b++)
+            if (!q4k_block(w + r * cols + 256 * b, out + (r * nb + b) * 144)) return false;
+        return true;
+    });
+    return ok ? DS4MOE_OK : DS4MOE_EBADDATA;
+}
+
+int ds4moe_dequantize_q4k(const void *src, int64_t rows, int64_t cols, float *dst) {
+    if (!src || !dst || !shape_ok(rows, cols)) return DS4MOE_EINVAL;
+    const int64_t nb = cols / 256;
+    const uint8_t *in = static_cast<const uint8_t *>(src);
+    for_rows(rows, [&](int64_t r) {
+        for (int64_t b = 0; b < nb; b++) q4k_block_values(in + (r * nb + b) * 144, dst + r * cols + 256 * b);
+        return true;
+    });
+    return DS4MOE_OK;
 }
 
 size_t ds4moe_iq2_bytes(int64_t rows, int64_t cols) {

@@ -36,6 +36,8 @@ struct DeviceWeights {
     uint16_t *sh_down;         // [D][F] bf16, or null
     uint16_t *sh_down_f16;     // [D][F] fp16 copy for the tensor-core path, or null
     uint8_t *tc_ok;            // [E] 1 if every dequantised weight of the expert fits fp16
+    int fmt;                   // 0: IQ2-style gate/up + Q2_K-style down; 1: the 4-bit variant (q4)
+    uint8_t *q4;               // fmt 1: Q4_K-style rows, see q4_row
     bool has_shared;
     bool shared_tc_ok;         // the shared expert's weights fit fp16
 };
@@ -53,6 +55,18 @@ struct DeviceWeights {
 #else
 #define DS4MOE_HD
 #endif
+
+// The 4-bit variant: expert e holds its gate rows, then its up rows (F rows of nbD blocks each),
+// then its down rows (D rows of nbF blocks), 144-byte Q4_K-style blocks in row order.
+DS4MOE_HD inline size_t q4_expert_bytes(const DeviceWeights &w) {
+    return (2 * static_cast<size_t>(w.F) * w.nbD + static_cast<size_t>(w.D) * w.nbF) * 144;
+}
+// Row r of gate (m = 0), up (m = 1) or down (m = 2) of expert e.
+DS4MOE_HD inline size_t q4_row_offset(const DeviceWeights &w, int m, int e, int r) {
+    const size_t base = static_cast<size_t>(e) * q4_expert_bytes(w);
+    if (m < 2) return base + (static_cast<size_t>(m) * w.F + r) * w.nbD * 144;
+    return base + 2 * static_cast<size_t>(w.F) * w.nbD * 144 + static_cast<size_t>(r) * w.nbF * 144;
+}
 
 constexpr int kIq2TileRows = 16;
 constexpr int kQ2kTileRows = 4;
@@ -87,6 +101,7 @@ DS4MOE_HD inline size_t q2k_dd_offset(const DeviceWeights &w, int e, int d) {
 // the same shared-memory banks; with it, eight consecutive rows cover all eight 16-byte bank groups,
 // and a row read chunk by chunk still covers each aligned group of eight chunks once.
 DS4MOE_HD inline int iq2_swz(const DeviceWeights &w, int r) { return r & ((w.nbD & 1) ? 3 : 7); }
+DS4MOE_HD inline const uint8_t *q4_row(const DeviceWeights &w, int m, int e, int r) { return w.q4 + q4_row_offset(w, m, e, r); }
 DS4MOE_HD inline const uint8_t *iq2_qs_row(const DeviceWeights &w, int m, int e, int r) {
     return w.iq2 + iq2_qs_offset(w, m, e, r);
 }

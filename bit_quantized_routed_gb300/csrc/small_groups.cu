@@ -742,7 +742,7 @@ HLayout h_layout(const Workspace &ws, int P, int F) {
 }  // namespace
 
 bool small_groups_supported(const DeviceWeights &w) {
-    return w.D <= kMaxD && w.F <= kMaxF && w.D % 256 == 0 && w.F % 256 == 0;
+    return w.fmt == 0 && w.D <= kMaxD && w.F <= kMaxF && w.D % 256 == 0 && w.F % 256 == 0;
 }
 
 int launch_prep_x(const Workspace &ws, const uint16_t *x, int T, int D, void *stream) {

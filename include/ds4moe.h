@@ -116,6 +116,8 @@ const char *ds4moe_strerror(int status);
  * (IQ2-style). 0 if rows < 0, cols <= 0 or cols % 256 != 0. */
 size_t ds4moe_q2k_bytes(int64_t rows, int64_t cols);
 size_t ds4moe_iq2_bytes(int64_t rows, int64_t cols);
+/* The 4-bit variant's Q4_K-style blocks (FORMAT.md): rows * cols/256 * 144 bytes. */
+size_t ds4moe_q4k_bytes(int64_t rows, int64_t cols);
 
 /* The IQ2-style grid (FORMAT.md): 256 entries x 8 magnitudes, entry-major, into out[2048]. */
 int ds4moe_iq2_grid(uint8_t *out);
@@ -128,10 +130,14 @@ int ds4moe_iq2_grid(uint8_t *out);
  * IQ2_XXS, down in Q2_K); the quantiser itself is FORMAT.md's reading. */
 int ds4moe_quantize_q2k(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
 int ds4moe_quantize_iq2(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
+/* The 4-bit variant ("DwarfStar" README, "模型权重": the q4 build keeps every routed-expert
+ * projection in 4 bits; the block layout and quantiser are FORMAT.md's Q4_K-style reading). */
+int ds4moe_quantize_q4k(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
 
 /* Host dequantisation to fp32 (the exact values of FORMAT.md), for tests and tools. */
 int ds4moe_dequantize_q2k(const void *src, int64_t rows, int64_t cols, float *dst);
 int ds4moe_dequantize_iq2(const void *src, int64_t rows, int64_t cols, float *dst);
+int ds4moe_dequantize_q4k(const void *src, int64_t rows, int64_t cols, float *dst);
 
 /* ------------------------------------------------------------------ weights handle */
 
@@ -160,6 +166,14 @@ typedef struct {
  * repacks them into the device layout, uploads them and allocates the workspace for
  * max_tokens x max_k pairs. Synchronous. EBADDATA names a non-finite fp16 scale. */
 int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out);
+
+/* A handle of the 4-bit variant: the three per-expert pointers of desc hold Q4_K-style blobs
+ * (gate and up [d_ff x d_model], down [d_model x d_ff], ds4moe_q4k_bytes each). Its routed
+ * experts run on the dequant-GEMV kernels at every T (not on the fused single-token, the
+ * small-group or the tensor-core kernels); the bf16 shared expert keeps its usual kernels.
+ * ds4moe_weights_dequantize gives their fp32 values (dst_f16 is EUNSUPPORTED). Otherwise as
+ * ds4moe_weights_create. */
+int ds4moe_weights_create_q4(const ds4moe_weights_desc *desc, ds4moe_weights **out);
 
 /* A handle whose routed experts stream from host memory into a pool of n_slots expert slots
  * in device memory ("DwarfStar" README, "运行大于 RAM 的模型": a model larger than memory

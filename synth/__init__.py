@@ -164,6 +164,39 @@ def random_q2k_blob(seed, expert, which, rows, cols):
     return b.reshape(-1)
 
 
+def random_q4k_blob(seed, expert, which, rows, cols):
+    """Random Q4_K-style blocks (144 B each, the 4-bit variant) with fp16 d and dmin drawn so
+    that the weights spread like N(0, 0.02) with roughly zero mean (mean code 7.5, mean 6-bit
+    scale and min about 31)."""
+    nb = rows * cols // 256
+    b, g = _rand_bytes(seed, expert, which, nb * 144)
+    b = b.reshape(nb, 144)
+    d = np.float32(0.7e-4) * (np.float32(0.5) + g.random(nb, dtype=np.float32))
+    dmin = d * np.float32(7.5) * (np.float32(0.75) + np.float32(0.5) * g.random(nb, dtype=np.float32))
+    b[:, 0:2] = d.astype(np.float16).view(np.uint8).reshape(nb, 2)
+    b[:, 2:4] = dmin.astype(np.float16).view(np.uint8).reshape(nb, 2)
+    return b.reshape(-1)
+
+
+def random_q4_expert_blobs(wl, experts=None, seed_offset=0):
+    """As random_expert_blobs, for the 4-bit variant: Q4_K-style gate, up and down blobs."""
+    experts = range(wl.E) if experts is None else sorted(set(int(e) for e in experts))
+    s = wl.seed + seed_offset
+    gate, up, down = [None] * wl.E, [None] * wl.E, [None] * wl.E
+
+    def one(e):
+        return (e, random_q4k_blob(s, e, GATE, wl.F, wl.D), random_q4k_blob(s, e, UP, wl.F, wl.D),
+                random_q4k_blob(s, e, DOWN, wl.D, wl.F))
+
+    for e, a, b, c in parallel_map(one, experts):
+        gate[e], up[e], down[e] = a, b, c
+    z = np.zeros(wl.F * wl.D // 256 * 144, np.uint8)
+    for e in range(wl.E):
+        if gate[e] is None:
+            gate[e], up[e], down[e] = z, z, z
+    return gate, up, down
+
+
 def parallel_map(fn, items, threads=None):
     """Run fn over items with a thread pool (numpy's generators release the GIL)."""
     threads = threads or min(32, os.cpu_count() or 1)

@@ -64,6 +64,7 @@ def test_quantizers_byte_identical_to_oracle(ds4, shape, seed):
     w = _weights(*shape, seed)
     assert np.array_equal(ds4.ds4moe_quantize_q2k(w), oracle.quantize_q2k(w))
     assert np.array_equal(ds4.ds4moe_quantize_iq2(w), oracle.quantize_iq2(w))
+    assert np.array_equal(ds4.ds4moe_quantize_q4k(w), oracle.quantize_q4k(w))
 
 
 def test_quantizers_byte_identical_on_expert_weights(ds4):
@@ -71,6 +72,7 @@ def test_quantizers_byte_identical_on_expert_weights(ds4):
     assert np.array_equal(ds4.ds4moe_quantize_iq2(w), oracle.quantize_iq2(w))
     w = synth.expert_weight(7, 3, synth.DOWN, 16, 1024)
     assert np.array_equal(ds4.ds4moe_quantize_q2k(w), oracle.quantize_q2k(w))
+    assert np.array_equal(ds4.ds4moe_quantize_q4k(w), oracle.quantize_q4k(w))
 
 
 def test_host_dequantizers_match_oracle_bitwise(ds4):
@@ -81,6 +83,9 @@ def test_host_dequantizers_match_oracle_bitwise(ds4):
     b = synth.random_q2k_blob(3, 0, 2, rows, cols)
     assert np.array_equal(ds4.ds4moe_dequantize_q2k(b, rows, cols).view(np.uint32),
                           oracle.dequant_q2k(b, rows, cols).view(np.uint32))
+    b = synth.random_q4k_blob(3, 0, 1, rows, cols)
+    assert np.array_equal(ds4.ds4moe_dequantize_q4k(b, rows, cols).view(np.uint32),
+                          oracle.dequant_q4k(b, rows, cols).view(np.uint32))
 
 
 def test_quantizer_rejects_non_finite(ds4):
