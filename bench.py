@@ -32,6 +32,16 @@ L2_BYTES = 129 * 10 ** 6
 METRIC = "routed-MoE tokens/s"
 IQ2_PER_EXPERT = lambda D, F: 2 * F * D // 256 * 66  # noqa: E731  gate + up
 Q2K_PER_EXPERT = lambda D, F: D * F // 256 * 84      # noqa: E731  down
+Q4_UP_PER_EXPERT = lambda D, F: 2 * F * D // 256 * 144  # noqa: E731  gate + up, the 4-bit variant
+Q4_DOWN_PER_EXPERT = lambda D, F: D * F // 256 * 144    # noqa: E731  down, the 4-bit variant
+
+
+def up_per_expert(wl):
+    return Q4_UP_PER_EXPERT(wl.D, wl.F) if wl.fmt == "q4" else IQ2_PER_EXPERT(wl.D, wl.F)
+
+
+def down_per_expert(wl):
+    return Q4_DOWN_PER_EXPERT(wl.D, wl.F) if wl.fmt == "q4" else Q2K_PER_EXPERT(wl.D, wl.F)
 
 
 def parse_args(argv=None):
@@ -151,6 +161,16 @@ def touched_experts(ds4, wl, L):
 def make_weights(ds4, wl, experts, mode):
     """Blobs for every expert: the touched ones quantised from N(0, 0.02) by the library's
     host quantiser (or random valid blocks), the others all-zero blocks (never read)."""
+    if wl.fmt == "q4":
+        if mode == "random":
+            return synth.random_q4_expert_blobs(wl, experts)
+        z = np.zeros(ds4.ds4moe_q4k_bytes(wl.F, wl.D), np.uint8)
+        gate, up, down = [z] * wl.E, [z] * wl.E, [z] * wl.E
+        for e in experts:
+            gate[e] = ds4.ds4moe_quantize_q4k(synth.expert_weight(wl.seed, e, synth.GATE, wl.F, wl.D))
+            up[e] = ds4.ds4moe_quantize_q4k(synth.expert_weight(wl.seed, e, synth.UP, wl.F, wl.D))
+            down[e] = ds4.ds4moe_quantize_q4k(synth.expert_weight(wl.seed, e, synth.DOWN, wl.D, wl.F))
+        return gate, up, down
     if mode == "random":
         return synth.random_expert_blobs(wl, experts)
     nbi = ds4.ds4moe_iq2_bytes(wl.F, wl.D)
@@ -167,7 +187,7 @@ def make_weights(ds4, wl, experts, mode):
 def small_path(wl):
     """Whether a multi-token call runs its small groups on the small-group kernels (the library's
     default for d_model <= 4096 and d_ff <= 2048)."""
-    return wl.T > 1 and wl.D <= 4096 and wl.F <= 2048
+    return wl.T > 1 and wl.D <= 4096 and wl.F <= 2048 and wl.fmt == "q2"
 
 
 def algorithmic(wl, counts):
@@ -178,8 +198,8 @@ def algorithmic(wl, counts):
     sh_up = 2 * F * D * 2 if wl.shared else 0
     sh_down = D * F * 2 if wl.shared else 0
     rows = P + (T if wl.shared else 0)
-    up_bytes = touched * IQ2_PER_EXPERT(D, F) + sh_up + T * D * 2 + rows * F * 4
-    down_bytes = touched * Q2K_PER_EXPERT(D, F) + sh_down + rows * F * 4 + rows * D * 4
+    up_bytes = touched * up_per_expert(wl) + sh_up + T * D * 2 + rows * F * 4
+    down_bytes = touched * down_per_expert(wl) + sh_down + rows * F * 4 + rows * D * 4
     if small_path(wl):
         # the small-group kernels' stages: routed groups below the tensor-core threshold only (the
         # shared expert and larger groups run in the tensor-core stages)
@@ -192,7 +212,7 @@ def algorithmic(wl, counts):
     flops_down = 2 * D * F * rows
     act_bytes = T * D * 2 + T * wl.E * 4 + 2 * T * D * 4 + 2 * rows * F * 4   # x, logits, out, h
     return {"touched": touched, "up_bytes": up_bytes, "down_bytes": down_bytes, "act_bytes": act_bytes,
-            "total_bytes": touched * (IQ2_PER_EXPERT(D, F) + Q2K_PER_EXPERT(D, F)) + sh_up + sh_down,
+            "total_bytes": touched * (up_per_expert(wl) + down_per_expert(wl)) + sh_up + sh_down,
             "flops_up": flops_up, "flops_down": flops_down}
 
 
@@ -216,7 +236,12 @@ SMALL_STAGE_KERNEL = {"up_gemv": ("small_up_kernel", "small_groups.cu"),
                       "down_gemv": ("small_down_kernel", "small_groups.cu")}
 
 
+Q4_STAGE_KERNEL = {"up_gemv": ("gemv_up_kernel", "gemv.cu"), "down_gemv": ("gemv_down_kernel", "gemv.cu")}
+
+
 def stage_kernel(stage, wl):
+    if wl.fmt == "q4" and stage in Q4_STAGE_KERNEL:
+        return Q4_STAGE_KERNEL[stage]
     if small_path(wl) and stage in SMALL_STAGE_KERNEL:
         return SMALL_STAGE_KERNEL[stage]
     return STAGE_KERNEL.get(stage, (stage, None))
@@ -287,7 +312,8 @@ def run_ours(args):
     experts = touched_experts(ds4, wl, L)
     gate, up, down = make_weights(ds4, wl, experts, mode)
     shared = synth.shared_weights(wl.seed, wl.D, wl.F) if wl.shared else None
-    W = ds4.ds4moe_weights_create(gate, up, down, wl.D, wl.F, shared=shared, max_tokens=wl.T, max_k=wl.k)
+    W = ds4.ds4moe_weights_create(gate, up, down, wl.D, wl.F, shared=shared, max_tokens=wl.T, max_k=wl.k,
+                                  fmt=wl.fmt)
     del gate, up, down
     Ld = torch.from_numpy(L).cuda()
     out = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
@@ -432,7 +458,8 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F, "experts": wl.E,
                        "top_k": wl.k, "shared_expert": "bf16" if wl.shared else None,
-                       "routed_weights": "2-bit IQ2-style gate/up + Q2_K-style down, " +
+                       "routed_weights": ("4-bit Q4_K-style gate/up/down, " if wl.fmt == "q4" else
+                                          "2-bit IQ2-style gate/up + Q2_K-style down, ") +
                                          ("host-quantised N(0,0.02)" if mode == "quantized" else "random valid blocks"),
                        "experts_touched": alg["touched"],
                        "l2": "flushed between steps (write then read 256 MB)" if flush else "working set > 4x L2",
@@ -641,9 +668,10 @@ def cpu_worker(workload, seconds):
     while el < seconds:
         toks = np.sort(rng.choice(wl.T, per, replace=False)) if wl.T > per else np.arange(wl.T)
         idx, _ = oracle.route(L[toks], wl.k)
-        gate, up, down = synth.random_expert_blobs(wl, np.unique(idx))
+        blobs = synth.random_q4_expert_blobs if wl.fmt == "q4" else synth.random_expert_blobs
+        gate, up, down = blobs(wl, np.unique(idx))
         t1 = time.perf_counter()
-        oracle.moe_ffn(x[toks], L[toks], wl.k, gate, up, down, wl.D, wl.F, shared=sh)
+        oracle.moe_ffn(x[toks], L[toks], wl.k, gate, up, down, wl.D, wl.F, shared=sh, fmt=wl.fmt)
         el += time.perf_counter() - t1
         n_tok += len(toks)
         calls += 1

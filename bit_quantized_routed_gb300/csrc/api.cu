@@ -546,8 +546,9 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     // decode kernels; groups of 2 .. gemm_min-1 tokens on the multi-token GEMV kernels, which
     // are launched only when such groups can exist; larger groups on the tensor cores.
     const bool multi_gemv = q4 || (!sg && (gemm_min == 0 ? T > 1 : gemm_min > 2));
-    const bool shared_single = w.has_shared && !shared_tc && T == 1;
-    const bool shared_multi = w.has_shared && !shared_tc && T > 1;
+    // (the 4-bit variant takes its shared expert into the GEMV launches at every T)
+    const bool shared_single = w.has_shared && !shared_tc && T == 1 && !q4;
+    const bool shared_multi = w.has_shared && !shared_tc && (T > 1 || q4);
     if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMV);
     if (sg) {
         if (!rc) rc = launch_prep_x(ws, x, T, w.D, stream);

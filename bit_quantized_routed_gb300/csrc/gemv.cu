@@ -148,27 +148,39 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
                     float ag[NT], au[NT];
 #pragma unroll
                     for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
-                    for (int c = lane; c < nbD * 8; c += 32) {  // 32-weight sub-block c of the row
-                        const int b = c >> 3, sub = c & 7;
-                        const uint4 hg = __ldg(reinterpret_cast<const uint4 *>(rg + b * 144));
-                        const uint4 hu = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144));
-                        const uint4 vg = __ldg(reinterpret_cast<const uint4 *>(rg + b * 144 + 16) + sub);
-                        const uint4 vu = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144 + 16) + sub);
-                        float dsg, dmg, dsu, dmu;
-                        q4_sub_scale(hg, sub, dsg, dmg);
-                        q4_sub_scale(hu, sub, dsu, dmu);
+                    // 32-weight sub-blocks c of the row, two per lane at a time: both loads in flight
+                    // before either is used
+                    const int nsub = nbD * 8;
+                    for (int c0 = lane; c0 < nsub; c0 += 64) {
+                        uint4 hg[2], hu[2], vg[2], vu[2];
 #pragma unroll
-                        for (int g = 0; g < 4; g++) {
-                            float wg[8], wu[8];
-                            q4_group(g == 0 ? vg.x : g == 1 ? vg.y : g == 2 ? vg.z : vg.w, dsg, dmg, wg);
-                            q4_group(g == 0 ? vu.x : g == 1 ? vu.y : g == 2 ? vu.z : vu.w, dsu, dmu, wu);
-                            const int xc = swz8(4 * c + g);
+                        for (int t = 0; t < 2; t++) {
+                            const int c = min(c0 + 32 * t, nsub - 1), b = c >> 3, sub = c & 7;
+                            hg[t] = __ldg(reinterpret_cast<const uint4 *>(rg + b * 144));
+                            hu[t] = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144));
+                            vg[t] = __ldg(reinterpret_cast<const uint4 *>(rg + b * 144 + 16) + sub);
+                            vu[t] = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144 + 16) + sub);
+                        }
 #pragma unroll
-                            for (int j = 0; j < NT; j++) {
-                                if (j < nt) {
-                                    const uint4 xv = xs[j * D8 + xc];
-                                    dot8_bf16(wg, xv, ag[j]);
-                                    dot8_bf16(wu, xv, au[j]);
+                        for (int t = 0; t < 2; t++) {
+                            const int c = c0 + 32 * t, sub = c & 7;
+                            if (c >= nsub) break;
+                            float dsg, dmg, dsu, dmu;
+                            q4_sub_scale(hg[t], sub, dsg, dmg);
+                            q4_sub_scale(hu[t], sub, dsu, dmu);
+#pragma unroll
+                            for (int g = 0; g < 4; g++) {
+                                float wg[8], wu[8];
+                                q4_group(g == 0 ? vg[t].x : g == 1 ? vg[t].y : g == 2 ? vg[t].z : vg[t].w, dsg, dmg, wg);
+                                q4_group(g == 0 ? vu[t].x : g == 1 ? vu[t].y : g == 2 ? vu[t].z : vu[t].w, dsu, dmu, wu);
+                                const int xc = swz8(4 * c + g);
+#pragma unroll
+                                for (int j = 0; j < NT; j++) {
+                                    if (j < nt) {
+                                        const uint4 xv = xs[j * D8 + xc];
+                                        dot8_bf16(wg, xv, ag[j]);
+                                        dot8_bf16(wu, xv, au[j]);
+                                    }
                                 }
                             }
                         }
@@ -320,10 +332,20 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
                     float acc[NT];
 #pragma unroll
                     for (int j = 0; j < NT; j++) acc[j] = 0.0f;
-                    for (int c = lane; c < nbF * 8; c += 32) {  // 32-weight sub-block c of the row
-                        const int b = c >> 3, sub = c & 7;
-                        const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(rd + b * 144));
-                        const uint4 vd = __ldg(reinterpret_cast<const uint4 *>(rd + b * 144 + 16) + sub);
+                    const int nsub = nbF * 8;
+                    for (int c0 = lane; c0 < nsub; c0 += 64) {  // two 32-weight sub-blocks per lane at a time
+                        uint4 hd2[2], vd2[2];
+#pragma unroll
+                        for (int t = 0; t < 2; t++) {
+                            const int c = min(c0 + 32 * t, nsub - 1), b = c >> 3, sub = c & 7;
+                            hd2[t] = __ldg(reinterpret_cast<const uint4 *>(rd + b * 144));
+                            vd2[t] = __ldg(reinterpret_cast<const uint4 *>(rd + b * 144 + 16) + sub);
+                        }
+#pragma unroll
+                        for (int t = 0; t < 2; t++) {
+                        const int c = c0 + 32 * t, sub = c & 7;
+                        if (c >= nsub) break;
+                        const uint4 hd = hd2[t], vd = vd2[t];
                         float ds, dm;
                         q4_sub_scale(hd, sub, ds, dm);
 #pragma unroll
@@ -338,6 +360,7 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
                                     acc[j] = dot4(make_float4(wv[4], wv[5], wv[6], wv[7]), h1, acc[j]);
                                 }
                             }
+                        }
                         }
                     }
 #pragma unroll

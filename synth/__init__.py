@@ -43,6 +43,7 @@ class Workload:
     shared: bool = True     # one always-on bf16 shared expert of the same shape
     slots: int = 0          # > 0: experts stream from host memory into this many device slots
     ring: int = 1           # distinct inputs cycled through, one per step (seeds seed .. seed+ring-1)
+    fmt: str = "q2"         # "q2": IQ2-style gate/up + Q2_K-style down; "q4": the 4-bit variant
 
     def replace(self, **kw):
         d = dict(self.__dict__)
@@ -61,6 +62,8 @@ WORKLOADS = {
         # decode with cold experts: 64 of the 256 experts fit in device memory, and each step is
         # a different token, so most of its experts must be copied in from host memory
         Workload("decode_t1_cold", T=1, D=4096, F=2048, E=256, k=8, seed=11, slots=64, ring=64),
+        # the 4-bit variant at the decode shape: Q4_K-style gate, up and down
+        Workload("decode_t1_q4", T=1, D=4096, F=2048, E=256, k=8, seed=12, fmt="q4"),
     ]
 }
 
