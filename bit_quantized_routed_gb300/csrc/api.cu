@@ -558,10 +558,10 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
             if (!rc) rc = launch_decode_up(w, ws, x, T, k, true, stream);
             h->launches++;
         }
-    } else if (!q4 || shared_single) {  // (the 4-bit variant: only the shared expert at T = 1)
+    } else if (!q4) {
         if (!rc) rc = launch_decode_up(w, ws, x, T, k, shared_single, stream);
-    } else {
-        h->launches--;  // the stage's kernel is the GEMV below, counted there
+    } else {  // the 4-bit variant: the tokens as int16 dp2a pairs for its GEMV
+        if (!rc) rc = launch_prep_x(ws, x, T, w.D, stream);
     }
     if (multi_gemv || shared_multi) {
         if (!rc) rc = launch_gemv_up(w, ws, x, T, k, shared_multi, stream);
@@ -583,10 +583,10 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
             if (!rc) rc = launch_decode_down(w, ws, T, k, true, stream);
             h->launches++;
         }
-    } else if (!q4 || shared_single) {
+    } else if (!q4) {
         if (!rc) rc = launch_decode_down(w, ws, T, k, shared_single, stream);
     } else {
-        h->launches--;
+        h->launches--;  // the stage's kernel is the GEMV below, counted there
     }
     if (multi_gemv || shared_multi) {
         if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_multi, stream);

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "step_common.cuh"
 
 namespace ds4moe {
 namespace {
@@ -91,6 +92,11 @@ struct UpParams {
     float *h;             // [P+T][F]
     int T, k, P;
     int shared;           // shared expert on this path
+    // the 4-bit variant: the tokens as int16 dp2a pairs (see prep_x_kernel), 8 x each 32-column
+    // sub-block's sum of them, and each token's factor back to x
+    const uint4 *xq;
+    const int *x8;
+    const float4 *xsc;
 };
 
 // Phase 1: h[pos][r] = silu(gate_r . x) * (up_r . x) for the group's tokens.
@@ -100,6 +106,10 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
     uint2 *grid_s = reinterpret_cast<uint2 *>(smem);              // 256 x 8 B
     uint4 *xs = reinterpret_cast<uint4 *>(smem + 2048);           // [NT][D/8] swizzled
     const int D = p.w.D, F = p.w.F, nbD = p.w.nbD, D8 = D / 8;
+    // the 4-bit variant also stages the int16 tokens: [NT][D/8] swizzled, then [NT][D/32], [NT]
+    uint4 *xqs = xs + NT * D8;
+    int *x8s = reinterpret_cast<int *>(xqs + (Q4 ? NT * D8 : 0));
+    float *xfs = reinterpret_cast<float *>(x8s + (Q4 ? NT * (D / 32) : 0));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < 256; i += kThreads) grid_s[i] = reinterpret_cast<const uint2 *>(p.grid)[i];
 
@@ -135,6 +145,18 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
                     const int j = i / D8, c = i - j * D8;
                     const int tok = is_routed ? p.perm[off + tok0 + j] / p.k : tok0 + j;
                     xs[j * D8 + swz8(c)] = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(tok) * D)[c];
+                    if (Q4) xqs[j * D8 + swz8(c)] = p.xq[static_cast<size_t>(tok) * D8 + c];
+                }
+                if (Q4) {
+                    for (int i = threadIdx.x; i < nt * (D / 32); i += kThreads) {
+                        const int j = i / (D / 32), c = i - j * (D / 32);
+                        const int tok = is_routed ? p.perm[off + tok0 + j] / p.k : tok0 + j;
+                        x8s[i] = p.x8[static_cast<size_t>(tok) * (D / 32) + c];
+                    }
+                    for (int j = threadIdx.x; j < nt; j += kThreads) {
+                        const int tok = is_routed ? p.perm[off + tok0 + j] / p.k : tok0 + j;
+                        xfs[j] = p.xsc[tok].x;
+                    }
                 }
                 __syncthreads();
                 staged_key = key;
@@ -168,19 +190,33 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
                             float dsg, dmg, dsu, dmu;
                             q4_sub_scale(hg[t], sub, dsg, dmg);
                             q4_sub_scale(hu[t], sub, dsu, dmu);
+                            // even codes of each group of 8 as bytes, odd codes as bytes: exact
+                            // integer dot products with the int16 token pairs
+                            uint32_t eg[4], og[4], eu[4], ou[4];
 #pragma unroll
                             for (int g = 0; g < 4; g++) {
-                                float wg[8], wu[8];
-                                q4_group(g == 0 ? vg[t].x : g == 1 ? vg[t].y : g == 2 ? vg[t].z : vg[t].w, dsg, dmg, wg);
-                                q4_group(g == 0 ? vu[t].x : g == 1 ? vu[t].y : g == 2 ? vu[t].z : vu[t].w, dsu, dmu, wu);
-                                const int xc = swz8(4 * c + g);
+                                const uint32_t wgw = g == 0 ? vg[t].x : g == 1 ? vg[t].y : g == 2 ? vg[t].z : vg[t].w;
+                                const uint32_t wuw = g == 0 ? vu[t].x : g == 1 ? vu[t].y : g == 2 ? vu[t].z : vu[t].w;
+                                eg[g] = wgw & 0x0F0F0F0Fu;
+                                og[g] = (wgw >> 4) & 0x0F0F0F0Fu;
+                                eu[g] = wuw & 0x0F0F0F0Fu;
+                                ou[g] = (wuw >> 4) & 0x0F0F0F0Fu;
+                            }
 #pragma unroll
-                                for (int j = 0; j < NT; j++) {
-                                    if (j < nt) {
-                                        const uint4 xv = xs[j * D8 + xc];
-                                        dot8_bf16(wg, xv, ag[j]);
-                                        dot8_bf16(wu, xv, au[j]);
+                            for (int j = 0; j < NT; j++) {
+                                if (j < nt) {
+                                    int sg = 0, su = 0;
+#pragma unroll
+                                    for (int g = 0; g < 4; g++) {
+                                        const uint4 xv = xqs[j * D8 + swz8(4 * c + g)];
+                                        sg = dp2a_hi_su(xv.y, eg[g], dp2a_lo_su(xv.x, eg[g], sg));
+                                        sg = dp2a_hi_su(xv.w, og[g], dp2a_lo_su(xv.z, og[g], sg));
+                                        su = dp2a_hi_su(xv.y, eu[g], dp2a_lo_su(xv.x, eu[g], su));
+                                        su = dp2a_hi_su(xv.w, ou[g], dp2a_lo_su(xv.z, ou[g], su));
                                     }
+                                    const float sx = static_cast<float>(x8s[j * (D / 32) + c] >> 3);  // sum of the 32 int16 x
+                                    ag[j] = fmaf(dsg, static_cast<float>(sg), fmaf(-dmg, sx, ag[j]));
+                                    au[j] = fmaf(dsu, static_cast<float>(su), fmaf(-dmu, sx, au[j]));
                                 }
                             }
                         }
@@ -188,7 +224,8 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
 #pragma unroll
                     for (int j = 0; j < NT; j++) {
                         if (j < nt) {
-                            const float g = warp_sum(ag[j]), u = warp_sum(au[j]);
+                            // the int16 tokens carry the factor xf back to x
+                            const float g = warp_sum(ag[j]) * xfs[j], u = warp_sum(au[j]) * xfs[j];
                             if (lane == 0) p.h[static_cast<size_t>(off + tok0 + j) * F + r] = swiglu(g, u);
                         }
                     }
@@ -531,7 +568,8 @@ int ctas_per_sm(size_t smem) {
 template <int NT, bool Q4>
 int launch_up_nt(const UpParams &p, cudaStream_t s) {
     static int seen[64];
-    const size_t smem = 2048 + static_cast<size_t>(NT) * p.w.D * 2;
+    const size_t smem = 2048 + static_cast<size_t>(NT) * p.w.D * 2 +
+                        (Q4 ? static_cast<size_t>(NT) * (p.w.D * 2 + p.w.D / 32 * 4 + 4) : 0);
     const int err = ensure_smem(reinterpret_cast<const void *>(gemv_up_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
     gemv_up_kernel<NT, Q4><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
@@ -565,6 +603,9 @@ int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *
     p.k = k;
     p.P = T * k;
     p.shared = shared_on_gemv && w.has_shared;
+    p.xq = reinterpret_cast<const uint4 *>(ws.xq);
+    p.x8 = ws.x8;
+    p.xsc = reinterpret_cast<const float4 *>(ws.xsc);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (w.fmt == 1) return T == 1 ? launch_up_nt<1, true>(p, s) : launch_up_nt<8, true>(p, s);
     return T == 1 ? launch_up_nt<1, false>(p, s) : launch_up_nt<8, false>(p, s);

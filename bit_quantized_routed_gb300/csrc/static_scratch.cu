@@ -77,6 +77,7 @@ extern "C" int ds4moe_expert_ffn_static(const uint16_t *x, const ds4moe_weights 
                                         int gate_mode, float *out, ds4moe_stream_t stream) {
     if (!h) return DS4MOE_EINVAL;
     if (h->pool.S) return DS4MOE_EUNSUPPORTED;  // the slot state lives in the handle's workspace
+    if (h->dw.fmt != 0) return DS4MOE_EUNSUPPORTED;  // the 4-bit variant's GEMV needs the int16 token scratch
     const DeviceWeights &w = h->dw;
     if (T < 0 || k < 1 || k > 32 || k > w.E) return DS4MOE_EINVAL;
     if (gate_mode != DS4MOE_GATE_SOFTMAX && gate_mode != DS4MOE_GATE_SIGMOID) return DS4MOE_EINVAL;
