@@ -74,3 +74,17 @@ def test_q4_ffn_matches_oracle(ds4, T, D, F, E, k, shared, mode, quantized):
     ref, _, _ = oracle.moe_ffn(x, L, k, gate, up, down, D, F, shared=sh, mode=mode, tokens=tok, fmt="q4")
     got = out.cpu().numpy() if tok is None else out.cpu().numpy()[tok]
     assert norm_max_err(got, ref) <= FFN_TOL
+
+
+def test_q4_handle_is_refused_by_the_allocation_free_entry(ds4):
+    import torch
+    wl = synth.Workload("q4_static", T=2, D=256, F=256, E=4, k=2, seed=3, shared=False)
+    gate, up, down = synth.random_q4_expert_blobs(wl)
+    W = ds4.ds4moe_weights_create(gate, up, down, wl.D, wl.F, max_tokens=2, max_k=2, fmt="q4")
+    L, x = synth.draw_inputs(wl)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.zeros((2, wl.D), dtype=torch.float32, device="cuda")
+    with pytest.raises(ds4.Ds4moeError) as ei:
+        ds4.ds4moe_expert_ffn_static(xd, W, torch.from_numpy(L).cuda(), 2, out)
+    assert ei.value.status == ds4.DS4MOE_EUNSUPPORTED
+    W.close()
