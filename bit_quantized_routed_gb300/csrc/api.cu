@@ -209,9 +209,10 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds
         TRY(dev_alloc(h, &w.iq2, 16));
         TRY(dev_alloc(h, &w.q2k, 16));
         TRY(dev_alloc(h, &w.tc_ok, E));
-        if (cudaMemset(w.tc_ok, 0, E) != cudaSuccess) TRY(DS4MOE_ECUDA);
         const size_t gb = nb_up * 144, db = nb_down * 144;
+        std::vector<uint8_t> ok(E);
         for (int e = 0; e < E; e++) {
+            double amax = 0.0;  // a bound on |weight|: 63 * 15 |d| + 63 |dmin| per block
             const uint8_t *mats[3] = {static_cast<const uint8_t *>(desc->gate_iq2[e]),
                                       static_cast<const uint8_t *>(desc->up_iq2[e]),
                                       static_cast<const uint8_t *>(desc->down_q2k[e])};
@@ -219,15 +220,19 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds
                 const size_t nbk = m < 2 ? nb_up : nb_down;
                 for (size_t b = 0; b < nbk; b++) {
                     const uint8_t *blk = mats[m] + b * 144;
-                    if (!host_f16_finite(static_cast<uint16_t>(blk[0] | (blk[1] << 8))) ||
-                        !host_f16_finite(static_cast<uint16_t>(blk[2] | (blk[3] << 8))))
-                        TRY(DS4MOE_EBADDATA);
+                    const uint16_t dv = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
+                    const uint16_t mv = static_cast<uint16_t>(blk[2] | (blk[3] << 8));
+                    if (!host_f16_finite(dv) || !host_f16_finite(mv)) TRY(DS4MOE_EBADDATA);
+                    const double bound = 945.0 * std::fabs(host_f16_value(dv)) + 63.0 * std::fabs(host_f16_value(mv));
+                    if (bound > amax) amax = bound;
                 }
             }
+            ok[e] = amax <= kF16Max ? 1 : 0;  // otherwise the expert stays on the GEMV path
             TRY(upload(w.q4 + e * q4b, mats[0], gb));
             TRY(upload(w.q4 + e * q4b + gb, mats[1], gb));
             TRY(upload(w.q4 + e * q4b + 2 * gb, mats[2], db));
         }
+        TRY(upload(w.tc_ok, ok.data(), E));
     }
     if (fmt == 0) {
         TRY(dev_alloc(h, &w.iq2, S * up_bytes));
@@ -513,9 +518,12 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     }
     // A group holds at most T tokens, so the tensor-core path can only be needed when
     // T reaches the threshold; the device decides per group after routing.
-    const bool q4 = w.fmt == 1;  // the 4-bit variant: every routed group on the dequant-GEMV kernels
+    const bool q4 = w.fmt == 1;  // the 4-bit variant: groups below the threshold on the dequant-GEMV kernels
     const bool sg_fits = !q4 && h->small_groups && small_groups_supported(w);
-    const int gm = q4 ? 0 : h->gemm_min_tokens >= 0 ? h->gemm_min_tokens : sg_fits ? (T <= 64 ? 0 : 7) : 2;
+    // (the 4-bit variant has no small-group kernels: from 2 tokens its groups are cheaper on the
+    // tensor cores than on the GEMV, measured on prefill_t2048_q4)
+    const int gm = h->gemm_min_tokens >= 0 ? h->gemm_min_tokens
+                   : q4 ? (T <= 64 ? 0 : 2) : sg_fits ? (T <= 64 ? 0 : 7) : 2;
     const int gemm_min = (gm > 0 && T >= gm) ? gm : 0;
     const bool shared_tc = w.has_shared && w.shared_tc_ok && h->shared_gemm_min_tokens > 0 &&
                            T >= h->shared_gemm_min_tokens;

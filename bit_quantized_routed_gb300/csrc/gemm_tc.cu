@@ -170,7 +170,7 @@ struct IQ2Fmt {
         return v;
     }
     __device__ __forceinline__ void prefetch(int kb) const { prefetch_l2(qs + 16 * (kb ^ swz)); }
-    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
+    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r, int = 0) const {
         const __half2 dh = u2h(v.d | (v.d << 16));
         const uint32_t iw = v.q.x, sw = v.q.y;
         // (s+1)/16, exact in fp16; G*(s+1)/16 is then exact and one multiply by d rounds once
@@ -221,7 +221,7 @@ struct Q2KFmt {
         prefetch_l2(blk);
         prefetch_l2(blk + 79);
     }
-    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r) const {
+    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r, int = 0) const {
         const float d = f16_to_f32(static_cast<uint16_t>(v.dd & 0xffffu));
         const float dmin = f16_to_f32(static_cast<uint16_t>(v.dd >> 16));
         const float ds = __fmul_rn(d, static_cast<float>(v.sc & 15u));
@@ -239,6 +239,87 @@ struct Q2KFmt {
             o.w = __byte_perm(p01, p23, s1.y);
             st_shared16(tile + sw128_off(r, 2 * qp + hh), o);
         }
+    }
+};
+
+// The 4-bit variant (Q4_K-style rows, 144-byte blocks of 8 sub-blocks of 32): each weight is
+// computed as its exact fp32 value (one rounding of d sc q - dmin m) and then RN-even to fp16,
+// as for the Q2_K-style rows. fetch keeps the block's d | dmin word and the two words that hold
+// the sub-block's scale and min bits.
+__device__ __forceinline__ void q4_scales(uint32_t dd, uint32_t lo_word, uint32_t hi_word, int sub, float &ds, float &dm) {
+    const uint32_t low = (lo_word >> (8 * (sub & 3))) & 0xffu;
+    const uint32_t high = (hi_word >> (8 * (sub >> 1) + 4 * (sub & 1))) & 15u;
+    ds = __fmul_rn(f16_to_f32(static_cast<uint16_t>(dd & 0xffffu)), static_cast<float>((low & 15u) | ((high & 3u) << 4)));
+    dm = __fmul_rn(f16_to_f32(static_cast<uint16_t>(dd >> 16)), static_cast<float>((low >> 4) | ((high >> 2) << 4)));
+}
+
+// Eight codes of a u32 (weight i in bits 4i..4i+3) as four fp16 pairs.
+__device__ __forceinline__ uint4 q4_to_f16x8(uint32_t word, float ds, float dm) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = q2k_weight(ds, dm, (word >> (4 * i)) & 15u);
+    return make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
+}
+
+// Gate/up rows of the 4-bit variant, half row: one 32-weight sub-block per stage.
+struct Q4UpFmt {
+    static constexpr int PF = 2;
+    static constexpr int PD = 0;
+    static constexpr int PE = 1;
+    struct Data {
+        uint4 q;
+        uint32_t dd, lo, hi;
+    };
+    const uint8_t *row;
+    int part;
+    __device__ __forceinline__ Data fetch(int kb) const {
+        const int b = kb >> 2, sub = 2 * (kb & 3) + part;
+        const uint8_t *blk = row + b * 144;
+        Data v;
+        v.q = __ldg(reinterpret_cast<const uint4 *>(blk + 16) + sub);
+        v.dd = __ldg(reinterpret_cast<const uint32_t *>(blk));
+        v.lo = __ldg(reinterpret_cast<const uint32_t *>(blk + 4) + (sub >> 2));
+        v.hi = __ldg(reinterpret_cast<const uint32_t *>(blk + 12));
+        return v;
+    }
+    __device__ __forceinline__ void prefetch(int) const {}
+    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r, int kb) const {
+        float ds, dm;
+        q4_scales(v.dd, v.lo, v.hi, 2 * (kb & 3) + part, ds, dm);
+        st_shared16(tile + sw128_off(r, 4 * part + 0), q4_to_f16x8(v.q.x, ds, dm));
+        st_shared16(tile + sw128_off(r, 4 * part + 1), q4_to_f16x8(v.q.y, ds, dm));
+        st_shared16(tile + sw128_off(r, 4 * part + 2), q4_to_f16x8(v.q.z, ds, dm));
+        st_shared16(tile + sw128_off(r, 4 * part + 3), q4_to_f16x8(v.q.w, ds, dm));
+    }
+};
+
+// Down rows of the 4-bit variant, quarter row: half a sub-block (16 weights) per stage.
+struct Q4DownFmt {
+    static constexpr int PF = 3;
+    static constexpr int PD = 0;
+    static constexpr int PE = 1;
+    struct Data {
+        uint2 q;
+        uint32_t dd, lo, hi;
+    };
+    const uint8_t *row;
+    int qp;
+    __device__ __forceinline__ Data fetch(int kb) const {
+        const int b = kb >> 2, sub = 2 * (kb & 3) + (qp >> 1);
+        const uint8_t *blk = row + b * 144;
+        Data v;
+        v.q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 16 * sub) + (qp & 1));
+        v.dd = __ldg(reinterpret_cast<const uint32_t *>(blk));
+        v.lo = __ldg(reinterpret_cast<const uint32_t *>(blk + 4) + (sub >> 2));
+        v.hi = __ldg(reinterpret_cast<const uint32_t *>(blk + 12));
+        return v;
+    }
+    __device__ __forceinline__ void prefetch(int) const {}
+    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r, int kb) const {
+        float ds, dm;
+        q4_scales(v.dd, v.lo, v.hi, 2 * (kb & 3) + (qp >> 1), ds, dm);
+        st_shared16(tile + sw128_off(r, 2 * qp + 0), q4_to_f16x8(v.q.x, ds, dm));
+        st_shared16(tile + sw128_off(r, 2 * qp + 1), q4_to_f16x8(v.q.y, ds, dm));
     }
 };
 
@@ -260,7 +341,7 @@ struct BF16Fmt {
         return d;
     }
     __device__ __forceinline__ void prefetch(int) const {}
-    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
+    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r, int = 0) const {
 #pragma unroll
         for (int c = 0; c < 4; c++) {
             const uint4 v = d.v[c];
@@ -289,7 +370,7 @@ struct F16Fmt {
         return d;
     }
     __device__ __forceinline__ void prefetch(int) const {}
-    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r) const {
+    __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r, int = 0) const {
 #pragma unroll
         for (int c = 0; c < 2; c++) st_shared16(tile + sw128_off(r, 2 * qp + c), d.v[c]);
     }
@@ -322,7 +403,7 @@ __device__ __forceinline__ bool produce_tile(const Fmt &f, int num_kb, uint8_t *
             if (Fmt::PD > 0 && (kb0 + i) % Fmt::PE == 0 && kb0 + i + Fmt::PD < num_kb) f.prefetch(kb0 + i + Fmt::PD);
             if (!mbar_wait(smem_u32(pp.bars + 2 * pp.S + pp.stage), pp.phase ^ 1u, pp.abort_flag, pp.status))
                 return false;
-            f.emit(cur, smem_u32(smem + pp.stage * stage_bytes + a_off), r);
+            f.emit(cur, smem_u32(smem + pp.stage * stage_bytes + a_off), r, kb0 + i);
             fence_proxy_async();
             mbar_arrive(smem_u32(pp.bars + pp.stage));
             if (++pp.stage == pp.S) {
@@ -348,7 +429,8 @@ __device__ __forceinline__ int box_index(int ntok) {
     return i;
 }
 
-template <int KIND>
+// FMT 0: IQ2-style gate/up, Q2_K-style down; FMT 1: the 4-bit variant's rows.
+template <int KIND, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ TokenMaps maps, GemmParams p) {
     using C = Cfg<KIND>;
     constexpr int S = C::STAGES;
@@ -516,6 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (ti.shared) {
                     BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D, part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
+                } else if (FMT == 1) {
+                    Q4UpFmt f{q4_row(p.w, sel, ti.e, wrow), part};
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else {
                     IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab, iq2_swz(p.w, wrow), part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
@@ -523,6 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             } else {
                 if (ti.shared) {
                     F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, part};
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
+                } else if (FMT == 1) {
+                    Q4DownFmt f{q4_row(p.w, 2, ti.e, wrow), part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
                 } else {
                     Q2KFmt f{q2k_sq_row(p.w, ti.e, wrow), q2k_dd_row(p.w, ti.e, wrow), part, tab};
@@ -671,15 +759,20 @@ int sm_count_tc() {
     return n;
 }
 
-template <int KIND>
-int launch_gemm(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) {
+template <int KIND, int FMT>
+int launch_gemm_fmt(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) {
     using C = Cfg<KIND>;
     const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * (C::NA * A_BYTES + B_BYTES) + kTableBytes + 256;
     static int seen[64];
-    const int err = ensure_smem(reinterpret_cast<const void *>(gemm_kernel<KIND>), static_cast<int>(smem), seen);
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemm_kernel<KIND, FMT>), static_cast<int>(smem), seen);
     if (err) return err;
-    gemm_kernel<KIND><<<sm_count_tc(), kThreads, smem, s>>>(maps, p);
+    gemm_kernel<KIND, FMT><<<sm_count_tc(), kThreads, smem, s>>>(maps, p);
     return static_cast<int>(cudaGetLastError());
+}
+
+template <int KIND>
+int launch_gemm(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) {
+    return p.w.fmt == 1 ? launch_gemm_fmt<KIND, 1>(maps, p, s) : launch_gemm_fmt<KIND, 0>(maps, p, s);
 }
 
 GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared) {

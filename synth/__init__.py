@@ -64,6 +64,7 @@ WORKLOADS = {
         Workload("decode_t1_cold", T=1, D=4096, F=2048, E=256, k=8, seed=11, slots=64, ring=64),
         # the 4-bit variant at the decode shape: Q4_K-style gate, up and down
         Workload("decode_t1_q4", T=1, D=4096, F=2048, E=256, k=8, seed=12, fmt="q4"),
+        Workload("prefill_t2048_q4", T=2048, D=4096, F=2048, E=256, k=8, seed=13, bias=("zipf", 1.0), fmt="q4"),
     ]
 }
 
