@@ -169,8 +169,9 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
 
 /* A handle of the 4-bit variant: the three per-expert pointers of desc hold Q4_K-style blobs
  * (gate and up [d_ff x d_model], down [d_model x d_ff], ds4moe_q4k_bytes each). Its routed
- * experts run on the dequant-GEMV kernels at every T (not on the fused single-token, the
- * small-group or the tensor-core kernels); the bf16 shared expert keeps its usual kernels.
+ * groups run on the dequant-GEMV kernels, and in calls of more than 64 tokens those of 2 or
+ * more tokens on the tensor-core kernels (not on the fused single-token or the small-group
+ * kernels); the bf16 shared expert keeps its usual kernels.
  * ds4moe_weights_dequantize gives their fp32 values (dst_f16 is EUNSUPPORTED);
  * ds4moe_expert_ffn_static is EUNSUPPORTED for them. Otherwise as ds4moe_weights_create. */
 int ds4moe_weights_create_q4(const ds4moe_weights_desc *desc, ds4moe_weights **out);
