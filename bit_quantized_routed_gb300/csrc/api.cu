@@ -356,6 +356,12 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds
     TRY(dev_alloc(h, &ws.xq, static_cast<size_t>(desc->max_tokens) * D * 2));
     TRY(dev_alloc(h, &ws.x8, static_cast<size_t>(desc->max_tokens) * (D / 32) * 4));
     TRY(dev_alloc(h, &ws.xsc, static_cast<size_t>(desc->max_tokens) * 16));
+    if (fmt == 1) {  // the 4-bit variant's int16 h (calls of up to 64 tokens)
+        const size_t P64 = static_cast<size_t>(std::min<int64_t>(P, 64 * desc->max_k));
+        TRY(dev_alloc(h, &ws.hq4, P64 * F * 2));
+        TRY(dev_alloc(h, &ws.hsum4, P64 * (F / 32) * 4));
+        TRY(dev_alloc(h, &ws.hsc4, P64 * 4));
+    }
     if (cudaMemset(ws.gbar, 0, 16) != cudaSuccess) TRY(DS4MOE_ECUDA);
     TRY(dev_alloc(h, &ws.grid_hi, 2048));
     {
@@ -593,11 +599,13 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         }
     } else if (!q4) {
         if (!rc) rc = launch_decode_down(w, ws, T, k, shared_single, stream);
+    } else if (T <= 64) {  // the 4-bit variant: each pair's h as int16 for its down GEMV
+        if (!rc) rc = launch_prep_h(ws, T * k, w.F, stream);
     } else {
         h->launches--;  // the stage's kernel is the GEMV below, counted there
     }
     if (multi_gemv || shared_multi) {
-        if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_multi, stream);
+        if (!rc) rc = launch_gemv_down(w, ws, T, k, shared_multi, stream, q4 && T <= 64);
         h->launches++;
     }
     if (any_tc) {

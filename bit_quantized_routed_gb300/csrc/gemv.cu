@@ -317,14 +317,65 @@ struct DownParams {
     float *y;        // [P+T][D]
     int T, P;
     int shared;
+    // the 4-bit variant, when given: each pair's h as int16 dp2a pairs (prep_h_kernel), the sum
+    // of each 32-column sub-block of them, and the factor back to h
+    const uint4 *hq;
+    const int *hsum;
+    const float *hsc;
 };
+
+// The 4-bit variant's down rows: each pair's fp32 h row as int16 pairs (h0,h2), (h4,h6), (h1,h3),
+// (h5,h7) per 8-column group with a power-of-two scale of its own, 2^(14-e) for the exponent e of
+// the row's largest |h|; the sum of each 32-column sub-block of them; the factor 2^(e-14) back.
+// One warp per row.
+__global__ void prep_h_kernel(const float *__restrict__ h, int rows, int F, uint4 *__restrict__ hq,
+                              int *__restrict__ hsum, float *__restrict__ hsc) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float4 *hr = reinterpret_cast<const float4 *>(h + static_cast<size_t>(row) * F);
+    float m = 0.0f;
+    for (int i = lane; i < F / 4; i += 32) {
+        const float4 v = hr[i];
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    int e = 0;
+    frexpf(m, &e);
+    e = m > 0.0f ? e : 0;
+    const float sc = ldexpf(1.0f, 14 - e);
+    for (int c = lane; c < F / 32; c += 32) {
+        int sum = 0;
+#pragma unroll
+        for (int g = 0; g < 4; g++) {
+            const float4 a = hr[8 * c + 2 * g], b = hr[8 * c + 2 * g + 1];
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t q[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                q[i] = round_to_int_bits(v[i] * sc);
+                sum += static_cast<int>(static_cast<int16_t>(q[i] & 0xffffu));
+            }
+            hq[static_cast<size_t>(row) * (F / 8) + 4 * c + g] =
+                make_uint4(__byte_perm(q[0], q[2], 0x5410), __byte_perm(q[4], q[6], 0x5410),
+                           __byte_perm(q[1], q[3], 0x5410), __byte_perm(q[5], q[7], 0x5410));
+        }
+        hsum[static_cast<size_t>(row) * (F / 32) + c] = sum;
+    }
+    if (lane == 0) hsc[row] = ldexpf(1.0f, e - 14);
+}
 
 // Phase 2: y[pos][r] = down_r . h[pos] for the group's tokens.
 template <int NT, bool Q4>
 __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     float4 *hs = reinterpret_cast<float4 *>(smem);  // [NT][F/4] swizzled
-    const int D = p.w.D, F = p.w.F, nbF = p.w.nbF, F4 = F / 4;
+    const int D = p.w.D, F = p.w.F, nbF = p.w.nbF, F4 = F / 4, F8 = F / 8;
+    // the 4-bit variant with int16 h: [NT][F/8] swizzled, then [NT][F/32] sums, [NT] factors
+    const bool ih = Q4 && p.hq != nullptr;
+    uint4 *hqs = reinterpret_cast<uint4 *>(hs + NT * F4);
+    int *hsums = reinterpret_cast<int *>(hqs + (Q4 ? NT * F8 : 0));
+    float *hfs = reinterpret_cast<float *>(hsums + (Q4 ? NT * (F / 32) : 0));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_gemv = p.meta->n_gemv;
     const int per_group = D / kDownRows;
@@ -357,6 +408,17 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
                     const int j = i / F4, c = i - j * F4;
                     hs[j * F4 + swz16(c)] = reinterpret_cast<const float4 *>(p.h + static_cast<size_t>(off + tok0 + j) * F)[c];
                 }
+                if (ih && is_routed) {
+                    for (int i = threadIdx.x; i < nt * F8; i += kThreads) {
+                        const int j = i / F8, c = i - j * F8;
+                        hqs[j * F8 + swz8(c)] = p.hq[static_cast<size_t>(off + tok0 + j) * F8 + c];
+                    }
+                    for (int i = threadIdx.x; i < nt * (F / 32); i += kThreads) {
+                        const int j = i / (F / 32), c = i - j * (F / 32);
+                        hsums[i] = p.hsum[static_cast<size_t>(off + tok0 + j) * (F / 32) + c];
+                    }
+                    for (int j = threadIdx.x; j < nt; j += kThreads) hfs[j] = p.hsc[off + tok0 + j];
+                }
                 __syncthreads();
                 staged_key = key;
                 staged_tok0 = tok0;
@@ -385,6 +447,30 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
                         const uint4 hd = hd2[t], vd = vd2[t];
                         float ds, dm;
                         q4_sub_scale(hd, sub, ds, dm);
+                        if (ih) {  // exact integer dot products of the codes with the int16 h
+                            uint32_t ev[4], ov[4];
+#pragma unroll
+                            for (int g = 0; g < 4; g++) {
+                                const uint32_t wd = g == 0 ? vd.x : g == 1 ? vd.y : g == 2 ? vd.z : vd.w;
+                                ev[g] = wd & 0x0F0F0F0Fu;
+                                ov[g] = (wd >> 4) & 0x0F0F0F0Fu;
+                            }
+#pragma unroll
+                            for (int j = 0; j < NT; j++) {
+                                if (j < nt) {
+                                    int sd = 0;
+#pragma unroll
+                                    for (int g = 0; g < 4; g++) {
+                                        const uint4 hv = hqs[j * F8 + swz8(4 * c + g)];
+                                        sd = dp2a_hi_su(hv.y, ev[g], dp2a_lo_su(hv.x, ev[g], sd));
+                                        sd = dp2a_hi_su(hv.w, ov[g], dp2a_lo_su(hv.z, ov[g], sd));
+                                    }
+                                    acc[j] = fmaf(ds, static_cast<float>(sd),
+                                                  fmaf(-dm, static_cast<float>(hsums[j * (F / 32) + c]), acc[j]));
+                                }
+                            }
+                            continue;
+                        }
 #pragma unroll
                         for (int g = 0; g < 4; g++) {
                             float wv[8];
@@ -403,7 +489,7 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
 #pragma unroll
                     for (int j = 0; j < NT; j++) {
                         if (j < nt) {
-                            const float v = warp_sum(acc[j]);
+                            const float v = warp_sum(acc[j]) * (ih ? hfs[j] : 1.0f);
                             if (lane == 0) p.y[static_cast<size_t>(off + tok0 + j) * D + r] = v;
                         }
                     }
@@ -579,7 +665,8 @@ int launch_up_nt(const UpParams &p, cudaStream_t s) {
 template <int NT, bool Q4>
 int launch_down_nt(const DownParams &p, cudaStream_t s) {
     static int seen[64];
-    const size_t smem = static_cast<size_t>(NT) * p.w.F * 4;
+    const size_t smem = static_cast<size_t>(NT) * p.w.F * 4 +
+                        (Q4 ? static_cast<size_t>(NT) * (p.w.F * 2 + p.w.F / 32 * 4 + 4) : 0);
     const int err = ensure_smem(reinterpret_cast<const void *>(gemv_down_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
     gemv_down_kernel<NT, Q4><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
@@ -611,7 +698,15 @@ int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *
     return T == 1 ? launch_up_nt<1, false>(p, s) : launch_up_nt<8, false>(p, s);
 }
 
-int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream) {
+int launch_prep_h(const Workspace &ws, int rows, int F, void *stream) {
+    if (rows <= 0) return 0;
+    prep_h_kernel<<<(rows + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        ws.h32, rows, F, reinterpret_cast<uint4 *>(ws.hq4), ws.hsum4, ws.hsc4);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream,
+                     bool int16_h) {
     DownParams p;
     p.w = w;
     p.offsets = ws.offsets;
@@ -622,6 +717,9 @@ int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, 
     p.T = T;
     p.P = T * k;
     p.shared = shared_on_gemv && w.has_shared;
+    p.hq = int16_h ? reinterpret_cast<const uint4 *>(ws.hq4) : nullptr;
+    p.hsum = ws.hsum4;
+    p.hsc = ws.hsc4;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (w.fmt == 1) return T == 1 ? launch_down_nt<1, true>(p, s) : launch_down_nt<8, true>(p, s);
     return T == 1 ? launch_down_nt<1, false>(p, s) : launch_down_nt<8, false>(p, s);

@@ -169,6 +169,9 @@ struct Workspace {
     uint32_t *xq;       // [T][D/8][4] tokens as int16 pairs for the small-group kernels (dp2a order)
     int32_t *x8;        // [T][D/32] 8 x the sum of each 32-column sub-block of xq
     float *xsc;         // [T][4] dequantisation factor of xq (element 0; the rest pad to 16 bytes)
+    uint32_t *hq4;      // 4-bit variant handles: [P][F/8][4] h as int16 dp2a pairs (prep_h)
+    int *hsum4;         // [P][F/32] sum of each 32-column sub-block of hq4
+    float *hsc4;        // [P] factor from hq4 back to h
 };
 
 }  // namespace ds4moe
@@ -238,8 +241,10 @@ int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16
 int decode_step_ctas();
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
                    bool shared_on_gemv, void *stream);
-int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv,
-                     void *stream);
+// int16_h: the 4-bit variant's down rows on int16 h (launch_prep_h first)
+int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream,
+                     bool int16_h = false);
+int launch_prep_h(const Workspace &ws, int rows, int F, void *stream);
 int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, float *out, void *stream);
 int launch_dequant(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, float *dst32,
                    uint16_t *dst16, void *stream);
