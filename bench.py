@@ -19,6 +19,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -106,7 +107,8 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+        # the raw samples (nvidia-smi CSV); the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), "ds4moe_clocks_%d.csv" % os.getpid())
 
     def __enter__(self):
         try:
