@@ -425,6 +425,7 @@ int ds4moe_set_option(ds4moe_weights *h, int option, int value) {
         case DS4MOE_OPT_SINGLE_STEP: h->single_step = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_SMALL_GROUPS: h->small_groups = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_TRACE: h->trace = value ? 1 : 0; return DS4MOE_OK;
+        case DS4MOE_OPT_WAIT_TEST: h->wait_test = value > 0 ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_PROFILE:
             if (value && !h->events[0]) {
                 for (auto &ev : h->events) {
@@ -510,7 +511,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         rc = clk.stage(DS4MOE_STAGE_STEP);
         if (!rc)
             rc = launch_decode_step(w, ws, x, logits, k, gate_mode, out, h->trace ? ws.trace : nullptr, E_route,
-                                    pooled ? h->pool.slot_of : nullptr, stream);
+                                    pooled ? h->pool.slot_of : nullptr, static_cast<unsigned int>(h->wait_test), stream);
         if (!rc) {
             rc = clk.finish();
             h->calls++;

@@ -111,6 +111,7 @@ struct StepParams {
     int *hexp;             // [k][F/16] its power-of-two exponent: h = hq * 2^(hexp - 14)
     float *hsh;            // [F] shared expert's h (fp32)
     unsigned long long *bar;  // grid barrier: arrivals since the workspace was made
+    unsigned int bar_extra;   // 0 (tests of the bounded wait: arrivals that never come)
     uint64_t *trace;       // null, or [gridDim][6] timestamps (ns)
     int *status;
 };
@@ -387,11 +388,13 @@ __device__ __forceinline__ float dot8_bf16(uint4 w, float4 xa, float4 xb, float 
 // CTAs of one call take tickets n*G .. n*G+G-1 and wait until the counter reaches (n+1)*G, so
 // the counter never needs resetting. The add releases this CTA's writes (observed by this
 // thread through the CTA barrier before it) at GPU scope; the polling load acquires the others'.
-__device__ bool grid_barrier(unsigned long long *count, int *status) {
+// extra: arrivals beyond the grid's to wait for (0; a test of the bounded wait sets more, which
+// never come, so the wait runs out and reports ST_TIMEOUT).
+__device__ bool grid_barrier(unsigned long long *count, int *status, unsigned int extra) {
     const unsigned long long G = gridDim.x;
     unsigned long long ticket;
     asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(ticket) : "l"(count) : "memory");
-    const unsigned long long target = (ticket / G + 1ull) * G;
+    const unsigned long long target = (ticket / G + 1ull) * G + extra;
     const long long t0 = clock64();
     while (true) {
         unsigned long long v;
@@ -733,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
     // ---------------------------------------------------------------- grid barrier: all h written
     bar_sync(kBarAll, kNAll);
     if (tr) tr[2] = now_ns();
-    if (threadIdx.x == 0 && !grid_barrier(p.bar, p.status)) *abort_flag = 1;
+    if (threadIdx.x == 0 && !grid_barrier(p.bar, p.status, p.bar_extra)) *abort_flag = 1;
     bar_sync(kBarCompute, kNCompute);
     if (tr) tr[3] = now_ns();
 
@@ -876,7 +879,8 @@ bool decode_step_supported(const DeviceWeights &w, int k) {
 }
 
 int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, const float *logits, int k,
-                       int gate_mode, float *out, uint64_t *trace, int E_route, const int32_t *slot_of, void *stream) {
+                       int gate_mode, float *out, uint64_t *trace, int E_route, const int32_t *slot_of,
+                       unsigned int bar_extra, void *stream) {
     static int seen[3][64];
     const int nq = w.D <= 1024 ? 1 : w.D <= 2048 ? 2 : 4;  // 1024-column quarters of x
     const void *kern = nq == 1   ? reinterpret_cast<const void *>(decode_step_kernel<1>)
@@ -902,6 +906,7 @@ int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16
     p.hexp = reinterpret_cast<int *>(hb + static_cast<size_t>(k) * w.F * 2);
     p.hsh = reinterpret_cast<float *>(p.hexp + static_cast<size_t>(k) * (w.F / 16));
     p.bar = reinterpret_cast<unsigned long long *>(ws.gbar);
+    p.bar_extra = bar_extra;
     p.trace = trace;
     p.status = ws.status;
     void *args[] = {&p};

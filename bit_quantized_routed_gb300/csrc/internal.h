@@ -186,6 +186,7 @@ struct ds4moe_weights {
     int single_step;  // T = 1 calls use the fused single-token kernel when it supports the shape
     int trace;        // record the single-token kernel's per-CTA timestamps
     int small_groups; // groups below the tensor-core threshold run on the small-group kernels
+    int wait_test;    // DS4MOE_OPT_WAIT_TEST
     void *events[DS4MOE_N_STAGES + 1];  // cudaEvent_t: start of each stage, end of the call
     bool stage_ran[DS4MOE_N_STAGES];
     bool events_recorded;
@@ -237,7 +238,8 @@ int launch_decode_down(const DeviceWeights &w, const Workspace &ws, int T, int k
 bool decode_step_supported(const DeviceWeights &w, int k);
 // E_route: experts the logits route over; slot_of: null, or a pooled handle's expert -> slot map
 int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, const float *logits, int k,
-                       int gate_mode, float *out, uint64_t *trace, int E_route, const int32_t *slot_of, void *stream);
+                       int gate_mode, float *out, uint64_t *trace, int E_route, const int32_t *slot_of,
+                       unsigned int bar_extra, void *stream);
 int decode_step_ctas();
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
                    bool shared_on_gemv, void *stream);

@@ -82,7 +82,12 @@ enum ds4moe_option {
      * and take the down projection pair by pair; used when d_model <= 4096 and d_ff <= 2048
      * and the bf16 shared expert, if any, is on the tensor cores (or T = 1). 0: the fused
      * dequant-GEMV kernels. Default 1. */
-    DS4MOE_OPT_SMALL_GROUPS = 5
+    DS4MOE_OPT_SMALL_GROUPS = 5,
+    /* Tests of the bounded device waits: value > 0 makes the single-token kernel's grid barrier
+     * wait for an arrival that never comes, so the wait runs out (about 2 s), every CTA finishes
+     * through its abort path, and ds4moe_last_status reports DS4MOE_ETIMEOUT; the handle stays
+     * usable. Default 0. */
+    DS4MOE_OPT_WAIT_TEST = 6
 };
 
 /* Stages of ds4moe_expert_ffn, in launch order (indices into ds4moe_stats.stage_ms). */

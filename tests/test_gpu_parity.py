@@ -340,3 +340,24 @@ def test_layer_from_hidden_states(ds4):
     W.close()
     ref, _, _ = lay.oracle_delta()
     assert norm_max_err(out.cpu().numpy(), ref) <= FFN_TOL
+
+
+def test_single_token_kernel_bounded_wait_runs_out_and_the_handle_recovers(ds4):
+    # the grid barrier waits for an arrival nothing sends: the wait gives up (about 2 s), every
+    # CTA leaves through its abort path, the status word says so, and the next call is normal
+    import torch
+    wl = synth.Workload("wait_test", T=1, D=512, F=2048, E=16, k=4, seed=61, shared=True)
+    lay = Layer(wl, quantized=False)
+    W = lay.upload(ds4)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_WAIT_TEST, 1)
+    x = torch.from_numpy(lay.x.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.zeros((1, wl.D), dtype=torch.float32, device="cuda")
+    before = ds4.ds4moe_get_stats(W)["launches"]
+    ds4.ds4moe_expert_ffn(x, W, torch.from_numpy(lay.L).cuda(), wl.k, out)
+    assert ds4.ds4moe_get_stats(W)["launches"] - before == 1   # the fused kernel took the call
+    assert ds4.ds4moe_last_status(W) == ds4.DS4MOE_ETIMEOUT
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_WAIT_TEST, 0)
+    got = lay.run(ds4, W)                                       # asserts a clean status
+    W.close()
+    ref, _, _ = lay.oracle_delta()
+    assert norm_max_err(got, ref) <= FFN_TOL
