@@ -628,16 +628,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             bool range_ok = true;
             for (int c0 = 16 * colq; c0 < ti.ntok; c0 += 64) {
                 if (KIND == UP) {
-                    float g[16], uu[16];
-                    tmem_ld16(tmem + lane_addr + c0, g);
-                    tmem_ld16(tmem + lane_addr + BN + c0, uu);
+#pragma unroll 1
+                    for (int cb = c0; cb < c0 + 16 && cb < ti.ntok; cb += 8) {  // 8 columns at a time
+                        float g[8], uu[8];
+                        tmem_ld8(tmem + lane_addr + cb, g);
+                        tmem_ld8(tmem + lane_addr + BN + cb, uu);
 #pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        if (c0 + j < ti.ntok) {
-                            const float h = swiglu(g[j], uu[j]);
-                            range_ok &= fabsf(h) <= 65504.0f;
-                            p.h16[static_cast<size_t>(ti.row0 + c0 + j) * F + orow] =
-                                __half_as_ushort(__float2half_rn(h));
+                        for (int j = 0; j < 8; j++) {
+                            if (cb + j < ti.ntok) {
+                                const float h = swiglu(g[j], uu[j]);
+                                range_ok &= fabsf(h) <= 65504.0f;
+                                p.h16[static_cast<size_t>(ti.row0 + cb + j) * F + orow] =
+                                    __half_as_ushort(__float2half_rn(h));
+                            }
                         }
                     }
                 } else {
