@@ -4,17 +4,18 @@
 // and is compute-rich; with many tokens per expert the expert FFN is a dense contraction,
 // so it runs on the 5th-generation tensor cores. Per (expert, 128 weight rows, up to 256
 // tokens) tile:
-//   * eight producer warps stream the packed 2-bit weight rows from HBM (a ring of register
-//     prefetches per thread), decode them to fp16 (RN-even of the exact fp32 value) and
-//     write them into shared memory in the canonical K-major SWIZZLE_128B layout (one
-//     128-row x 64-column atom column per stage);
+//   * sixteen producer warps stream the packed weight rows from HBM (each thread one slice of
+//     a row: half of a gate/up row's sub-blocks or a quarter of a down row's, with a ring of
+//     register prefetches and L2 prefetches ahead of it), decode them to fp16 (RN-even of the
+//     exact fp32 value) and write them into shared memory in the canonical K-major
+//     SWIZZLE_128B layout (one 128-row x 64-column atom column per stage);
 //   * one warp issues TMA loads of the group's token rows (fp16, gathered per group) into
 //     the same layout;
 //   * one thread issues tcgen05.mma (M=128, N=tokens rounded up to 16, K=16) into fp32
 //     accumulators in tensor memory: gate and up side by side for the first GEMM;
-//   * the producer warps then read the accumulators back with tcgen05.ld (two warps per
-//     TMEM lane quarter) and apply the epilogue: h = silu(gate) * up (fp16 out) for the first GEMM, y (fp32 out) for the down
-//     GEMM.
+//   * the producer warps then read the accumulators back with tcgen05.ld (four warps per
+//     TMEM lane quarter) and apply the epilogue: h = silu(gate) * up (fp16 out) for the
+//     first GEMM, y (fp32 out) for the down GEMM.
 // Swap-AB: weights are the M side and tokens the N side, so groups of a few dozen tokens
 // still fill MMAs. Every wait on an mbarrier is bounded: after ~2 s it records
 // DS4MOE_ETIMEOUT in the handle's status word and the CTA drains its copies, frees its
@@ -636,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                         for (int j = 0; j < 8; j++) {
                             if (cb + j < ti.ntok) {
-                                const float h = swiglu(g[j], uu[j]);
+                                const float h = swiglu_fast(g[j], uu[j]);
                                 range_ok &= fabsf(h) <= 65504.0f;
                                 p.h16[static_cast<size_t>(ti.row0 + cb + j) * F + orow] =
                                     __half_as_ushort(__float2half_rn(h));
