@@ -31,11 +31,18 @@ struct Items {
 };
 
 // Contiguous item range of this CTA, so consecutive items usually share a group and the
-// staged tokens are reused.
-__device__ __forceinline__ void cta_range(int total, int &begin, int &end) {
-    const int per = (total + gridDim.x - 1) / gridDim.x;
-    begin = min(total, blockIdx.x * per);
-    end = min(total, begin + per);
+// staged tokens are reused. The routed items come first, then the shared expert's; the ranges
+// split the bytes evenly (a routed item streams cr bytes, a shared one cs): item i starts at
+// byte offset c_i, and CTA b takes the items with c_i in [B*b/G, B*(b+1)/G) of the total B.
+__device__ __forceinline__ int item_at(long long c, int routed, long long cr, long long cs) {
+    const long long cr_all = routed * cr;
+    if (c <= cr_all) return static_cast<int>((c + cr - 1) / cr);
+    return routed + static_cast<int>((c - cr_all + cs - 1) / cs);
+}
+__device__ __forceinline__ void cta_range(int routed, int shared, long long cr, long long cs, int &begin, int &end) {
+    const long long B = routed * cr + shared * cs, G = gridDim.x;
+    begin = item_at(B * blockIdx.x / G, routed, cr, cs);
+    end = item_at(B * (blockIdx.x + 1) / G, routed, cr, cs);
 }
 
 // Swizzled index of 16-byte chunk c in a staged token row (bank-conflict-free for the
@@ -116,9 +123,11 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
     const int n_gemv = p.meta->n_gemv;
     const int per_group = F / kUpRows;
     const int routed = n_gemv * per_group;
-    const int total = routed + (p.shared ? F / kUpSharedRows : 0);
+    const int n_shared = p.shared ? F / kUpSharedRows : 0;
+    // bytes per item: 16 rows of gate and up in the routed format (per 256 columns), 8 bf16 rows
+    const long long cr = 2LL * kUpRows * (Q4 ? 144 : 66), cs = 2LL * kUpSharedRows * 512;
     int begin, end;
-    cta_range(total, begin, end);
+    cta_range(routed, n_shared, cr, cs, begin, end);
     int staged_key = -1, staged_tok0 = -1;  // which tokens sit in xs
     __syncthreads();
 
@@ -170,13 +179,14 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
                     float ag[NT], au[NT];
 #pragma unroll
                     for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
-                    // 32-weight sub-blocks c of the row, two per lane at a time: both loads in flight
-                    // before either is used
+                    // 32-weight sub-blocks c of the row, U per lane at a time: all their loads in flight
+                    // before any is used (a single token has little else to hide the latency with)
+                    constexpr int U = NT == 1 ? 4 : 2;
                     const int nsub = nbD * 8;
-                    for (int c0 = lane; c0 < nsub; c0 += 64) {
-                        uint4 hg[2], hu[2], vg[2], vu[2];
+                    for (int c0 = lane; c0 < nsub; c0 += 32 * U) {
+                        uint4 hg[U], hu[U], vg[U], vu[U];
 #pragma unroll
-                        for (int t = 0; t < 2; t++) {
+                        for (int t = 0; t < U; t++) {
                             const int c = min(c0 + 32 * t, nsub - 1), b = c >> 3, sub = c & 7;
                             hg[t] = __ldg(reinterpret_cast<const uint4 *>(rg + b * 144));
                             hu[t] = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144));
@@ -184,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
                             vu[t] = __ldg(reinterpret_cast<const uint4 *>(ru + b * 144 + 16) + sub);
                         }
 #pragma unroll
-                        for (int t = 0; t < 2; t++) {
+                        for (int t = 0; t < U; t++) {
                             const int c = c0 + 32 * t, sub = c & 7;
                             if (c >= nsub) break;
                             float dsg, dmg, dsu, dmu;
@@ -283,17 +293,30 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
                 float ag[NT], au[NT];
 #pragma unroll
                 for (int j = 0; j < NT; j++) ag[j] = au[j] = 0.0f;
-                for (int c = lane; c < D8; c += 32) {
-                    float wg[8], wu[8];
-                    bf16x8(__ldg(sg + c), wg);
-                    bf16x8(__ldg(su + c), wu);
-                    const int xc = swz8(c);
+                constexpr int US = NT == 1 ? 8 : 1;  // 16-byte chunks per lane in flight
+                for (int c0 = lane; c0 < D8; c0 += 32 * US) {
+                    uint4 vg[US], vu[US];
 #pragma unroll
-                    for (int j = 0; j < NT; j++) {
-                        if (j < nt) {
-                            const uint4 xv = xs[j * D8 + xc];
-                            dot8_bf16(wg, xv, ag[j]);
-                            dot8_bf16(wu, xv, au[j]);
+                    for (int t = 0; t < US; t++) {
+                        const int c = min(c0 + 32 * t, D8 - 1);
+                        vg[t] = __ldg(sg + c);
+                        vu[t] = __ldg(su + c);
+                    }
+#pragma unroll
+                    for (int t = 0; t < US; t++) {
+                        const int c = c0 + 32 * t;
+                        if (c >= D8) break;
+                        float wg[8], wu[8];
+                        bf16x8(vg[t], wg);
+                        bf16x8(vu[t], wu);
+                        const int xc = swz8(c);
+#pragma unroll
+                        for (int j = 0; j < NT; j++) {
+                            if (j < nt) {
+                                const uint4 xv = xs[j * D8 + xc];
+                                dot8_bf16(wg, xv, ag[j]);
+                                dot8_bf16(wu, xv, au[j]);
+                            }
                         }
                     }
                 }
@@ -380,9 +403,11 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
     const int n_gemv = p.meta->n_gemv;
     const int per_group = D / kDownRows;
     const int routed = n_gemv * per_group;
-    const int total = routed + (p.shared ? D / kDownSharedRows : 0);
+    const int n_shared = p.shared ? D / kDownSharedRows : 0;
+    // bytes per item: 32 rows in the routed format (per 256 columns), 8 bf16 rows
+    const long long cr = static_cast<long long>(kDownRows) * (Q4 ? 144 : 84), cs = kDownSharedRows * 512LL;
     int begin, end;
-    cta_range(total, begin, end);
+    cta_range(routed, n_shared, cr, cs, begin, end);
     int staged_key = -1, staged_tok0 = -1;
 
     for (int item = begin; item < end; item++) {
@@ -423,7 +448,88 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
                 staged_key = key;
                 staged_tok0 = tok0;
             }
-            if (is_routed && Q4) {
+            if (is_routed && Q4 && NT == 1) {
+                constexpr int RP = 2;  // rows per pass: their loads in flight together
+#pragma unroll 1
+                for (int rr = 0; rr < kDownRows / kWarps; rr += RP) {
+                    const uint8_t *rdq[RP];
+                    float acc[RP][NT];
+#pragma unroll
+                    for (int q = 0; q < RP; q++) {
+                        rdq[q] = q4_row(p.w, 2, e, r0 + warp + (rr + q) * kWarps);
+#pragma unroll
+                        for (int j = 0; j < NT; j++) acc[q][j] = 0.0f;
+                    }
+                    const int nsub = nbF * 8;
+                    for (int c0 = lane; c0 < nsub; c0 += 64) {  // two 32-weight sub-blocks per lane and row at a time
+                        uint4 hd2[RP][2], vd2[RP][2];
+#pragma unroll
+                        for (int q = 0; q < RP; q++)
+#pragma unroll
+                            for (int t = 0; t < 2; t++) {
+                                const int c = min(c0 + 32 * t, nsub - 1), b = c >> 3, sub = c & 7;
+                                hd2[q][t] = __ldg(reinterpret_cast<const uint4 *>(rdq[q] + b * 144));
+                                vd2[q][t] = __ldg(reinterpret_cast<const uint4 *>(rdq[q] + b * 144 + 16) + sub);
+                            }
+#pragma unroll
+                        for (int q = 0; q < RP; q++)
+#pragma unroll
+                        for (int t = 0; t < 2; t++) {
+                        const int c = c0 + 32 * t, sub = c & 7;
+                        if (c >= nsub) break;
+                        const uint4 hd = hd2[q][t], vd = vd2[q][t];
+                        float ds, dm;
+                        q4_sub_scale(hd, sub, ds, dm);
+                        if (ih) {  // exact integer dot products of the codes with the int16 h
+                            uint32_t ev[4], ov[4];
+#pragma unroll
+                            for (int g = 0; g < 4; g++) {
+                                const uint32_t wd = g == 0 ? vd.x : g == 1 ? vd.y : g == 2 ? vd.z : vd.w;
+                                ev[g] = wd & 0x0F0F0F0Fu;
+                                ov[g] = (wd >> 4) & 0x0F0F0F0Fu;
+                            }
+#pragma unroll
+                            for (int j = 0; j < NT; j++) {
+                                if (j < nt) {
+                                    int sd = 0;
+#pragma unroll
+                                    for (int g = 0; g < 4; g++) {
+                                        const uint4 hv = hqs[j * F8 + swz8(4 * c + g)];
+                                        sd = dp2a_hi_su(hv.y, ev[g], dp2a_lo_su(hv.x, ev[g], sd));
+                                        sd = dp2a_hi_su(hv.w, ov[g], dp2a_lo_su(hv.z, ov[g], sd));
+                                    }
+                                    acc[q][j] = fmaf(ds, static_cast<float>(sd),
+                                                     fmaf(-dm, static_cast<float>(hsums[j * (F / 32) + c]), acc[q][j]));
+                                }
+                            }
+                            continue;
+                        }
+#pragma unroll
+                        for (int g = 0; g < 4; g++) {
+                            float wv[8];
+                            q4_group(g == 0 ? vd.x : g == 1 ? vd.y : g == 2 ? vd.z : vd.w, ds, dm, wv);
+#pragma unroll
+                            for (int j = 0; j < NT; j++) {
+                                if (j < nt) {
+                                    const float4 h0 = hs[j * F4 + swz16(8 * c + 2 * g)], h1 = hs[j * F4 + swz16(8 * c + 2 * g + 1)];
+                                    acc[q][j] = dot4(make_float4(wv[0], wv[1], wv[2], wv[3]), h0, acc[q][j]);
+                                    acc[q][j] = dot4(make_float4(wv[4], wv[5], wv[6], wv[7]), h1, acc[q][j]);
+                                }
+                            }
+                        }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < RP; q++)
+#pragma unroll
+                        for (int j = 0; j < NT; j++) {
+                            if (j < nt) {
+                                const float v = warp_sum(acc[q][j]) * (ih ? hfs[j] : 1.0f);
+                                if (lane == 0) p.y[static_cast<size_t>(off + tok0 + j) * D + r0 + warp + (rr + q) * kWarps] = v;
+                            }
+                        }
+                }
+            } else if (is_routed && Q4) {  // several tokens: one row at a time
 #pragma unroll 1
                 for (int rr = 0; rr < kDownRows / kWarps; rr++) {
                     const int r = r0 + warp + rr * kWarps;
@@ -545,15 +651,24 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
                 float acc[NT];
 #pragma unroll
                 for (int j = 0; j < NT; j++) acc[j] = 0.0f;
-                for (int c = lane; c < F / 8; c += 32) {
-                    float wv[8];
-                    bf16x8(__ldg(sd + c), wv);
+                constexpr int US = NT == 1 ? 8 : 1;  // 16-byte chunks per lane in flight
+                for (int c0 = lane; c0 < F8; c0 += 32 * US) {
+                    uint4 vd[US];
 #pragma unroll
-                    for (int j = 0; j < NT; j++) {
-                        if (j < nt) {
-                            const float4 h0 = hs[j * F4 + swz16(2 * c)], h1 = hs[j * F4 + swz16(2 * c + 1)];
-                            acc[j] = dot4(make_float4(wv[0], wv[1], wv[2], wv[3]), h0, acc[j]);
-                            acc[j] = dot4(make_float4(wv[4], wv[5], wv[6], wv[7]), h1, acc[j]);
+                    for (int t = 0; t < US; t++) vd[t] = __ldg(sd + min(c0 + 32 * t, F8 - 1));
+#pragma unroll
+                    for (int t = 0; t < US; t++) {
+                        const int c = c0 + 32 * t;
+                        if (c >= F8) break;
+                        float wv[8];
+                        bf16x8(vd[t], wv);
+#pragma unroll
+                        for (int j = 0; j < NT; j++) {
+                            if (j < nt) {
+                                const float4 h0 = hs[j * F4 + swz16(2 * c)], h1 = hs[j * F4 + swz16(2 * c + 1)];
+                                acc[j] = dot4(make_float4(wv[0], wv[1], wv[2], wv[3]), h0, acc[j]);
+                                acc[j] = dot4(make_float4(wv[4], wv[5], wv[6], wv[7]), h1, acc[j]);
+                            }
                         }
                     }
                 }
@@ -644,11 +759,17 @@ int sm_count() {
     return n;
 }
 
-// CTAs per SM that fit the shared memory of one CTA (228 KB per SM, 1 KB reserved per CTA).
-int ctas_per_sm(size_t smem) {
-    const size_t per = smem + 1024;
-    const int n = static_cast<int>((228 * 1024) / per);
-    return n < 1 ? 1 : (n > 4 ? 4 : n);
+// CTAs of a kernel resident on one SM at once (registers, shared memory, threads), so the
+// grid is one wave. Cached for the last shared-memory size asked.
+template <class Kernel>
+int resident_ctas(Kernel kernel, size_t smem, int &cached_smem, int &cached_n) {
+    if (cached_smem != static_cast<int>(smem)) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem) != cudaSuccess || n < 1) n = 1;
+        cached_n = n;
+        cached_smem = static_cast<int>(smem);
+    }
+    return cached_n;
 }
 
 template <int NT, bool Q4>
@@ -656,9 +777,11 @@ int launch_up_nt(const UpParams &p, cudaStream_t s) {
     static int seen[64];
     const size_t smem = 2048 + static_cast<size_t>(NT) * p.w.D * 2 +
                         (Q4 ? static_cast<size_t>(NT) * (p.w.D * 2 + p.w.D / 32 * 4 + 4) : 0);
+    static int cached_smem = -1, cached_n = 0;
     const int err = ensure_smem(reinterpret_cast<const void *>(gemv_up_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
-    gemv_up_kernel<NT, Q4><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
+    const int per_sm = resident_ctas(gemv_up_kernel<NT, Q4>, smem, cached_smem, cached_n);
+    gemv_up_kernel<NT, Q4><<<sm_count() * per_sm, kThreads, smem, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -667,9 +790,11 @@ int launch_down_nt(const DownParams &p, cudaStream_t s) {
     static int seen[64];
     const size_t smem = static_cast<size_t>(NT) * p.w.F * 4 +
                         (Q4 ? static_cast<size_t>(NT) * (p.w.F * 2 + p.w.F / 32 * 4 + 4) : 0);
+    static int cached_smem = -1, cached_n = 0;
     const int err = ensure_smem(reinterpret_cast<const void *>(gemv_down_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
-    gemv_down_kernel<NT, Q4><<<sm_count() * ctas_per_sm(smem), kThreads, smem, s>>>(p);
+    const int per_sm = resident_ctas(gemv_down_kernel<NT, Q4>, smem, cached_smem, cached_n);
+    gemv_down_kernel<NT, Q4><<<sm_count() * per_sm, kThreads, smem, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
