@@ -239,9 +239,13 @@ SMALL_STAGE_KERNEL = {"up_gemv": ("small_up_kernel", "small_groups.cu"),
 
 
 Q4_STAGE_KERNEL = {"up_gemv": ("gemv_up_kernel", "gemv.cu"), "down_gemv": ("gemv_down_kernel", "gemv.cu")}
+# one token: the streamed GEMV kernels (when their shared-memory ring fits the shape)
+Q4_T1_STAGE_KERNEL = {"up_gemv": ("gemv_up_stream_kernel", "gemv.cu"), "down_gemv": ("gemv_down_stream_kernel", "gemv.cu")}
 
 
 def stage_kernel(stage, wl):
+    if wl.fmt == "q4" and wl.T == 1 and stage in Q4_T1_STAGE_KERNEL:
+        return Q4_T1_STAGE_KERNEL[stage]
     if wl.fmt == "q4" and stage in Q4_STAGE_KERNEL:
         return Q4_STAGE_KERNEL[stage]
     if small_path(wl) and stage in SMALL_STAGE_KERNEL:

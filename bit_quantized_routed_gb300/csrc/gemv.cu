@@ -104,6 +104,7 @@ struct UpParams {
     const uint4 *xq;
     const int *x8;
     const float4 *xsc;
+    int *status;  // the handle's status word (bounded waits of the streamed kernel)
 };
 
 // Phase 1: h[pos][r] = silu(gate_r . x) * (up_r . x) for the group's tokens.
@@ -345,47 +346,53 @@ struct DownParams {
     const uint4 *hq;
     const int *hsum;
     const float *hsc;
+    int *status;  // the handle's status word (bounded waits of the streamed kernel)
 };
 
 // The 4-bit variant's down rows: each pair's fp32 h row as int16 pairs (h0,h2), (h4,h6), (h1,h3),
 // (h5,h7) per 8-column group with a power-of-two scale of its own, 2^(14-e) for the exponent e of
 // the row's largest |h|; the sum of each 32-column sub-block of them; the factor 2^(e-14) back.
-// One warp per row.
-__global__ void prep_h_kernel(const float *__restrict__ h, int rows, int F, uint4 *__restrict__ hq,
-                              int *__restrict__ hsum, float *__restrict__ hsc) {
-    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+// One CTA per row (256 threads, one 8-column group per thread and pass).
+__global__ void __launch_bounds__(256) prep_h_kernel(const float *__restrict__ h, int rows, int F,
+                                                     uint4 *__restrict__ hq, int *__restrict__ hsum,
+                                                     float *__restrict__ hsc) {
+    __shared__ float wmax[8];
+    const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (row >= rows) return;
     const float4 *hr = reinterpret_cast<const float4 *>(h + static_cast<size_t>(row) * F);
     float m = 0.0f;
-    for (int i = lane; i < F / 4; i += 32) {
+    for (int i = threadIdx.x; i < F / 4; i += 256) {
         const float4 v = hr[i];
         m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; i++) m = fmaxf(m, wmax[i]);
     int e = 0;
     frexpf(m, &e);
     e = m > 0.0f ? e : 0;
     const float sc = ldexpf(1.0f, 14 - e);
-    for (int c = lane; c < F / 32; c += 32) {
+    for (int gi = threadIdx.x; gi < F / 8; gi += 256) {  // F / 8 is a multiple of 32: whole warps
+        const float4 a = hr[2 * gi], b = hr[2 * gi + 1];
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t q[8];
         int sum = 0;
 #pragma unroll
-        for (int g = 0; g < 4; g++) {
-            const float4 a = hr[8 * c + 2 * g], b = hr[8 * c + 2 * g + 1];
-            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            uint32_t q[8];
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                q[i] = round_to_int_bits(v[i] * sc);
-                sum += static_cast<int>(static_cast<int16_t>(q[i] & 0xffffu));
-            }
-            hq[static_cast<size_t>(row) * (F / 8) + 4 * c + g] =
-                make_uint4(__byte_perm(q[0], q[2], 0x5410), __byte_perm(q[4], q[6], 0x5410),
-                           __byte_perm(q[1], q[3], 0x5410), __byte_perm(q[5], q[7], 0x5410));
+        for (int i = 0; i < 8; i++) {
+            q[i] = round_to_int_bits(v[i] * sc);
+            sum += static_cast<int>(static_cast<int16_t>(q[i] & 0xffffu));
         }
-        hsum[static_cast<size_t>(row) * (F / 32) + c] = sum;
+        hq[static_cast<size_t>(row) * (F / 8) + gi] =
+            make_uint4(__byte_perm(q[0], q[2], 0x5410), __byte_perm(q[4], q[6], 0x5410),
+                       __byte_perm(q[1], q[3], 0x5410), __byte_perm(q[5], q[7], 0x5410));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if ((gi & 3) == 0) hsum[static_cast<size_t>(row) * (F / 32) + (gi >> 2)] = sum;
     }
-    if (lane == 0) hsc[row] = ldexpf(1.0f, e - 14);
+    if (threadIdx.x == 0) hsc[row] = ldexpf(1.0f, e - 14);
 }
 
 // Phase 2: y[pos][r] = down_r . h[pos] for the group's tokens.
@@ -748,6 +755,359 @@ __global__ void dequant_kernel(DeviceWeights w, int expert, int matrix, const ui
     }
 }
 
+// ------------------------------------------------------------------ one token, 4-bit: streamed
+//
+// A single token reads every byte once and does little arithmetic per byte, so the kernels
+// above leave their warps waiting on loads. These two keep the loads off the compute warps: one
+// producer warp bulk-copies each item's packed rows (and, for down, the item's h) into a ring
+// of shared-memory stages, and three groups of eight compute warps decode and dot from shared
+// memory, the groups taking the items in turn. One CTA per SM; items are split over the CTAs by
+// bytes as above. Every wait is bounded; a warp that
+// gives up keeps its barrier arrivals without computing, so the CTA always finishes, and the
+// producer lets its copies land before the CTA exits.
+
+constexpr int kSWarps = 8;                               // compute warps per group
+constexpr int kSGroups = 3;                              // groups, taking items in turn
+constexpr int kSThreads = 32 * (kSGroups * kSWarps + 1);  // and one producer warp
+constexpr int kSStageMax = 65536;              // bytes of one ring stage at most
+constexpr int kSMaxStages = 6;
+constexpr int kSDownRows = 32;                 // routed down rows per item (four per warp)
+constexpr int kSDownSharedRows = 8;            // shared down rows per item (one per warp)
+
+struct StreamCfg {
+    int stage_bytes;  // one ring stage (multiple of 128)
+    int stages;       // ring depth
+    int sh_rows;      // shared gate/up rows per item (a power of two dividing kSWarps)
+    int ring_off;     // the x / table region follows the ring at this offset
+};
+
+// Phase 1 for one token: item = 8 rows of gate and of up of one routed expert (one row per
+// warp), or sh_rows bf16 rows of the shared gate and up (8 / sh_rows warps per row, each a
+// column range; the row's first warp adds the partial sums).
+__global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p, StreamCfg cfg) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int D = p.w.D, F = p.w.F, nbD = p.w.nbD, D8 = D / 8;
+    const int row_bytes = nbD * 144;
+    uint8_t *ring = smem;
+    uint4 *xs = reinterpret_cast<uint4 *>(smem + cfg.ring_off);  // bf16 x [D]
+    uint4 *xq_raw = xs + D8;                                     // int16 pairs as prepared [D/8]
+    uint4 *xqs = xq_raw + D8;                                    // the same, swizzled
+    int *x8s = reinterpret_cast<int *>(xqs + D8);                // [D/32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(x8s + D / 32);  // full[S], empty[S], xbar
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * cfg.stages + 1);
+    float *part = reinterpret_cast<float *>(bars + 2 * cfg.stages + 2);  // [kSGroups][2][kSWarps][2]
+    const int S = cfg.stages, SB = cfg.stage_bytes;
+    auto full = [&](int s) { return smem_u32(bars + s); };
+    auto empty = [&](int s) { return smem_u32(bars + S + s); };
+    const uint32_t xbar = smem_u32(bars + 2 * S);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int cg = wid / kSWarps, warp = wid - cg * kSWarps;  // compute group, warp within it
+
+    const int n_gemv = p.meta->n_gemv;
+    const int per_group = F / kSWarps;
+    const int routed = n_gemv * per_group;
+    const int n_shared = p.shared ? F / cfg.sh_rows : 0;
+    const long long cr = 2LL * kSWarps * 144, cs = 2LL * cfg.sh_rows * 512;  // bytes per 256 columns
+    int begin, end;
+    cta_range(routed, n_shared, cr, cs, begin, end);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kSWarps);
+        }
+        mbar_init(xbar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (cg == kSGroups) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint32_t xbytes = static_cast<uint32_t>(D * 2 + D * 2 + D / 32 * 4);
+            mbar_expect_tx(xbar, xbytes);
+            bulk_load(smem_u32(xs), p.x, D * 2, xbar);
+            bulk_load(smem_u32(xq_raw), p.xq, D * 2, xbar);
+            bulk_load(smem_u32(x8s), p.x8, D / 32 * 4, xbar);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued[kSMaxStages];
+            for (int s = 0; s < kSMaxStages; s++) issued[s] = -1;
+            bool ok = true;
+            for (int item = begin; item < end && ok; item++) {
+                if (!wait_phase(empty(stage), phase ^ 1u, abort_flag, p.status) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = smem_u32(ring + stage * SB);
+                if (item < routed) {
+                    const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSWarps;
+                    const uint32_t nb = static_cast<uint32_t>(kSWarps * row_bytes);
+                    mbar_expect_tx(full(stage), 2 * nb);
+                    bulk_load(dst, q4_row(p.w, 0, e, r0), nb, full(stage));
+                    bulk_load(dst + nb, q4_row(p.w, 1, e, r0), nb, full(stage));
+                } else {
+                    const int r0 = (item - routed) * cfg.sh_rows;
+                    const uint32_t nb = static_cast<uint32_t>(cfg.sh_rows * D * 2);
+                    mbar_expect_tx(full(stage), 2 * nb);
+                    bulk_load(dst, p.w.sh_gate + static_cast<size_t>(r0) * D, nb, full(stage));
+                    bulk_load(dst + nb, p.w.sh_up + static_cast<size_t>(r0) * D, nb, full(stage));
+                }
+                issued[stage] = static_cast<int>(phase);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            mbar_drain(xbar, 0);  // the token's copies always land before the CTA exits
+            if (!ok)
+                for (int s = 0; s < S; s++)
+                    if (issued[s] >= 0) mbar_drain(full(s), static_cast<uint32_t>(issued[s]));
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- compute warps
+    bool ok = wait_phase(xbar, 0, abort_flag, p.status);
+    if (ok)
+        for (int i = threadIdx.x; i < D8; i += kSGroups * kSWarps * 32) xqs[swz8(i)] = xq_raw[i];
+    bar_sync(kSGroups + 1, kSGroups * kSWarps * 32);
+    const float xf = p.xsc[0].x;  // the int16 token's factor back to x
+    const int nsub = nbD * 8;
+    const int wpr = kSWarps / cfg.sh_rows, cols8 = D8 / wpr;  // shared items: warps per row, chunks per warp
+    for (int item = begin + cg; item < end; item += kSGroups) {
+        const int stage = (item - begin) % S;  // the producer fills the items in order
+        const uint32_t phase = static_cast<uint32_t>((item - begin) / S) & 1u;
+        ok = ok && wait_phase(full(stage), phase, abort_flag, p.status);
+        const uint8_t *st = ring + stage * SB;
+        if (item < routed) {
+            if (ok) {
+                const int e = p.gemv_list[item / per_group];
+                const int r = (item % per_group) * kSWarps + warp;
+                const uint8_t *rg = st + warp * row_bytes, *ru = st + (kSWarps + warp) * row_bytes;
+                float ag[2] = {0.0f, 0.0f}, au[2] = {0.0f, 0.0f};
+                // two sub-blocks per lane at a time and one dp2a chain per 8-weight group (the
+                // integer sums are exact in any order): independent work for the scheduler
+                for (int c0 = lane; c0 < nsub; c0 += 64) {
+#pragma unroll
+                    for (int t = 0; t < 2; t++) {
+                        const int c = c0 + 32 * t;
+                        if (c >= nsub) break;
+                        const int b = c >> 3, sub = c & 7;
+                        const uint4 hg = *reinterpret_cast<const uint4 *>(rg + b * 144);
+                        const uint4 hu = *reinterpret_cast<const uint4 *>(ru + b * 144);
+                        const uint4 vg = *(reinterpret_cast<const uint4 *>(rg + b * 144 + 16) + sub);
+                        const uint4 vu = *(reinterpret_cast<const uint4 *>(ru + b * 144 + 16) + sub);
+                        float dsg, dmg, dsu, dmu;
+                        q4_sub_scale(hg, sub, dsg, dmg);
+                        q4_sub_scale(hu, sub, dsu, dmu);
+                        int sgp[4], sup[4];
+#pragma unroll
+                        for (int g = 0; g < 4; g++) {
+                            const uint32_t wgw = g == 0 ? vg.x : g == 1 ? vg.y : g == 2 ? vg.z : vg.w;
+                            const uint32_t wuw = g == 0 ? vu.x : g == 1 ? vu.y : g == 2 ? vu.z : vu.w;
+                            const uint4 xv = xqs[swz8(4 * c + g)];
+                            const uint32_t eg = wgw & 0x0F0F0F0Fu, og = (wgw >> 4) & 0x0F0F0F0Fu;
+                            const uint32_t eu = wuw & 0x0F0F0F0Fu, ou = (wuw >> 4) & 0x0F0F0F0Fu;
+                            sgp[g] = dp2a_hi_su(xv.w, og, dp2a_lo_su(xv.z, og, dp2a_hi_su(xv.y, eg, dp2a_lo_su(xv.x, eg, 0))));
+                            sup[g] = dp2a_hi_su(xv.w, ou, dp2a_lo_su(xv.z, ou, dp2a_hi_su(xv.y, eu, dp2a_lo_su(xv.x, eu, 0))));
+                        }
+                        const int sg = (sgp[0] + sgp[1]) + (sgp[2] + sgp[3]);
+                        const int su = (sup[0] + sup[1]) + (sup[2] + sup[3]);
+                        const float sx = static_cast<float>(x8s[c] >> 3);  // sum of the sub-block's 32 int16 x
+                        ag[t] = fmaf(dsg, static_cast<float>(sg), fmaf(-dmg, sx, ag[t]));
+                        au[t] = fmaf(dsu, static_cast<float>(su), fmaf(-dmu, sx, au[t]));
+                    }
+                }
+                const float g = warp_sum(ag[0] + ag[1]) * xf, u = warp_sum(au[0] + au[1]) * xf;
+                if (lane == 0) p.h[static_cast<size_t>(p.offsets[e]) * F + r] = swiglu(g, u);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(stage));
+        } else {
+            const int row = warp / wpr, q = warp - row * wpr;
+            float g = 0.0f, u = 0.0f;
+            if (ok) {
+                const uint4 *sg = reinterpret_cast<const uint4 *>(st + static_cast<size_t>(row) * D * 2) + q * cols8;
+                const uint4 *su = reinterpret_cast<const uint4 *>(st + static_cast<size_t>(cfg.sh_rows + row) * D * 2) + q * cols8;
+                const uint4 *xr = xs + q * cols8;
+                for (int c = lane; c < cols8; c += 32) {
+                    float wg[8], wu[8];
+                    bf16x8(sg[c], wg);
+                    bf16x8(su[c], wu);
+                    const uint4 xv = xr[c];
+                    dot8_bf16(wg, xv, g);
+                    dot8_bf16(wu, xv, u);
+                }
+                g = warp_sum(g);
+                u = warp_sum(u);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(stage));
+            // two buffers per group: one barrier per item suffices
+            float *pp = part + (cg * 2 + (((item - begin) / kSGroups) & 1)) * 2 * kSWarps;
+            if (lane == 0) {
+                pp[2 * warp] = g;
+                pp[2 * warp + 1] = u;
+            }
+            bar_sync(1 + cg, kSWarps * 32);
+            if (q == 0 && lane == 0 && ok) {
+                float G = 0.0f, U = 0.0f;
+                for (int i = 0; i < wpr; i++) {
+                    G += pp[2 * (warp + i)];
+                    U += pp[2 * (warp + i) + 1];
+                }
+                p.h[static_cast<size_t>(p.P) * F + (item - routed) * cfg.sh_rows + row] = swiglu(G, U);
+            }
+        }
+    }
+}
+
+// Phase 2 for one token: item = 32 rows of one routed expert's down (four per warp) with the
+// pair's int16 h, or 8 bf16 rows of the shared down (one per warp) with the fp32 shared h.
+__global__ void __launch_bounds__(kSThreads, 1) gemv_down_stream_kernel(DownParams p, StreamCfg cfg) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int D = p.w.D, F = p.w.F, nbF = p.w.nbF, F8 = F / 8;
+    const int row_bytes = nbF * 144;
+    const uint32_t wbytes = static_cast<uint32_t>(kSDownRows * row_bytes);  // a routed item's rows
+    const uint32_t sbytes = static_cast<uint32_t>(kSDownSharedRows * F * 2);  // a shared item's rows
+    uint8_t *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + cfg.ring_off);  // full[S], empty[S]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * cfg.stages);
+    const int S = cfg.stages, SB = cfg.stage_bytes;
+    auto full = [&](int s) { return smem_u32(bars + s); };
+    auto empty = [&](int s) { return smem_u32(bars + S + s); };
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int cg = wid / kSWarps, warp = wid - cg * kSWarps;  // compute group, warp within it
+
+    const int n_gemv = p.meta->n_gemv;
+    const int per_group = D / kSDownRows;
+    const int routed = n_gemv * per_group;
+    const int n_shared = p.shared ? D / kSDownSharedRows : 0;
+    const long long cr = static_cast<long long>(kSDownRows) * 144, cs = kSDownSharedRows * 512LL;
+    int begin, end;
+    cta_range(routed, n_shared, cr, cs, begin, end);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kSWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (cg == kSGroups) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued[kSMaxStages];
+            for (int s = 0; s < kSMaxStages; s++) issued[s] = -1;
+            bool ok = true;
+            for (int item = begin; item < end && ok; item++) {
+                if (!wait_phase(empty(stage), phase ^ 1u, abort_flag, p.status) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = smem_u32(ring + stage * SB);
+                if (item < routed) {  // rows, then the pair's int16 h and its sub-block sums
+                    const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSDownRows;
+                    const int off = p.offsets[e];
+                    mbar_expect_tx(full(stage), wbytes + F * 2 + F / 32 * 4);
+                    bulk_load(dst, q4_row(p.w, 2, e, r0), wbytes, full(stage));
+                    bulk_load(dst + wbytes, p.hq + static_cast<size_t>(off) * F8, F * 2, full(stage));
+                    bulk_load(dst + wbytes + F * 2, p.hsum + static_cast<size_t>(off) * (F / 32), F / 32 * 4, full(stage));
+                } else {  // rows, then the shared h (fp32)
+                    const int r0 = (item - routed) * kSDownSharedRows;
+                    mbar_expect_tx(full(stage), sbytes + F * 4);
+                    bulk_load(dst, p.w.sh_down + static_cast<size_t>(r0) * F, sbytes, full(stage));
+                    bulk_load(dst + sbytes, p.h + static_cast<size_t>(p.P) * F, F * 4, full(stage));
+                }
+                issued[stage] = static_cast<int>(phase);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                for (int s = 0; s < S; s++)
+                    if (issued[s] >= 0) mbar_drain(full(s), static_cast<uint32_t>(issued[s]));
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- compute warps
+    bool ok = true;
+    const int nsub = nbF * 8;
+    for (int item = begin + cg; item < end; item += kSGroups) {
+        const int stage = (item - begin) % S;  // the producer fills the items in order
+        const uint32_t phase = static_cast<uint32_t>((item - begin) / S) & 1u;
+        ok = ok && wait_phase(full(stage), phase, abort_flag, p.status);
+        const uint8_t *st = ring + stage * SB;
+        if (ok && item < routed) {
+            const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSDownRows;
+            const int off = p.offsets[e];
+            const uint4 *hq = reinterpret_cast<const uint4 *>(st + wbytes);
+            const int *hsum = reinterpret_cast<const int *>(st + wbytes + F * 2);
+            const float hf = p.hsc[off];
+#pragma unroll 1
+            for (int rr = 0; rr < kSDownRows / kSWarps; rr++) {
+                const int rl = warp + rr * kSWarps;  // row within the item
+                const uint8_t *rd = st + rl * row_bytes;
+                float accs[2] = {0.0f, 0.0f};
+                for (int c0 = lane; c0 < nsub; c0 += 64) {  // two sub-blocks per lane at a time
+#pragma unroll
+                    for (int t = 0; t < 2; t++) {
+                    const int c = c0 + 32 * t;
+                    if (c >= nsub) break;
+                    const int b = c >> 3, sub = c & 7;
+                    const uint4 hd = *reinterpret_cast<const uint4 *>(rd + b * 144);
+                    const uint4 vd = *(reinterpret_cast<const uint4 *>(rd + b * 144 + 16) + sub);
+                    float ds, dm;
+                    q4_sub_scale(hd, sub, ds, dm);
+                    // the four 8-weight groups in an order rotated by (c >> 1) & 3, so the lanes of a
+                    // quarter warp read eight different bank groups of h (the integer sum is exact)
+                    const int rot = (c >> 1) & 3;
+                    uint4 w4 = vd;
+                    if (rot & 1) w4 = make_uint4(w4.y, w4.z, w4.w, w4.x);
+                    if (rot & 2) w4 = make_uint4(w4.z, w4.w, w4.x, w4.y);
+                    int sdp[4];  // one dp2a chain per 8-weight group (exact integer sums)
+#pragma unroll
+                    for (int g = 0; g < 4; g++) {
+                        const uint32_t wd = g == 0 ? w4.x : g == 1 ? w4.y : g == 2 ? w4.z : w4.w;
+                        const uint32_t ev = wd & 0x0F0F0F0Fu, ov = (wd >> 4) & 0x0F0F0F0Fu;
+                        const uint4 hv = hq[4 * c + ((g + rot) & 3)];
+                        sdp[g] = dp2a_hi_su(hv.w, ov, dp2a_lo_su(hv.z, ov, dp2a_hi_su(hv.y, ev, dp2a_lo_su(hv.x, ev, 0))));
+                    }
+                    const int sd = (sdp[0] + sdp[1]) + (sdp[2] + sdp[3]);
+                    accs[t] = fmaf(ds, static_cast<float>(sd), fmaf(-dm, static_cast<float>(hsum[c]), accs[t]));
+                    }
+                }
+                const float v = warp_sum(accs[0] + accs[1]) * hf;
+                if (lane == 0) p.y[static_cast<size_t>(off) * D + r0 + rl] = v;
+            }
+        } else if (ok) {
+            const int r = (item - routed) * kSDownSharedRows + warp;
+            const uint4 *sd = reinterpret_cast<const uint4 *>(st + static_cast<size_t>(warp) * F * 2);
+            const float4 *hs = reinterpret_cast<const float4 *>(st + sbytes);
+            float acc = 0.0f;
+            for (int c = lane; c < F8; c += 32) {
+                float wv[8];
+                bf16x8(sd[c], wv);
+                acc = dot4(make_float4(wv[0], wv[1], wv[2], wv[3]), hs[2 * c], acc);
+                acc = dot4(make_float4(wv[4], wv[5], wv[6], wv[7]), hs[2 * c + 1], acc);
+            }
+            const float v = warp_sum(acc);
+            if (lane == 0) p.y[static_cast<size_t>(p.P) * D + r] = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(stage));
+    }
+}
+
 int sm_count() {
     static int n = 0;
     if (!n) {
@@ -798,6 +1158,68 @@ int launch_down_nt(const DownParams &p, cudaStream_t s) {
     return static_cast<int>(cudaGetLastError());
 }
 
+// Ring plans of the streamed kernels; stages == 0 when they do not fit one CTA's shared memory.
+constexpr size_t kSmemLimit = 227 * 1024;
+
+StreamCfg plan_up_stream(const DeviceWeights &w, size_t &smem) {
+    StreamCfg c{0, 0, 0, 0};
+    const size_t D = static_cast<size_t>(w.D);
+    // stages as small as a routed item, so that more of them are in flight: shared items of as
+    // many rows as fit one (at least one)
+    const size_t routed = 2ull * kSWarps * w.nbD * 144;
+    int sh = kSWarps;
+    while (sh > 1 && 2 * sh * D * 2 > routed) sh >>= 1;
+    const size_t shared = 2ull * sh * D * 2;
+    const size_t stage = ((routed > shared ? routed : shared) + 127) / 128 * 128;
+    if (stage > static_cast<size_t>(kSStageMax) || 2 * sh * D * 2 > static_cast<size_t>(kSStageMax)) return c;
+    // x as bf16, as int16 pairs twice (as prepared, swizzled), the sub-block sums, barriers, partial sums
+    const size_t fixed = 6 * D + D / 8 + (2 * kSMaxStages + 2) * 8 + kSGroups * 2 * kSWarps * 2 * 4;
+    int S = kSMaxStages;
+    while (S >= 2 && S * stage + fixed > kSmemLimit) S--;
+    if (S < 2) return c;
+    c.stage_bytes = static_cast<int>(stage);
+    c.stages = S;
+    c.sh_rows = sh;
+    c.ring_off = static_cast<int>(S * stage);
+    smem = S * stage + fixed;
+    return c;
+}
+
+StreamCfg plan_down_stream(const DeviceWeights &w, size_t &smem) {
+    StreamCfg c{0, 0, 0, 0};
+    const size_t F = static_cast<size_t>(w.F);
+    const size_t routed = static_cast<size_t>(kSDownRows) * w.nbF * 144 + F * 2 + F / 32 * 4;
+    const size_t shared = static_cast<size_t>(kSDownSharedRows) * F * 2 + F * 4;
+    const size_t stage = ((routed > shared ? routed : shared) + 127) / 128 * 128;
+    if (stage > static_cast<size_t>(kSStageMax) || F % 128 != 0) return c;
+    const size_t fixed = (2 * kSMaxStages + 1) * 8 + 8;
+    int S = kSMaxStages;
+    while (S >= 2 && S * stage + fixed > kSmemLimit) S--;
+    if (S < 2) return c;
+    c.stage_bytes = static_cast<int>(stage);
+    c.stages = S;
+    c.sh_rows = kSDownSharedRows;
+    c.ring_off = static_cast<int>(S * stage);
+    smem = S * stage + fixed;
+    return c;
+}
+
+int launch_up_stream(const UpParams &p, const StreamCfg &c, size_t smem, cudaStream_t s) {
+    static int seen[64];
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_up_stream_kernel), static_cast<int>(smem), seen);
+    if (err) return err;
+    gemv_up_stream_kernel<<<sm_count(), kSThreads, smem, s>>>(p, c);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_down_stream(const DownParams &p, const StreamCfg &c, size_t smem, cudaStream_t s) {
+    static int seen[64];
+    const int err = ensure_smem(reinterpret_cast<const void *>(gemv_down_stream_kernel), static_cast<int>(smem), seen);
+    if (err) return err;
+    gemv_down_stream_kernel<<<sm_count(), kSThreads, smem, s>>>(p, c);
+    return static_cast<int>(cudaGetLastError());
+}
+
 }  // namespace
 
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, bool shared_on_gemv,
@@ -818,14 +1240,22 @@ int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *
     p.xq = reinterpret_cast<const uint4 *>(ws.xq);
     p.x8 = ws.x8;
     p.xsc = reinterpret_cast<const float4 *>(ws.xsc);
+    p.status = ws.status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (w.fmt == 1 && T == 1) {  // streamed when its ring fits and every copy source is 16-byte aligned
+        size_t smem = 0;
+        const StreamCfg c = plan_up_stream(w, smem);
+        const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(ws.xq) |
+                               reinterpret_cast<uintptr_t>(ws.x8)) & 15u) == 0;
+        if (c.stages > 0 && aligned) return launch_up_stream(p, c, smem, s);
+    }
     if (w.fmt == 1) return T == 1 ? launch_up_nt<1, true>(p, s) : launch_up_nt<8, true>(p, s);
     return T == 1 ? launch_up_nt<1, false>(p, s) : launch_up_nt<8, false>(p, s);
 }
 
 int launch_prep_h(const Workspace &ws, int rows, int F, void *stream) {
     if (rows <= 0) return 0;
-    prep_h_kernel<<<(rows + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    prep_h_kernel<<<rows, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         ws.h32, rows, F, reinterpret_cast<uint4 *>(ws.hq4), ws.hsum4, ws.hsc4);
     return static_cast<int>(cudaGetLastError());
 }
@@ -845,7 +1275,15 @@ int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, 
     p.hq = int16_h ? reinterpret_cast<const uint4 *>(ws.hq4) : nullptr;
     p.hsum = ws.hsum4;
     p.hsc = ws.hsc4;
+    p.status = ws.status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (w.fmt == 1 && T == 1 && int16_h) {  // streamed when its ring fits and every copy source is 16-byte aligned
+        size_t smem = 0;
+        const StreamCfg c = plan_down_stream(w, smem);
+        const bool aligned = ((reinterpret_cast<uintptr_t>(ws.hq4) | reinterpret_cast<uintptr_t>(ws.hsum4) |
+                               reinterpret_cast<uintptr_t>(ws.h32)) & 15u) == 0;
+        if (c.stages > 0 && aligned) return launch_down_stream(p, c, smem, s);
+    }
     if (w.fmt == 1) return T == 1 ? launch_down_nt<1, true>(p, s) : launch_down_nt<8, true>(p, s);
     return T == 1 ? launch_down_nt<1, false>(p, s) : launch_down_nt<8, false>(p, s);
 }

@@ -43,17 +43,20 @@ constexpr int kMaxF = 2048;
 
 // ---------------------------------------------------------------- x quantisation
 
-// One warp per token: xq[t][g] = the int16 pairs (x0,x2), (x4,x6), (x1,x3), (x5,x7) of columns
-// 8g..8g+7 scaled by 2^(14-e) (e: exponent of the token's largest |x|), x8[t][c] = 8 x the sum of
-// the 32 int16 values of sub-block c, xsc[t][0] = 2^(e-14).
-__global__ void prep_x_kernel(const uint16_t *__restrict__ x, int T, int D, uint4 *__restrict__ xq,
-                              int *__restrict__ x8, float4 *__restrict__ xsc) {
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+// One CTA per token (256 threads, one 8-column group per thread and pass): xq[t][g] = the int16
+// pairs (x0,x2), (x4,x6), (x1,x3), (x5,x7) of columns 8g..8g+7 scaled by 2^(14-e) (e: exponent of
+// the token's largest |x|), x8[t][c] = 8 x the sum of the 32 int16 values of sub-block c (four
+// neighbouring threads), xsc[t][0] = 2^(e-14).
+__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int T, int D,
+                                                     uint4 *__restrict__ xq, int *__restrict__ x8,
+                                                     float4 *__restrict__ xsc) {
+    __shared__ float wmax[8];
+    const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (t >= T) return;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * D);
-    const int G = D / 8;
+    const int G = D / 8;  // a multiple of 32: whole warps take part in the shuffles below
     float m = 0.0f;
-    for (int g = lane; g < G; g += 32) {
+    for (int g = threadIdx.x; g < G; g += 256) {
         const uint4 v = __ldg(xr + g);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -61,31 +64,34 @@ __global__ void prep_x_kernel(const uint16_t *__restrict__ x, int T, int D, uint
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; i++) m = fmaxf(m, wmax[i]);
     int e = 0;
     frexpf(m, &e);
     e = m > 0.0f ? e : 0;
     const float sc = ldexpf(1.0f, 14 - e);
     uint4 *qo = xq + static_cast<size_t>(t) * G;
-    for (int c = lane; c < D / 32; c += 32) {
+    for (int g = threadIdx.x; g < G; g += 256) {
+        const uint4 v = __ldg(xr + g);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            q[2 * i] = round_to_int_bits(bf16_lo(u[i]) * sc);
+            q[2 * i + 1] = round_to_int_bits(bf16_hi(u[i]) * sc);
+        }
         int s = 0;
 #pragma unroll
-        for (int g4 = 0; g4 < 4; g4++) {
-            const uint4 v = __ldg(xr + 4 * c + g4);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-            uint32_t q[8];
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                q[2 * i] = round_to_int_bits(bf16_lo(u[i]) * sc);
-                q[2 * i + 1] = round_to_int_bits(bf16_hi(u[i]) * sc);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; i++) s += static_cast<int>(static_cast<int16_t>(q[i] & 0xffffu));
-            qo[4 * c + g4] = make_uint4(__byte_perm(q[0], q[2], 0x5410), __byte_perm(q[4], q[6], 0x5410),
-                                        __byte_perm(q[1], q[3], 0x5410), __byte_perm(q[5], q[7], 0x5410));
-        }
-        x8[static_cast<size_t>(t) * (D / 32) + c] = 8 * s;
+        for (int i = 0; i < 8; i++) s += static_cast<int>(static_cast<int16_t>(q[i] & 0xffffu));
+        qo[g] = make_uint4(__byte_perm(q[0], q[2], 0x5410), __byte_perm(q[4], q[6], 0x5410),
+                           __byte_perm(q[1], q[3], 0x5410), __byte_perm(q[5], q[7], 0x5410));
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if ((g & 3) == 0) x8[static_cast<size_t>(t) * (D / 32) + (g >> 2)] = 8 * s;
     }
-    if (lane == 0) xsc[t] = make_float4(ldexpf(1.0f, e - 14), 0.0f, 0.0f, 0.0f);
+    if (threadIdx.x == 0) xsc[t] = make_float4(ldexpf(1.0f, e - 14), 0.0f, 0.0f, 0.0f);
 }
 
 // ---------------------------------------------------------------- gate/up + SwiGLU
@@ -747,7 +753,7 @@ bool small_groups_supported(const DeviceWeights &w) {
 
 int launch_prep_x(const Workspace &ws, const uint16_t *x, int T, int D, void *stream) {
     if (T <= 0) return 0;
-    prep_x_kernel<<<(T + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    prep_x_kernel<<<T, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         x, T, D, reinterpret_cast<uint4 *>(ws.xq), ws.x8, reinterpret_cast<float4 *>(ws.xsc));
     return static_cast<int>(cudaGetLastError());
 }

@@ -44,6 +44,8 @@ def test_q4_device_dequant_bitexact(ds4):
 @pytest.mark.parametrize("T,D,F,E,k,shared,mode,quantized", [
     (1, 1024, 512, 16, 4, True, 0, False),
     (1, 4096, 2048, 32, 8, True, 0, True),     # the decode shape, host-quantised N(0, 0.02) experts
+    (1, 7168, 512, 16, 4, True, 1, False),     # d_model 7168: two ring stages, four warps per shared row
+    (1, 256, 256, 8, 2, False, 0, False),      # the smallest shape, no shared expert
     (5, 512, 768, 16, 4, True, 1, False),
     (40, 512, 512, 24, 4, False, 0, False),
     (100, 512, 512, 24, 4, True, 0, False),    # shared expert on the tensor cores, routed on the GEMV
