@@ -760,14 +760,16 @@ __global__ void dequant_kernel(DeviceWeights w, int expert, int matrix, const ui
 // A single token reads every byte once and does little arithmetic per byte, so the kernels
 // above leave their warps waiting on loads. These two keep the loads off the compute warps: one
 // producer warp bulk-copies each item's packed rows (and, for down, the item's h) into a ring
-// of shared-memory stages, and three groups of eight compute warps decode and dot from shared
-// memory, the groups taking the items in turn. One CTA per SM; items are split over the CTAs by
-// bytes as above. Every wait is bounded; a warp that
+// of shared-memory stages, and two groups of eight compute warps decode and dot from shared
+// memory, the groups taking the items in turn. Each group has stages of its own (stage
+// g + G*i, i < S/G, for group g of G) and is their only consumer, so it never waits for a phase
+// more than one ahead of the last it consumed (a parity wait cannot tell those apart). One CTA
+// per SM; items are split over the CTAs by bytes as above. Every wait is bounded; a warp that
 // gives up keeps its barrier arrivals without computing, so the CTA always finishes, and the
-// producer lets its copies land before the CTA exits.
+// producer lets all its copies land before it exits.
 
 constexpr int kSWarps = 8;                               // compute warps per group
-constexpr int kSGroups = 3;                              // groups, taking items in turn
+constexpr int kSGroups = 2;                              // groups, taking items in turn
 constexpr int kSThreads = 32 * (kSGroups * kSWarps + 1);  // and one producer warp
 constexpr int kSStageMax = 65536;              // bytes of one ring stage at most
 constexpr int kSMaxStages = 6;
@@ -830,16 +832,14 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p
             bulk_load(smem_u32(xs), p.x, D * 2, xbar);
             bulk_load(smem_u32(xq_raw), p.xq, D * 2, xbar);
             bulk_load(smem_u32(x8s), p.x8, D / 32 * 4, xbar);
-            int stage = 0;
-            uint32_t phase = 0;
+            const int SG = S / kSGroups;  // stages per group
             int issued[kSMaxStages];
             for (int s = 0; s < kSMaxStages; s++) issued[s] = -1;
-            bool ok = true;
-            for (int item = begin; item < end && ok; item++) {
-                if (!wait_phase(empty(stage), phase ^ 1u, abort_flag, p.status) || *abort_flag) {
-                    ok = false;
-                    break;
-                }
+            for (int item = begin; item < end; item++) {
+                const int j = item - begin, q = j / kSGroups;
+                const int stage = j - q * kSGroups + kSGroups * (q % SG);  // group j % G, its q-th item
+                const uint32_t phase = static_cast<uint32_t>(q / SG) & 1u;  // the stage's fill parity
+                if (!wait_phase(empty(stage), phase ^ 1u, abort_flag, p.status) || *abort_flag) break;
                 const uint32_t dst = smem_u32(ring + stage * SB);
                 if (item < routed) {
                     const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSWarps;
@@ -855,15 +855,11 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p
                     bulk_load(dst + nb, p.w.sh_up + static_cast<size_t>(r0) * D, nb, full(stage));
                 }
                 issued[stage] = static_cast<int>(phase);
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
-            mbar_drain(xbar, 0);  // the token's copies always land before the CTA exits
-            if (!ok)
-                for (int s = 0; s < S; s++)
-                    if (issued[s] >= 0) mbar_drain(full(s), static_cast<uint32_t>(issued[s]));
+            // every copy lands before the CTA can exit, whatever the compute warps did
+            mbar_drain(xbar, 0);
+            for (int s = 0; s < S; s++)
+                if (issued[s] >= 0) mbar_drain(full(s), static_cast<uint32_t>(issued[s]));
         }
         return;
     }
@@ -877,8 +873,9 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p
     const int nsub = nbD * 8;
     const int wpr = kSWarps / cfg.sh_rows, cols8 = D8 / wpr;  // shared items: warps per row, chunks per warp
     for (int item = begin + cg; item < end; item += kSGroups) {
-        const int stage = (item - begin) % S;  // the producer fills the items in order
-        const uint32_t phase = static_cast<uint32_t>((item - begin) / S) & 1u;
+        const int q = (item - begin) / kSGroups;  // this group's q-th item
+        const int stage = cg + kSGroups * (q % (S / kSGroups));
+        const uint32_t phase = static_cast<uint32_t>(q / (S / kSGroups)) & 1u;
         ok = ok && wait_phase(full(stage), phase, abort_flag, p.status);
         const uint8_t *st = ring + stage * SB;
         if (item < routed) {
@@ -1002,16 +999,14 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_down_stream_kernel(DownPara
     if (cg == kSGroups) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            const int SG = S / kSGroups;  // stages per group
             int issued[kSMaxStages];
             for (int s = 0; s < kSMaxStages; s++) issued[s] = -1;
-            bool ok = true;
-            for (int item = begin; item < end && ok; item++) {
-                if (!wait_phase(empty(stage), phase ^ 1u, abort_flag, p.status) || *abort_flag) {
-                    ok = false;
-                    break;
-                }
+            for (int item = begin; item < end; item++) {
+                const int j = item - begin, q = j / kSGroups;
+                const int stage = j - q * kSGroups + kSGroups * (q % SG);  // group j % G, its q-th item
+                const uint32_t phase = static_cast<uint32_t>(q / SG) & 1u;  // the stage's fill parity
+                if (!wait_phase(empty(stage), phase ^ 1u, abort_flag, p.status) || *abort_flag) break;
                 const uint32_t dst = smem_u32(ring + stage * SB);
                 if (item < routed) {  // rows, then the pair's int16 h and its sub-block sums
                     const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSDownRows;
@@ -1027,14 +1022,10 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_down_stream_kernel(DownPara
                     bulk_load(dst + sbytes, p.h + static_cast<size_t>(p.P) * F, F * 4, full(stage));
                 }
                 issued[stage] = static_cast<int>(phase);
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
-            if (!ok)
-                for (int s = 0; s < S; s++)
-                    if (issued[s] >= 0) mbar_drain(full(s), static_cast<uint32_t>(issued[s]));
+            // every copy lands before the CTA can exit, whatever the compute warps did
+            for (int s = 0; s < S; s++)
+                if (issued[s] >= 0) mbar_drain(full(s), static_cast<uint32_t>(issued[s]));
         }
         return;
     }
@@ -1043,8 +1034,9 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_down_stream_kernel(DownPara
     bool ok = true;
     const int nsub = nbF * 8;
     for (int item = begin + cg; item < end; item += kSGroups) {
-        const int stage = (item - begin) % S;  // the producer fills the items in order
-        const uint32_t phase = static_cast<uint32_t>((item - begin) / S) & 1u;
+        const int q = (item - begin) / kSGroups;  // this group's q-th item
+        const int stage = cg + kSGroups * (q % (S / kSGroups));
+        const uint32_t phase = static_cast<uint32_t>(q / (S / kSGroups)) & 1u;
         ok = ok && wait_phase(full(stage), phase, abort_flag, p.status);
         const uint8_t *st = ring + stage * SB;
         if (ok && item < routed) {
@@ -1174,9 +1166,9 @@ StreamCfg plan_up_stream(const DeviceWeights &w, size_t &smem) {
     if (stage > static_cast<size_t>(kSStageMax) || 2 * sh * D * 2 > static_cast<size_t>(kSStageMax)) return c;
     // x as bf16, as int16 pairs twice (as prepared, swizzled), the sub-block sums, barriers, partial sums
     const size_t fixed = 6 * D + D / 8 + (2 * kSMaxStages + 2) * 8 + kSGroups * 2 * kSWarps * 2 * 4;
-    int S = kSMaxStages;
-    while (S >= 2 && S * stage + fixed > kSmemLimit) S--;
-    if (S < 2) return c;
+    int S = kSMaxStages / kSGroups * kSGroups;  // a multiple of the groups: each has S / G stages
+    while (S >= kSGroups && S * stage + fixed > kSmemLimit) S -= kSGroups;
+    if (S < kSGroups) return c;
     c.stage_bytes = static_cast<int>(stage);
     c.stages = S;
     c.sh_rows = sh;
@@ -1193,9 +1185,9 @@ StreamCfg plan_down_stream(const DeviceWeights &w, size_t &smem) {
     const size_t stage = ((routed > shared ? routed : shared) + 127) / 128 * 128;
     if (stage > static_cast<size_t>(kSStageMax) || F % 128 != 0) return c;
     const size_t fixed = (2 * kSMaxStages + 1) * 8 + 8;
-    int S = kSMaxStages;
-    while (S >= 2 && S * stage + fixed > kSmemLimit) S--;
-    if (S < 2) return c;
+    int S = kSMaxStages / kSGroups * kSGroups;  // a multiple of the groups: each has S / G stages
+    while (S >= kSGroups && S * stage + fixed > kSmemLimit) S -= kSGroups;
+    if (S < kSGroups) return c;
     c.stage_bytes = static_cast<int>(stage);
     c.stages = S;
     c.sh_rows = kSDownSharedRows;
