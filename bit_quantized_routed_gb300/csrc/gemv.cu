@@ -798,6 +798,8 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p
     uint64_t *bars = reinterpret_cast<uint64_t *>(x8s + D / 32);  // full[S], empty[S], xbar
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * cfg.stages + 1);
     float *part = reinterpret_cast<float *>(bars + 2 * cfg.stages + 2);  // [kSGroups][2][kSWarps][2]
+    // per stage: the h row of the item's pair, written by the producer before it arms the stage
+    int *info = reinterpret_cast<int *>(part + kSGroups * 2 * kSWarps * 2);
     const int S = cfg.stages, SB = cfg.stage_bytes;
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto empty = [&](int s) { return smem_u32(bars + S + s); };
@@ -844,6 +846,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p
                 if (item < routed) {
                     const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSWarps;
                     const uint32_t nb = static_cast<uint32_t>(kSWarps * row_bytes);
+                    info[4 * stage] = p.offsets[e];  // visible to the group through the stage's barrier
                     mbar_expect_tx(full(stage), 2 * nb);
                     bulk_load(dst, q4_row(p.w, 0, e, r0), nb, full(stage));
                     bulk_load(dst + nb, q4_row(p.w, 1, e, r0), nb, full(stage));
@@ -880,7 +883,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p
         const uint8_t *st = ring + stage * SB;
         if (item < routed) {
             if (ok) {
-                const int e = p.gemv_list[item / per_group];
+                const int off = info[4 * stage];  // the pair's h row (set by the producer)
                 const int r = (item % per_group) * kSWarps + warp;
                 const uint8_t *rg = st + warp * row_bytes, *ru = st + (kSWarps + warp) * row_bytes;
                 float ag[2] = {0.0f, 0.0f}, au[2] = {0.0f, 0.0f};
@@ -918,7 +921,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_up_stream_kernel(UpParams p
                     }
                 }
                 const float g = warp_sum(ag[0] + ag[1]) * xf, u = warp_sum(au[0] + au[1]) * xf;
-                if (lane == 0) p.h[static_cast<size_t>(p.offsets[e]) * F + r] = swiglu(g, u);
+                if (lane == 0) p.h[static_cast<size_t>(off) * F + r] = swiglu(g, u);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(stage));
@@ -972,6 +975,8 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_down_stream_kernel(DownPara
     uint8_t *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + cfg.ring_off);  // full[S], empty[S]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * cfg.stages);
+    // per stage: the pair's y row and h factor, written by the producer before it arms the stage
+    int *info = reinterpret_cast<int *>(bars + 2 * cfg.stages + 1);
     const int S = cfg.stages, SB = cfg.stage_bytes;
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto empty = [&](int s) { return smem_u32(bars + S + s); };
@@ -1011,6 +1016,8 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_down_stream_kernel(DownPara
                 if (item < routed) {  // rows, then the pair's int16 h and its sub-block sums
                     const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSDownRows;
                     const int off = p.offsets[e];
+                    info[4 * stage] = off;  // visible to the group through the stage's barrier
+                    info[4 * stage + 1] = __float_as_int(p.hsc[off]);
                     mbar_expect_tx(full(stage), wbytes + F * 2 + F / 32 * 4);
                     bulk_load(dst, q4_row(p.w, 2, e, r0), wbytes, full(stage));
                     bulk_load(dst + wbytes, p.hq + static_cast<size_t>(off) * F8, F * 2, full(stage));
@@ -1040,11 +1047,11 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_down_stream_kernel(DownPara
         ok = ok && wait_phase(full(stage), phase, abort_flag, p.status);
         const uint8_t *st = ring + stage * SB;
         if (ok && item < routed) {
-            const int e = p.gemv_list[item / per_group], r0 = (item % per_group) * kSDownRows;
-            const int off = p.offsets[e];
+            const int r0 = (item % per_group) * kSDownRows;
+            const int off = info[4 * stage];  // the pair's y row and h factor (set by the producer)
+            const float hf = __int_as_float(info[4 * stage + 1]);
             const uint4 *hq = reinterpret_cast<const uint4 *>(st + wbytes);
             const int *hsum = reinterpret_cast<const int *>(st + wbytes + F * 2);
-            const float hf = p.hsc[off];
 #pragma unroll 1
             for (int rr = 0; rr < kSDownRows / kSWarps; rr++) {
                 const int rl = warp + rr * kSWarps;  // row within the item
@@ -1165,7 +1172,7 @@ StreamCfg plan_up_stream(const DeviceWeights &w, size_t &smem) {
     const size_t stage = ((routed > shared ? routed : shared) + 127) / 128 * 128;
     if (stage > static_cast<size_t>(kSStageMax) || 2 * sh * D * 2 > static_cast<size_t>(kSStageMax)) return c;
     // x as bf16, as int16 pairs twice (as prepared, swizzled), the sub-block sums, barriers, partial sums
-    const size_t fixed = 6 * D + D / 8 + (2 * kSMaxStages + 2) * 8 + kSGroups * 2 * kSWarps * 2 * 4;
+    const size_t fixed = 6 * D + D / 8 + (2 * kSMaxStages + 2) * 8 + kSGroups * 2 * kSWarps * 2 * 4 + kSMaxStages * 16;
     int S = kSMaxStages / kSGroups * kSGroups;  // a multiple of the groups: each has S / G stages
     while (S >= kSGroups && S * stage + fixed > kSmemLimit) S -= kSGroups;
     if (S < kSGroups) return c;
@@ -1184,7 +1191,7 @@ StreamCfg plan_down_stream(const DeviceWeights &w, size_t &smem) {
     const size_t shared = static_cast<size_t>(kSDownSharedRows) * F * 2 + F * 4;
     const size_t stage = ((routed > shared ? routed : shared) + 127) / 128 * 128;
     if (stage > static_cast<size_t>(kSStageMax) || F % 128 != 0) return c;
-    const size_t fixed = (2 * kSMaxStages + 1) * 8 + 8;
+    const size_t fixed = (2 * kSMaxStages + 1) * 8 + 8 + kSMaxStages * 16;
     int S = kSMaxStages / kSGroups * kSGroups;  // a multiple of the groups: each has S / G stages
     while (S >= kSGroups && S * stage + fixed > kSmemLimit) S -= kSGroups;
     if (S < kSGroups) return c;
