@@ -128,6 +128,30 @@ def test_ffn_matches_naive_loops():
         assert np.max(np.abs(np.array(ref) - delta[t])) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
 
 
+def test_ffn_q4_matches_naive_loops():
+    # the 4-bit variant's branch: Q4_K-style gate, up and down, on a non-square layer (d_ff != d_model)
+    # so that a transposed or swapped matrix cannot pass
+    T, D, F, E, k, seed = 2, 256, 512, 4, 2, 3
+    wl = synth.Workload("t4", T=T, D=D, F=F, E=E, k=k, seed=seed, shared=True)
+    L, x = synth.draw_inputs(wl)
+    gate = [oracle.quantize_q4k(synth.expert_weight(seed, e, synth.GATE, F, D)) for e in range(E)]
+    up = [oracle.quantize_q4k(synth.expert_weight(seed, e, synth.UP, F, D)) for e in range(E)]
+    down = [oracle.quantize_q4k(synth.expert_weight(seed, e, synth.DOWN, D, F)) for e in range(E)]
+    sh = synth.shared_weights(seed, D, F)
+    delta, idx, g = oracle.moe_ffn(x, L, k, gate, up, down, D, F, shared=sh, fmt="q4")
+    xf = oracle.bf16_to_f64(x)
+    sg, su, sd = (oracle.bf16_to_f64(s).reshape(-1, D if i < 2 else F).tolist() for i, s in enumerate(sh))
+    for t in range(T):
+        xv = xf[t].tolist()
+        ref = _naive_expert(xv, sg, su, sd)
+        for s_ in range(k):
+            e = int(idx[t, s_])
+            y = _naive_expert(xv, oracle.dequant_q4k(gate[e], F, D).tolist(), oracle.dequant_q4k(up[e], F, D).tolist(),
+                              oracle.dequant_q4k(down[e], D, F).tolist())
+            ref = [a + g[t, s_] * b for a, b in zip(ref, y)]
+        assert np.max(np.abs(np.array(ref) - delta[t])) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
 def test_ffn_zero_input_gives_zero():
     wl, L, x, gate, up, down, sh = _tiny_layer()
     delta, _, _ = oracle.moe_ffn(np.zeros_like(x), L, wl.k, gate, up, down, wl.D, wl.F, shared=sh)
