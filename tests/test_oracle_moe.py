@@ -111,7 +111,8 @@ def _naive_expert(xv, wg, wu, wd):
 
 
 def test_ffn_matches_naive_loops():
-    wl, L, x, gate, up, down, sh = _tiny_layer(T=2, k=2)
+    # non-square (d_ff != d_model), so that a transposed or swapped matrix cannot pass
+    wl, L, x, gate, up, down, sh = _tiny_layer(T=2, k=2, F=512)
     delta, idx, g = oracle.moe_ffn(x, L, wl.k, gate, up, down, wl.D, wl.F, shared=sh)
     xf = oracle.bf16_to_f64(x)
     sg, su, sd = (oracle.bf16_to_f64(s).reshape(-1, wl.D if i < 2 else wl.F).tolist() for i, s in enumerate(sh))
