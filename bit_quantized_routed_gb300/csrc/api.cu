@@ -614,7 +614,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         if (!rc) rc = launch_gemm_down(w, ws, h->tmap_h16, T, k, shared_tc, stream);
     }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_COMBINE);
-    if (!rc) rc = launch_combine(w, ws, T, k, out, stream);
+    if (!rc) rc = launch_combine(w, ws, T, k, gemm_min, shared_tc, out, stream);
     if (!rc) rc = clk.finish();
     h->calls++;
     return cuda_status(rc);

@@ -1,6 +1,8 @@
 // Gate-weighted combine into the residual:
 //   out[t] += y_shared[t] + sum over slots s (in slot order) of g[t,s] * y[pos(t,s)].
-// A gather per token (no atomics), so the result is bit-reproducible run to run.
+// A gather per token (no atomics), so the result is bit-reproducible run to run. The rows the
+// tensor-core down GEMM produced hold fp16 values in the first half of their fp32 slot; the
+// kernel tells them apart by the same test the grouping used to send a group there.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -10,43 +12,103 @@
 namespace ds4moe {
 namespace {
 
-__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, const int32_t *__restrict__ inv,
-                                                      const float *__restrict__ g, int T, int k, int D, int P,
-                                                      int shared, float *__restrict__ out) {
-    const int D4 = D / 4;
-    const size_t n = static_cast<size_t>(T) * D4;
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / D4);
-        const int c = static_cast<int>(i - static_cast<size_t>(t) * D4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (shared) acc = reinterpret_cast<const float4 *>(y + static_cast<size_t>(P + t) * D)[c];
-        for (int s = 0; s < k; s++) {
-            const int pos = inv[t * k + s];
-            const float gw = g[t * k + s];
-            const float4 v = reinterpret_cast<const float4 *>(y + static_cast<size_t>(pos) * D)[c];
-            acc.x = fmaf(gw, v.x, acc.x);
-            acc.y = fmaf(gw, v.y, acc.y);
-            acc.z = fmaf(gw, v.z, acc.z);
-            acc.w = fmaf(gw, v.w, acc.w);
+struct CombineParams {
+    const float *y;          // [P+T] rows of D fp32 (or D fp16 in the slot's first half)
+    const int32_t *inv;      // [T*k] row of each (token, slot)
+    const float *g;          // [T*k] gate weights
+    const int32_t *idx;      // [T*k] expert (slot) of each (token, slot)
+    const int32_t *counts;   // [E] tokens per expert
+    const uint8_t *tc_ok;    // [E] the expert may run on the tensor cores
+    int T, k, D, P, E;
+    int gemm_min;            // > 0: groups of at least this many tokens ran on the tensor cores
+    int shared;              // rows P.. hold the shared expert's output
+    int shared_f16;          // ... in fp16
+    float *out;
+};
+
+__device__ __forceinline__ void load8(const float *row, int c, bool f16, float v[8]) {
+    if (f16) {
+        const uint4 u = reinterpret_cast<const uint4 *>(row)[c];  // 8 fp16 values, columns 8c .. 8c+7
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
         }
-        float4 *o = reinterpret_cast<float4 *>(out + static_cast<size_t>(t) * D) + c;
-        float4 r = *o;
-        r.x += acc.x;
-        r.y += acc.y;
-        r.z += acc.z;
-        r.w += acc.w;
-        *o = r;
+    } else {
+        const float4 a = reinterpret_cast<const float4 *>(row)[2 * c];
+        const float4 b = reinterpret_cast<const float4 *>(row)[2 * c + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// One CTA per token (grid-stride over tokens); each thread 8 columns at a time.
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+    __shared__ int s_pos[32];
+    __shared__ float s_g[32];
+    __shared__ int s_f16[32];
+    const int D8 = p.D / 8;
+    for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+        if (threadIdx.x < p.k) {
+            const int s = threadIdx.x;
+            const int e = p.idx[t * p.k + s];
+            s_pos[s] = p.inv[t * p.k + s];
+            s_g[s] = p.g[t * p.k + s];
+            // (an index outside [0, E) has been reported by the grouping kernel, which grouped it as expert 0)
+            const int ec = (e >= 0 && e < p.E) ? e : 0;
+            s_f16[s] = p.gemm_min > 0 && p.counts[ec] >= p.gemm_min && p.tc_ok[ec];
+        }
+        __syncthreads();
+        for (int c = threadIdx.x; c < D8; c += blockDim.x) {
+            float acc[8];
+            if (p.shared) {
+                load8(p.y + static_cast<size_t>(p.P + t) * p.D, c, p.shared_f16 != 0, acc);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[i] = 0.0f;
+            }
+            for (int s = 0; s < p.k; s++) {
+                float v[8];
+                load8(p.y + static_cast<size_t>(s_pos[s]) * p.D, c, s_f16[s] != 0, v);
+                const float gw = s_g[s];
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[i] = fmaf(gw, v[i], acc[i]);
+            }
+            float4 *o = reinterpret_cast<float4 *>(p.out + static_cast<size_t>(t) * p.D) + 2 * c;
+            float4 a = o[0], b = o[1];
+            a.x += acc[0]; a.y += acc[1]; a.z += acc[2]; a.w += acc[3];
+            b.x += acc[4]; b.y += acc[5]; b.z += acc[6]; b.w += acc[7];
+            o[0] = a;
+            o[1] = b;
+        }
+        __syncthreads();
     }
 }
 
 }  // namespace
 
-int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, float *out, void *stream) {
-    const size_t n = static_cast<size_t>(T) * (w.D / 4);
-    const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 152 * 16));
-    combine_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(ws.y, ws.inv, ws.topk_w, T, k, w.D, T * k,
-                                                                          w.has_shared ? 1 : 0, out);
+int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, int gemm_min, bool shared_f16,
+                   float *out, void *stream) {
+    CombineParams p;
+    p.y = ws.y;
+    p.inv = ws.inv;
+    p.g = ws.topk_w;
+    p.idx = ws.topk_idx;
+    p.counts = ws.counts;
+    p.tc_ok = w.tc_ok;
+    p.T = T;
+    p.k = k;
+    p.D = w.D;
+    p.P = T * k;
+    p.E = w.E;
+    p.gemm_min = gemm_min;
+    p.shared = w.has_shared ? 1 : 0;
+    p.shared_f16 = (w.has_shared && shared_f16) ? 1 : 0;
+    p.out = out;
+    const int blocks = std::min(T, 152 * 8);
+    combine_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

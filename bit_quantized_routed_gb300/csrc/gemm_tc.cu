@@ -3,19 +3,20 @@
 // "DwarfStar" README, "速度" and "基准测试": prefill runs in chunks of thousands of tokens
 // and is compute-rich; with many tokens per expert the expert FFN is a dense contraction,
 // so it runs on the 5th-generation tensor cores. Per (expert, 128 weight rows, up to 256
-// tokens) tile:
-//   * sixteen producer warps stream the packed weight rows from HBM (each thread one slice of
-//     a row: half of a gate/up row's sub-blocks or a quarter of a down row's, with a ring of
-//     register prefetches and L2 prefetches ahead of it), decode them to fp16 (RN-even of the
-//     exact fp32 value) and write them into shared memory in the canonical K-major
-//     SWIZZLE_128B layout (one 128-row x 64-column atom column per stage);
+// tokens) tile -- for the down GEMM (expert, 256 weight rows, up to 256 tokens), so that each
+// token tile copied in feeds two MMAs per K step in both GEMMs:
+//   * sixteen producer warps stream the packed weight rows from HBM (each thread one half of
+//     a row's columns per stage, with a ring of register prefetches and L2 prefetches ahead of
+//     it), decode them to fp16 (RN-even of the exact fp32 value) and write them into shared
+//     memory in the canonical K-major SWIZZLE_128B layout (128-row x 64-column atom columns);
 //   * one warp issues TMA loads of the group's token rows (fp16, gathered per group) into
 //     the same layout;
 //   * one thread issues tcgen05.mma (M=128, N=tokens rounded up to 16, K=16) into fp32
-//     accumulators in tensor memory: gate and up side by side for the first GEMM;
+//     accumulators in tensor memory: gate and up side by side for the first GEMM, the two
+//     128-row halves side by side for the down GEMM;
 //   * the producer warps then read the accumulators back with tcgen05.ld (four warps per
 //     TMEM lane quarter) and apply the epilogue: h = silu(gate) * up (fp16 out) for the
-//     first GEMM, y (fp32 out) for the down GEMM.
+//     first GEMM, y (fp16 out, into the first half of the row's fp32 slot) for the down GEMM.
 // Swap-AB: weights are the M side and tokens the N side, so groups of a few dozen tokens
 // still fill MMAs. Every wait on an mbarrier is bounded: after ~2 s it records
 // DS4MOE_ETIMEOUT in the handle's status word and the CTA drains its copies, frees its
@@ -49,9 +50,9 @@ struct Cfg<UP> {
 };
 template <>
 struct Cfg<DOWN> {
-    static constexpr int NA = 1;
-    static constexpr int STAGES = 4;
-    static constexpr int TMEM_COLS = 256;
+    static constexpr int NA = 2;  // two 128-row weight tiles on one token tile
+    static constexpr int STAGES = 3;
+    static constexpr int TMEM_COLS = 512;
 };
 
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
@@ -92,7 +93,8 @@ struct GemmParams {
     const GroupMeta *meta;
     const uint8_t *grid;
     uint16_t *h16;  // UP output, [rows][F]
-    float *y;       // DOWN output, [rows][D]
+    uint16_t *y16;  // DOWN output: row r's fp16 values at y16 + 2 * D * r (the first half of the
+                    // row's fp32 slot in the y buffer, which the GEMV paths fill in fp32)
     int T, P, shared;
     int *status;
 };
@@ -102,7 +104,7 @@ struct Tile {
     int e;       // routed expert
     int row0;    // first token row (x16 / h16 / y row)
     int ntok;    // token rows in the tile (1..BN)
-    int m;       // weight-row tile
+    int m;       // weight-row tile (128 rows of gate and up for the first GEMM, 256 down rows)
 };
 
 // Tiles t = nt * m_tiles + m: token tile nt (the routed experts' tiles first, in the order of
@@ -134,12 +136,13 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_ti
 
 // ------------------------------------------------------------------ producers
 //
-// Each of the 512 producer threads owns one slice of one tile row per stage: first GEMM, one
-// 32-column half of a row of gate or up (thread u: row (u >> 1) & 127, matrix u >> 8, half u & 1,
-// so two neighbouring lanes read the two halves of one 16-byte chunk); down GEMM, one 16-column
-// quarter of a row (row (u >> 2) & 127, quarter u & 3). A format fetches the packed data of a
-// stage into registers (a ring of PF stages in flight hides the HBM latency) and emits it as fp16
-// into the swizzled A tile. Every fp16 value is RN-even of the weight's exact fp32 value.
+// Each of the 512 producer threads owns one 32-column half of one tile row per stage (thread u:
+// row (u >> 1) & 127 of A tile u >> 8, half u & 1, so two neighbouring lanes read the two halves
+// of one 16-byte chunk). The first GEMM's two A tiles are the same 128 rows of gate and of up; the
+// down GEMM's are two consecutive 128-row tiles, so one token tile feeds 256 output rows. A format
+// fetches the packed data of a stage into registers (a ring of PF stages in flight hides the HBM
+// latency) and emits it as fp16 into the swizzled A tile. Every fp16 value is RN-even of the
+// weight's exact fp32 value.
 
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 __device__ __forceinline__ void prefetch_l2(const void *a) { asm volatile("prefetch.global.L2 [%0];" ::"l"(a)); }
@@ -192,7 +195,7 @@ struct IQ2Fmt {
     }
 };
 
-// Q2_K-style rows, quarter row: one 16-weight sub-block per stage. The 4 possible values of the
+// Q2_K-style rows, half row: two 16-weight sub-blocks per stage. The 4 possible values of a
 // sub-block, RN-even(fp32(d*sc*q - dmin*m)) for q = 0..3, are formed once; each code byte then
 // selects its four values with two byte permutations (selectors from a table).
 struct Q2KFmt {
@@ -200,20 +203,20 @@ struct Q2KFmt {
     static constexpr int PD = 8;  // L2 prefetch distance (stages), every 4 stages (one 80-byte block)
     static constexpr int PE = 4;
     struct Data {
-        uint32_t q;   // 16 codes
-        uint32_t sc;  // scale byte (low 4 bits sc, high 4 bits m)
+        uint2 q;      // 2 x 16 codes
+        uint32_t sc;  // two scale bytes (low 4 bits sc, high 4 bits m)
         uint32_t dd;
     };
     const uint8_t *sq;    // this row's blocks (scales, codes)
     const uint32_t *ddp;  // this row's d | dmin words
-    int qp;               // which quarter of the stage's 64 columns
+    int half;             // which half of the stage's 64 columns
     const uint2 *st;  // code byte -> two byte_perm selectors, this lane's replica
     __device__ __forceinline__ Data fetch(int kb) const {
         const int b = kb >> 2, part = kb & 3;
         const uint8_t *blk = sq + b * 80;
         Data v;
-        v.q = __ldg(reinterpret_cast<const uint32_t *>(blk + 16 + 16 * part + 4 * qp));
-        v.sc = __ldg(blk + 4 * part + qp);
+        v.q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 16 * part + 8 * half));
+        v.sc = __ldg(reinterpret_cast<const uint16_t *>(blk + 4 * part + 2 * half));
         v.dd = __ldg(ddp + b);
         return v;
     }
@@ -225,20 +228,25 @@ struct Q2KFmt {
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r, int = 0) const {
         const float d = f16_to_f32(static_cast<uint16_t>(v.dd & 0xffffu));
         const float dmin = f16_to_f32(static_cast<uint16_t>(v.dd >> 16));
-        const float ds = __fmul_rn(d, static_cast<float>(v.sc & 15u));
-        const float dm = __fmul_rn(dmin, static_cast<float>((v.sc >> 4) & 15u));
-        const uint32_t p01 = pack_h2(q2k_weight(ds, dm, 0u), q2k_weight(ds, dm, 1u));
-        const uint32_t p23 = pack_h2(q2k_weight(ds, dm, 2u), q2k_weight(ds, dm, 3u));
 #pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-            const uint2 s0 = st[((v.q >> (16 * hh)) & 255u) << 4];
-            const uint2 s1 = st[((v.q >> (16 * hh + 8)) & 255u) << 4];
-            uint4 o;
-            o.x = __byte_perm(p01, p23, s0.x);
-            o.y = __byte_perm(p01, p23, s0.y);
-            o.z = __byte_perm(p01, p23, s1.x);
-            o.w = __byte_perm(p01, p23, s1.y);
-            st_shared16(tile + sw128_off(r, 2 * qp + hh), o);
+        for (int j = 0; j < 2; j++) {  // sub-block 2 * half + j of the stage
+            const uint32_t sc = v.sc >> (8 * j);
+            const uint32_t q = j ? v.q.y : v.q.x;
+            const float ds = __fmul_rn(d, static_cast<float>(sc & 15u));
+            const float dm = __fmul_rn(dmin, static_cast<float>((sc >> 4) & 15u));
+            const uint32_t p01 = pack_h2(q2k_weight(ds, dm, 0u), q2k_weight(ds, dm, 1u));
+            const uint32_t p23 = pack_h2(q2k_weight(ds, dm, 2u), q2k_weight(ds, dm, 3u));
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                const uint2 s0 = st[((q >> (16 * hh)) & 255u) << 4];
+                const uint2 s1 = st[((q >> (16 * hh + 8)) & 255u) << 4];
+                uint4 o;
+                o.x = __byte_perm(p01, p23, s0.x);
+                o.y = __byte_perm(p01, p23, s0.y);
+                o.z = __byte_perm(p01, p23, s1.x);
+                o.w = __byte_perm(p01, p23, s1.y);
+                st_shared16(tile + sw128_off(r, 4 * half + 2 * j + hh), o);
+            }
         }
     }
 };
@@ -262,8 +270,8 @@ __device__ __forceinline__ uint4 q4_to_f16x8(uint32_t word, float ds, float dm) 
     return make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
 }
 
-// Gate/up rows of the 4-bit variant, half row: one 32-weight sub-block per stage.
-struct Q4UpFmt {
+// Rows of the 4-bit variant (gate, up or down), half row: one 32-weight sub-block per stage.
+struct Q4Fmt {
     static constexpr int PF = 2;
     static constexpr int PD = 0;
     static constexpr int PE = 1;
@@ -291,36 +299,6 @@ struct Q4UpFmt {
         st_shared16(tile + sw128_off(r, 4 * part + 1), q4_to_f16x8(v.q.y, ds, dm));
         st_shared16(tile + sw128_off(r, 4 * part + 2), q4_to_f16x8(v.q.z, ds, dm));
         st_shared16(tile + sw128_off(r, 4 * part + 3), q4_to_f16x8(v.q.w, ds, dm));
-    }
-};
-
-// Down rows of the 4-bit variant, quarter row: half a sub-block (16 weights) per stage.
-struct Q4DownFmt {
-    static constexpr int PF = 3;
-    static constexpr int PD = 0;
-    static constexpr int PE = 1;
-    struct Data {
-        uint2 q;
-        uint32_t dd, lo, hi;
-    };
-    const uint8_t *row;
-    int qp;
-    __device__ __forceinline__ Data fetch(int kb) const {
-        const int b = kb >> 2, sub = 2 * (kb & 3) + (qp >> 1);
-        const uint8_t *blk = row + b * 144;
-        Data v;
-        v.q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 16 * sub) + (qp & 1));
-        v.dd = __ldg(reinterpret_cast<const uint32_t *>(blk));
-        v.lo = __ldg(reinterpret_cast<const uint32_t *>(blk + 4) + (sub >> 2));
-        v.hi = __ldg(reinterpret_cast<const uint32_t *>(blk + 12));
-        return v;
-    }
-    __device__ __forceinline__ void prefetch(int) const {}
-    __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r, int kb) const {
-        float ds, dm;
-        q4_scales(v.dd, v.lo, v.hi, 2 * (kb & 3) + (qp >> 1), ds, dm);
-        st_shared16(tile + sw128_off(r, 2 * qp + 0), q4_to_f16x8(v.q.x, ds, dm));
-        st_shared16(tile + sw128_off(r, 2 * qp + 1), q4_to_f16x8(v.q.y, ds, dm));
     }
 };
 
@@ -353,27 +331,27 @@ struct BF16Fmt {
     }
 };
 
-// fp16 rows (shared down), quarter row: 16 columns per stage -> copied.
+// fp16 rows (shared down), half row: 32 columns per stage -> copied.
 struct F16Fmt {
-    static constexpr int PF = 2;
+    static constexpr int PF = 1;
     static constexpr int PD = 0;
     static constexpr int PE = 1;
     struct Data {
-        uint4 v[2];
+        uint4 v[4];
     };
     const uint16_t *row;
-    int qp;
+    int half;
     __device__ __forceinline__ Data fetch(int kb) const {
         Data d;
-        const uint4 *src = reinterpret_cast<const uint4 *>(row + kb * BK + 16 * qp);
+        const uint4 *src = reinterpret_cast<const uint4 *>(row + kb * BK + 32 * half);
 #pragma unroll
-        for (int c = 0; c < 2; c++) d.v[c] = __ldg(src + c);
+        for (int c = 0; c < 4; c++) d.v[c] = __ldg(src + c);
         return d;
     }
     __device__ __forceinline__ void prefetch(int) const {}
     __device__ __forceinline__ void emit(const Data &d, uint32_t tile, int r, int = 0) const {
 #pragma unroll
-        for (int c = 0; c < 2; c++) st_shared16(tile + sw128_off(r, 2 * qp + c), d.v[c]);
+        for (int c = 0; c < 4; c++) st_shared16(tile + sw128_off(r, 4 * half + c), d.v[c]);
     }
 };
 
@@ -447,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = p.w.D, F = p.w.F;
-    const int m_tiles = (KIND == UP ? F : D) / BM;
+    constexpr int MR = KIND == UP ? BM : BM * C::NA;  // weight rows per m-tile
+    const int m_tiles = (KIND == UP ? F : D) / MR;
     const int routed = p.meta->n_tiles;
     const int total = n_tiles_total(p, m_tiles, routed);
     if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA, before any allocation
@@ -580,11 +559,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else {
         // ---------------------------------------------------------- producers, then epilogue
         const int u = (warp - 2) * 32 + lane;  // 0..511
-        // first GEMM: row (u >> 1) & 127 of matrix u >> 8 (gate/up), half u & 1; down GEMM: row
-        // (u >> 2) & 127, quarter u & 3
-        const int r = KIND == UP ? (u >> 1) & 127 : (u >> 2) & 127;  // tile row
-        const int sel = KIND == UP ? u >> 8 : 0;
-        const int part = KIND == UP ? u & 1 : u & 3;
+        // row (u >> 1) & 127 of A tile u >> 8 (gate / up, or the first / second 128 down rows), half u & 1
+        const int r = (u >> 1) & 127;  // tile row
+        const int sel = u >> 8;
+        const int part = u & 1;
         const int q = warp & 3;                // TMEM lane quarter this warp may access
         const int colq = (warp - 2) >> 2;      // epilogue: which 16-column chunks (one of four)
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
@@ -594,13 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = decode_tile(p, t, m_tiles, routed);
-            const int wrow = ti.m * BM + r;
+            const int wrow = ti.m * MR + (KIND == DOWN ? sel * BM : 0) + r;
             if (KIND == UP) {
                 if (ti.shared) {
                     BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D, part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else if (FMT == 1) {
-                    Q4UpFmt f{q4_row(p.w, sel, ti.e, wrow), part};
+                    Q4Fmt f{q4_row(p.w, sel, ti.e, wrow), part};
                     ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else {
                     IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab, iq2_swz(p.w, wrow), part};
@@ -609,13 +587,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             } else {
                 if (ti.shared) {
                     F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, part};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else if (FMT == 1) {
-                    Q4DownFmt f{q4_row(p.w, 2, ti.e, wrow), part};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
+                    Q4Fmt f{q4_row(p.w, 2, ti.e, wrow), part};
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 } else {
                     Q2KFmt f{q2k_sq_row(p.w, ti.e, wrow), q2k_dd_row(p.w, ti.e, wrow), part, tab};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, 0, r, pp);
+                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
                 }
             }
             if (!ok) break;
@@ -625,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 break;
             }
             tc_fence_after();
-            const int orow = ti.m * BM + q * 32 + lane;
+            const int orow = ti.m * MR + q * 32 + lane;
             bool range_ok = true;
             for (int c0 = 16 * colq; c0 < ti.ntok; c0 += 64) {
                 if (KIND == UP) {
@@ -645,11 +623,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         }
                     }
                 } else {
-                    float v[16];
-                    tmem_ld16(tmem + lane_addr + c0, v);
+#pragma unroll 1
+                    for (int a = 0; a < C::NA; a++) {  // the two 128-row tiles
+                        float v[16];
+                        tmem_ld16(tmem + lane_addr + a * BN + c0, v);
 #pragma unroll
-                    for (int j = 0; j < 16; j++)
-                        if (c0 + j < ti.ntok) p.y[static_cast<size_t>(ti.row0 + c0 + j) * D + orow] = v[j];
+                        for (int j = 0; j < 16; j++) {
+                            if (c0 + j < ti.ntok) {
+                                range_ok &= fabsf(v[j]) <= 65504.0f;
+                                p.y16[static_cast<size_t>(ti.row0 + c0 + j) * (2 * D) + orow + a * BM] =
+                                    __half_as_ushort(__float2half_rn(v[j]));
+                            }
+                        }
+                    }
                 }
             }
             if (!range_ok) report(p.status, ST_RANGE);
@@ -675,11 +661,10 @@ __global__ void __launch_bounds__(kProducers) producer_dump_kernel(DeviceWeights
     __shared__ __align__(1024) uint8_t tile[A_BYTES];
     __shared__ uint2 table[256 * 16];
     const int lane = threadIdx.x & 31;
-    // the GEMM producers' slices: down, row (u >> 2) & 127, quarter u & 3; gate/up (one matrix),
-    // row (u >> 1) & 127, half u & 1 for u < 256
+    // the GEMM producers' slices of one A tile: row (u >> 1) & 127, half u & 1 for u < 256
     const int u = threadIdx.x;
     const bool down = matrix == DS4MOE_DOWN;
-    const int r = down ? (u >> 2) & 127 : (u >> 1) & 127;
+    const int r = (u >> 1) & 127;
     for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
         const uint32_t e = static_cast<uint32_t>(i >> 4);
         uint2 v;
@@ -701,8 +686,8 @@ __global__ void __launch_bounds__(kProducers) producer_dump_kernel(DeviceWeights
     const int wrow = m * BM + r;
     const uint32_t t = smem_u32(tile);
     const uint2 *tab = table + (lane & 15);
-    if (down) {
-        Q2KFmt f{q2k_sq_row(w, expert, wrow), q2k_dd_row(w, expert, wrow), u & 3, tab};
+    if (down && u < 256) {
+        Q2KFmt f{q2k_sq_row(w, expert, wrow), q2k_dd_row(w, expert, wrow), u & 1, tab};
         f.emit(f.fetch(kb), t, r);
     } else if (u < 256) {
         const int m = matrix == DS4MOE_GATE ? 0 : 1;
@@ -786,7 +771,7 @@ GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k
     p.meta = ws.meta;
     p.grid = ws.grid;
     p.h16 = ws.h16;
-    p.y = ws.y;
+    p.y16 = reinterpret_cast<uint16_t *>(ws.y);
     p.T = T;
     p.P = T * k;
     p.shared = shared ? 1 : 0;

@@ -160,7 +160,8 @@ struct Workspace {
     float *h32;         // [P+T][F] fp32 intermediate of the GEMV path (rows P.. = shared expert)
     uint16_t *h16;      // [P+T][F] fp16 intermediate of the tensor-core path
     uint16_t *x16;      // [P+T][D] fp16 tokens gathered per group for the tensor-core path
-    float *y;           // [P+T][D] per-pair expert outputs (rows P.. = shared expert)
+    float *y;           // [P+T][D] per-pair expert outputs (rows P.. = shared expert); the tensor-core
+                        // down GEMM writes its rows as D fp16 values in the first half of the row
     int *status;        // device status word
     unsigned *gbar;     // grid barrier of the single-token kernel: count, generation
     float *hmax;        // [1024][8] per-CTA maxima of the single-token kernel
@@ -247,7 +248,10 @@ int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *
 int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream,
                      bool int16_h = false);
 int launch_prep_h(const Workspace &ws, int rows, int F, void *stream);
-int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, float *out, void *stream);
+// gemm_min > 0: the pairs of groups of at least gemm_min tokens (tc_ok experts) ran on the
+// tensor-core down GEMM and their y rows hold fp16; shared_f16: so does the shared expert's.
+int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, int gemm_min, bool shared_f16,
+                   float *out, void *stream);
 int launch_dequant(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, float *dst32,
                    uint16_t *dst16, void *stream);
 

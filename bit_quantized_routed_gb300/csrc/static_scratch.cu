@@ -106,6 +106,6 @@ extern "C" int ds4moe_expert_ffn_static(const uint16_t *x, const ds4moe_weights 
                           ws.gemm_list, nullptr, nullptr, nullptr, nullptr, ws.meta, ws.status, stream);
     if (!rc) rc = launch_gemv_up(w, ws, x, T, k, true, stream);
     if (!rc) rc = launch_gemv_down(w, ws, T, k, true, stream);
-    if (!rc) rc = launch_combine(w, ws, T, k, out, stream);
+    if (!rc) rc = launch_combine(w, ws, T, k, 0, false, out, stream);
     return rc ? DS4MOE_ECUDA : DS4MOE_OK;
 }
