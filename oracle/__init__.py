@@ -174,8 +174,10 @@ GATE_SIGMOID = 1
 
 
 def route(logits, k, mode=GATE_SOFTMAX):
-    """Top-k experts per token (logit descending, ties to the lower index) and gate weights
-    (fp64). Returns idx int32 [T,k], g float64 [T,k]."""
+    """Top-k experts per token (logit descending, ties to the lower index, a NaN logit ranked as
+    -inf) and gate weights (fp64): softmax over the selected logits, or normalised sigmoids, with
+    equal selected logits (equal infinities included) weighted equally. Returns idx int32 [T,k],
+    g float64 [T,k]."""
     logits = np.ascontiguousarray(logits, np.float32)
     T, E = logits.shape
     idx = np.zeros((T, k), np.int32)

@@ -378,38 +378,56 @@ void or_iq2_dequant(const uint8_t *src, int64_t rows, int64_t cols, const uint8_
 
 /* ------------------------------------------------------------------ routing */
 
-/* Top-k per token. Order: logit descending, ties to the lower expert index. Gate weights:
- * mode 0 = softmax over the k selected logits, mode 1 = sigmoid(l) / sum of sigmoids.
- * idx [T,k] and g [T,k] follow the selection order. */
+/* Routing ("DwarfStar 深度解析" §2.1: every token picks its experts from the router's logits).
+ * Readings of this library, where the pages are silent:
+ *   - order: logit descending, ties to the lower expert index; a NaN logit counts as -inf;
+ *   - gate weights over the k selected logits v_0 >= ... >= v_{k-1} (NaN taken as -inf):
+ *     mode 0 (softmax) g_s = exp(v_s - v_0) / sum_j exp(v_j - v_0), where a term with v_s equal to
+ *     v_0 counts as exp(0) = 1 also when both are infinite (the limit of equal logits): an all -inf
+ *     selection gets 1/k each, and a +inf logit takes the weight from every finite one;
+ *     mode 1 (sigmoid) g_s = sigmoid(v_s) / sum_j sigmoid(v_j), evaluated as the mode-0 rule over
+ *     log sigmoid(v) = min(v, 0) - log1p(exp(-|v|)) (the same ratio, with no underflow to 0/0). */
+static double route_key(float v) { return isnan(v) ? -INFINITY : (double)v; }
+
+/* 1 if expert a is ranked before expert b in the logits l of one token. */
+static int route_before(const float *l, int a, int b) {
+    const double ka = route_key(l[a]), kb = route_key(l[b]);
+    if (ka != kb) return ka > kb;
+    return a < b;
+}
+
+static double log_sigmoid(double v) { return fmin(v, 0.0) - log1p(exp(-fabs(v))); }
+
+/* exp(v - top), with exp(0) = 1 where v equals top (infinities included). */
+static double gate_term(double v, double top) { return v == top ? 1.0 : exp(v - top); }
+
+/* Top-k per token and its gate weights: idx [T,k] and g [T,k] in the selection order. */
 void or_route(const float *logits, int T, int E, int k, int mode, int32_t *idx, double *g) {
     int *order = (int *)malloc(sizeof(int) * (size_t)E);
+    double *v = (double *)malloc(sizeof(double) * (size_t)k);
     for (int t = 0; t < T; t++) {
         const float *l = logits + (int64_t)t * E;
-        /* insertion sort by (-logit, index): stable, so equal logits keep index order */
+        /* insertion sort of the expert indices by route_before */
         for (int e = 0; e < E; e++) {
             int pos = e;
-            while (pos > 0 && l[order[pos - 1]] < l[e]) {
+            while (pos > 0 && route_before(l, e, order[pos - 1])) {
                 order[pos] = order[pos - 1];
                 pos--;
             }
             order[pos] = e;
         }
-        double den = 0.0;
-        double *num = (double *)malloc(sizeof(double) * (size_t)k);
         for (int s = 0; s < k; s++) {
-            double ls = (double)l[order[s]];
-            if (mode == 0)
-                num[s] = exp(ls - (double)l[order[0]]);
-            else
-                num[s] = 1.0 / (1.0 + exp(-ls));
-            den += num[s];
+            v[s] = route_key(l[order[s]]);
+            if (mode != 0) v[s] = log_sigmoid(v[s]);
         }
+        double den = 0.0;
+        for (int s = 0; s < k; s++) den += gate_term(v[s], v[0]);
         for (int s = 0; s < k; s++) {
             idx[(int64_t)t * k + s] = order[s];
-            g[(int64_t)t * k + s] = num[s] / den;
+            g[(int64_t)t * k + s] = gate_term(v[s], v[0]) / den;
         }
-        free(num);
     }
+    free(v);
     free(order);
 }
 

@@ -47,6 +47,63 @@ def test_route_special_cases():
     assert all(sorted(r) == list(range(16)) for r in idx)
 
 
+def _keys(l):
+    """The ranking keys of one token's logits: NaN counts as -inf."""
+    k = l.astype(np.float64)
+    k[np.isnan(k)] = -np.inf
+    return k
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_route_nan_and_infinite_logits(mode):
+    """NaN ranks as -inf (ties to the lower index), +inf and -inf rank where they belong; the
+    selection is numpy's lexsort over the keys. Gate weights: closed forms of the stated rule."""
+    nan, inf = np.float32(np.nan), np.float32(np.inf)
+    rows = [
+        [1.0, nan, 7.0, 2.0, 0.5, -3.0, 4.0, 0.0],     # one NaN: never chosen over a finite logit
+        [nan, 9.0, nan, 8.0, 1.0, 2.0, 3.0, 4.0],      # NaNs among the top logits
+        [0.5, inf, 3.0, -1.0, inf, 2.0, 1.0, 0.0],     # two +inf: they share the weight
+        [-inf, 2.0, -inf, 1.0, 0.0, -1.0, -2.0, -3.0],  # -inf at the bottom
+        [nan] * 8,                                     # all NaN: experts 0..k-1, equal weights
+        [-inf] * 8,                                    # all -inf: the same
+        [nan, -inf, nan, -inf, 5.0, nan, -inf, nan],   # one finite logit; NaN and -inf tie
+    ]
+    L = np.array(rows, np.float32)
+    k = 4
+    idx, g = oracle.route(L, k, mode)
+    for t in range(len(rows)):
+        keys = _keys(L[t])
+        sel = np.lexsort((np.arange(8), -keys))[:k]
+        assert list(idx[t]) == list(sel), t
+        assert abs(g[t].sum() - 1.0) <= 1e-12, t
+    assert list(idx[0]) == [2, 6, 3, 0]
+    assert list(idx[1]) == [1, 3, 7, 6]
+    assert list(idx[4]) == [0, 1, 2, 3] and np.all(g[4] == 0.25)
+    assert list(idx[5]) == [0, 1, 2, 3] and np.all(g[5] == 0.25)
+    assert list(idx[6]) == [4, 0, 1, 2]       # the finite logit, then NaN and -inf tie, by index
+    if mode == 0:
+        assert list(g[2]) == [0.5, 0.5, 0.0, 0.0]
+        assert list(g[6]) == [1.0, 0.0, 0.0, 0.0]
+        ls = np.array([2.0, 1.0, 0.0, -1.0])
+        assert np.allclose(g[3], softmax(ls), rtol=0, atol=1e-15)
+    else:
+        s = expit(np.array([inf, inf, 3.0, 2.0], np.float64))
+        assert np.allclose(g[2], s / s.sum(), rtol=0, atol=1e-15)
+        assert list(g[6]) == [1.0, 0.0, 0.0, 0.0]
+        s = expit(np.array([2.0, 1.0, 0.0, -1.0]))
+        assert np.allclose(g[3], s / s.sum(), rtol=0, atol=1e-15)
+
+
+def test_route_sigmoid_gates_far_below_zero():
+    """The sigmoid weights keep their ratio where sigmoid itself underflows double precision: for
+    v far below 0, sigmoid(v) = exp(v) (1 + O(exp(v))), so the weights are the softmax of v."""
+    L = np.array([[-800.0, -801.0, -803.0, -900.0, -5000.0]], np.float32)
+    idx, g = oracle.route(L, 3, 1)
+    assert list(idx[0]) == [0, 1, 2]
+    ref = softmax(np.array([-800.0, -801.0, -803.0]))
+    assert np.allclose(g[0], ref, rtol=0, atol=1e-15)
+
+
 def test_route_boundary_ties_of_the_tie_workload():
     wl = synth.WORKLOADS["prefill_t8192_d7168"].replace(T=400, D=256)
     L, _ = synth.draw_inputs(wl)
