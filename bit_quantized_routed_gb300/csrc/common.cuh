@@ -35,6 +35,21 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Gate numerator of a selected logit v against the first (largest) selected logit top, both
+// with NaN already taken as -inf ("DwarfStar 深度解析" §2.1 routes each token by its logits; the
+// weights below are this library's reading): softmax mode exp(v - top), counted as exp(0) = 1
+// where v equals top, also when both are infinite (the limit of equal logits: an all -inf
+// selection gets 1/k each, a +inf logit takes the weight from every finite one); sigmoid mode
+// the same over log sigmoid(v) = min(v, 0) - log1p(exp(-|v|)), since sigmoid(v) / sum of
+// sigmoids is the softmax of the log-sigmoids, which never underflows to 0 / 0.
+__device__ __forceinline__ float gate_numerator(float v, float top, int mode) {
+    if (mode != DS4MOE_GATE_SOFTMAX) {
+        v = fminf(v, 0.0f) - log1pf(expf(-fabsf(v)));
+        top = fminf(top, 0.0f) - log1pf(expf(-fabsf(top)));
+    }
+    return v == top ? 1.0f : expf(v - top);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 

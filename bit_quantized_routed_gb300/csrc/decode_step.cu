@@ -260,7 +260,7 @@ __device__ void route_warp(const StepParams &p, int lane, int *sidx, float *sgw)
     }
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     float num = 0.0f;
-    if (lane < p.k) num = (p.mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+    if (lane < p.k) num = gate_numerator(my_v, top, p.mode);
     const float den = warp_sum(num);
     if (lane < p.k) {
         sidx[lane] = p.slot_of ? p.slot_of[my_i] : my_i;  // a pooled handle's experts sit in slots
@@ -334,7 +334,7 @@ __device__ void route_sorted8(const StepParams &p, int lane, int *sidx, float *s
     }
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     float num = 0.0f;
-    if (lane < p.k) num = (p.mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+    if (lane < p.k) num = gate_numerator(my_v, top, p.mode);
     const float den = warp_sum(num);
     if (lane < p.k) {
         sidx[lane] = p.slot_of ? p.slot_of[my_i] : my_i;  // a pooled handle's experts sit in slots

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
     }
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     float num = 0.0f;
-    if (lane < k) num = (mode == DS4MOE_GATE_SOFTMAX) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+    if (lane < k) num = gate_numerator(my_v, top, mode);
     const float den = warp_sum(num);
     if (lane < k) {
         idx[static_cast<size_t>(t) * k + lane] = my_i;

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import FFN_TOL, Layer, norm_max_err
+from helpers import FFN_TOL, Layer, norm_max_err, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +35,38 @@ def test_route_bitexact(ds4, T, E, k, mode):
     idx, w = ds4.ds4moe_route(torch.from_numpy(L).cuda(), k, mode)
     assert np.array_equal(idx.cpu().numpy(), idx_ref)
     assert np.max(np.abs(w.cpu().numpy() - g_ref)) <= 1e-6
+
+
+_NAN, _INF = np.float32(np.nan), np.float32(np.inf)
+# rows of 8 logits: a NaN ranks as -inf (ties to the lower index), +inf and -inf where they belong
+_SPECIAL_ROWS = [
+    [1.0, _NAN, 7.0, 2.0, 0.5, -3.0, 4.0, 0.0],
+    [_NAN, 9.0, _NAN, 8.0, 1.0, 2.0, 3.0, 4.0],
+    [0.5, _INF, 3.0, -1.0, _INF, 2.0, 1.0, 0.0],
+    [-_INF, 2.0, -_INF, 1.0, 0.0, -1.0, -2.0, -3.0],
+    [_NAN] * 8,
+    [-_INF] * 8,
+    [_NAN, -_INF, _NAN, -_INF, 5.0, _NAN, -_INF, _NAN],
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("E", [8, 256, 1000])
+def test_route_nan_and_infinite_logits(ds4, mode, E):
+    import torch
+    rng = np.random.default_rng(E + mode)
+    L = rng.standard_normal((len(_SPECIAL_ROWS) + 1, E)).astype(np.float32)
+    for t, row in enumerate(_SPECIAL_ROWS):
+        L[t] = -np.inf if E > 8 else 0.0     # wider rows: the special values, then -inf
+        L[t, :8] = row
+    L[-1, E // 2] = np.nan                   # a NaN among ordinary logits
+    for k in (1, 4, 8):
+        idx_ref, g_ref = oracle.route(L, k, mode)
+        idx, w = ds4.ds4moe_route(torch.from_numpy(L).cuda(), k, mode)
+        w = w.cpu().numpy()
+        assert np.array_equal(idx.cpu().numpy(), idx_ref)
+        assert np.all(np.isfinite(w))
+        assert np.max(np.abs(w - g_ref)) <= 1e-6
 
 
 def test_route_zero_tokens(ds4):
@@ -138,16 +170,15 @@ def test_ffn_deterministic(ds4):
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
-@pytest.mark.parametrize("name,tokens", [("decode_t1", None), ("decode_t32", [0, 13, 31]),
-                                         ("prefill_t2048", [0, 777, 2047]),
-                                         ("prefill_t8192_d7168", [1, 4100, 8191])])
-def test_ffn_full_size_sampled(ds4, name, tokens):
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t32", "prefill_t2048", "prefill_t8192_d7168"])
+def test_ffn_full_size_sampled(ds4, name):
+    """Every workload at its full size, in the call the benchmark times: all tokens of the decode
+    workloads; for the prefill chunks, tokens at 64 column positions of the largest group's
+    256-token tiles and at both ends of its ragged last tile, tokens of one-token, small and mid
+    groups, and tied tokens (helpers.sample_tokens)."""
     wl = synth.WORKLOADS[name]
     lay = Layer(wl, quantized=False)
-    if name == "prefill_t8192_d7168":  # include a tied token
-        o = np.argsort(-lay.L, axis=1, kind="stable")
-        tied = np.nonzero(lay.L[np.arange(wl.T), o[:, 0]] == lay.L[np.arange(wl.T), o[:, 1]])[0]
-        tokens = sorted(set(tokens) | {int(tied[0])})
+    tokens = None if wl.T <= 32 else sample_tokens(lay.L, wl.k)
     W = lay.upload(ds4)
     got = lay.run(ds4, W)
     W.close()
@@ -249,8 +280,9 @@ def test_small_groups_at_one_token_without_the_fused_kernel(ds4):
 # (D, E, k, shared, mode, fused): the fused kernel covers F == 2048, D <= 4096; D = 7168 takes
 # the separate single-token kernels. D = 3072 leaves half of the second x half empty.
 @pytest.mark.parametrize("D,E,k,shared,mode,fused", [
-    (4096, 256, 8, True, 0, True), (2048, 64, 6, True, 1, True), (1024, 16, 8, False, 0, True),
-    (3072, 32, 4, True, 1, True), (4096, 300, 1, False, 1, True), (7168, 64, 6, True, 1, False)])
+    (4096, 256, 8, True, 0, True), (4096, 256, 8, True, 1, True), (2048, 64, 6, True, 1, True),
+    (1024, 16, 8, False, 0, True), (3072, 32, 4, True, 1, True), (4096, 300, 1, False, 1, True),
+    (4096, 8, 8, True, 0, True), (2048, 8, 8, False, 1, True), (7168, 64, 6, True, 1, False)])
 def test_single_token_kernel_matches_oracle(ds4, D, E, k, shared, mode, fused):
     wl = synth.Workload("one", T=1, D=D, F=2048, E=E, k=k, seed=D + E, shared=shared)
     lay = Layer(wl, quantized=False)
@@ -281,6 +313,30 @@ def test_single_token_kernel_breaks_ties_like_the_oracle(ds4, mode):
     assert norm_max_err(got, ref) <= FFN_TOL
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("E", [64, 300])   # the fused kernel's two top-k routines (E <= 256, above)
+def test_single_token_kernel_nan_and_infinite_logits(ds4, mode, E):
+    """The fused kernel's own top-k and gate weights on NaN, +inf and -inf logits, through the
+    whole layer: a different selection or a NaN weight would change the output far beyond the
+    tolerance (every expert's blocks differ)."""
+    wl = synth.Workload("nan1", T=1, D=1024, F=2048, E=E, k=8, seed=91 + E, shared=True)
+    lay = Layer(wl, quantized=False, experts=range(E))
+    W = lay.upload(ds4)
+    rng = np.random.default_rng(E)
+    for row in _SPECIAL_ROWS:
+        L = np.full((1, E), -np.inf, np.float32)
+        L[0, :8] = row
+        perm = rng.permutation(E)                # the special values at scattered experts
+        lay.L = L[:, np.argsort(perm)]
+        before = ds4.ds4moe_get_stats(W)["launches"]
+        got = lay.run(ds4, W, mode=mode)
+        assert ds4.ds4moe_get_stats(W)["launches"] - before == 1   # the fused kernel ran
+        ref, idx, g = lay.oracle_delta(mode=mode)
+        assert np.all(np.isfinite(g)) and np.all(np.isfinite(got))
+        assert norm_max_err(got, ref) <= FFN_TOL, (row, norm_max_err(got, ref))
+    W.close()
+
+
 def test_single_token_kernel_equals_separate_kernels_and_is_deterministic(ds4):
     import torch
     wl = synth.WORKLOADS["decode_t1"]
@@ -297,37 +353,83 @@ def test_single_token_kernel_equals_separate_kernels_and_is_deterministic(ds4):
 
 # ---------------------------------------------------------------- router logits in front of routing
 
+def _valid_selection(sel, ref, bound):
+    """Whether the expert set sel can be the top-k of some logits within bound of ref: every
+    selected expert's upper end reaches every unselected expert's lower end."""
+    mask = np.zeros(ref.size, bool)
+    mask[sel] = True
+    if mask.all():
+        return True
+    return np.min(ref[mask] + bound[mask]) >= np.max(ref[~mask] - bound[~mask])
+
+
 @pytest.mark.parametrize("T,D,E,bias", [(1, 4096, 256, True), (37, 512, 64, False), (4, 256, 8, True),
                                         (130, 1024, 128, True), (3, 7168, 256, False)])
-def test_router_logits_bitexact_and_the_selection_from_them(ds4, T, D, E, bias):
+def test_router_logits_within_the_fp32_bound_and_the_selection_from_them(ds4, T, D, E, bias):
+    """The device's fp32 logits against the exact (fp64) sum: within the fp32 summation bound.
+    The selection is then exact wherever the k-th and (k+1)-th exact logits are further apart than
+    their bounds allow to swap, and a valid top-k within the bounds elsewhere; the selection from
+    the device's own logits is the oracle's selection from the same fp32 values, bit for bit."""
     import torch
-    from oracle.router import router_logits
+    from oracle.router import fp32_bound, router_logits
     rng = np.random.default_rng(T + D + E)
     x = synth.f32_to_bf16_bits(rng.standard_normal((T, D)).astype(np.float32))
     w = synth.f32_to_bf16_bits((0.02 * rng.standard_normal((E, D))).astype(np.float32))
     b = (0.1 * rng.standard_normal(E)).astype(np.float32) if bias else None
     ref = router_logits(x, w, b)
+    bound = fp32_bound(x, w, b)
     xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     wd = torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16)
     bd = torch.from_numpy(b).cuda() if bias else None
     got = ds4.ds4moe_router_logits(xd, wd, bd)
-    assert np.array_equal(got.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    g = got.cpu().numpy()
+    assert np.all(np.abs(g.astype(np.float64) - ref) <= bound)
     k = min(8, E)
     idx, _ = ds4.ds4moe_route(got, k)
-    ref_idx, _ = oracle.route(ref, k)
-    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    idx = idx.cpu().numpy()
+    assert np.array_equal(idx, oracle.route(g, k)[0])
+    n_exact = 0
+    for t in range(T):
+        o = np.lexsort((np.arange(E), -ref[t]))
+        if k < E and ref[t, o[k - 1]] - ref[t, o[k]] > bound[t, o[k - 1]] + bound[t, o[k]]:
+            assert set(idx[t]) == set(o[:k]), t
+            n_exact += 1
+        assert _valid_selection(idx[t], ref[t], bound[t]), t
+    assert n_exact >= (T + 1) // 2 or k == E
+
+
+def test_router_logits_follow_the_documented_order(ds4):
+    """The library's documented summation order is a property of its kernel: lane 0's columns 0
+    and 1 add 2^30 and -2^30 before any other term, so the 1s that the other 31 lanes carry survive
+    (the logit is exactly 31, the exact sum); an order that adds a 1 to 2^30 first loses it."""
+    import torch
+    D, E = 256, 8
+    x = np.zeros((1, D), np.float32)
+    w = np.zeros((E, D), np.float32)
+    x[0, 0], x[0, 1] = 2.0 ** 15, 2.0 ** 15
+    w[:, 0], w[:, 1] = 2.0 ** 15, -(2.0 ** 15)
+    x[0, 8:D:8] = 1.0
+    w[:, 8:D:8] = 1.0
+    xd = torch.from_numpy(synth.f32_to_bf16_bits(x).view(np.int16)).cuda().view(torch.bfloat16)
+    wd = torch.from_numpy(synth.f32_to_bf16_bits(w).view(np.int16)).cuda().view(torch.bfloat16)
+    got = ds4.ds4moe_router_logits(xd, wd).cpu().numpy()
+    assert np.all(got == 31.0)
 
 
 def test_layer_from_hidden_states(ds4):
     # router in front: the logits come from the router on the device, the oracle takes its own
     import torch
-    from oracle.router import router_logits
+    from oracle.router import fp32_bound, router_logits
     wl = synth.Workload("hid", T=1, D=4096, F=2048, E=256, k=8, seed=41, shared=True)
     rng = np.random.default_rng(41)
     lay = Layer(wl, quantized=False)
     w = synth.f32_to_bf16_bits((0.02 * rng.standard_normal((wl.E, wl.D))).astype(np.float32))
     b = (0.1 * rng.standard_normal(wl.E)).astype(np.float32)
-    lay.L = router_logits(lay.x, w, b)
+    exact = router_logits(lay.x, w, b)
+    lay.L = exact.astype(np.float32)
+    # the selection is unambiguous: the 8th and 9th exact logits lie further apart than the fp32 bound
+    o = np.sort(exact[0])[::-1]
+    assert o[wl.k - 1] - o[wl.k] > 2 * np.max(fp32_bound(lay.x, w, b))
     # the layer's random blobs were made for the experts of the drawn logits: cover these too
     lay.gate, lay.up, lay.down = synth.random_expert_blobs(wl, np.unique(oracle.route(lay.L, wl.k)[0]))
     W = lay.upload(ds4)
