@@ -15,6 +15,9 @@ unquantised); "DwarfStar 深度解析" §2.1 (per-token dynamic expert choice) a
 SwiGLU (silu(gate) * up) is the plain reading of the gate/up pair the pages list; the
 pages do not spell the activation out.
 """
+from concurrent.futures import ThreadPoolExecutor
+import os
+
 import numpy as np
 
 from . import dequant_iq2, dequant_q2k, dequant_q4k, permute, route
@@ -41,7 +44,7 @@ def expert_ffn_dense(x, w_gate, w_up, w_down):
 
 
 def moe_ffn(x_bf16, logits, k, gate_blobs, up_blobs, down_blobs, d_model, d_ff,
-            shared=None, mode=0, tokens=None, fmt="q2"):
+            shared=None, mode=0, tokens=None, fmt="q2", threads=None):
     """Delta added to the residual by one routed-MoE expert FFN.
 
     x_bf16      uint16 [T, D] (bf16 bits);  logits float32 [T, E]
@@ -50,11 +53,13 @@ def moe_ffn(x_bf16, logits, k, gate_blobs, up_blobs, down_blobs, d_model, d_ff,
     fmt:        "q2" (the above) or "q4": all three per-expert blobs Q4_K-style
     shared:     None, or (gate, up, down) bf16 bits of shapes [F, D], [F, D], [D, F]
     tokens:     None for all tokens, or the token ids to evaluate (others are not computed)
+    threads:    experts evaluated at a time (default: the host's cores, at most 16)
 
     Returns (delta float64 [n_tokens, D], idx int32 [T, k], g float64 [T, k]).
     """
     T, E = logits.shape
     D, F = d_model, d_ff
+    threads = threads or min(16, os.cpu_count() or 1)
     idx, g = route(logits, k, mode)
     counts, offsets, perm, _ = permute(idx, E)
     tok = np.arange(T) if tokens is None else np.asarray(tokens, np.int64)
@@ -62,11 +67,13 @@ def moe_ffn(x_bf16, logits, k, gate_blobs, up_blobs, down_blobs, d_model, d_ff,
     x = bf16_to_f64(x_bf16)
 
     y = np.zeros((len(tok), k, D), np.float64)
-    for e in range(E):
+
+    def one_expert(e):
+        """The SwiGLU outputs of expert e for its evaluated pairs (rows, slots, y)."""
         pairs = perm[offsets[e]:offsets[e + 1]]
         pairs = [int(p) for p in pairs if int(p) // k in pos_of]
         if not pairs:
-            continue
+            return None
         if fmt == "q4":
             wg = dequant_q4k(gate_blobs[e], F, D).astype(np.float64)
             wu = dequant_q4k(up_blobs[e], F, D).astype(np.float64)
@@ -77,7 +84,15 @@ def moe_ffn(x_bf16, logits, k, gate_blobs, up_blobs, down_blobs, d_model, d_ff,
             wd = dequant_q2k(down_blobs[e], D, F).astype(np.float64)
         rows = np.array([pos_of[p // k] for p in pairs])
         slots = np.array([p % k for p in pairs])
-        y[rows, slots] = expert_ffn_dense(x[tok[rows]], wg, wu, wd)
+        return rows, slots, expert_ffn_dense(x[tok[rows]], wg, wu, wd)
+
+    # experts are independent: several at a time (threads; the C dequantisers and numpy's
+    # matrix products release the interpreter lock), each written to its own (row, slot) cells
+    with ThreadPoolExecutor(max(1, min(threads, E))) as ex:
+        for res in ex.map(one_expert, range(E)):
+            if res is not None:
+                rows, slots, ye = res
+                y[rows, slots] = ye
 
     delta = np.zeros((len(tok), D), np.float64)
     if shared is not None:

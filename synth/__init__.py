@@ -65,6 +65,10 @@ WORKLOADS = {
         # the 4-bit variant at the decode shape: Q4_K-style gate, up and down
         Workload("decode_t1_q4", T=1, D=4096, F=2048, E=256, k=8, seed=12, fmt="q4"),
         Workload("prefill_t2048_q4", T=2048, D=4096, F=2048, E=256, k=8, seed=13, bias=("zipf", 1.0), fmt="q4"),
+        # a profiling stand-in for the tensor-core kernels at d_model 7168: groups of about a
+        # thousand tokens (mostly full 256-token tiles, as in the large prefill chunk's big
+        # groups) on a device footprint of about 1.5 GB
+        Workload("prefill_t2048_d7168_e16", T=2048, D=7168, F=2048, E=16, k=8, seed=14, bias=("zipf", 1.2)),
     ]
 }
 

@@ -54,6 +54,37 @@ class Layer:
         return out.cpu().numpy()
 
 
+def sample_tokens(L, k, n_pos=64, n_ties=8, gemm_min=7):
+    """Tokens for a sampled full-size parity check, chosen to reach the paths the kernels take:
+    tokens whose pairs sit at n_pos evenly spread column positions of the largest group's 256-token
+    tiles (cycling over its tiles), the first and the last pair of its last (ragged) tile, tokens of
+    four one-token groups, four groups below gemm_min tokens and four groups from gemm_min to 64
+    tokens, and the first n_ties tokens whose top two logits tie."""
+    T, E = L.shape
+    idx, _ = oracle.route(L, k)
+    counts, offsets, perm, _ = oracle.permute(idx, E)
+    big = int(np.argmax(counts))
+    n = int(counts[big])
+    ntile = (n + 255) // 256
+    toks = set()
+    for i, c in enumerate(range(0, 256, max(1, 256 // n_pos))):
+        for j in range(ntile):
+            r = ((i + j) % ntile) * 256 + c
+            if r < n:
+                toks.add(int(perm[offsets[big] + r]) // k)
+                break
+    last0 = (ntile - 1) * 256
+    toks.add(int(perm[offsets[big] + last0]) // k)
+    toks.add(int(perm[offsets[big] + n - 1]) // k)
+    for lo, hi in ((1, 1), (2, gemm_min - 1), (gemm_min, 64)):
+        for e in np.nonzero((counts >= lo) & (counts <= hi))[0][:4]:
+            toks.add(int(perm[offsets[e]]) // k)
+    o = np.argsort(-L, axis=1, kind="stable")
+    tied = np.nonzero(L[np.arange(T), o[:, 0]] == L[np.arange(T), o[:, 1]])[0]
+    toks.update(int(t) for t in tied[:n_ties])
+    return sorted(toks)
+
+
 def norm_max_err(got, ref):
     ref = np.asarray(ref, np.float64)
     return float(np.max(np.abs(np.asarray(got, np.float64) - ref)) / max(np.max(np.abs(ref)), 1e-30))

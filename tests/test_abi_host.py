@@ -123,3 +123,44 @@ def test_device_entry_points_reject_bad_arguments_on_host(ds4):
     assert L.ds4moe_weights_create_pooled(None, 4, None) == ds4.DS4MOE_EINVAL
     assert L.ds4moe_weights_create_pooled(None, 0, None) == ds4.DS4MOE_EINVAL
     assert L.ds4moe_pool_info(None, None, None, None, None) == ds4.DS4MOE_EINVAL
+
+
+def _blobs(wl, fmt="q2"):
+    if fmt == "q4":
+        return [list(b) for b in synth.random_q4_expert_blobs(wl)]
+    return [list(b) for b in synth.random_expert_blobs(wl)]
+
+
+@pytest.mark.parametrize("fmt,mat,byte", [("q2", 0, 0), ("q2", 1, 0), ("q2", 2, 80), ("q2", 2, 82),
+                                          ("q4", 0, 0), ("q4", 2, 2)])
+@pytest.mark.parametrize("bad", [0x7E00, 0x7C00, 0xFC00])   # NaN, +inf, -inf as fp16
+def test_weights_create_rejects_a_non_finite_block_scale_before_any_device_call(ds4, fmt, mat, byte, bad):
+    """A corrupted blob (one block's fp16 d or dmin not finite) is refused with EBADDATA. The check
+    comes before the handle touches the device, so it runs here, without a GPU."""
+    wl = synth.Workload("bad", T=1, D=256, F=512, E=3, k=2, seed=5, shared=False)
+    gate, up, down = _blobs(wl, fmt)
+    mats = [gate, up, down]
+    blk = 144 if fmt == "q4" else (84 if mat == 2 else 66)
+    b = mats[mat][1].copy()
+    at = 5 * blk + byte                       # block 5 of expert 1
+    b[at], b[at + 1] = bad & 0xFF, bad >> 8
+    mats[mat][1] = b
+    with pytest.raises(ds4.Ds4moeError) as ei:
+        ds4.ds4moe_weights_create(gate, up, down, wl.D, wl.F, max_tokens=1, max_k=2, fmt=fmt)
+    assert ei.value.status == ds4.DS4MOE_EBADDATA
+
+
+def test_misaligned_device_pointers_are_refused_on_host(ds4):
+    L = ds4.lib()
+    # router logits: x and the router must be 16-byte aligned, logits and bias 4-byte aligned;
+    # the pointers are never dereferenced when the check fails
+    assert L.ds4moe_router_logits(0x1002, 0x2000, None, 1, 256, 8, 0x3000, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_router_logits(0x1000, 0x2008, None, 1, 256, 8, 0x3000, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_router_logits(0x1000, 0x2000, 0x4002, 1, 256, 8, 0x3000, None) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_router_logits(0x1000, 0x2000, None, 1, 256, 8, 0x3001, None) == ds4.DS4MOE_EINVAL
+
+
+def test_allocation_failure_hook_arguments(ds4):
+    L = ds4.lib()
+    assert L.ds4moe_test_fail_allocation(-1) == ds4.DS4MOE_EINVAL
+    assert L.ds4moe_test_fail_allocation(0) == ds4.DS4MOE_OK

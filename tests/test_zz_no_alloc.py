@@ -3,9 +3,9 @@
 It serves callers that cannot allocate device memory while they run (a plug-in whose host
 framework owns every device allocation, a serving loop that must not call cudaMalloc): its
 intermediates live in the library's static device region. Its output must match the regular
-entry point, ds4moe_expert_ffn, on the same inputs, on two calls in a row (the region keeps
-the previous call's contents, which must not leak into the next result). This file is named
-to be collected last."""
+entry point, ds4moe_expert_ffn, and the oracle, on the same inputs, on two calls in a row (the
+region keeps the previous call's contents, which must not leak into the next result); calls
+beyond the region's size are refused. This file is named to be collected last."""
 import numpy as np
 import pytest
 
@@ -44,12 +44,37 @@ def test_static_entry_matches_expert_ffn(ds4, wl):
     ref = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
     ds4.ds4moe_expert_ffn(x, W, logits, wl.k, ref)
     ref = ref.cpu().numpy()
+    exact, _, _ = lay.oracle_delta()
     for _ in range(2):
         out = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
         ds4.ds4moe_expert_ffn_static(x, W, logits, wl.k, out)
         assert ds4.ds4moe_last_status(W) == 0
-        err = norm_max_err(out.cpu().numpy(), ref)
-        assert err <= FFN_TOL, err
+        got = out.cpu().numpy()
+        assert norm_max_err(got, ref) <= FFN_TOL, norm_max_err(got, ref)      # the regular entry point
+        assert norm_max_err(got, exact) <= FFN_TOL, norm_max_err(got, exact)  # and the oracle itself
+    W.close()
+
+
+def test_static_entry_size_limit_at_d_model_7168(ds4):
+    """At top-8 with d_model 7168 and d_ff 2048 the region holds 9 tokens (9 x 9 rows of
+    (7168 + 2048) fp32 values, 2.99 MB) and not 10 (3.32 MB): 9 runs and matches the oracle, 10 is
+    refused with EINVAL before anything is launched."""
+    import torch
+    wl = synth.Workload("lim", T=10, D=7168, F=2048, E=16, k=8, seed=29, shared=False)
+    lay = Layer(wl, quantized=False)
+    W = lay.upload(ds4)
+    x, logits = _inputs(lay)
+    out = torch.zeros((9, wl.D), dtype=torch.float32, device="cuda")
+    ds4.ds4moe_expert_ffn_static(x[:9], W, logits[:9], wl.k, out)
+    assert ds4.ds4moe_last_status(W) == 0
+    ref, _, _ = lay.oracle_delta(tokens=list(range(9)))
+    assert norm_max_err(out.cpu().numpy(), ref) <= FFN_TOL
+    out10 = torch.zeros((10, wl.D), dtype=torch.float32, device="cuda")
+    with pytest.raises(ds4.Ds4moeError) as ei:
+        ds4.ds4moe_expert_ffn_static(x, W, logits, wl.k, out10)
+    assert ei.value.status == ds4.DS4MOE_EINVAL
+    torch.cuda.synchronize()
+    assert float(out10.abs().max()) == 0.0
     W.close()
 
 
