@@ -3,9 +3,11 @@
 
 A step is one call of ds4moe_expert_ffn over one batch of synthetic input: routing,
 grouping, the SwiGLU experts (packed 2-bit routed experts plus the bf16 shared expert) and
-the gate-weighted combine. The default workload is single-token decode (T=1, d_model 4096,
-d_ff 2048, 256 experts, top-8, bf16 shared expert). Under torchrun every rank runs an
-independent replica (no data-path collective; weak scaling).
+the gate-weighted combine. The default workload is the largest single-GPU configuration, the
+prefill chunk of 8192 tokens (d_model 7168, d_ff 2048, 256 experts, top-8, Zipf s=1.2 routing
+with 5% tied tokens, bf16 shared expert); --workload picks another (decode_t1 is single-token
+decode). Under torchrun every rank runs an independent replica (no data-path collective; weak
+scaling).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -51,7 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_t1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="prefill_t8192_d7168", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--weights", choices=["quantized", "random"], default=None,
                     help="routed-expert blobs: host-quantised N(0,0.02) (default for decode) or random valid blocks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -192,6 +194,24 @@ def small_path(wl):
     return wl.T > 1 and wl.D <= 4096 and wl.F <= 2048 and wl.fmt == "q2"
 
 
+def gemm_rows(wl, counts):
+    """Token rows the tensor-core GEMMs take in one call under the library's default dispatch:
+    the routed groups of at least the threshold's tokens (every expert's weights fit fp16 here),
+    plus the shared expert's T rows from 2 tokens on (its gate/up on the warp-MMA kernel up to
+    48 tokens: (routed rows, shared rows of the up GEMM, shared rows of the down GEMM))."""
+    T = wl.T
+    if wl.fmt == "q4":
+        gm = 0 if T <= 64 else 2
+    elif small_path(wl):
+        gm = 0 if T <= 64 else 7
+    else:
+        gm = 2
+    routed = int(counts[counts >= gm].sum()) if gm > 0 and T >= gm else 0
+    sh_down = T if wl.shared and T >= 2 else 0
+    sh_up = 0 if small_path(wl) and T <= 48 else sh_down
+    return routed, sh_up, sh_down
+
+
 def algorithmic(wl, counts):
     """Bytes and FLOPs the method must move / compute for one call, per stage."""
     D, F, T, k = wl.D, wl.F, wl.T, wl.k
@@ -210,12 +230,15 @@ def algorithmic(wl, counts):
         n_small, p_small = int(np.count_nonzero(sel)), int(counts[sel].sum())
         up_bytes = n_small * IQ2_PER_EXPERT(D, F) + T * D * 2 + p_small * F * 4
         down_bytes = n_small * Q2K_PER_EXPERT(D, F) + p_small * F * 4 + p_small * D * 4
-    flops_up = 2 * 2 * F * D * rows
-    flops_down = 2 * D * F * rows
+    # the tensor-core stages' FLOPs: the rows those kernels ran, not every pair of the call
+    r_tc, sh_up_tc, sh_down_tc = gemm_rows(wl, counts)
+    flops_up = 2 * 2 * F * D * (r_tc + sh_up_tc)
+    flops_down = 2 * D * F * (r_tc + sh_down_tc)
+    flops_call = 6 * D * F * rows
     act_bytes = T * D * 2 + T * wl.E * 4 + 2 * T * D * 4 + 2 * rows * F * 4   # x, logits, out, h
     return {"touched": touched, "up_bytes": up_bytes, "down_bytes": down_bytes, "act_bytes": act_bytes,
             "total_bytes": touched * (up_per_expert(wl) + down_per_expert(wl)) + sh_up + sh_down,
-            "flops_up": flops_up, "flops_down": flops_down}
+            "flops_up": flops_up, "flops_down": flops_down, "flops_call": flops_call}
 
 
 def src_sha(*names):
@@ -274,6 +297,43 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def default_weights(wl, args):
+    """Routed-expert blobs of a run: host-quantised N(0, 0.02) for decode-sized workloads, random
+    valid blocks (same kernels, same time) for the large ones, unless --weights says otherwise."""
+    return args.weights or ("quantized" if wl.T <= 32 else "random")
+
+
+def config_dict(wl, mode, touched, flush, world, router):
+    """The workload's description in the JSON line (the same for both arms)."""
+    return {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F, "experts": wl.E,
+            "top_k": wl.k, "shared_expert": "bf16" if wl.shared else None,
+            "routed_weights": ("4-bit Q4_K-style gate/up/down, " if wl.fmt == "q4" else
+                               "2-bit IQ2-style gate/up + Q2_K-style down, ") +
+                              ("host-quantised N(0,0.02)" if mode == "quantized" else "random valid blocks"),
+            "experts_touched": touched,
+            "l2": "flushed between steps (write then read 256 MB)" if flush else "working set > 4x L2",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            **({"router": "bf16 [E x D] + fp32 bias, logits computed on the device in front of routing"}
+               if router else {})}
+
+
+def reference_config(args, world):
+    """Our arm's config dict for the reference arm's line, computed on the host: the experts the
+    workload touches come from the oracle's routing of the same logits."""
+    import oracle
+    wl = synth.WORKLOADS[args.workload]
+    if wl.slots:   # the pooled workload's line describes its pool instead; the plain keys are shared
+        return {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F, "experts": wl.E,
+                "top_k": wl.k}
+    L, _ = synth.draw_inputs(wl)
+    idx = oracle.route(L, wl.k)[0]
+    touched = int(np.unique(idx).size)
+    counts = np.bincount(idx.reshape(-1), minlength=wl.E)
+    alg = algorithmic(wl, counts)
+    flush = alg["total_bytes"] < 4 * L2_BYTES
+    return config_dict(wl, default_weights(wl, args), touched, flush, world, args.router)
+
+
 # ------------------------------------------------------------------ our arm
 
 def capture(fn):
@@ -305,7 +365,7 @@ def run_ours(args):
         wl = wl.replace(seed=wl.seed + 1000 * rank)   # each replica its own batch
     if wl.slots:
         return run_pooled(args, wl)
-    mode = args.weights or ("quantized" if wl.T <= 32 else "random")
+    mode = default_weights(wl, args)
     L, x = synth.draw_inputs(wl)
     xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     if args.router:
@@ -461,17 +521,10 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": max_ms / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F, "experts": wl.E,
-                       "top_k": wl.k, "shared_expert": "bf16" if wl.shared else None,
-                       "routed_weights": ("4-bit Q4_K-style gate/up/down, " if wl.fmt == "q4" else
-                                          "2-bit IQ2-style gate/up + Q2_K-style down, ") +
-                                         ("host-quantised N(0,0.02)" if mode == "quantized" else "random valid blocks"),
-                       "experts_touched": alg["touched"],
-                       "l2": "flushed between steps (write then read 256 MB)" if flush else "working set > 4x L2",
-                       "parallelism": "replicas" if world > 1 else "single GPU",
-                       **({"router": "bf16 [E x D] + fp32 bias, logits computed on the device in front of routing"}
-                          if args.router else {})},
+            "scaling": "weak", "vs_baseline": None,
+            # the arithmetic of the dominant stage: fp16 tensor-core operands (fp32 accumulate), or fp32
+            "dtype": "f16" if roof["bound"] == "tensor" else "f32", "data": "synthetic",
+            "config": config_dict(wl, mode, alg["touched"], flush, world, args.router),
             "gpu_launches": int(launches),
             "e2e": {"value": whole_job_rate(K * wl.T, world, e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -677,7 +730,7 @@ def cpu_worker(workload, seconds):
         blobs = synth.random_q4_expert_blobs if wl.fmt == "q4" else synth.random_expert_blobs
         gate, up, down = blobs(wl, np.unique(idx))
         t1 = time.perf_counter()
-        oracle.moe_ffn(x[toks], L[toks], wl.k, gate, up, down, wl.D, wl.F, shared=sh, fmt=wl.fmt)
+        oracle.moe_ffn(x[toks], L[toks], wl.k, gate, up, down, wl.D, wl.F, shared=sh, fmt=wl.fmt, threads=1)
         el += time.perf_counter() - t1
         n_tok += len(toks)
         calls += 1
@@ -697,8 +750,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": (1e3 * wl.T / v) if v else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F,
-                                            "experts": wl.E, "top_k": wl.k},
+            "data": "synthetic", "config": reference_config(args, world),
             "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                         "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

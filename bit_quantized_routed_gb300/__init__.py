@@ -39,7 +39,7 @@ EXPORTED = [
     "ds4moe_dequantize_iq2", "ds4moe_dequantize_q4k",
     "ds4moe_weights_create", "ds4moe_weights_create_q4", "ds4moe_weights_create_pooled", "ds4moe_pool_info", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
     "ds4moe_router_logits", "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
-    "ds4moe_expert_ffn_static", "ds4moe_step_trace",
+    "ds4moe_expert_ffn_static", "ds4moe_step_trace", "ds4moe_test_fail_allocation",
 ]
 
 
@@ -103,6 +103,7 @@ def lib():
             "ds4moe_last_status": ([vp, vp], i32),
             "ds4moe_expert_ffn_static": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
             "ds4moe_step_trace": ([vp, vp, i32, ctypes.POINTER(i32)], i32),
+            "ds4moe_test_fail_allocation": ([i32], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -115,6 +116,11 @@ def lib():
 def _check(rc, where):
     if rc != DS4MOE_OK:
         raise Ds4moeError(rc, where)
+
+
+def ds4moe_test_fail_allocation(n):
+    """Test hook: the n-th device allocation of any later handle creation fails (0: off)."""
+    _check(lib().ds4moe_test_fail_allocation(int(n)), "ds4moe_test_fail_allocation")
 
 
 def ds4moe_strerror(status):

@@ -1,8 +1,10 @@
 // The C ABI: weights handle (validation, repack, upload, workspace), the device entry points
 // and their launch sequence. Arguments are checked here, on the host, before any launch.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -17,10 +19,21 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Test hook (ds4moe_test_fail_allocation): the n-th device allocation from now fails.
+std::atomic<int> g_fail_countdown{0};
+
+bool forced_failure() {
+    int n = g_fail_countdown.load();
+    while (n > 0 && !g_fail_countdown.compare_exchange_weak(n, n - 1)) {
+    }
+    return n == 1;
+}
+
 template <class T>
 int dev_alloc(ds4moe_weights *h, T **p, size_t bytes) {
     *p = nullptr;
     if (h->n_allocs >= static_cast<int>(sizeof(h->allocs) / sizeof(h->allocs[0]))) return DS4MOE_ENOMEM;
+    if (forced_failure()) return DS4MOE_ENOMEM;
     void *q = nullptr;
     if (cudaMalloc(&q, bytes ? bytes : 16) != cudaSuccess) {
         cudaGetLastError();
@@ -129,17 +142,61 @@ uint16_t bf16_to_f16(uint16_t b) {
     return static_cast<uint16_t>(sign | h);
 }
 
+// Every block of a handle's blobs must have finite fp16 scales; checked before anything is
+// allocated, so a rejected blob costs no device call.
+bool blobs_valid(const ds4moe_weights_desc *desc, int fmt) {
+    const size_t nb_up = static_cast<size_t>(desc->d_ff) * (desc->d_model / 256);
+    const size_t nb_down = static_cast<size_t>(desc->d_model) * (desc->d_ff / 256);
+    auto ok = [](const uint8_t *blk, int at) {
+        return host_f16_finite(static_cast<uint16_t>(blk[at] | (blk[at + 1] << 8)));
+    };
+    for (int e = 0; e < desc->n_experts; e++) {
+        const uint8_t *mats[3] = {static_cast<const uint8_t *>(desc->gate_iq2[e]),
+                                  static_cast<const uint8_t *>(desc->up_iq2[e]),
+                                  static_cast<const uint8_t *>(desc->down_q2k[e])};
+        for (int m = 0; m < 3; m++) {
+            const size_t nb = m < 2 ? nb_up : nb_down;
+            for (size_t b = 0; b < nb; b++) {
+                if (fmt == 1) {  // Q4_K-style: d, dmin at bytes 0 and 2 of 144
+                    const uint8_t *blk = mats[m] + b * 144;
+                    if (!ok(blk, 0) || !ok(blk, 2)) return false;
+                } else if (m < 2) {  // IQ2-style: d at byte 0 of 66
+                    if (!ok(mats[m] + b * 66, 0)) return false;
+                } else {  // Q2_K-style: d, dmin at bytes 80 and 82 of 84
+                    const uint8_t *blk = mats[m] + b * 84;
+                    if (!ok(blk, 80) || !ok(blk, 82)) return false;
+                }
+            }
+        }
+    }
+    return true;
+}
+
 // Counts launches per stage and, when profiling, records an event at each stage start and
-// one at the end of the call, all on the call's stream.
+// one at the end of the call, all on the call's stream. Each stage is also an NVTX range
+// ("ds4moe:<stage>") on the host thread that issues its launches, for timeline tools.
+const char *const kStageNames[DS4MOE_N_STAGES] = {
+    "ds4moe:route", "ds4moe:group", "ds4moe:gather", "ds4moe:up_gemv", "ds4moe:up_gemm",
+    "ds4moe:down_gemv", "ds4moe:down_gemm", "ds4moe:combine", "ds4moe:step", "ds4moe:pool"};
+
 struct StageClock {
     ds4moe_weights *h;
     cudaStream_t s;
+    bool range_open = false;
     StageClock(ds4moe_weights *h_, ds4moe_stream_t s_) : h(h_), s(s_) {
         for (bool &r : h->stage_ran) r = false;
         h->events_recorded = false;
         h->n_stage_order = 0;
     }
+    ~StageClock() { close_range(); }
+    void close_range() {
+        if (range_open) nvtxRangePop();
+        range_open = false;
+    }
     int stage(int i) {
+        close_range();
+        nvtxRangePushA(kStageNames[i]);
+        range_open = true;
         h->stage_ran[i] = true;
         h->stage_order[h->n_stage_order++] = i;
         h->launches++;
@@ -147,6 +204,7 @@ struct StageClock {
         return static_cast<int>(cudaEventRecord(static_cast<cudaEvent_t>(h->events[i]), s));
     }
     int finish() {
+        close_range();
         if (!h->profile) return 0;
         h->events_recorded = true;
         return static_cast<int>(cudaEventRecord(static_cast<cudaEvent_t>(h->events[DS4MOE_N_STAGES]), s));
@@ -177,6 +235,7 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds
     if (n_shared != 0 && n_shared != 3) return DS4MOE_EINVAL;
     const int64_t P = static_cast<int64_t>(desc->max_tokens) * desc->max_k;
     if (P > (int64_t(1) << 30)) return DS4MOE_EINVAL;
+    if (!blobs_valid(desc, fmt)) return DS4MOE_EBADDATA;
 
     ds4moe_weights *h = new (std::nothrow) ds4moe_weights();
     if (!h) return DS4MOE_ENOMEM;
@@ -378,6 +437,12 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds
 }
 
 int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out) { return create_impl(desc, 0, 0, out); }
+
+int ds4moe_test_fail_allocation(int n) {
+    if (n < 0) return DS4MOE_EINVAL;
+    g_fail_countdown.store(n);
+    return DS4MOE_OK;
+}
 
 int ds4moe_weights_create_q4(const ds4moe_weights_desc *desc, ds4moe_weights **out) { return create_impl(desc, 0, 1, out); }
 

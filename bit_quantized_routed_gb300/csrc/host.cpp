@@ -1,10 +1,11 @@
 // Host side of the library: status strings, the IQ2-style grid, binary16 rounding, the
 // two quantisers and host dequantisers. No CUDA here.
 //
-// The formats and quantisers are the ones FORMAT.md freezes (the pages -- "DwarfStar"
-// README, "模型权重" -- name IQ2_XXS for up/gate and Q2_K for down but print no layout).
-// Every floating-point step follows FORMAT.md's order with no fused multiply-add (this file
-// is compiled with -ffp-contract=off), so the bytes are reproducible across machines.
+// The formats and quantisers are the library's own fixed layouts and rules (the pages --
+// "DwarfStar" README, "模型权重" -- name IQ2_XXS for up/gate and Q2_K for down but print no
+// layout). Every floating-point step follows the quantisers' written order with no fused
+// multiply-add (this file is compiled with -ffp-contract=off), so the bytes are reproducible
+// across machines.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -89,7 +90,7 @@ struct Grid {
     double gt[8][256];  // transposed as doubles, for the search
     double norm2[256];
     Grid() {
-        uint64_t state = 0x6473346D6F654951ull;  // FORMAT.md seed
+        uint64_t state = 0x6473346D6F654951ull;  // the grid's fixed seed
         auto next = [&state]() {
             // splitmix64: Weyl step by the 64-bit golden ratio, then the variant-13 mix
             state += 0x9E3779B97F4A7C15ull;

@@ -11,8 +11,9 @@
  * unquantised); "DwarfStar 深度解析" §2.1 (per-token dynamic expert choice, irregular
  * compute) and §3.4.3 (the quantisation split, the router kept at full precision);
  * "Part 5: 服务层" §6 "会话批处理" (several sessions' decode steps in one batched kernel).
- * The block layouts are this library's own IQ2-style and Q2_K-style formats, frozen in
- * FORMAT.md (the pages name the formats but print no layout).
+ * The block layouts are this library's own IQ2-style, Q2_K-style and Q4_K-style formats
+ * (the pages name the formats but print no layout; the library's format notes fix them).
+ * Where a declaration below says "library reading", the pages are silent on that point.
  *
  * Conventions.
  *   - Every function returns a status (DS4MOE_OK = 0) and never throws or aborts.
@@ -50,9 +51,14 @@ enum ds4moe_status {
     DS4MOE_ECAPACITY = 8     /* a call touched more experts than a pooled handle's slots */
 };
 
+/* Gate weights over the k selected logits l_0 >= ... >= l_{k-1} (a NaN logit counts as -inf).
+ * Library reading of "DwarfStar 深度解析" §2.1 (the pages name no gate function): a term whose
+ * logit equals l_0 counts as exp(0) = 1 also when both are infinite (the limit of equal logits),
+ * so an all -inf selection gets 1/k each and a +inf logit takes the weight of every finite one. */
 enum ds4moe_gate_mode {
     DS4MOE_GATE_SOFTMAX = 0, /* g_s = exp(l_s - l_0) / sum_j exp(l_j - l_0) over the k selected */
-    DS4MOE_GATE_SIGMOID = 1  /* g_s = sigmoid(l_s) / sum_j sigmoid(l_j) over the k selected */
+    DS4MOE_GATE_SIGMOID = 1  /* g_s = sigmoid(l_s) / sum_j sigmoid(l_j) over the k selected,
+                                evaluated as the softmax rule over log sigmoid(l_s) (same ratio) */
 };
 
 /* Matrices of one expert, for ds4moe_weights_dequantize(). */
@@ -112,34 +118,42 @@ typedef struct {
                                         the stage did not run or profiling is off */
 } ds4moe_stats;
 
-/* Human-readable text of a status code (static storage). */
+/* Human-readable text of a status code (static storage). Library reading, no passage. */
 const char *ds4moe_strerror(int status);
 
 /* ------------------------------------------------------------------ host: formats */
 
 /* Bytes of a packed [rows x cols] matrix: rows * cols/256 * 84 (Q2_K-style) or * 66
- * (IQ2-style). 0 if rows < 0, cols <= 0 or cols % 256 != 0. */
+ * (IQ2-style). 0 if rows < 0, cols <= 0 or cols % 256 != 0. The block sizes follow the formats
+ * the pages name ("DwarfStar" README, "模型权重": Q2_K and IQ2_XXS, 256-weight super-blocks);
+ * the exact byte counts are the library's layouts (library reading). */
 size_t ds4moe_q2k_bytes(int64_t rows, int64_t cols);
 size_t ds4moe_iq2_bytes(int64_t rows, int64_t cols);
-/* The 4-bit variant's Q4_K-style blocks (FORMAT.md): rows * cols/256 * 144 bytes. */
+/* The 4-bit variant's Q4_K-style blocks ("DwarfStar" README, "模型权重": the q4 build; the
+ * 144-byte layout is the library's reading): rows * cols/256 * 144 bytes. */
 size_t ds4moe_q4k_bytes(int64_t rows, int64_t cols);
 
-/* The IQ2-style grid (FORMAT.md): 256 entries x 8 magnitudes, entry-major, into out[2048]. */
+/* The IQ2-style grid: 256 entries x 8 magnitudes in {1, 3, 5, 7}, entry-major, into out[2048]
+ * (entry 0 all ones, the rest drawn by splitmix64 from the library's fixed seed; library reading
+ * of the codebook format the pages name in "DwarfStar" README, "模型权重"). */
 int ds4moe_iq2_grid(uint8_t *out);
 
 /* Quantise a row-major fp32 matrix w [rows x cols] (cols % 256 == 0) into dst (dst_bytes
- * at least the size above) following FORMAT.md's quantisers; the output is byte-identical
- * to any implementation that follows them. Runs on all host cores.
- * EINVAL: bad sizes or null pointers; EBADDATA: a non-finite weight or an fp16 scale
- * overflow (dst is then unspecified). Source: "DwarfStar" README, "模型权重" (up/gate in
- * IQ2_XXS, down in Q2_K); the quantiser itself is FORMAT.md's reading. */
+ * at least the size above) with the library's quantisers (plain min/max affine for the Q2_K-style
+ * blocks; an exhaustive scale and grid search for the IQ2-style blocks; fp64 decisions, ties to
+ * the lowest index); the output is byte-identical to any implementation that follows them. Runs
+ * on all host cores. EINVAL: bad sizes or null pointers; EBADDATA: a non-finite weight or an fp16
+ * scale overflow (dst is then unspecified). Source: "DwarfStar" README, "模型权重" (up/gate in
+ * IQ2_XXS, down in Q2_K); the quantisers themselves are the library's reading. */
 int ds4moe_quantize_q2k(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
 int ds4moe_quantize_iq2(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
 /* The 4-bit variant ("DwarfStar" README, "模型权重": the q4 build keeps every routed-expert
- * projection in 4 bits; the block layout and quantiser are FORMAT.md's Q4_K-style reading). */
+ * projection in 4 bits; the Q4_K-style block layout and its min/max quantiser are the library's
+ * reading). */
 int ds4moe_quantize_q4k(const float *w, int64_t rows, int64_t cols, void *dst, size_t dst_bytes);
 
-/* Host dequantisation to fp32 (the exact values of FORMAT.md), for tests and tools. */
+/* Host dequantisation to fp32 (each weight's exact value in the library's formats), for tests
+ * and tools. Library reading of the formats named in "DwarfStar" README, "模型权重". */
 int ds4moe_dequantize_q2k(const void *src, int64_t rows, int64_t cols, float *dst);
 int ds4moe_dequantize_iq2(const void *src, int64_t rows, int64_t cols, float *dst);
 int ds4moe_dequantize_q4k(const void *src, int64_t rows, int64_t cols, float *dst);
@@ -167,9 +181,12 @@ typedef struct {
     int max_k;      /* largest k of any later call, 1..min(32, n_experts) */
 } ds4moe_weights_desc;
 
-/* Create a handle on the current CUDA device: validates the blobs (finite fp16 scales),
- * repacks them into the device layout, uploads them and allocates the workspace for
- * max_tokens x max_k pairs. Synchronous. EBADDATA names a non-finite fp16 scale. */
+/* Create a handle on the current CUDA device: validates the blobs (finite fp16 scales, before
+ * any device call), repacks them into the device layout, uploads them and allocates the
+ * workspace for max_tokens x max_k pairs. Synchronous. EBADDATA names a non-finite fp16 scale;
+ * ENOMEM a failed device allocation (nothing is kept). Source: "DwarfStar" README, "模型权重" (the
+ * routed experts are held quantised, the shared expert unquantised); holding them resident in
+ * device memory, the layout and the workspace are the library's reading. */
 int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out);
 
 /* A handle of the 4-bit variant: the three per-expert pointers of desc hold Q4_K-style blobs
@@ -178,7 +195,8 @@ int ds4moe_weights_create(const ds4moe_weights_desc *desc, ds4moe_weights **out)
  * more tokens on the tensor-core kernels (not on the fused single-token or the small-group
  * kernels); the bf16 shared expert keeps its usual kernels.
  * ds4moe_weights_dequantize gives their fp32 values (dst_f16 is EUNSUPPORTED);
- * ds4moe_expert_ffn_static is EUNSUPPORTED for them. Otherwise as ds4moe_weights_create. */
+ * ds4moe_expert_ffn_static is EUNSUPPORTED for them. Otherwise as ds4moe_weights_create.
+ * Source: "DwarfStar" README, "模型权重" (the q4 build, and the q2-q4 mix). */
 int ds4moe_weights_create_q4(const ds4moe_weights_desc *desc, ds4moe_weights **out);
 
 /* A handle whose routed experts stream from host memory into a pool of n_slots expert slots
@@ -191,8 +209,9 @@ int ds4moe_weights_create_q4(const ds4moe_weights_desc *desc, ds4moe_weights **o
  *     each missing expert, in increasing expert order, takes the slot not used by this call
  *     that was used least recently (empty slots first, then the oldest last use, ties to the
  *     lower slot), evicting its expert, and is copied in (a miss);
- *   - the experts then run on the same kernels as a resident handle's (not the fused
- *     single-token kernel), with results identical bit for bit to a resident handle's.
+ *   - the experts then run on the same kernels as a resident handle's, over slot indices
+ *     (a call of one token on the fused single-token kernel, through its expert-to-slot
+ *     map), with results identical bit for bit to a resident handle's.
  * A call that touches more than n_slots experts records DS4MOE_ECAPACITY in the status word
  * (ds4moe_last_status), changes no slot and leaves out unspecified.
  * max_k <= n_slots <= n_experts. Other arguments and errors as ds4moe_weights_create. */
@@ -200,18 +219,29 @@ int ds4moe_weights_create_pooled(const ds4moe_weights_desc *desc, int n_slots, d
 
 /* Pool state of a pooled handle (synchronises the device): its slot count, the hits and
  * misses since creation, and (slot_expert: n_slots ints, may be NULL) the expert held by each
- * slot or -1. Any output pointer may be NULL. EINVAL for a handle that is not pooled. */
+ * slot or -1. Any output pointer may be NULL. EINVAL for a handle that is not pooled.
+ * Library reading, no passage (a diagnostic of the streamed-expert pool above). */
 int ds4moe_pool_info(ds4moe_weights *w, int *n_slots, uint64_t *hits, uint64_t *misses, int32_t *slot_expert);
 
-/* Free a handle (NULL is allowed). Synchronises the device first. */
+/* Test hook for failure handling: the n-th device allocation that any handle creation makes from
+ * now on fails as if the device were out of memory (the creation then returns DS4MOE_ENOMEM and
+ * frees what it had allocated); n = 0 turns the hook off. Process-wide. EINVAL for n < 0.
+ * Library reading, no passage. */
+int ds4moe_test_fail_allocation(int n);
+
+/* Free a handle (NULL is allowed). Synchronises the device first. Library reading, no passage. */
 void ds4moe_weights_destroy(ds4moe_weights *w);
 
+/* Set one of the options above on a handle. EINVAL for an unknown option or a negative value
+ * (except -1 for DS4MOE_OPT_GEMM_MIN_TOKENS). Library reading, no passage. */
 int ds4moe_set_option(ds4moe_weights *w, int option, int value);
 
 /* Dequantise one resident expert matrix on the device, through the device decode the
  * kernels use: fp32 values (the GEMV path's weights) into dst_f32 (rows*cols floats, may be
  * NULL), and into dst_f16 (may be NULL) the fp16 operand bytes exactly as the tensor-core
- * producers write them, which are RN-even of the fp32 values. Asynchronous. */
+ * producers write them, which are RN-even of the fp32 values. Asynchronous. EINVAL for a bad
+ * expert or matrix or two NULL outputs; EUNSUPPORTED for a pooled handle. A test entry point:
+ * library reading, no passage (the formats it decodes: "DwarfStar" README, "模型权重"). */
 int ds4moe_weights_dequantize(const ds4moe_weights *w, int expert, int matrix, float *dst_f32,
                               uint16_t *dst_f16, ds4moe_stream_t stream);
 
@@ -244,33 +274,46 @@ int ds4moe_route(const float *logits, int T, int E, int k, int gate_mode, int32_
 /* Group the T*k (token, slot) pairs by expert: a stable counting sort in (token, slot)
  * order. counts int32 [E]; offsets int32 [E+1] (exclusive scan, offsets[E] = T*k);
  * perm int32 [T*k] (pair id t*k+s at each grouped position); inv int32 [T*k] (grouped
- * position of pair t*k+s). Deterministic. */
+ * position of pair t*k+s). Deterministic. An index outside [0, E) is grouped as expert 0 (inside
+ * ds4moe_expert_ffn it is also recorded, and ds4moe_last_status reports EINVAL). Device pointers,
+ * asynchronous; EINVAL for bad sizes or null pointers. Source: "Part 5: 服务层" §6 "会话批处理"
+ * (read-only weight work done once for the whole batch: each expert's tokens gathered so its
+ * weights stream once) and "DwarfStar 深度解析" §2.1 (per-token expert choice makes MoE compute
+ * irregular); the stable order is the library's reading. */
 int ds4moe_group(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
                  int32_t *perm, int32_t *inv, ds4moe_stream_t stream);
 
 /* The expert FFN: out[t] += y_shared[t] + sum_s g[t,s] * y_{idx[t,s]}(x[t]), for t < T.
- *   x       bf16 [T x d_model], 16-byte aligned;
- *   logits  fp32 [T x n_experts] (router logits, bias already added);
- *   out     fp32 [T x d_model] residual, updated in place, 16-byte aligned.
+ *   x         bf16 [T x d_model], 16-byte aligned;
+ *   logits    fp32 [T x n_experts] (router logits, bias already added);
+ *   gate_mode DS4MOE_GATE_SOFTMAX or DS4MOE_GATE_SIGMOID (above);
+ *   out       fp32 [T x d_model] residual, updated in place, 16-byte aligned.
  * Routing, grouping, the SwiGLU experts and the combine all run on the device with no
  * host synchronisation; results are bit-reproducible run to run. T <= max_tokens and
- * k <= max_k of the handle. EINVAL on bad arguments; device-side errors (ERANGE, ...)
- * are reported by ds4moe_last_status(). */
+ * k <= max_k of the handle. EINVAL on bad arguments; device-side errors (ERANGE: a token, an h
+ * or a y value beyond the fp16 range of the tensor-core path; ...) are reported by
+ * ds4moe_last_status(). Source: "DwarfStar" README, "模型权重" (routed up/gate in IQ2_XXS, down
+ * in Q2_K, the shared expert unquantised) and "DwarfStar 深度解析" §2.1 and §3.4.3 (the routed
+ * MoE layer and its expert tree). Library readings: T added to the signature, gate_mode (the
+ * pages name no gate function), SwiGLU as the activation, the shared expert at weight 1, and out
+ * an fp32 residual updated in place. */
 int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *w, const float *logits, int T, int k,
                       int gate_mode, float *out, ds4moe_stream_t stream);
 
 /* Counters of the handle, and (when DS4MOE_OPT_PROFILE is on) the per-stage device times of
- * the last call, read from its CUDA events (waits for them). */
+ * the last call, read from its CUDA events (waits for them). Library reading, no passage. */
 int ds4moe_get_stats(ds4moe_weights *w, ds4moe_stats *out);
 
-/* Diagnostics of the single-token kernel (with DS4MOE_OPT_TRACE on): synchronises the device
+/* Diagnostics of the single-token kernel (with DS4MOE_OPT_TRACE on; library reading, no
+ * passage): synchronises the device
  * and copies up to max_values timestamps of the last call into out: per CTA six globaltimer
  * values in ns -- start, prologue done, gate/up phase done, grid barrier passed, h staged,
  * down phase done. *n_values receives the number copied (6 per CTA). */
 int ds4moe_step_trace(ds4moe_weights *w, uint64_t *out, int max_values, int *n_values);
 
 /* Synchronise the stream, then return and clear the handle's device status word
- * (DS4MOE_OK when no kernel reported an error since the last call). */
+ * (DS4MOE_OK when no kernel reported an error since the last call). Library reading, no
+ * passage (how device-side errors reach the host). */
 int ds4moe_last_status(ds4moe_weights *w, ds4moe_stream_t stream);
 
 /* The expert FFN without any device allocation, for callers that cannot allocate device
@@ -286,10 +329,12 @@ int ds4moe_last_status(ds4moe_weights *w, ds4moe_stream_t stream);
  * grouping, h and y) live in one static 3 MiB region of device memory that every GPU which
  * loads the library holds until the process exits; the handle's own workspace is not used,
  * so T and k are not limited by the handle's max_tokens and max_k, only by the region:
- * calls needing more than 3 MiB (about T*(k+1)*(d_model + d_ff)*4 bytes, e.g. more than 8
+ * calls needing more than 3 MiB (about T*(k+1)*(d_model + d_ff)*4 bytes, e.g. more than 9
  * tokens at top-8 with d_model 7168 and d_ff 2048) return DS4MOE_EINVAL without launching.
  * The current device must be the handle's. The first call on a device looks up the region's
- * device address (cudaGetSymbolAddress); make that first call before any stream capture.
+ * device address (cudaGetSymbolAddress) and keeps it for the life of the process; make that
+ * first call before any stream capture. The kept address does not survive a reset of the device
+ * (cudaDeviceReset): after one, this entry point must not be called again in that process.
  * All calls share the region: calls that overlap on the GPU (other streams, other threads,
  * other handles) race and must be ordered by the caller. Device-side errors are reported
  * through the handle, by ds4moe_last_status(). Nothing here calls cudaMalloc or cudaFree. */

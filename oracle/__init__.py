@@ -11,7 +11,7 @@ Sources (page titles and sections):
     IQ2_XXS and down to Q2_K; shared expert, projections and router stay unquantised.
   * "DwarfStar 深度解析", §2.1 (routed MoE: the experts a token uses are chosen per token)
     and §3.4.3 (the quantisation split; the router stays at full precision).
-  * The byte layouts, the grid and the quantisers are readings fixed in FORMAT.md, including
+  * The byte layouts, the grid and the quantisers are the library's fixed readings, including
     the Q4_K-style block of the 4-bit variant ("DwarfStar" README, "模型权重": the q4 build).
 
 Parity pins: every function here is checked in ``tests/test_oracle_*.py`` against something
@@ -101,7 +101,7 @@ _grid = None
 
 
 def iq2_grid():
-    """The 256 x 8 grid of magnitudes (uint8), built from the seed in FORMAT.md."""
+    """The 256 x 8 grid of magnitudes (uint8), built by splitmix64 from the grid's fixed seed."""
     global _grid
     if _grid is None:
         g = np.zeros(2048, np.uint8)
@@ -121,7 +121,7 @@ def quantize_q2k(w):
 
 
 def quantize_q4k(w):
-    """FORMAT.md's Q4_K-style quantiser (the 4-bit variant) of fp32 [rows, cols]."""
+    """The Q4_K-style quantiser (the 4-bit variant) of fp32 [rows, cols]."""
     w = np.ascontiguousarray(w, np.float32)
     rows, cols = w.shape
     assert cols % 256 == 0

@@ -10,8 +10,8 @@
  * Sources. "DwarfStar" (the ds4 README), section "模型权重": only the routed experts are
  * quantised, up/gate to IQ2_XXS and down to Q2_K; shared expert, projections and router
  * stay unquantised. "DwarfStar 深度解析" §3.4.3 draws the same split. The pages name the
- * formats but print no table; the byte layouts, the grid and the quantisers follow the
- * repository's FORMAT.md, which fixes them (every choice there is a reading, not a page fact).
+ * formats but print no table; the byte layouts, the grid and the quantisers here are the
+ * library's fixed readings (every such choice is a reading, not a page fact).
  *
  * Numerics. Every decision is an fp64 operation in the written order. Build with
  * -ffp-contract=off so that no multiply-add is fused.
@@ -162,7 +162,7 @@ static void q4k_scale_min(const uint8_t *blk, int j, int *sc, int *m) {
     *m = (lo >> 4) | ((hi >> 2) << 4);
 }
 
-/* Quantise 256 weights into one 144-byte block (FORMAT.md, Q4_K-style). Returns 0, or -1 on
+/* Quantise 256 weights into one 144-byte Q4_K-style block (the 4-bit variant's layout). Returns 0, or -1 on
  * non-finite input or an fp16 overflow of d/dmin. */
 int or_q4k_quantize_block(const float *w, uint8_t *out) {
     double a[8], b[8];
