@@ -594,8 +594,10 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     const bool sg_fits = !q4 && h->small_groups && small_groups_supported(w);
     // (the 4-bit variant has no small-group kernels: from 2 tokens its groups are cheaper on the
     // tensor cores than on the GEMV, measured on prefill_t2048_q4)
+    // (without the small-group kernels, above 64 tokens even one-token groups are cheaper on the
+    // tensor cores than on the single-token decode kernels: prefill_t8192_d7168 has ~30 of them)
     const int gm = h->gemm_min_tokens >= 0 ? h->gemm_min_tokens
-                   : q4 ? (T <= 64 ? 0 : 2) : sg_fits ? (T <= 64 ? 0 : 7) : 2;
+                   : q4 ? (T <= 64 ? 0 : 2) : sg_fits ? (T <= 64 ? 0 : 7) : (T <= 64 ? 2 : 1);
     const int gemm_min = (gm > 0 && T >= gm) ? gm : 0;
     const bool shared_tc = w.has_shared && w.shared_tc_ok && h->shared_gemm_min_tokens > 0 &&
                            T >= h->shared_gemm_min_tokens;
@@ -629,7 +631,12 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     // (the 4-bit variant takes its shared expert into the GEMV launches at every T)
     const bool shared_single = w.has_shared && !shared_tc && T == 1 && !q4;
     const bool shared_multi = w.has_shared && !shared_tc && (T > 1 || q4);
-    if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMV);
+    // (with a threshold of 1 every routed group is on the tensor cores: no one-token groups)
+    const bool decode_kernels = !sg && !q4 && (gemm_min != 1 || shared_single);
+    if (sg || q4 || decode_kernels || multi_gemv || shared_multi) {
+        if (!rc) rc = clk.stage(DS4MOE_STAGE_UP_GEMV);
+        if (!sg && !q4 && !decode_kernels) h->launches--;  // the stage's kernel is the GEMV below
+    }
     if (sg) {
         if (!rc) rc = launch_prep_x(ws, x, T, w.D, stream);
         if (!rc) rc = launch_small_up(w, ws, T, k, stream);
@@ -638,9 +645,9 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
             if (!rc) rc = launch_decode_up(w, ws, x, T, k, true, stream);
             h->launches++;
         }
-    } else if (!q4) {
+    } else if (decode_kernels) {
         if (!rc) rc = launch_decode_up(w, ws, x, T, k, shared_single, stream);
-    } else {  // the 4-bit variant: the tokens as int16 dp2a pairs for its GEMV
+    } else if (q4) {  // the 4-bit variant: the tokens as int16 dp2a pairs for its GEMV
         if (!rc) rc = launch_prep_x(ws, x, T, w.D, stream);
     }
     if (multi_gemv || shared_multi) {
@@ -656,15 +663,19 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
         else h->launches++;
         if (!rc) rc = launch_gemm_up(w, ws, h->tmap_x16, T, k, shared_tc && !shared_up_small, stream);
     }
-    if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMV);
+    if (sg || q4 || decode_kernels || multi_gemv || shared_multi) {
+        if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMV);
+        if (!sg && !q4 && !decode_kernels) h->launches--;  // the stage's kernel is the GEMV below
+    }
     if (sg) {
         if (!rc) rc = launch_small_down(w, ws, T, k, stream);
         if (shared_single) {
             if (!rc) rc = launch_decode_down(w, ws, T, k, true, stream);
             h->launches++;
         }
-    } else if (!q4) {
+    } else if (decode_kernels) {
         if (!rc) rc = launch_decode_down(w, ws, T, k, shared_single, stream);
+    } else if (!q4) {
     } else if (T <= 64) {  // the 4-bit variant: each pair's h as int16 for its down GEMV
         if (!rc) rc = launch_prep_h(ws, T * k, w.F, stream);
     } else {

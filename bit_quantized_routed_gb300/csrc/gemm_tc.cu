@@ -107,29 +107,32 @@ struct Tile {
     int m;       // weight-row tile (128 rows of gate and up for the first GEMM, 256 down rows)
 };
 
-// Tiles t = nt * m_tiles + m: token tile nt (the routed experts' tiles first, in the order of
-// tile_desc, then the shared expert's), weight-row tile m. routed = meta->n_tiles.
+// Tiles t = nt * m_tiles + m: token tile nt, weight-row tile m. The token tiles go longest
+// first: the routed experts' full tiles (tile_desc[0, n_full)), the shared expert's, then the
+// routed ragged tiles by decreasing size (tile_desc[n_full, routed)). routed = meta->n_tiles.
 __device__ __forceinline__ int n_tiles_total(const GemmParams &p, int m_tiles, int routed) {
     const int sh = p.shared ? (p.T + BN - 1) / BN : 0;
     return (routed + sh) * m_tiles;
 }
 
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_tiles, int routed) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int m_tiles, int n_full) {
     Tile ti;
     ti.m = t % m_tiles;
-    const int nt = t / m_tiles;
-    if (nt < routed) {
+    int nt = t / m_tiles;
+    const int sh = p.shared ? (p.T + BN - 1) / BN : 0;
+    if (nt >= n_full && nt < n_full + sh) {
+        const int lt = nt - n_full;
+        ti.shared = 1;
+        ti.e = -1;
+        ti.row0 = p.P + lt * BN;
+        ti.ntok = min(BN, p.T - lt * BN);
+    } else {
+        if (nt >= n_full) nt -= sh;
         const int4 d = __ldg(p.tile_desc + nt);  // expert, first row, tokens
         ti.shared = 0;
         ti.e = d.x;
         ti.row0 = d.y;
         ti.ntok = d.z;
-    } else {
-        const int lt = nt - routed;
-        ti.shared = 1;
-        ti.e = -1;
-        ti.row0 = p.P + lt * BN;
-        ti.ntok = min(BN, p.T - lt * BN);
     }
     return ti;
 }
@@ -428,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     constexpr int MR = KIND == UP ? BM : BM * C::NA;  // weight rows per m-tile
     const int m_tiles = (KIND == UP ? F : D) / MR;
     const int routed = p.meta->n_tiles;
+    const int n_full = p.meta->n_full;
     const int total = n_tiles_total(p, m_tiles, routed);
     if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA, before any allocation
     const int num_kb = (KIND == UP ? D : F) / BK;
@@ -490,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int s = 0; s < S; s++) issued_parity[s] = -1;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = decode_tile(p, t, m_tiles, routed);
+                const Tile ti = decode_tile(p, t, m_tiles, n_full);
                 const int bi = box_index(ti.ntok);
                 const CUtensorMap *map = &maps.m[bi];
                 const uint32_t bytes = static_cast<uint32_t>(16 << bi) * BK * 2;
@@ -519,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = decode_tile(p, t, m_tiles, routed);
+                const Tile ti = decode_tile(p, t, m_tiles, n_full);
                 if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -571,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile ti = decode_tile(p, t, m_tiles, routed);
+            const Tile ti = decode_tile(p, t, m_tiles, n_full);
             const int wrow = ti.m * MR + (KIND == DOWN ? sel * BM : 0) + r;
             if (KIND == UP) {
                 if (ti.shared) {
@@ -703,7 +707,9 @@ __global__ void __launch_bounds__(kProducers) producer_dump_kernel(DeviceWeights
     }
 }
 
-// x (bf16) -> x16 (fp16) for rows of tensor-core groups and of the shared expert.
+// x (bf16) -> x16 (fp16) for rows of tensor-core groups and of the shared expert. One warp per
+// row: lane 0 resolves the row's token (or that the row is not on the tensor cores), then the
+// warp converts the token's D values, 8 per lane and step.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
                                                      const int32_t *__restrict__ topk_idx,
                                                      const int32_t *__restrict__ counts,
@@ -711,28 +717,33 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict_
                                                      int P, int T, int shared, uint16_t *__restrict__ x16,
                                                      int *status) {
     const int D8 = D / 8;
-    const size_t n = static_cast<size_t>(P + T) * D8;
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
     bool range_ok = true;
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const int row = static_cast<int>(i / D8), c = static_cast<int>(i - static_cast<size_t>(row) * D8);
-        int tok;
-        if (row < P) {
-            const int pair = perm[row];
-            const int e = topk_idx[pair];
-            if (gemm_min <= 0 || counts[e] < gemm_min || !tc_ok[e]) continue;
-            tok = pair / k;
-        } else {
-            if (!shared) continue;
-            tok = row - P;
+    for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < P + T; row += warps) {
+        int tok = -1;
+        if (lane == 0) {
+            if (row < P) {
+                const int pair = perm[row];
+                const int e = topk_idx[pair];
+                if (gemm_min > 0 && counts[e] >= gemm_min && tc_ok[e]) tok = pair / k;
+            } else if (shared) {
+                tok = row - P;
+            }
         }
-        const uint4 v = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * D)[c];
-        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        tok = __shfl_sync(0xffffffffu, tok, 0);
+        if (tok < 0) continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * D);
+        uint4 *dst = reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(row) * D);
+#pragma unroll 4
+        for (int c = lane; c < D8; c += 32) {
+            const uint4 v = __ldg(src + c);
+            const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
-        for (int j = 0; j < 8; j++) range_ok &= fabsf(f[j]) <= 65504.0f;
-        reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(row) * D)[c] =
-            make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+            for (int j = 0; j < 8; j++) range_ok &= fabsf(f[j]) <= 65504.0f;
+            dst[c] = make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+        }
     }
     if (!range_ok) report(status, ST_RANGE);
 }
@@ -784,8 +795,7 @@ GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k
 int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, int gemm_min,
                   bool shared, void *stream) {
     const int P = T * k;
-    const size_t n = static_cast<size_t>(P + T) * (w.D / 8);
-    const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, static_cast<size_t>(sm_count_tc()) * 8));
+    const int blocks = std::min((P + T + 7) / 8, sm_count_tc() * 8);  // a warp per row, 8 rows per CTA
     gather_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, ws.perm, ws.topk_idx, ws.counts, w.tc_ok,
                                                                          gemm_min, k, w.D, P, T, shared ? 1 : 0,
                                                                          ws.x16, ws.status);

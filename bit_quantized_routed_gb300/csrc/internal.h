@@ -122,6 +122,8 @@ struct GroupMeta {
     int n_single;  // experts with exactly one token (when split off), listed in single_list
     int n_small_pairs;  // pairs of the gemv_list experts (positions listed in small_pos when requested)
     int n_tiles;   // tensor-core token tiles of the gemm_list experts (ceil(n_e / kGemmBN) each)
+    int n_full;    // of which full (kGemmBN tokens): tile_desc holds them first, then the ragged ones,
+                   // largest first
 };
 
 // Streamed experts (pooled handles): the host store and the slot state. The store holds every
@@ -154,6 +156,7 @@ struct Workspace {
     int32_t *single_list; // [E]
     int32_t *tile_prefix; // [E+1] exclusive prefix of ceil(n_e / kGemmBN) over gemm_list
     int32_t *tile_desc;   // [E + P/kGemmBN][4] per tensor-core token tile: expert, first row, tokens, 0
+                          // (full tiles first, then the ragged ones by decreasing size)
     GroupMeta *meta;
     uint8_t *grid;      // [256][8] IQ2-style grid
     uint8_t *grid_hi;   // [256][8] the grid's magnitudes as fp16 high bytes (1, 3, 5, 7 -> 3C, 42, 45, 47)

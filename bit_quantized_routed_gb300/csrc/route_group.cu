@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     extern __shared__ int sm[];
     int *hist = sm;                      // [kGroupWarps][E]: counts, then base positions
     int *tmp = sm + kGroupWarps * E;     // [32]
+    int *part = tmp + 32;                // [E] tokens of each tensor-core expert's ragged last tile (0: none)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kGroupWarps * E; i += kGroupThreads) hist[i] = 0;
     __syncthreads();
@@ -157,6 +158,18 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     const int ps = block_exclusive_scan(small ? 1 : 0, tmp, &n_small);
     const int pb = block_exclusive_scan(big ? 1 : 0, tmp, &n_big);
     const int pt = block_exclusive_scan(big ? (tot + kGemmBN - 1) / kGemmBN : 0, tmp, &n_tiles);
+    // tensor-core token tiles, longest first: the full tiles in expert order, then each expert's
+    // ragged last tile by decreasing size (ties to the lower expert), so that the GEMMs' CTAs,
+    // which take tiles in a fixed stride, take tiles of similar cost side by side
+    const int nfull = big ? tot / kGemmBN : 0;
+    const int rag = big ? tot % kGemmBN : 0;
+    int n_full = 0;
+    const int pf = block_exclusive_scan(nfull, tmp, &n_full);
+    if (e < E) part[e] = rag;
+    __syncthreads();
+    int rank = 0;
+    if (rag > 0)
+        for (int o = 0; o < E; o++) rank += (part[o] > rag || (part[o] == rag && o < e)) ? 1 : 0;
     if (small && gemv_list) gemv_list[ps] = e;
     // positions of the small groups' pairs, in expert order (the small-group down kernel's slots)
     int n_small_pairs = 0;
@@ -167,15 +180,19 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
     if (big && tile_prefix) tile_prefix[pb] = pt;
     if (threadIdx.x == 0 && tile_prefix) tile_prefix[n_big] = n_tiles;
     // one descriptor per tensor-core token tile (expert, first row, tokens), in tile order
-    if (big && tile_desc)
-        for (int lt = 0; lt * kGemmBN < tot; lt++)
-            reinterpret_cast<int4 *>(tile_desc)[pt + lt] = make_int4(e, off + lt * kGemmBN, min(kGemmBN, tot - lt * kGemmBN), 0);
+    if (big && tile_desc) {
+        for (int lt = 0; lt < nfull; lt++)
+            reinterpret_cast<int4 *>(tile_desc)[pf + lt] = make_int4(e, off + lt * kGemmBN, kGemmBN, 0);
+        if (rag > 0)
+            reinterpret_cast<int4 *>(tile_desc)[n_full + rank] = make_int4(e, off + nfull * kGemmBN, rag, 0);
+    }
     if (threadIdx.x == 0 && meta) {
         meta->n_gemv = n_small;
         meta->n_gemm = n_big;
         meta->n_single = n_single;
         meta->n_small_pairs = n_small_pairs;
         meta->n_tiles = n_tiles;
+        meta->n_full = n_full;
     }
     __syncthreads();
     // stable positions
@@ -228,7 +245,7 @@ int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const ui
                  int32_t *single_list, int32_t *tile_prefix, int32_t *tile_desc, int32_t *small_pos, GroupMeta *meta, int *status,
                  void *stream) {
     const int P = T * k;
-    const size_t smem = (static_cast<size_t>(kGroupWarps) * E + 32) * sizeof(int);
+    const size_t smem = (static_cast<size_t>(kGroupWarps) * E + 32 + E) * sizeof(int);
     static int seen[64];
     const int err = ensure_smem(reinterpret_cast<const void *>(group_kernel), static_cast<int>(smem), seen);
     if (err) return err;
