@@ -31,6 +31,7 @@ DS4MOE_OPT_SINGLE_STEP = 3
 DS4MOE_OPT_TRACE = 4
 DS4MOE_OPT_SMALL_GROUPS = 5
 DS4MOE_OPT_WAIT_TEST = 6
+DS4MOE_OPT_GEMM_PAIRS = 7
 STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step", "pool"]
 
 EXPORTED = [

@@ -248,6 +248,7 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds
     h->shared_gemm_min_tokens = 2;
     h->single_step = 1;
     h->small_groups = 1;
+    h->gemm_pairs = 0;
     DeviceWeights &w = h->dw;
     w.D = D;
     w.F = F;
@@ -491,6 +492,7 @@ int ds4moe_set_option(ds4moe_weights *h, int option, int value) {
         case DS4MOE_OPT_SMALL_GROUPS: h->small_groups = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_TRACE: h->trace = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_WAIT_TEST: h->wait_test = value > 0 ? 1 : 0; return DS4MOE_OK;
+        case DS4MOE_OPT_GEMM_PAIRS: h->gemm_pairs = value ? 1 : 0; return DS4MOE_OK;
         case DS4MOE_OPT_PROFILE:
             if (value && !h->events[0]) {
                 for (auto &ev : h->events) {
@@ -661,7 +663,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     if (up_tc) {
         if (!rc && !shared_up_small) rc = clk.stage(DS4MOE_STAGE_UP_GEMM);
         else h->launches++;
-        if (!rc) rc = launch_gemm_up(w, ws, h->tmap_x16, T, k, shared_tc && !shared_up_small, stream);
+        if (!rc) rc = launch_gemm_up(w, ws, h->tmap_x16, T, k, shared_tc && !shared_up_small, h->gemm_pairs != 0, stream);
     }
     if (sg || q4 || decode_kernels || multi_gemv || shared_multi) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMV);
@@ -687,7 +689,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     }
     if (any_tc) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMM);
-        if (!rc) rc = launch_gemm_down(w, ws, h->tmap_h16, T, k, shared_tc, stream);
+        if (!rc) rc = launch_gemm_down(w, ws, h->tmap_h16, T, k, shared_tc, h->gemm_pairs != 0, stream);
     }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_COMBINE);
     if (!rc) rc = launch_combine(w, ws, T, k, gemm_min, shared_tc, out, stream);

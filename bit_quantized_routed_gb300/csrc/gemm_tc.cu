@@ -40,23 +40,19 @@ constexpr int kTableBytes = 256 * 16 * 8;  // replicated lookup table (grid or c
 
 enum { UP = 0, DOWN = 1 };
 
-template <int KIND>
-struct Cfg;
-template <>
-struct Cfg<UP> {
-    static constexpr int NA = 2;  // gate and up
-    static constexpr int STAGES = 3;
+// PAIR: the kernel runs on clusters of two CTAs (cta_group::2): each MMA covers 256 weight rows
+// (128 in each CTA's shared memory) and each CTA holds half of the token tile, so per SM a stage
+// carries half the token bytes and four stages fit where one CTA alone holds three.
+template <int KIND, bool PAIR>
+struct Cfg {
+    static constexpr int NA = 2;  // first GEMM: gate and up; down GEMM: two 128-row weight tiles
+    static constexpr int STAGES = PAIR ? 4 : 3;
     static constexpr int TMEM_COLS = 512;
-};
-template <>
-struct Cfg<DOWN> {
-    static constexpr int NA = 2;  // two 128-row weight tiles on one token tile
-    static constexpr int STAGES = 3;
-    static constexpr int TMEM_COLS = 512;
+    static constexpr int CTAS = PAIR ? 2 : 1;
+    static constexpr int BROWS = PAIR ? kGemmBN / 2 : kGemmBN;  // token rows of a stage in one CTA
 };
 
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 
 // Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row atoms 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -411,29 +407,42 @@ __device__ __forceinline__ int box_index(int ntok) {
     return i;
 }
 
-// FMT 0: IQ2-style gate/up, Q2_K-style down; FMT 1: the 4-bit variant's rows.
-template <int KIND, int FMT>
+// FMT 0: IQ2-style gate/up, Q2_K-style down; FMT 1: the 4-bit variant's rows. PAIR: see Cfg.
+// Roles: warp 0 lane 0 issues the token-tile copies; warp 1 allocates tensor memory and one lane
+// issues the MMAs (in a pair, only rank 0 does; rank 1's lane forwards its stages' readiness and
+// its epilogue's release of the accumulators to rank 0); warps 2..17 produce and then read back.
+template <int KIND, int FMT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ TokenMaps maps, GemmParams p) {
-    using C = Cfg<KIND>;
+    using C = Cfg<KIND, PAIR>;
     constexpr int S = C::STAGES;
-    constexpr int STAGE_BYTES = C::NA * A_BYTES + B_BYTES;
+    constexpr int NA = C::NA;
+    constexpr int CTAS = C::CTAS;
+    constexpr int B_BYTES = C::BROWS * BK * 2;
+    constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
     extern __shared__ uint8_t smem_raw[];
-    // align by an integer offset so that every pointer below stays a shared-memory pointer
+    // align by an integer offset so that every pointer below stays a shared-memory pointer (the
+    // offset is the same in both CTAs of a pair, as the pair's MMAs require)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint2 *table = reinterpret_cast<uint2 *>(smem + S * STAGE_BYTES);  // [256][16] replicated lookup table
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * STAGE_BYTES + kTableBytes);
-    // bars: full_a[S], full_b[S], empty[S], acc_full, acc_empty, spare
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 3 * S + 3);
+    // bars: full_a[S], full_b[S], empty[S], acc_full, acc_empty, spare, (pairs) peer_full[S], peer_acc
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 4 * S + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = p.w.D, F = p.w.F;
-    constexpr int MR = KIND == UP ? BM : BM * C::NA;  // weight rows per m-tile
+    // weight rows per m-tile, over the pair: the first GEMM's 128 (per CTA) rows of gate and of up,
+    // the down GEMM's two 128-row tiles (per CTA)
+    constexpr int MR = (KIND == UP ? BM : BM * NA) * CTAS;
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;  // rank in the pair (0 issues the MMAs)
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     const int m_tiles = (KIND == UP ? F : D) / MR;
     const int routed = p.meta->n_tiles;
     const int n_full = p.meta->n_full;
     const int total = n_tiles_total(p, m_tiles, routed);
-    if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA, before any allocation
+    // (a pair never leaves early: both CTAs take part in the joint allocation and the cluster barriers)
+    if (!PAIR && unit >= total) return;  // uniform over the CTA, before any allocation
     const int num_kb = (KIND == UP ? D : F) / BK;
 
     auto full_a = [&](int s) { return smem_u32(bars + s); };
@@ -442,17 +451,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t acc_full = smem_u32(bars + 3 * S), acc_empty = smem_u32(bars + 3 * S + 1);
     const uint32_t spare = smem_u32(bars + 3 * S + 2);
     auto a_tile = [&](int s, int a) { return smem_u32(smem + s * STAGE_BYTES + a * A_BYTES); };
-    auto b_tile = [&](int s) { return smem_u32(smem + s * STAGE_BYTES + C::NA * A_BYTES); };
+    auto b_tile = [&](int s) { return smem_u32(smem + s * STAGE_BYTES + NA * A_BYTES); };
+    // pairs: rank 1's lane of warp 1 forwards, for each stage, that its half (producers' rows
+    // and token copy) is in (peer_full on rank 0), and for each tile, that its epilogue has read
+    // the accumulators (peer_acc on rank 0)
+    auto peer_full = [&](int s) { return smem_u32(bars + 3 * S + 3 + s); };
+    const uint32_t peer_acc = smem_u32(bars + 4 * S + 3);
+    auto wait = [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, abort_flag, p.status); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(full_a(s), kProducers);
             mbar_init(full_b(s), 1);
             mbar_init(empty(s), 1);
+            mbar_init(peer_full(s), 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kProducers);
         mbar_init(spare, 1);
+        mbar_init(peer_acc, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -474,18 +491,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         table[i] = v;
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
-                     "r"(C::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {  // one warp of each CTA of the pair allocates, jointly
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                         "r"(C::TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                         "r"(C::TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
+    // token rows of a tile: MMA N = tokens rounded up to 16 per CTA's half (a pair's N is at least 32)
+    auto mma_n = [](int ntok) { return PAIR ? max(32, (ntok + 31) & ~31) : max(16, (ntok + 15) & ~15); };
+
     if (warp == 0) {
-        // ---------------------------------------------------------- TMA: token tiles
+        // ---------------------------------------------------------- TMA: token tiles (this CTA's half)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -493,18 +521,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
             for (int s = 0; s < S; s++) issued_parity[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = unit; t < total && ok; t += units) {
                 const Tile ti = decode_tile(p, t, m_tiles, n_full);
-                const int bi = box_index(ti.ntok);
+                const int half = mma_n(ti.ntok) / CTAS;
+                const int bi = box_index(half);
                 const CUtensorMap *map = &maps.m[bi];
                 const uint32_t bytes = static_cast<uint32_t>(16 << bi) * BK * 2;
+                const int row = ti.row0 + static_cast<int>(crank) * half;
                 for (int kb = 0; kb < num_kb; kb++) {
-                    if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, p.status)) {
+                    if (!wait(empty(stage), phase ^ 1u)) {
                         ok = false;
                         break;
                     }
                     mbar_expect_tx(full_b(stage), bytes);
-                    tma_load_2d(b_tile(stage), map, kb * BK, ti.row0, full_b(stage));
+                    tma_load_2d(b_tile(stage), map, kb * BK, row, full_b(stage));
                     issued_parity[stage] = static_cast<int>(phase);
                     if (++stage == S) {
                         stage = 0;
@@ -516,48 +546,91 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int s = 0; s < S; s++)
                     if (issued_parity[s] >= 0) mbar_drain(full_b(s), static_cast<uint32_t>(issued_parity[s]));
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && crank == 0) {
         // ---------------------------------------------------------- MMA issue (one thread)
         if (lane == 0) {
+            const uint32_t peer_acc_full = PAIR ? map_shared(acc_full, 1u) : 0u;
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = unit; t < total && ok; t += units) {
                 const Tile ti = decode_tile(p, t, m_tiles, n_full);
-                if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) {
+                // both CTAs' epilogues have read the previous tile's accumulators
+                if (!wait(acc_empty, acc_phase ^ 1u) || (PAIR && !wait(peer_acc, acc_phase ^ 1u))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int N = max(16, (ti.ntok + 15) & ~15);
-                const uint32_t idesc = idesc_f16(BM, N);
+                const uint32_t idesc = idesc_f16(BM * CTAS, mma_n(ti.ntok));
                 for (int kb = 0; kb < num_kb; kb++) {
-                    if (!mbar_wait(full_a(stage), phase, abort_flag, p.status) ||
-                        !mbar_wait(full_b(stage), phase, abort_flag, p.status)) {
+                    if (!wait(full_a(stage), phase) || !wait(full_b(stage), phase) ||
+                        (PAIR && !wait(peer_full(stage), phase))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int a = 0; a < C::NA; a++)
+                    for (int a = 0; a < NA; a++)
 #pragma unroll
-                        for (int k = 0; k < BK / 16; k++)
-                            tc_mma(tmem + a * BN, sw128_desc(a_tile(stage, a) + k * 32),
-                                   sw128_desc(b_tile(stage) + k * 32), idesc, (kb | k) != 0);
+                        for (int k = 0; k < BK / 16; k++) {
+                            const uint64_t ad = sw128_desc(a_tile(stage, a) + k * 32);
+                            const uint64_t bd = sw128_desc(b_tile(stage) + k * 32);
+                            if (PAIR)
+                                tc_mma_pair(tmem + a * BN, ad, bd, idesc, (kb | k) != 0);
+                            else
+                                tc_mma(tmem + a * BN, ad, bd, idesc, (kb | k) != 0);
+                        }
                     issued = true;
-                    tc_commit(empty(stage));
+                    if (PAIR) {  // the stage is free in both CTAs once these MMAs are done
+                        tc_commit_pair(empty(stage));
+                        tc_commit_pair(map_shared(empty(stage), 1u));
+                    } else {
+                        tc_commit(empty(stage));
+                    }
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(acc_full);
+                if (PAIR) {
+                    tc_commit_pair(acc_full);
+                    tc_commit_pair(peer_acc_full);
+                } else {
+                    tc_commit(acc_full);
+                }
                 acc_phase ^= 1u;
             }
             if (!ok && issued) {  // wait for the MMAs in flight before the memory goes away
-                tc_commit(spare);
+                if (PAIR)
+                    tc_commit_pair(spare);
+                else
+                    tc_commit(spare);
                 mbar_drain(spare, 0);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- a pair's rank 1: forward readiness
+        if (PAIR && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = unit; t < total && ok; t += units) {
+                for (int kb = 0; kb < num_kb; kb++) {
+                    if (!wait(full_a(stage), phase) || !wait(full_b(stage), phase)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_remote(map_shared(peer_full(stage), 0u));  // this CTA's half of the stage is in
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                // this CTA's epilogue of the tile has read its accumulators: rank 0 may start the next tile
+                if (!ok || !wait(acc_empty, acc_phase)) break;
+                mbar_arrive_remote(map_shared(peer_acc, 0u));
+                acc_phase ^= 1u;
             }
         }
     } else {
@@ -571,12 +644,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int colq = (warp - 2) >> 2;      // epilogue: which 16-column chunks (one of four)
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint2 *tab = table + (lane & 15);
+        // first row of this CTA's A tile a within the m-tile
+        auto tile_row0 = [&](int a) {
+            return (KIND == DOWN ? a * BM * CTAS : 0) + static_cast<int>(crank) * BM;
+        };
         Pipe pp{bars, S, 0, 0u, abort_flag, p.status};
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int t = unit; t < total && ok; t += units) {
             const Tile ti = decode_tile(p, t, m_tiles, n_full);
-            const int wrow = ti.m * MR + (KIND == DOWN ? sel * BM : 0) + r;
+            const int wrow = ti.m * MR + tile_row0(sel) + r;
             if (KIND == UP) {
                 if (ti.shared) {
                     BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D, part};
@@ -602,15 +679,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             if (!ok) break;
             // epilogue: accumulators -> registers -> global; four warps per TMEM lane quarter
-            if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) {
+            if (!wait(acc_full, acc_phase)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int orow = ti.m * MR + q * 32 + lane;
             bool range_ok = true;
             for (int c0 = 16 * colq; c0 < ti.ntok; c0 += 64) {
                 if (KIND == UP) {
+                    const int orow = ti.m * MR + tile_row0(0) + q * 32 + lane;
 #pragma unroll 1
                     for (int cb = c0; cb < c0 + 16 && cb < ti.ntok; cb += 8) {  // 8 columns at a time
                         float g[8], uu[8];
@@ -628,14 +705,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                 } else {
 #pragma unroll 1
-                    for (int a = 0; a < C::NA; a++) {  // the two 128-row tiles
+                    for (int a = 0; a < NA; a++) {  // the two 128-row tiles
+                        const int orow = ti.m * MR + tile_row0(a) + q * 32 + lane;
                         float v[16];
                         tmem_ld16(tmem + lane_addr + a * BN + c0, v);
 #pragma unroll
                         for (int j = 0; j < 16; j++) {
                             if (c0 + j < ti.ntok) {
                                 range_ok &= fabsf(v[j]) <= 65504.0f;
-                                p.y16[static_cast<size_t>(ti.row0 + c0 + j) * (2 * D) + orow + a * BM] =
+                                p.y16[static_cast<size_t>(ti.row0 + c0 + j) * (2 * D) + orow] =
                                     __half_as_ushort(__float2half_rn(v[j]));
                             }
                         }
@@ -651,9 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the pair's MMAs may still touch its memory
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
     }
 }
 
@@ -759,20 +841,40 @@ int sm_count_tc() {
     return n;
 }
 
-template <int KIND, int FMT>
+template <int KIND, int FMT, bool PAIR>
 int launch_gemm_fmt(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) {
-    using C = Cfg<KIND>;
-    const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * (C::NA * A_BYTES + B_BYTES) + kTableBytes + 256;
+    using C = Cfg<KIND, PAIR>;
+    const size_t smem = 1024 + static_cast<size_t>(C::STAGES) * (C::NA * A_BYTES + C::BROWS * BK * 2) + kTableBytes + 256;
     static int seen[64];
-    const int err = ensure_smem(reinterpret_cast<const void *>(gemm_kernel<KIND, FMT>), static_cast<int>(smem), seen);
+    const void *fn = reinterpret_cast<const void *>(gemm_kernel<KIND, FMT, PAIR>);
+    const int err = ensure_smem(fn, static_cast<int>(smem), seen);
     if (err) return err;
-    gemm_kernel<KIND, FMT><<<sm_count_tc(), kThreads, smem, s>>>(maps, p);
-    return static_cast<int>(cudaGetLastError());
+    if (!PAIR) {
+        gemm_kernel<KIND, FMT, PAIR><<<sm_count_tc(), kThreads, smem, s>>>(maps, p);
+        return static_cast<int>(cudaGetLastError());
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count_tc() & ~1));  // one CTA per SM, in pairs
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return static_cast<int>(cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, FMT, PAIR>, maps, p));
 }
 
+// CTA pairs when the weight rows split into 256-row (first GEMM) or 512-row (down GEMM) m-tiles.
 template <int KIND>
-int launch_gemm(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) {
-    return p.w.fmt == 1 ? launch_gemm_fmt<KIND, 1>(maps, p, s) : launch_gemm_fmt<KIND, 0>(maps, p, s);
+int launch_gemm(const TokenMaps &maps, const GemmParams &p, bool pairs, cudaStream_t s) {
+    const bool pair = pairs && (KIND == UP ? p.w.F % 256 == 0 : p.w.D % 512 == 0);
+    if (p.w.fmt == 1)
+        return pair ? launch_gemm_fmt<KIND, 1, true>(maps, p, s) : launch_gemm_fmt<KIND, 1, false>(maps, p, s);
+    return pair ? launch_gemm_fmt<KIND, 0, true>(maps, p, s) : launch_gemm_fmt<KIND, 0, false>(maps, p, s);
 }
 
 GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared) {
@@ -812,14 +914,14 @@ int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert
 }
 
 int launch_gemm_up(const DeviceWeights &w, const Workspace &ws, const void *tmap_x16, int T, int k, bool shared,
-                   void *stream) {
-    return launch_gemm<UP>(*static_cast<const TokenMaps *>(tmap_x16), make_params(w, ws, T, k, shared),
+                   bool pairs, void *stream) {
+    return launch_gemm<UP>(*static_cast<const TokenMaps *>(tmap_x16), make_params(w, ws, T, k, shared), pairs,
                            static_cast<cudaStream_t>(stream));
 }
 
 int launch_gemm_down(const DeviceWeights &w, const Workspace &ws, const void *tmap_h16, int T, int k, bool shared,
-                     void *stream) {
-    return launch_gemm<DOWN>(*static_cast<const TokenMaps *>(tmap_h16), make_params(w, ws, T, k, shared),
+                     bool pairs, void *stream) {
+    return launch_gemm<DOWN>(*static_cast<const TokenMaps *>(tmap_h16), make_params(w, ws, T, k, shared), pairs,
                              static_cast<cudaStream_t>(stream));
 }
 

@@ -191,6 +191,7 @@ struct ds4moe_weights {
     int trace;        // record the single-token kernel's per-CTA timestamps
     int small_groups; // groups below the tensor-core threshold run on the small-group kernels
     int wait_test;    // DS4MOE_OPT_WAIT_TEST
+    int gemm_pairs;   // DS4MOE_OPT_GEMM_PAIRS
     void *events[DS4MOE_N_STAGES + 1];  // cudaEvent_t: start of each stage, end of the call
     bool stage_ran[DS4MOE_N_STAGES];
     bool events_recorded;
@@ -228,10 +229,11 @@ int launch_shared_up_small(const DeviceWeights &w, const Workspace &ws, const ui
                            void *stream);
 int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, int gemm_min,
                   bool shared, void *stream);
+// pairs: run on clusters of two CTAs (cta_group::2) where the shape allows
 int launch_gemm_up(const DeviceWeights &w, const Workspace &ws, const void *tmap_x16, int T, int k, bool shared,
-                   void *stream);
+                   bool pairs, void *stream);
 int launch_gemm_down(const DeviceWeights &w, const Workspace &ws, const void *tmap_h16, int T, int k, bool shared,
-                     void *stream);
+                     bool pairs, void *stream);
 int encode_token_map(void *map_out, void *base, int rows, int cols, int box_rows);
 int encode_token_maps(void *maps_out, void *base, int rows, int cols);
 int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, uint16_t *dst16,

@@ -93,7 +93,12 @@ enum ds4moe_option {
      * wait for an arrival that never comes, so the wait runs out (about 2 s), every CTA finishes
      * through its abort path, and ds4moe_last_status reports DS4MOE_ETIMEOUT; the handle stays
      * usable. Default 0. */
-    DS4MOE_OPT_WAIT_TEST = 6
+    DS4MOE_OPT_WAIT_TEST = 6,
+    /* 1: the tensor-core kernels run on pairs of CTAs (clusters of two, one MMA over both CTAs'
+     * shared memory: 256 weight rows per MMA, each CTA holding half of the token tile) where the
+     * shape allows (d_ff a multiple of 256 for the first GEMM, d_model a multiple of 512 for the
+     * down GEMM); 0: one CTA per tile. Library reading, no passage. */
+    DS4MOE_OPT_GEMM_PAIRS = 7
 };
 
 /* Stages of ds4moe_expert_ffn, in launch order (indices into ds4moe_stats.stage_ms). */

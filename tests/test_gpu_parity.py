@@ -198,6 +198,41 @@ def test_ffn_tensor_core_path_forced(ds4, T, D, F, E, k, shared):
     assert err <= FFN_TOL, err
 
 
+@pytest.mark.parametrize("T,D,F,E,k,shared,fmt", [(300, 1024, 512, 6, 4, True, "q2"), (37, 512, 768, 8, 3, True, "q2"),
+                                                  (600, 512, 512, 4, 2, False, "q2"), (70, 768, 512, 6, 4, True, "q2"),
+                                                  (130, 1024, 512, 8, 4, True, "q4")])
+def test_ffn_tensor_core_cta_pairs(ds4, T, D, F, E, k, shared, fmt):
+    """The tensor-core kernels on CTA pairs (cta_group::2: one MMA over two CTAs' shared memory,
+    256 weight rows, each CTA holding half of the token tile) against the oracle, and equal to
+    the single-CTA kernels bit for bit (every output element is accumulated in the same order).
+    d_model 768 takes pairs for the first GEMM only (the down GEMM needs a multiple of 512)."""
+    import torch
+    wl = synth.Workload("pair", T=T, D=D, F=F, E=E, k=k, seed=T + D, bias=("zipf", 1.0), shared=shared)
+    L, x = synth.draw_inputs(wl)
+    if fmt == "q4":
+        gate, up, down = synth.random_q4_expert_blobs(wl)
+    else:
+        gate, up, down = synth.random_expert_blobs(wl)
+    sh = synth.shared_weights(wl.seed, D, F) if shared else None
+    W = ds4.ds4moe_weights_create(gate, up, down, D, F, shared=sh, max_tokens=T, max_k=k, fmt=fmt)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_MIN_TOKENS, 1)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS, 1)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    Ld = torch.from_numpy(L).cuda()
+    outs = []
+    for pairs in (0, 1, 1):
+        ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_PAIRS, pairs)
+        out = torch.zeros((T, D), dtype=torch.float32, device="cuda")
+        ds4.ds4moe_expert_ffn(xd, W, Ld, k, out)
+        assert ds4.ds4moe_last_status(W) == 0
+        outs.append(out.cpu().numpy())
+    W.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert np.array_equal(outs[1].view(np.uint32), outs[2].view(np.uint32))
+    ref, _, _ = oracle.moe_ffn(x, L, k, gate, up, down, D, F, shared=sh, fmt=fmt)
+    assert norm_max_err(outs[1], ref) <= FFN_TOL
+
+
 def test_ffn_mixed_gemv_and_tensor_core_groups(ds4):
     wl = synth.Workload("mix", T=300, D=512, F=512, E=16, k=4, seed=17, bias=("zipf", 1.2))
     L, _ = synth.draw_inputs(wl)
