@@ -46,6 +46,7 @@ __device__ __forceinline__ void load8(const float *row, int c, bool f16, float v
 
 // One CTA per token (grid-stride over tokens); each thread 8 columns at a time.
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+    pdl_wait();
     __shared__ int s_pos[32];
     __shared__ float s_g[32];
     __shared__ int s_f16[32];
@@ -108,8 +109,7 @@ int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, in
     p.shared_f16 = (w.has_shared && shared_f16) ? 1 : 0;
     p.out = out;
     const int blocks = std::min(T, 152 * 8);
-    combine_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, static_cast<cudaStream_t>(stream), p);
 }
 
 }  // namespace ds4moe

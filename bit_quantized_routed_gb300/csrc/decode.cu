@@ -87,6 +87,7 @@ struct DecParams {
 // ------------------------------------------------------------------ phase 1: gate/up + SwiGLU
 
 __global__ void __launch_bounds__(kThreads) decode_up_kernel(DecParams p) {
+    pdl_wait();
     __shared__ uint2 gtab[256 * 16];  // [entry][copy]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(kThreads) decode_up_kernel(DecParams p) {
 // ------------------------------------------------------------------ phase 2: down
 
 __global__ void __launch_bounds__(kThreads) decode_down_kernel(DecParams p) {
+    pdl_wait();
     __shared__ uint2 qtab[256 * 16];  // [code byte][copy]: four fp16 codes
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
@@ -397,15 +399,13 @@ DecParams make(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, i
 
 int launch_decode_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, bool shared,
                      void *stream) {
-    decode_up_kernel<<<sm_count_dec() * 4, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        make(w, ws, x, T, k, shared));
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(decode_up_kernel, dim3(sm_count_dec() * 4), dim3(kThreads), 0, static_cast<cudaStream_t>(stream),
+                      make(w, ws, x, T, k, shared));
 }
 
 int launch_decode_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared, void *stream) {
-    decode_down_kernel<<<sm_count_dec() * 4, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        make(w, ws, nullptr, T, k, shared));
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(decode_down_kernel, dim3(sm_count_dec() * 4), dim3(kThreads), 0, static_cast<cudaStream_t>(stream),
+                      make(w, ws, nullptr, T, k, shared));
 }
 
 }  // namespace ds4moe

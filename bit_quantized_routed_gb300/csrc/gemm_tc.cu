@@ -413,6 +413,7 @@ __device__ __forceinline__ int box_index(int ntok) {
 // its epilogue's release of the accumulators to rank 0); warps 2..17 produce and then read back.
 template <int KIND, int FMT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ TokenMaps maps, GemmParams p) {
+    pdl_wait();
     using C = Cfg<KIND, PAIR>;
     constexpr int S = C::STAGES;
     constexpr int NA = C::NA;
@@ -798,6 +799,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict_
                                                      const uint8_t *__restrict__ tc_ok, int gemm_min, int k, int D,
                                                      int P, int T, int shared, uint16_t *__restrict__ x16,
                                                      int *status) {
+    pdl_wait();
     const int D8 = D / 8;
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
@@ -849,22 +851,21 @@ int launch_gemm_fmt(const TokenMaps &maps, const GemmParams &p, cudaStream_t s) 
     const void *fn = reinterpret_cast<const void *>(gemm_kernel<KIND, FMT, PAIR>);
     const int err = ensure_smem(fn, static_cast<int>(smem), seen);
     if (err) return err;
-    if (!PAIR) {
-        gemm_kernel<KIND, FMT, PAIR><<<sm_count_tc(), kThreads, smem, s>>>(maps, p);
-        return static_cast<int>(cudaGetLastError());
-    }
+    if (!PAIR) return launch_pdl(gemm_kernel<KIND, FMT, PAIR>, dim3(sm_count_tc()), dim3(kThreads), smem, s, maps, p);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sm_count_tc() & ~1));  // one CTA per SM, in pairs
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return static_cast<int>(cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, FMT, PAIR>, maps, p));
 }
 
@@ -898,10 +899,10 @@ int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x
                   bool shared, void *stream) {
     const int P = T * k;
     const int blocks = std::min((P + T + 7) / 8, sm_count_tc() * 8);  // a warp per row, 8 rows per CTA
-    gather_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, ws.perm, ws.topk_idx, ws.counts, w.tc_ok,
-                                                                         gemm_min, k, w.D, P, T, shared ? 1 : 0,
-                                                                         ws.x16, ws.status);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(gather_kernel, dim3(blocks), dim3(256), 0, static_cast<cudaStream_t>(stream), x,
+                      static_cast<const int32_t *>(ws.perm), static_cast<const int32_t *>(ws.topk_idx),
+                      static_cast<const int32_t *>(ws.counts), static_cast<const uint8_t *>(w.tc_ok), gemm_min,
+                      k, w.D, P, T, shared ? 1 : 0, ws.x16, ws.status);
 }
 
 int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, uint16_t *dst16,

@@ -110,6 +110,7 @@ struct UpParams {
 // Phase 1: h[pos][r] = silu(gate_r . x) * (up_r . x) for the group's tokens.
 template <int NT, bool Q4>
 __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
+    pdl_wait();
     extern __shared__ __align__(16) uint8_t smem[];
     uint2 *grid_s = reinterpret_cast<uint2 *>(smem);              // 256 x 8 B
     uint4 *xs = reinterpret_cast<uint4 *>(smem + 2048);           // [NT][D/8] swizzled
@@ -356,6 +357,7 @@ struct DownParams {
 __global__ void __launch_bounds__(256) prep_h_kernel(const float *__restrict__ h, int rows, int F,
                                                      uint4 *__restrict__ hq, int *__restrict__ hsum,
                                                      float *__restrict__ hsc) {
+    pdl_wait();
     __shared__ float wmax[8];
     const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (row >= rows) return;
@@ -398,6 +400,7 @@ __global__ void __launch_bounds__(256) prep_h_kernel(const float *__restrict__ h
 // Phase 2: y[pos][r] = down_r . h[pos] for the group's tokens.
 template <int NT, bool Q4>
 __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
+    pdl_wait();
     extern __shared__ __align__(16) uint8_t smem[];
     float4 *hs = reinterpret_cast<float4 *>(smem);  // [NT][F/4] swizzled
     const int D = p.w.D, F = p.w.F, nbF = p.w.nbF, F4 = F / 4, F8 = F / 8;
@@ -1140,8 +1143,7 @@ int launch_up_nt(const UpParams &p, cudaStream_t s) {
     const int err = ensure_smem(reinterpret_cast<const void *>(gemv_up_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
     const int per_sm = resident_ctas(gemv_up_kernel<NT, Q4>, smem, cached_smem, cached_n);
-    gemv_up_kernel<NT, Q4><<<sm_count() * per_sm, kThreads, smem, s>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(gemv_up_kernel<NT, Q4>, dim3(sm_count() * per_sm), dim3(kThreads), smem, s, p);
 }
 
 template <int NT, bool Q4>
@@ -1153,8 +1155,7 @@ int launch_down_nt(const DownParams &p, cudaStream_t s) {
     const int err = ensure_smem(reinterpret_cast<const void *>(gemv_down_kernel<NT, Q4>), static_cast<int>(smem), seen);
     if (err) return err;
     const int per_sm = resident_ctas(gemv_down_kernel<NT, Q4>, smem, cached_smem, cached_n);
-    gemv_down_kernel<NT, Q4><<<sm_count() * per_sm, kThreads, smem, s>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(gemv_down_kernel<NT, Q4>, dim3(sm_count() * per_sm), dim3(kThreads), smem, s, p);
 }
 
 // Ring plans of the streamed kernels; stages == 0 when they do not fit one CTA's shared memory.
@@ -1254,9 +1255,8 @@ int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *
 
 int launch_prep_h(const Workspace &ws, int rows, int F, void *stream) {
     if (rows <= 0) return 0;
-    prep_h_kernel<<<rows, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        ws.h32, rows, F, reinterpret_cast<uint4 *>(ws.hq4), ws.hsum4, ws.hsc4);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(prep_h_kernel, dim3(rows), dim3(256), 0, static_cast<cudaStream_t>(stream),
+                      static_cast<const float *>(ws.h32), rows, F, reinterpret_cast<uint4 *>(ws.hq4), ws.hsum4, ws.hsc4);
 }
 
 int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream,

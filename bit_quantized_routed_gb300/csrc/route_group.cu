@@ -20,6 +20,7 @@ template <int PER>
 __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int T, int E, int k,
                                                     int mode, int32_t *__restrict__ idx,
                                                     float *__restrict__ wout) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
                  int32_t *__restrict__ inv, int32_t *__restrict__ gemv_list, int32_t *__restrict__ gemm_list,
                  int32_t *__restrict__ single_list, int32_t *__restrict__ tile_prefix, int32_t *__restrict__ tile_desc,
                  int32_t *__restrict__ small_pos, GroupMeta *meta, int *status) {
+    pdl_wait();
     extern __shared__ int sm[];
     int *hist = sm;                      // [kGroupWarps][E]: counts, then base positions
     int *tmp = sm + kGroupWarps * E;     // [32]
@@ -225,19 +227,20 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
     const int warps = 8;
     dim3 grid((T + warps - 1) / warps), block(32 * warps);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc;
     if (per <= 1)
-        route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, gate_mode, idx, w);
+        rc = launch_pdl(route_kernel<1>, grid, block, 0, s, logits, T, E, k, gate_mode, idx, w);
     else if (per <= 2)
-        route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, gate_mode, idx, w);
+        rc = launch_pdl(route_kernel<2>, grid, block, 0, s, logits, T, E, k, gate_mode, idx, w);
     else if (per <= 4)
-        route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, gate_mode, idx, w);
+        rc = launch_pdl(route_kernel<4>, grid, block, 0, s, logits, T, E, k, gate_mode, idx, w);
     else if (per <= 8)
-        route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, gate_mode, idx, w);
+        rc = launch_pdl(route_kernel<8>, grid, block, 0, s, logits, T, E, k, gate_mode, idx, w);
     else if (per <= 16)
-        route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, gate_mode, idx, w);
+        rc = launch_pdl(route_kernel<16>, grid, block, 0, s, logits, T, E, k, gate_mode, idx, w);
     else
-        route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, gate_mode, idx, w);
-    return static_cast<int>(cudaGetLastError());
+        rc = launch_pdl(route_kernel<32>, grid, block, 0, s, logits, T, E, k, gate_mode, idx, w);
+    return rc;
 }
 
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok, int32_t *counts,
@@ -249,10 +252,9 @@ int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const ui
     static int seen[64];
     const int err = ensure_smem(reinterpret_cast<const void *>(group_kernel), static_cast<int>(smem), seen);
     if (err) return err;
-    group_kernel<<<1, kGroupThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        idx, P, E, gemm_min, tc_ok, counts, offsets, perm, inv, gemv_list, gemm_list, single_list, tile_prefix,
-        tile_desc, small_pos, meta, status);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(group_kernel, dim3(1), dim3(kGroupThreads), smem, static_cast<cudaStream_t>(stream), idx, P, E,
+                      gemm_min, tc_ok, counts, offsets, perm, inv, gemv_list, gemm_list, single_list, tile_prefix,
+                      tile_desc, small_pos, meta, status);
 }
 
 }  // namespace ds4moe

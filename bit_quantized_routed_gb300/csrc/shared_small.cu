@@ -46,6 +46,7 @@ struct SharedParams {
 // the step's first k16 MMA, 4-5 and 6-7 those of its second; weights and tokens use the same map.
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) shared_up_kernel(SharedParams p) {
+    pdl_wait();
     extern __shared__ float red[];  // [kWarps][2][kRows][NT * 8]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int D = p.D, F = p.F, T = p.T, row0 = blockIdx.x * kRows;
@@ -121,8 +122,7 @@ int launch_nt(const SharedParams &p, cudaStream_t s) {
     const int smem = kWarps * 2 * kRows * NT * 8 * 4;
     const int err = ensure_smem(reinterpret_cast<const void *>(shared_up_kernel<NT>), smem, seen);
     if (err) return err;
-    shared_up_kernel<NT><<<p.F / kRows, kThreads, smem, s>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(shared_up_kernel<NT>, dim3(p.F / kRows), dim3(kThreads), static_cast<size_t>(smem), s, p);
 }
 
 }  // namespace

@@ -50,6 +50,7 @@ constexpr int kMaxF = 2048;
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int T, int D,
                                                      uint4 *__restrict__ xq, int *__restrict__ x8,
                                                      float4 *__restrict__ xsc) {
+    pdl_wait();
     __shared__ float wmax[8];
     const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (t >= T) return;
@@ -305,6 +306,7 @@ __device__ __forceinline__ void unit_dot(const uint8_t *st, const uint8_t *tab, 
 }
 
 __global__ void __launch_bounds__(kThreads, 1) small_up_kernel(UpParams p) {
+    pdl_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;  // fixed offsets from the symbol: the table's base folds into its loads
     uint8_t *ring = smem, *tab = smem + kUpTabOff, *xs = smem + kUpXOff;
@@ -550,6 +552,7 @@ struct DownParams {
 // Thread (s2 = tid >> 6, j2 = tid & 63) owns slot s2 and columns 32 j2 .. 32 j2 + 31 (two 16-column
 // sub-blocks) of its pair's h, kept in registers while the slot group lasts.
 __global__ void __launch_bounds__(kThreads, 1) small_down_kernel(DownParams p) {
+    pdl_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *ring = smem_raw;
     float *red = reinterpret_cast<float *>(smem_raw + kDnRedOff);  // [2][kCompute][8]
@@ -753,9 +756,8 @@ bool small_groups_supported(const DeviceWeights &w) {
 
 int launch_prep_x(const Workspace &ws, const uint16_t *x, int T, int D, void *stream) {
     if (T <= 0) return 0;
-    prep_x_kernel<<<T, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        x, T, D, reinterpret_cast<uint4 *>(ws.xq), ws.x8, reinterpret_cast<float4 *>(ws.xsc));
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(prep_x_kernel, dim3(T), dim3(256), 0, static_cast<cudaStream_t>(stream), x, T, D,
+                      reinterpret_cast<uint4 *>(ws.xq), ws.x8, reinterpret_cast<float4 *>(ws.xsc));
 }
 
 int launch_small_up(const DeviceWeights &w, const Workspace &ws, int T, int k, void *stream) {
@@ -778,8 +780,7 @@ int launch_small_up(const DeviceWeights &w, const Workspace &ws, int T, int k, v
     p.hsum = l.hsum;
     p.k = k;
     p.status = ws.status;
-    small_up_kernel<<<n_sms_sg(), kThreads, kUpSmem, static_cast<cudaStream_t>(stream)>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(small_up_kernel, dim3(n_sms_sg()), dim3(kThreads), kUpSmem, static_cast<cudaStream_t>(stream), p);
 }
 
 int launch_small_down(const DeviceWeights &w, const Workspace &ws, int T, int k, void *stream) {
@@ -798,8 +799,7 @@ int launch_small_down(const DeviceWeights &w, const Workspace &ws, int T, int k,
     p.hsum = l.hsum;
     p.y = ws.y;
     p.status = ws.status;
-    small_down_kernel<<<n_sms_sg(), kThreads, kDnSmem, static_cast<cudaStream_t>(stream)>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return launch_pdl(small_down_kernel, dim3(n_sms_sg()), dim3(kThreads), kDnSmem, static_cast<cudaStream_t>(stream), p);
 }
 
 }  // namespace ds4moe
