@@ -32,7 +32,8 @@ DS4MOE_OPT_TRACE = 4
 DS4MOE_OPT_SMALL_GROUPS = 5
 DS4MOE_OPT_WAIT_TEST = 6
 DS4MOE_OPT_GEMM_PAIRS = 7
-STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step", "pool"]
+STAGES = ["route", "group", "gather", "up_gemv", "up_gemm", "down_gemv", "down_gemm", "combine", "step", "pool",
+          "repair"]
 
 EXPORTED = [
     "ds4moe_strerror", "ds4moe_q2k_bytes", "ds4moe_iq2_bytes", "ds4moe_q4k_bytes", "ds4moe_iq2_grid",
@@ -62,7 +63,7 @@ class _Desc(ctypes.Structure):
 
 
 class _Stats(ctypes.Structure):
-    _fields_ = [("calls", ctypes.c_uint64), ("launches", ctypes.c_uint64), ("stage_ms", ctypes.c_float * 10)]
+    _fields_ = [("calls", ctypes.c_uint64), ("launches", ctypes.c_uint64), ("stage_ms", ctypes.c_float * len(STAGES))]
 
 
 _lib = None

@@ -177,7 +177,7 @@ bool blobs_valid(const ds4moe_weights_desc *desc, int fmt) {
 // ("ds4moe:<stage>") on the host thread that issues its launches, for timeline tools.
 const char *const kStageNames[DS4MOE_N_STAGES] = {
     "ds4moe:route", "ds4moe:group", "ds4moe:gather", "ds4moe:up_gemv", "ds4moe:up_gemm",
-    "ds4moe:down_gemv", "ds4moe:down_gemm", "ds4moe:combine", "ds4moe:step", "ds4moe:pool"};
+    "ds4moe:down_gemv", "ds4moe:down_gemm", "ds4moe:combine", "ds4moe:step", "ds4moe:pool", "ds4moe:repair"};
 
 struct StageClock {
     ds4moe_weights *h;
@@ -399,6 +399,10 @@ static int create_impl(const ds4moe_weights_desc *desc, int n_slots, int fmt, ds
     TRY(dev_alloc(h, &ws.tile_prefix, (E + 1) * 4));
     TRY(dev_alloc(h, &ws.tile_desc, (E + P / kGemmBN + 1) * 16));
     TRY(dev_alloc(h, &ws.meta, sizeof(GroupMeta)));
+    TRY(dev_alloc(h, &ws.meta2, sizeof(GroupMeta)));
+    TRY(dev_alloc(h, &ws.ovf, (E + 1) * 4));
+    TRY(dev_alloc(h, &ws.repair_list, E * 4));
+    if (cudaMemset(ws.ovf, 0, (E + 1) * 4) != cudaSuccess) TRY(DS4MOE_ECUDA);
     TRY(dev_alloc(h, &ws.grid, 2048));
     TRY(dev_alloc(h, &ws.h32, rows * F * 4));
     const size_t rows_tc = std::max<size_t>(rows, kGemmBN);  // at least one full token box
@@ -621,7 +625,7 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     if (!rc)
         rc = launch_group(ws.topk_idx, T, k, w.E, gemm_min, w.tc_ok, ws.counts, ws.offsets, ws.perm, ws.inv,
                           ws.gemv_list, ws.gemm_list, (sg || q4) ? nullptr : ws.single_list, ws.tile_prefix, ws.tile_desc,
-                          sg ? ws.small_pos : nullptr, ws.meta, ws.status, stream);
+                          sg ? ws.small_pos : nullptr, ws.meta, ws.status, stream, ws.ovf);
     if (up_tc) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_GATHER);
         if (!rc) rc = launch_gather(w, ws, x, T, k, gemm_min, shared_tc && !shared_up_small, stream);
@@ -690,6 +694,18 @@ int ds4moe_expert_ffn(const uint16_t *x, ds4moe_weights *h, const float *logits,
     if (any_tc) {
         if (!rc) rc = clk.stage(DS4MOE_STAGE_DOWN_GEMM);
         if (!rc) rc = launch_gemm_down(w, ws, h->tmap_h16, T, k, shared_tc, h->gemm_pairs != 0, stream);
+        // Groups (and the shared expert) whose token, h or y values overflowed fp16 on the tensor
+        // cores are flagged by those kernels; they are recomputed here in fp32 on the GEMV kernels
+        // (which find nothing to do when no flag is set), and the combine reads their fp32 rows.
+        Workspace wr = ws;
+        wr.gemv_list = ws.repair_list;
+        wr.meta = ws.meta2;
+        const int32_t *shared_flag = ws.ovf + w.E;
+        if (!rc) rc = clk.stage(DS4MOE_STAGE_REPAIR);
+        if (!rc) rc = launch_repair_list(w, ws, gemm_min, stream);
+        if (!rc) rc = launch_gemv_up(w, wr, x, T, k, shared_tc, stream, shared_flag);
+        if (!rc) rc = launch_gemv_down(w, wr, T, k, shared_tc, stream, false, shared_flag);
+        h->launches += 2;
     }
     if (!rc) rc = clk.stage(DS4MOE_STAGE_COMBINE);
     if (!rc) rc = launch_combine(w, ws, T, k, gemm_min, shared_tc, out, stream);

@@ -23,6 +23,7 @@ struct CombineParams {
     int gemm_min;            // > 0: groups of at least this many tokens ran on the tensor cores
     int shared;              // rows P.. hold the shared expert's output
     int shared_f16;          // ... in fp16
+    const int32_t *ovf;      // [E+1] or null: the expert's tensor-core rows were recomputed in fp32
     float *out;
 };
 
@@ -51,6 +52,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
     __shared__ float s_g[32];
     __shared__ int s_f16[32];
     const int D8 = p.D / 8;
+    // the shared expert's rows: fp16 unless its tensor-core result was recomputed in fp32
+    const bool sh16 = p.shared_f16 != 0 && !(p.ovf && p.ovf[p.E]);
     for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
         if (threadIdx.x < p.k) {
             const int s = threadIdx.x;
@@ -59,13 +62,13 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
             s_g[s] = p.g[t * p.k + s];
             // (an index outside [0, E) has been reported by the grouping kernel, which grouped it as expert 0)
             const int ec = (e >= 0 && e < p.E) ? e : 0;
-            s_f16[s] = p.gemm_min > 0 && p.counts[ec] >= p.gemm_min && p.tc_ok[ec];
+            s_f16[s] = p.gemm_min > 0 && p.counts[ec] >= p.gemm_min && p.tc_ok[ec] && !(p.ovf && p.ovf[ec]);
         }
         __syncthreads();
         for (int c = threadIdx.x; c < D8; c += blockDim.x) {
             float acc[8];
             if (p.shared) {
-                load8(p.y + static_cast<size_t>(p.P + t) * p.D, c, p.shared_f16 != 0, acc);
+                load8(p.y + static_cast<size_t>(p.P + t) * p.D, c, sh16, acc);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; i++) acc[i] = 0.0f;
@@ -88,7 +91,42 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
     }
 }
 
+// One CTA of 1024 threads (E <= 1024): the experts whose tensor-core results overflowed fp16, in
+// expert order, as the GEMV kernels' work list (meta->n_gemv of them); the shared expert's flag
+// stays in ovf[E].
+__global__ void __launch_bounds__(1024) repair_list_kernel(const int32_t *__restrict__ ovf, int E,
+                                                           int32_t *__restrict__ list, GroupMeta *meta) {
+    pdl_wait();
+    __shared__ int wcount[32];
+    const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool f = e < E && ovf[e] != 0;
+    const unsigned m = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) wcount[warp] = __popc(m);
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of the warps' counts
+        const int c = wcount[lane];
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        wcount[lane] = x - c;
+        if (lane == 31) {
+            meta->n_gemv = x;
+            meta->n_gemm = meta->n_single = meta->n_small_pairs = meta->n_tiles = meta->n_full = 0;
+        }
+    }
+    __syncthreads();
+    if (f) list[wcount[warp] + __popc(m & ((1u << lane) - 1u))] = e;
+}
+
 }  // namespace
+
+int launch_repair_list(const DeviceWeights &w, const Workspace &ws, int, void *stream) {
+    return launch_pdl(repair_list_kernel, dim3(1), dim3(1024), 0, static_cast<cudaStream_t>(stream),
+                      static_cast<const int32_t *>(ws.ovf), w.E, ws.repair_list, ws.meta2);
+}
 
 int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, int gemm_min, bool shared_f16,
                    float *out, void *stream) {
@@ -107,6 +145,7 @@ int launch_combine(const DeviceWeights &w, const Workspace &ws, int T, int k, in
     p.gemm_min = gemm_min;
     p.shared = w.has_shared ? 1 : 0;
     p.shared_f16 = (w.has_shared && shared_f16) ? 1 : 0;
+    p.ovf = ws.ovf;
     p.out = out;
     const int blocks = std::min(T, 152 * 8);
     return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, static_cast<cudaStream_t>(stream), p);

@@ -93,6 +93,7 @@ struct GemmParams {
                     // row's fp32 slot in the y buffer, which the GEMV paths fill in fp32)
     int T, P, shared;
     int *status;
+    int32_t *ovf;  // [E+1] an fp16 overflow of a tile's h or y flags its expert (E: the shared expert)
 };
 
 struct Tile {
@@ -721,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                 }
             }
-            if (!range_ok) report(p.status, ST_RANGE);
+            if (!range_ok) p.ovf[ti.shared ? p.w.E : ti.e] = 1;  // recomputed in fp32 before the combine
             tc_fence_before();
             mbar_arrive(acc_empty);
             acc_phase ^= 1u;
@@ -792,31 +793,33 @@ __global__ void __launch_bounds__(kProducers) producer_dump_kernel(DeviceWeights
 
 // x (bf16) -> x16 (fp16) for rows of tensor-core groups and of the shared expert. One warp per
 // row: lane 0 resolves the row's token (or that the row is not on the tensor cores), then the
-// warp converts the token's D values, 8 per lane and step.
+// warp converts the token's D values, 8 per lane and step. A value beyond fp16's range flags the
+// row's expert (ovf[E]: the shared expert), whose results are then recomputed in fp32.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
                                                      const int32_t *__restrict__ topk_idx,
                                                      const int32_t *__restrict__ counts,
                                                      const uint8_t *__restrict__ tc_ok, int gemm_min, int k, int D,
                                                      int P, int T, int shared, uint16_t *__restrict__ x16,
-                                                     int *status) {
+                                                     int32_t *__restrict__ ovf, int E) {
     pdl_wait();
     const int D8 = D / 8;
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
-    bool range_ok = true;
     for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < P + T; row += warps) {
-        int tok = -1;
+        int tok = -1, owner = E;
         if (lane == 0) {
             if (row < P) {
                 const int pair = perm[row];
                 const int e = topk_idx[pair];
                 if (gemm_min > 0 && counts[e] >= gemm_min && tc_ok[e]) tok = pair / k;
+                owner = e;
             } else if (shared) {
                 tok = row - P;
             }
         }
         tok = __shfl_sync(0xffffffffu, tok, 0);
         if (tok < 0) continue;
+        bool range_ok = true;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * D);
         uint4 *dst = reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(row) * D);
 #pragma unroll 4
@@ -828,8 +831,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict_
             for (int j = 0; j < 8; j++) range_ok &= fabsf(f[j]) <= 65504.0f;
             dst[c] = make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
         }
+        if (!__all_sync(0xffffffffu, range_ok) && lane == 0) ovf[owner] = 1;
     }
-    if (!range_ok) report(status, ST_RANGE);
 }
 
 int sm_count_tc() {
@@ -890,6 +893,7 @@ GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k
     p.P = T * k;
     p.shared = shared ? 1 : 0;
     p.status = ws.status;
+    p.ovf = ws.ovf;
     return p;
 }
 
@@ -902,7 +906,7 @@ int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x
     return launch_pdl(gather_kernel, dim3(blocks), dim3(256), 0, static_cast<cudaStream_t>(stream), x,
                       static_cast<const int32_t *>(ws.perm), static_cast<const int32_t *>(ws.topk_idx),
                       static_cast<const int32_t *>(ws.counts), static_cast<const uint8_t *>(w.tc_ok), gemm_min,
-                      k, w.D, P, T, shared ? 1 : 0, ws.x16, ws.status);
+                      k, w.D, P, T, shared ? 1 : 0, ws.x16, ws.ovf, w.E);
 }
 
 int launch_producer_dump(const DeviceWeights &w, const uint8_t *grid, int expert, int matrix, uint16_t *dst16,

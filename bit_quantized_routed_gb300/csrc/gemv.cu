@@ -99,6 +99,7 @@ struct UpParams {
     float *h;             // [P+T][F]
     int T, k, P;
     int shared;           // shared expert on this path
+    const int32_t *shared_flag;  // non-null: the shared expert only when *shared_flag (a repair)
     // the 4-bit variant: the tokens as int16 dp2a pairs (see prep_x_kernel), 8 x each 32-column
     // sub-block's sum of them, and each token's factor back to x
     const uint4 *xq;
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) gemv_up_kernel(UpParams p) {
     const int n_gemv = p.meta->n_gemv;
     const int per_group = F / kUpRows;
     const int routed = n_gemv * per_group;
-    const int n_shared = p.shared ? F / kUpSharedRows : 0;
+    const int n_shared = (p.shared && (!p.shared_flag || *p.shared_flag)) ? F / kUpSharedRows : 0;
     // bytes per item: 16 rows of gate and up in the routed format (per 256 columns), 8 bf16 rows
     const long long cr = 2LL * kUpRows * (Q4 ? 144 : 66), cs = 2LL * kUpSharedRows * 512;
     int begin, end;
@@ -342,6 +343,7 @@ struct DownParams {
     float *y;        // [P+T][D]
     int T, P;
     int shared;
+    const int32_t *shared_flag;  // non-null: the shared expert only when *shared_flag (a repair)
     // the 4-bit variant, when given: each pair's h as int16 dp2a pairs (prep_h_kernel), the sum
     // of each 32-column sub-block of them, and the factor back to h
     const uint4 *hq;
@@ -413,7 +415,7 @@ __global__ void __launch_bounds__(kThreads) gemv_down_kernel(DownParams p) {
     const int n_gemv = p.meta->n_gemv;
     const int per_group = D / kDownRows;
     const int routed = n_gemv * per_group;
-    const int n_shared = p.shared ? D / kDownSharedRows : 0;
+    const int n_shared = (p.shared && (!p.shared_flag || *p.shared_flag)) ? D / kDownSharedRows : 0;
     // bytes per item: 32 rows in the routed format (per 256 columns), 8 bf16 rows
     const long long cr = static_cast<long long>(kDownRows) * (Q4 ? 144 : 84), cs = kDownSharedRows * 512LL;
     int begin, end;
@@ -1223,7 +1225,7 @@ int launch_down_stream(const DownParams &p, const StreamCfg &c, size_t smem, cud
 }  // namespace
 
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, bool shared_on_gemv,
-                   void *stream) {
+                   void *stream, const int32_t *shared_flag) {
     UpParams p;
     p.w = w;
     p.x = x;
@@ -1237,12 +1239,13 @@ int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *
     p.k = k;
     p.P = T * k;
     p.shared = shared_on_gemv && w.has_shared;
+    p.shared_flag = shared_flag;
     p.xq = reinterpret_cast<const uint4 *>(ws.xq);
     p.x8 = ws.x8;
     p.xsc = reinterpret_cast<const float4 *>(ws.xsc);
     p.status = ws.status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (w.fmt == 1 && T == 1) {  // streamed when its ring fits and every copy source is 16-byte aligned
+    if (w.fmt == 1 && T == 1 && !shared_flag) {  // streamed when its ring fits and every copy source is 16-byte aligned
         size_t smem = 0;
         const StreamCfg c = plan_up_stream(w, smem);
         const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(ws.xq) |
@@ -1260,7 +1263,7 @@ int launch_prep_h(const Workspace &ws, int rows, int F, void *stream) {
 }
 
 int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream,
-                     bool int16_h) {
+                     bool int16_h, const int32_t *shared_flag) {
     DownParams p;
     p.w = w;
     p.offsets = ws.offsets;
@@ -1271,6 +1274,7 @@ int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, 
     p.T = T;
     p.P = T * k;
     p.shared = shared_on_gemv && w.has_shared;
+    p.shared_flag = shared_flag;
     p.hq = int16_h ? reinterpret_cast<const uint4 *>(ws.hq4) : nullptr;
     p.hsum = ws.hsum4;
     p.hsc = ws.hsc4;

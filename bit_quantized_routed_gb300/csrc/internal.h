@@ -176,6 +176,10 @@ struct Workspace {
     uint32_t *hq4;      // 4-bit variant handles: [P][F/8][4] h as int16 dp2a pairs (prep_h)
     int *hsum4;         // [P][F/32] sum of each 32-column sub-block of hq4
     float *hsc4;        // [P] factor from hq4 back to h
+    int32_t *ovf;       // [E+1] per call: the expert's (E: the shared expert's) tensor-core result
+                        // overflowed fp16 and is recomputed in fp32 before the combine
+    int32_t *repair_list; // [E] the experts to recompute
+    GroupMeta *meta2;   // their count (n_gemv; the other fields 0)
 };
 
 }  // namespace ds4moe
@@ -216,10 +220,11 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
                  void *stream);
 int launch_pool_assign(const SlotPool &sp, int32_t *idx, int P, int *status, void *stream);
 int launch_pool_fill(const SlotPool &sp, const DeviceWeights &w, int n_sms, void *stream);
+// ovf (may be null): the call's overflow flags [E+1], cleared here
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok,
                  int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list,
                  int32_t *gemm_list, int32_t *single_list, int32_t *tile_prefix, int32_t *tile_desc, int32_t *small_pos, GroupMeta *meta,
-                 int *status, void *stream);
+                 int *status, void *stream, int32_t *ovf = nullptr);
 bool small_groups_supported(const DeviceWeights &w);
 int launch_prep_x(const Workspace &ws, const uint16_t *x, int T, int D, void *stream);
 int launch_small_up(const DeviceWeights &w, const Workspace &ws, int T, int k, void *stream);
@@ -247,11 +252,16 @@ int launch_decode_step(const DeviceWeights &w, const Workspace &ws, const uint16
                        int gate_mode, float *out, uint64_t *trace, int E_route, const int32_t *slot_of,
                        unsigned int bar_extra, void *stream);
 int decode_step_ctas();
+// shared_flag: non-null for a repair (launch_repair_list): the shared expert only when *shared_flag
 int launch_gemv_up(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k,
-                   bool shared_on_gemv, void *stream);
+                   bool shared_on_gemv, void *stream, const int32_t *shared_flag = nullptr);
 // int16_h: the 4-bit variant's down rows on int16 h (launch_prep_h first)
 int launch_gemv_down(const DeviceWeights &w, const Workspace &ws, int T, int k, bool shared_on_gemv, void *stream,
-                     bool int16_h = false);
+                     bool int16_h = false, const int32_t *shared_flag = nullptr);
+// After the tensor-core GEMMs: the experts whose tensor-core results overflowed fp16 (ovf, set by
+// the gather and the GEMM epilogues) into repair_list and meta2->n_gemv, for the GEMV kernels to
+// recompute in fp32 (ovf[E] is the shared expert's flag).
+int launch_repair_list(const DeviceWeights &w, const Workspace &ws, int gemm_min, void *stream);
 int launch_prep_h(const Workspace &ws, int rows, int F, void *stream);
 // gemm_min > 0: the pairs of groups of at least gemm_min tokens (tc_ok experts) ran on the
 // tensor-core down GEMM and their y rows hold fp16; shared_f16: so does the shared expert's.

@@ -110,8 +110,11 @@ __global__ void __launch_bounds__(kGroupThreads, 1)
                  int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                  int32_t *__restrict__ inv, int32_t *__restrict__ gemv_list, int32_t *__restrict__ gemm_list,
                  int32_t *__restrict__ single_list, int32_t *__restrict__ tile_prefix, int32_t *__restrict__ tile_desc,
-                 int32_t *__restrict__ small_pos, GroupMeta *meta, int *status) {
+                 int32_t *__restrict__ small_pos, GroupMeta *meta, int *status, int32_t *__restrict__ ovf) {
     pdl_wait();
+    if (ovf) {  // the call's overflow flags start clear (E + 1 of them)
+        for (int i = threadIdx.x; i <= E; i += kGroupThreads) ovf[i] = 0;
+    }
     extern __shared__ int sm[];
     int *hist = sm;                      // [kGroupWarps][E]: counts, then base positions
     int *tmp = sm + kGroupWarps * E;     // [32]
@@ -246,7 +249,7 @@ int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_
 int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const uint8_t *tc_ok, int32_t *counts,
                  int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *gemv_list, int32_t *gemm_list,
                  int32_t *single_list, int32_t *tile_prefix, int32_t *tile_desc, int32_t *small_pos, GroupMeta *meta, int *status,
-                 void *stream) {
+                 void *stream, int32_t *ovf) {
     const int P = T * k;
     const size_t smem = (static_cast<size_t>(kGroupWarps) * E + 32 + E) * sizeof(int);
     static int seen[64];
@@ -254,7 +257,7 @@ int launch_group(const int32_t *idx, int T, int k, int E, int gemm_min, const ui
     if (err) return err;
     return launch_pdl(group_kernel, dim3(1), dim3(kGroupThreads), smem, static_cast<cudaStream_t>(stream), idx, P, E,
                       gemm_min, tc_ok, counts, offsets, perm, inv, gemv_list, gemm_list, single_list, tile_prefix,
-                      tile_desc, small_pos, meta, status);
+                      tile_desc, small_pos, meta, status, ovf);
 }
 
 }  // namespace ds4moe

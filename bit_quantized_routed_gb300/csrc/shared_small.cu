@@ -37,7 +37,7 @@ struct SharedParams {
     const uint16_t *wu;
     uint16_t *h16;       // fp16 [T][F]: the shared expert's rows of the tensor-core path's h
     int T, D, F;
-    int *status;
+    int32_t *ovf_shared;  // set when an h value exceeds fp16: the shared expert is recomputed in fp32
 };
 
 // Fragment mapping of one 32-column step s (columns 32s .. 32s+31): thread (g = lane >> 2,
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_up_kernel(SharedParams p) 
             us += red[((w * 2 + 1) * kRows + r) * TT + t];
         }
         const float hv = swiglu(gs, us);
-        if (!(fabsf(hv) <= 65504.0f)) report(p.status, ST_RANGE);
+        if (!(fabsf(hv) <= 65504.0f)) *p.ovf_shared = 1;
         p.h16[static_cast<size_t>(t) * F + row0 + r] = __half_as_ushort(__float2half_rn(hv));
     }
 }
@@ -139,7 +139,7 @@ int launch_shared_up_small(const DeviceWeights &w, const Workspace &ws, const ui
     p.T = T;
     p.D = w.D;
     p.F = w.F;
-    p.status = ws.status;
+    p.ovf_shared = ws.ovf + w.E;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch ((T + 7) / 8) {
         case 1: return launch_nt<1>(p, s);

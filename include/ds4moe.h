@@ -47,7 +47,8 @@ enum ds4moe_status {
     DS4MOE_EBADDATA = 4,     /* input data rejected (non-finite weights, bad packed scale) */
     DS4MOE_ETIMEOUT = 5,     /* a bounded device-side wait gave up */
     DS4MOE_EUNSUPPORTED = 6, /* shape or device not supported by this build */
-    DS4MOE_ERANGE = 7,       /* a value overflowed the fp16 operand range of the tensor-core path */
+    DS4MOE_ERANGE = 7,       /* not returned by this version: tensor-core groups whose fp16 values
+                                overflow are recomputed in fp32 within the call */
     DS4MOE_ECAPACITY = 8     /* a call touched more experts than a pooled handle's slots */
 };
 
@@ -113,7 +114,8 @@ enum ds4moe_stage {
     DS4MOE_STAGE_COMBINE = 7,   /* gate-weighted combine into the residual */
     DS4MOE_STAGE_STEP = 8,      /* the single-token kernel: the whole call */
     DS4MOE_STAGE_POOL = 9,      /* pooled handles: slot assignment and the copies of missing experts */
-    DS4MOE_N_STAGES = 10
+    DS4MOE_STAGE_REPAIR = 10,   /* tensor-core groups whose fp16 values overflowed, recomputed in fp32 */
+    DS4MOE_N_STAGES = 11
 };
 
 typedef struct {
@@ -295,9 +297,9 @@ int ds4moe_group(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, 
  *   out       fp32 [T x d_model] residual, updated in place, 16-byte aligned.
  * Routing, grouping, the SwiGLU experts and the combine all run on the device with no
  * host synchronisation; results are bit-reproducible run to run. T <= max_tokens and
- * k <= max_k of the handle. EINVAL on bad arguments; device-side errors (ERANGE: a token, an h
- * or a y value beyond the fp16 range of the tensor-core path; ...) are reported by
- * ds4moe_last_status(). Source: "DwarfStar" README, "模型权重" (routed up/gate in IQ2_XXS, down
+ * k <= max_k of the handle. EINVAL on bad arguments; device-side errors are reported by
+ * ds4moe_last_status(). A group on the tensor-core path (and the shared expert there) whose token,
+ * h or y values overflow fp16 is recomputed in fp32 on the GEMV kernels within the same call. Source: "DwarfStar" README, "模型权重" (routed up/gate in IQ2_XXS, down
  * in Q2_K, the shared expert unquantised) and "DwarfStar 深度解析" §2.1 and §3.4.3 (the routed
  * MoE layer and its expert tree). Library readings: T added to the signature, gate_mode (the
  * pages name no gate function), SwiGLU as the activation, the shared expert at weight 1, and out

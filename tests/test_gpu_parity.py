@@ -242,22 +242,36 @@ def test_ffn_mixed_gemv_and_tensor_core_groups(ds4):
     assert err <= FFN_TOL, err
 
 
-def test_ffn_tensor_core_reports_fp16_overflow(ds4):
+@pytest.mark.parametrize("case", ["x", "h", "h_shared", "h_pairs", "h_shared_small"])
+def test_ffn_tensor_core_fp16_overflow_is_recomputed(ds4, case):
+    """Values beyond fp16's range on the tensor-core path (a bf16 token of 1e5, or tokens whose
+    SwiGLU h exceeds 65504) flag their group (or the shared expert); the call recomputes it in
+    fp32 on the GEMV kernels and the result matches the oracle, with a clean status."""
     import torch
-    wl = synth.Workload("ovf", T=40, D=256, F=256, E=2, k=1, seed=5)
+    shared = case in ("h_shared", "h_pairs", "h_shared_small")
+    wl = synth.Workload("ovf", T=40, D=512, F=256, E=4, k=2, seed=5, shared=shared)
     lay = Layer(wl, quantized=False)
-    lay.x[3, 7] = synth.f32_to_bf16_bits(np.array([1e5], np.float32))[0]   # beyond fp16
+    xf = (lay.x.astype(np.uint32) << 16).view(np.float32).copy()
+    if case == "x":
+        xf[3, 7] = 1e5                      # beyond fp16
+    else:
+        xf[5, :16] = 30000.0                # fits fp16, but h = silu(v) u is far beyond it
+    lay.x = synth.f32_to_bf16_bits(xf)
     W = lay.upload(ds4)
-    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_MIN_TOKENS, 1)
-    x = torch.from_numpy(lay.x.view(np.int16)).cuda().view(torch.bfloat16)
-    out = torch.zeros((wl.T, wl.D), dtype=torch.float32, device="cuda")
-    ds4.ds4moe_expert_ffn(x, W, torch.from_numpy(lay.L).cuda(), wl.k, out)
-    assert ds4.ds4moe_last_status(W) == ds4.DS4MOE_ERANGE
-    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_MIN_TOKENS, 0)      # the fp32 GEMV path has no such limit
-    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS, 0)
-    ds4.ds4moe_expert_ffn(x, W, torch.from_numpy(lay.L).cuda(), wl.k, out)
-    assert ds4.ds4moe_last_status(W) == 0
+    if case != "h_shared_small":  # (default thresholds: routed groups on the small-group kernels and
+        # the shared expert's gate/up on its warp-MMA kernel, its down on the tensor cores)
+        ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_MIN_TOKENS, 1)
+        ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SHARED_GEMM_MIN_TOKENS, 1)
+    if case == "h_pairs":
+        ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_GEMM_PAIRS, 1)
+    got = lay.run(ds4, W)                   # asserts a clean status
+    again = lay.run(ds4, W)
     W.close()
+    assert np.array_equal(got.view(np.uint32), again.view(np.uint32))
+    ref, _, _ = lay.oracle_delta()
+    assert norm_max_err(got, ref) <= FFN_TOL, norm_max_err(got, ref)
+    if case != "x":
+        assert np.max(np.abs(ref)) > 65504.0   # the overflow was real
 
 
 # ---------------------------------------------------------------- the small-group kernels
