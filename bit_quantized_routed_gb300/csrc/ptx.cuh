@@ -52,10 +52,9 @@ __device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, u
     return ok != 0;
 }
 
-// Waits for the phase of the given parity to complete. Gives up (false) when the CTA's
-// abort flag is raised or after kWaitCycles, raising the flag and the status bit itself.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status) {
-    if (mbar_test(bar, parity)) return true;
+// The loop of mbar_wait once the first test has failed (out of line: it is the rare path).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                   int *status) {
     const long long t0 = clock64();
     while (true) {
         if (mbar_test_sleep(bar, parity, 20000u)) return true;
@@ -66,6 +65,13 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
             return false;
         }
     }
+}
+
+// Waits for the phase of the given parity to complete. Gives up (false) when the CTA's
+// abort flag is raised or after kWaitCycles, raising the flag and the status bit itself. A phase
+// that is already complete costs one test in line, without a call.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status) {
+    return mbar_test(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, status);
 }
 
 // ------------------------------------------------------------------ CTA pairs (clusters of two)
