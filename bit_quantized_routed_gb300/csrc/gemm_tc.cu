@@ -364,25 +364,27 @@ struct Pipe {  // the producers' view of the stage ring
     int *status;
 };
 
-// Produces the A operand of all K stages of one tile for this thread's row (slice).
+// Produces the A operand of K stages [kb_begin, kb_end) of one tile (num_kb stages) for this
+// thread's row (slice).
 template <class Fmt>
-__device__ __forceinline__ bool produce_tile(const Fmt &f, int num_kb, uint8_t *smem, int stage_bytes, int a_off,
-                                             int r, Pipe &pp) {
+__device__ __forceinline__ bool produce_tile(const Fmt &f, int kb_begin, int kb_end, int num_kb, uint8_t *smem,
+                                             int stage_bytes, int a_off, int r, Pipe &pp) {
     constexpr int PF = Fmt::PF;
     typename Fmt::Data ring[PF];
 #pragma unroll
     for (int i = 0; i < PF; i++)
-        if (i < num_kb) ring[i] = f.fetch(i);
-    for (int kb0 = 0; kb0 < num_kb; kb0 += PF) {
+        if (kb_begin + i < kb_end) ring[i] = f.fetch(kb_begin + i);
+    for (int kb0 = kb_begin; kb0 < kb_end; kb0 += PF) {
 #pragma unroll
         for (int i = 0; i < PF; i++) {
-            if (kb0 + i >= num_kb) break;
+            const int kb = kb0 + i;
+            if (kb >= kb_end) break;
             const typename Fmt::Data cur = ring[i];
-            if (kb0 + i + PF < num_kb) ring[i] = f.fetch(kb0 + i + PF);
-            if (Fmt::PD > 0 && (kb0 + i) % Fmt::PE == 0 && kb0 + i + Fmt::PD < num_kb) f.prefetch(kb0 + i + Fmt::PD);
+            if (kb + PF < kb_end) ring[i] = f.fetch(kb + PF);
+            if (Fmt::PD > 0 && kb % Fmt::PE == 0 && kb + Fmt::PD < num_kb) f.prefetch(kb + Fmt::PD);
             if (!mbar_wait(smem_u32(pp.bars + 2 * pp.S + pp.stage), pp.phase ^ 1u, pp.abort_flag, pp.status))
                 return false;
-            f.emit(cur, smem_u32(smem + pp.stage * stage_bytes + a_off), r, kb0 + i);
+            f.emit(cur, smem_u32(smem + pp.stage * stage_bytes + a_off), r, kb);
             fence_proxy_async();
             mbar_arrive(smem_u32(pp.bars + pp.stage));
             if (++pp.stage == pp.S) {
@@ -565,7 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tc_fence_after();
                 const uint32_t idesc = idesc_f16(BM * CTAS, mma_n(ti.ntok));
                 for (int kb = 0; kb < num_kb; kb++) {
-                    if (!wait(full_a(stage), phase) || !wait(full_b(stage), phase) ||
+                    // both halves of the stage (producers' rows, token copy), tested together first
+                    if ((!mbar_test2(full_a(stage), full_b(stage), phase) &&
+                         (!wait(full_a(stage), phase) || !wait(full_b(stage), phase))) ||
                         (PAIR && !wait(peer_full(stage), phase))) {
                         ok = false;
                         break;
@@ -651,34 +655,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             return (KIND == DOWN ? a * BM * CTAS : 0) + static_cast<int>(crank) * BM;
         };
         Pipe pp{bars, S, 0, 0u, abort_flag, p.status};
+        // K stages [kb_begin, kb_end) of tile tt's A operand, in the tile's weight format
+        auto produce = [&](const Tile &tt, int kb_begin, int kb_end) -> bool {
+            const int wrow = tt.m * MR + tile_row0(sel) + r;
+            const int a_off = sel * A_BYTES;
+            if (KIND == UP) {
+                if (tt.shared) {
+                    BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D, part};
+                    return produce_tile(f, kb_begin, kb_end, num_kb, smem, STAGE_BYTES, a_off, r, pp);
+                } else if (FMT == 1) {
+                    Q4Fmt f{q4_row(p.w, sel, tt.e, wrow), part};
+                    return produce_tile(f, kb_begin, kb_end, num_kb, smem, STAGE_BYTES, a_off, r, pp);
+                } else {
+                    IQ2Fmt f{iq2_qs_row(p.w, sel, tt.e, wrow), iq2_d_row(p.w, sel, tt.e, wrow), tab, iq2_swz(p.w, wrow),
+                             part};
+                    return produce_tile(f, kb_begin, kb_end, num_kb, smem, STAGE_BYTES, a_off, r, pp);
+                }
+            } else {
+                if (tt.shared) {
+                    F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, part};
+                    return produce_tile(f, kb_begin, kb_end, num_kb, smem, STAGE_BYTES, a_off, r, pp);
+                } else if (FMT == 1) {
+                    Q4Fmt f{q4_row(p.w, 2, tt.e, wrow), part};
+                    return produce_tile(f, kb_begin, kb_end, num_kb, smem, STAGE_BYTES, a_off, r, pp);
+                } else {
+                    Q2KFmt f{q2k_sq_row(p.w, tt.e, wrow), q2k_dd_row(p.w, tt.e, wrow), part, tab};
+                    return produce_tile(f, kb_begin, kb_end, num_kb, smem, STAGE_BYTES, a_off, r, pp);
+                }
+            }
+        };
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int t = unit; t < total && ok; t += units) {
             const Tile ti = decode_tile(p, t, m_tiles, n_full);
-            const int wrow = ti.m * MR + tile_row0(sel) + r;
-            if (KIND == UP) {
-                if (ti.shared) {
-                    BF16Fmt f{(sel ? p.w.sh_up : p.w.sh_gate) + static_cast<size_t>(wrow) * D, part};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
-                } else if (FMT == 1) {
-                    Q4Fmt f{q4_row(p.w, sel, ti.e, wrow), part};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
-                } else {
-                    IQ2Fmt f{iq2_qs_row(p.w, sel, ti.e, wrow), iq2_d_row(p.w, sel, ti.e, wrow), tab, iq2_swz(p.w, wrow), part};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
-                }
-            } else {
-                if (ti.shared) {
-                    F16Fmt f{p.w.sh_down_f16 + static_cast<size_t>(wrow) * F, part};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
-                } else if (FMT == 1) {
-                    Q4Fmt f{q4_row(p.w, 2, ti.e, wrow), part};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
-                } else {
-                    Q2KFmt f{q2k_sq_row(p.w, ti.e, wrow), q2k_dd_row(p.w, ti.e, wrow), part, tab};
-                    ok = produce_tile(f, num_kb, smem, STAGE_BYTES, sel * A_BYTES, r, pp);
-                }
-            }
+            ok = produce(ti, 0, num_kb);
             if (!ok) break;
             // epilogue: accumulators -> registers -> global; four warps per TMEM lane quarter
             if (!wait(acc_full, acc_phase)) {
@@ -687,36 +697,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             tc_fence_after();
             bool range_ok = true;
+            static_assert(NA == 2, "the epilogue reads two accumulators");
             for (int c0 = 16 * colq; c0 < ti.ntok; c0 += 64) {
+                // 16 columns of both accumulators (gate and up, or the two down tiles), one wait
+                uint32_t v0[16], v1[16];
+                tmem_ld16_start(tmem + lane_addr + c0, v0);
+                tmem_ld16_start(tmem + lane_addr + BN + c0, v1);
+                tmem_wait_ld(v0, v1);
+                // two columns (tokens) per conversion: one packed fp32 -> fp16x2 round-to-nearest-even
                 if (KIND == UP) {
-                    const int orow = ti.m * MR + tile_row0(0) + q * 32 + lane;
-#pragma unroll 1
-                    for (int cb = c0; cb < c0 + 16 && cb < ti.ntok; cb += 8) {  // 8 columns at a time
-                        float g[8], uu[8];
-                        tmem_ld8(tmem + lane_addr + cb, g);
-                        tmem_ld8(tmem + lane_addr + BN + cb, uu);
+                    uint16_t *dst = p.h16 + static_cast<size_t>(ti.row0 + c0) * F + ti.m * MR + tile_row0(0) + q * 32 + lane;
 #pragma unroll
-                        for (int j = 0; j < 8; j++) {
-                            if (cb + j < ti.ntok) {
-                                const float h = swiglu_fast(g[j], uu[j]);
-                                range_ok &= fabsf(h) <= 65504.0f;
-                                p.h16[static_cast<size_t>(ti.row0 + cb + j) * F + orow] =
-                                    __half_as_ushort(__float2half_rn(h));
-                            }
+                    for (int j = 0; j < 16; j += 2) {
+                        const float h0 = swiglu_fast(__uint_as_float(v0[j]), __uint_as_float(v1[j]));
+                        const float h1 = swiglu_fast(__uint_as_float(v0[j + 1]), __uint_as_float(v1[j + 1]));
+                        const uint32_t hp = pack_h2(h0, h1);
+                        if (c0 + j < ti.ntok) {
+                            range_ok &= fabsf(h0) <= 65504.0f;
+                            dst[static_cast<size_t>(j) * F] = static_cast<uint16_t>(hp & 0xffffu);
+                        }
+                        if (c0 + j + 1 < ti.ntok) {
+                            range_ok &= fabsf(h1) <= 65504.0f;
+                            dst[static_cast<size_t>(j + 1) * F] = static_cast<uint16_t>(hp >> 16);
                         }
                     }
                 } else {
 #pragma unroll 1
                     for (int a = 0; a < NA; a++) {  // the two 128-row tiles
-                        const int orow = ti.m * MR + tile_row0(a) + q * 32 + lane;
-                        float v[16];
-                        tmem_ld16(tmem + lane_addr + a * BN + c0, v);
+                        uint16_t *dst = p.y16 + static_cast<size_t>(ti.row0 + c0) * (2 * D) + ti.m * MR + tile_row0(a) +
+                                        q * 32 + lane;
 #pragma unroll
-                        for (int j = 0; j < 16; j++) {
+                        for (int j = 0; j < 16; j += 2) {
+                            const float y0 = __uint_as_float(a ? v1[j] : v0[j]);
+                            const float y1 = __uint_as_float(a ? v1[j + 1] : v0[j + 1]);
+                            const uint32_t yp = pack_h2(y0, y1);
                             if (c0 + j < ti.ntok) {
-                                range_ok &= fabsf(v[j]) <= 65504.0f;
-                                p.y16[static_cast<size_t>(ti.row0 + c0 + j) * (2 * D) + orow] =
-                                    __half_as_ushort(__float2half_rn(v[j]));
+                                range_ok &= fabsf(y0) <= 65504.0f;
+                                dst[static_cast<size_t>(j) * (2 * D)] = static_cast<uint16_t>(yp & 0xffffu);
+                            }
+                            if (c0 + j + 1 < ti.ntok) {
+                                range_ok &= fabsf(y1) <= 65504.0f;
+                                dst[static_cast<size_t>(j + 1) * (2 * D)] = static_cast<uint16_t>(yp >> 16);
                             }
                         }
                     }

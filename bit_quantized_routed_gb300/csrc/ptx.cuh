@@ -40,6 +40,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // As mbar_test, but a thread whose phase is not complete may sleep up to ~hint_ns in the
 // instruction (it wakes when the phase completes): waiting warps then issue almost nothing.
+// Tests two barriers' phases of the same parity with both tests in flight together.
+__device__ __forceinline__ bool mbar_test2(uint32_t bar_a, uint32_t bar_b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred pa, pb;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 pa, [%1], %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 pb, [%2], %3;\n\t"
+        "and.pred pa, pa, pb;\n\t"
+        "selp.u32 %0, 1, 0, pa;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_a), "r"(bar_b), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
@@ -151,29 +166,23 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         : "memory");
 }
 
-// 32 TMEM lanes x 16 columns of 32-bit: this thread's lane, columns taddr.col .. +15.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-    uint32_t r[16];
+// 32 TMEM lanes x 16 columns of 32-bit (this thread's lane, columns taddr.col .. +15), without the
+// wait: the registers are valid only after tmem_wait_ld(r...).
+__device__ __forceinline__ void tmem_ld16_start(uint32_t taddr, uint32_t r[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
-// Eight consecutive fp32 accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float v[8]) {
-    uint32_t r[8];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
+// Waits for this thread's outstanding tcgen05.ld; the registers of the loads are passed through
+// so that no use of them is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t a[16], uint32_t b[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 8; i++) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; i++) asm volatile("" : "+r"(a[i]), "+r"(b[i]));
 }
 
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
