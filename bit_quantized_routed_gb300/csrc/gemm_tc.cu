@@ -54,12 +54,12 @@ struct Cfg {
 
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 
-// Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row atoms 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-           (static_cast<uint64_t>(2) << 61);
-}
+// Shared-memory matrix descriptor (K-major, SWIZZLE_128B, 8-row atoms 1024 bytes apart) as two words:
+// the low word holds the start address >> 4 (14 bits) and the leading-byte offset 1; the high word,
+// the same for every operand, the 1024-byte stride, the descriptor version bit and the swizzle mode.
+// A start address 16 * n bytes further is the low word + n (shared addresses stay below 2^18).
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) { return ((saddr >> 4) & 0x3FFFu) | (1u << 16); }
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
 
 // Instruction descriptor of kind::f16: fp16 A and B (K-major), fp32 accumulate, M x N.
 __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
@@ -575,16 +575,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         break;
                     }
                     tc_fence_after();
+                    // one add per operand descriptor: this thread shares its issue slots with producers
+                    const uint32_t a_lo = sw128_desc_lo(a_tile(stage, 0)), b_lo = sw128_desc_lo(b_tile(stage));
 #pragma unroll
                     for (int a = 0; a < NA; a++)
 #pragma unroll
                         for (int k = 0; k < BK / 16; k++) {
-                            const uint64_t ad = sw128_desc(a_tile(stage, a) + k * 32);
-                            const uint64_t bd = sw128_desc(b_tile(stage) + k * 32);
+                            const uint32_t ad = a_lo + static_cast<uint32_t>((a * A_BYTES + k * 32) >> 4);
+                            const uint32_t bd = b_lo + static_cast<uint32_t>((k * 32) >> 4);
                             if (PAIR)
-                                tc_mma_pair(tmem + a * BN, ad, bd, idesc, (kb | k) != 0);
+                                tc_mma_pair(tmem + a * BN, ad, bd, kSw128DescHi, idesc, (kb | k) != 0);
                             else
-                                tc_mma(tmem + a * BN, ad, bd, idesc, (kb | k) != 0);
+                                tc_mma(tmem + a * BN, ad, bd, kSw128DescHi, idesc, (kb | k) != 0);
                         }
                     issued = true;
                     if (PAIR) {  // the stage is free in both CTAs once these MMAs are done
