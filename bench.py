@@ -241,9 +241,15 @@ def algorithmic(wl, counts):
             "flops_up": flops_up, "flops_down": flops_down, "flops_call": flops_call}
 
 
+# headers whose inline code (waits, copies, MMA and decode helpers) the kernels compile in
+SHARED_HEADERS = ("common.cuh", "ptx.cuh", "step_common.cuh", "internal.h")
+
+
 def src_sha(*names):
+    """Hash of a kernel's source file and the shared headers: a traffic record is reported only
+    while this matches the one taken with it."""
     h = hashlib.sha256()
-    for n in names:
+    for n in names + SHARED_HEADERS:
         with open(os.path.join(ROOT, "bit_quantized_routed_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
