@@ -40,7 +40,7 @@ EXPORTED = [
     "ds4moe_quantize_q2k", "ds4moe_quantize_iq2", "ds4moe_quantize_q4k", "ds4moe_dequantize_q2k",
     "ds4moe_dequantize_iq2", "ds4moe_dequantize_q4k",
     "ds4moe_weights_create", "ds4moe_weights_create_q4", "ds4moe_weights_create_pooled", "ds4moe_pool_info", "ds4moe_weights_destroy", "ds4moe_set_option", "ds4moe_weights_dequantize",
-    "ds4moe_router_logits", "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
+    "ds4moe_router_logits", "ds4moe_router_last_status", "ds4moe_route", "ds4moe_group", "ds4moe_expert_ffn", "ds4moe_get_stats", "ds4moe_last_status",
     "ds4moe_expert_ffn_static", "ds4moe_step_trace", "ds4moe_test_fail_allocation",
 ]
 
@@ -98,6 +98,7 @@ def lib():
             "ds4moe_set_option": ([vp, i32, i32], i32),
             "ds4moe_weights_dequantize": ([vp, i32, i32, vp, vp, vp], i32),
             "ds4moe_router_logits": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
+            "ds4moe_router_last_status": ([vp], i32),
             "ds4moe_route": ([vp, i32, i32, i32, i32, vp, vp, vp], i32),
             "ds4moe_group": ([vp, i32, i32, i32, vp, vp, vp, vp, vp], i32),
             "ds4moe_expert_ffn": ([vp, vp, vp, i32, i32, i32, vp, vp], i32),
@@ -379,6 +380,11 @@ def ds4moe_step_trace(weights, max_ctas=1024):
     n = ctypes.c_int(0)
     _check(lib().ds4moe_step_trace(weights.handle, out.ctypes.data, out.size, ctypes.byref(n)), "ds4moe_step_trace")
     return out[:n.value].reshape(-1, 6)
+
+
+def ds4moe_router_last_status(stream=None):
+    """DS4MOE_ETIMEOUT if a tensor-core router call since the last query gave up a bounded wait."""
+    return lib().ds4moe_router_last_status(_stream(stream))
 
 
 def ds4moe_last_status(weights, stream=None):

@@ -534,6 +534,19 @@ int ds4moe_router_logits(const void *x, const void *w_router, const float *bias,
                                      D, E, logits, stream));
 }
 
+int ds4moe_router_last_status(ds4moe_stream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4MOE_ECUDA;
+    }
+    int st = 0;
+    if (router_read_status(&st)) {
+        cudaGetLastError();
+        return DS4MOE_ECUDA;
+    }
+    return (st & ST_TIMEOUT) ? DS4MOE_ETIMEOUT : DS4MOE_OK;
+}
+
 int ds4moe_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *topk_idx, float *topk_w,
                  ds4moe_stream_t stream) {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return DS4MOE_EINVAL;

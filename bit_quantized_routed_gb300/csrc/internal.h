@@ -216,6 +216,12 @@ namespace ds4moe {
 // Launchers (return a cudaError_t as int; 0 = success).
 int launch_router(const uint16_t *x, const uint16_t *w, const float *bias, int T, int D, int E, float *logits,
                   void *stream);
+// The tensor-core router (router_tc.cu): calls of at least 64 tokens with E a multiple of 128.
+bool router_tc_supported(int T, int D, int E);
+int launch_router_tc(const uint16_t *x, const uint16_t *w, const float *bias, int T, int D, int E, float *logits,
+                     void *stream);
+// Reads and clears the tensor-core router's status bits (ST_TIMEOUT); 0 on success.
+int router_read_status(int *st);
 int launch_route(const float *logits, int T, int E, int k, int gate_mode, int32_t *idx, float *w,
                  void *stream);
 int launch_pool_assign(const SlotPool &sp, int32_t *idx, int P, int *status, void *stream);

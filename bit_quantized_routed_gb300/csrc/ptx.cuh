@@ -185,6 +185,13 @@ __device__ __forceinline__ void tmem_ld16_start(uint32_t taddr, uint32_t r[16]) 
         : "r"(taddr));
 }
 
+// As tmem_wait_ld below, for one load's registers.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t a[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) asm volatile("" : "+r"(a[i]));
+}
+
 // Waits for this thread's outstanding tcgen05.ld; the registers of the loads are passed through
 // so that no use of them is scheduled before the wait.
 __device__ __forceinline__ void tmem_wait_ld(uint32_t a[16], uint32_t b[16]) {

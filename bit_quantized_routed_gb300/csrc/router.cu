@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace ds4moe {
 namespace {
@@ -110,6 +111,7 @@ int launch_tt(const uint16_t *x, const uint16_t *w, const float *bias, int T, in
 int launch_router(const uint16_t *x, const uint16_t *w, const float *bias, int T, int D, int E, float *logits,
                   void *stream) {
     if (T == 0) return 0;
+    if (router_tc_supported(T, D, E)) return launch_router_tc(x, w, bias, T, D, E, logits, stream);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return T < 4 ? launch_tt<1>(x, w, bias, T, D, E, logits, s) : launch_tt<4>(x, w, bias, T, D, E, logits, s);
 }

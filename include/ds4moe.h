@@ -258,16 +258,26 @@ int ds4moe_weights_dequantize(const ds4moe_weights *w, int expert, int matrix, f
  * + bias[e]. x bf16 [T x D] and w_router bf16 [E x D] row-major, 16-byte aligned; bias fp32 [E]
  * or NULL; logits fp32 [T x E]. D a multiple of 256 (<= 8192), E a multiple of 8 (<= 1024),
  * T >= 0 (T = 0 is a no-op). Device pointers, asynchronous on the stream.
- * Fixed fp32 order (the top-k compares these values, so the order is part of the result): the
- * columns are cut into segments of 1024 (the last one shorter when D is not a multiple); per
- * (t, e) and segment, 32 partial sums p_l, each adding in increasing d the products of the
- * segment's columns d with (d / 8) % 32 == l (each bf16 x bf16 product is exact in fp32; one FMA
- * per product), then p_l += p_(l xor o) for o = 16, 8, 4, 2, 1; the segment sums are added in
- * increasing segment order, then bias[e]; every addition rounds to nearest even.
+ * The fp32 order is fixed for a given (T, D, E), so the top-k after it is reproducible run to
+ * run. T < 64, or E not a multiple of 128 (CUDA cores): the columns are cut into segments of 1024
+ * (the last one shorter when D is not a multiple); per (t, e) and segment, 32 partial sums p_l,
+ * each adding in increasing d the products of the segment's columns d with (d / 8) % 32 == l (each
+ * bf16 x bf16 product is exact in fp32; one FMA per product), then p_l += p_(l xor o) for
+ * o = 16, 8, 4, 2, 1; the segment sums are added in increasing segment order, then bias[e]; every
+ * addition rounds to nearest even. T >= 64 and E a multiple of 128 (tensor cores): the products of
+ * 16 consecutive columns are added to an fp32 accumulator in increasing column blocks (the order
+ * within a block is the hardware's), then bias[e]. A bounded wait that gives up (no completion of
+ * a copy or an MMA within about 2 s) leaves that CTA's logits unwritten and is reported by
+ * ds4moe_router_last_status().
  * Source: "DwarfStar" README, "模型权重", and "DwarfStar 深度解析" §3.4.3 (the router stays
  * unquantised; bf16 weights and an fp32 bias are this library's reading). */
 int ds4moe_router_logits(const void *x, const void *w_router, const float *bias, int T, int D, int E,
                          float *logits, ds4moe_stream_t stream);
+
+/* Synchronises the stream and reports whether a tensor-core router call since the last query had
+ * a bounded wait give up: DS4MOE_ETIMEOUT (then clears it), DS4MOE_OK, or DS4MOE_ECUDA. The state
+ * is per process (the router takes no handle). */
+int ds4moe_router_last_status(ds4moe_stream_t stream);
 
 /* Top-k routing: per token t, the k experts with the largest logits (ties to the lower
  * expert index; NaN orders as -inf), in that order, and their gate weights (mode above).

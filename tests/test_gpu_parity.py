@@ -412,27 +412,37 @@ def _valid_selection(sel, ref, bound):
     return np.min(ref[mask] + bound[mask]) >= np.max(ref[~mask] - bound[~mask])
 
 
+def _router_on_tensor_cores(T, E):
+    return T >= 64 and E % 128 == 0
+
+
 @pytest.mark.parametrize("T,D,E,bias", [(1, 4096, 256, True), (37, 512, 64, False), (4, 256, 8, True),
-                                        (130, 1024, 128, True), (3, 7168, 256, False)])
+                                        (130, 1024, 128, True), (3, 7168, 256, False), (64, 256, 128, False),
+                                        (200, 4096, 256, False), (321, 7168, 256, True), (63, 2048, 256, True)])
 def test_router_logits_within_the_fp32_bound_and_the_selection_from_them(ds4, T, D, E, bias):
-    """The device's fp32 logits against the exact (fp64) sum: within the fp32 summation bound.
-    The selection is then exact wherever the k-th and (k+1)-th exact logits are further apart than
-    their bounds allow to swap, and a valid top-k within the bounds elsewhere; the selection from
-    the device's own logits is the oracle's selection from the same fp32 values, bit for bit."""
+    """The device's fp32 logits against the exact (fp64) sum: within the fp32 summation bound of
+    the order the call takes (CUDA cores below 64 tokens, the tensor cores' 16-column blocks from 64
+    tokens on). The selection is then exact wherever the k-th and (k+1)-th exact logits are further
+    apart than their bounds allow to swap, and a valid top-k within the bounds elsewhere; the
+    selection from the device's own logits is the oracle's selection from the same fp32 values,
+    bit for bit."""
     import torch
-    from oracle.router import fp32_bound, router_logits
+    from oracle.router import fp32_bound, router_logits, tensor_core_depth
     rng = np.random.default_rng(T + D + E)
     x = synth.f32_to_bf16_bits(rng.standard_normal((T, D)).astype(np.float32))
     w = synth.f32_to_bf16_bits((0.02 * rng.standard_normal((E, D))).astype(np.float32))
     b = (0.1 * rng.standard_normal(E)).astype(np.float32) if bias else None
     ref = router_logits(x, w, b)
-    bound = fp32_bound(x, w, b)
+    bound = fp32_bound(x, w, b, depth=tensor_core_depth(D) if _router_on_tensor_cores(T, E) else None)
     xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     wd = torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16)
     bd = torch.from_numpy(b).cuda() if bias else None
     got = ds4.ds4moe_router_logits(xd, wd, bd)
+    assert ds4.ds4moe_router_last_status() == 0
     g = got.cpu().numpy()
     assert np.all(np.abs(g.astype(np.float64) - ref) <= bound)
+    again = ds4.ds4moe_router_logits(xd, wd, bd).cpu().numpy()
+    assert np.array_equal(again.view(np.uint32), g.view(np.uint32))  # the same bits on every run
     k = min(8, E)
     idx, _ = ds4.ds4moe_route(got, k)
     idx = idx.cpu().numpy()
@@ -463,6 +473,24 @@ def test_router_logits_follow_the_documented_order(ds4):
     wd = torch.from_numpy(synth.f32_to_bf16_bits(w).view(np.int16)).cuda().view(torch.bfloat16)
     got = ds4.ds4moe_router_logits(xd, wd).cpu().numpy()
     assert np.all(got == 31.0)
+
+
+def test_router_logits_tensor_core_order(ds4):
+    """From 64 tokens on, 16-column blocks are added in increasing order into one fp32 accumulator:
+    2^30 (column 0), then 1 (column 16, lost: the fp32 spacing at 2^30 is 128), then -2^30 (column
+    32) leaves exactly 0; an order that cancels the large terms first keeps the 1 (the CUDA-core
+    order of fewer tokens gives 1)."""
+    import torch
+    D, E = 256, 128
+    w = np.zeros((E, D), np.float32)
+    w[:, 0], w[:, 16], w[:, 32] = 2.0 ** 15, 1.0, -(2.0 ** 15)
+    wd = torch.from_numpy(synth.f32_to_bf16_bits(w).view(np.int16)).cuda().view(torch.bfloat16)
+    for T, want in ((64, 0.0), (200, 0.0), (63, 1.0)):
+        x = np.zeros((T, D), np.float32)
+        x[:, 0], x[:, 16], x[:, 32] = 2.0 ** 15, 1.0, 2.0 ** 15
+        xd = torch.from_numpy(synth.f32_to_bf16_bits(x).view(np.int16)).cuda().view(torch.bfloat16)
+        got = ds4.ds4moe_router_logits(xd, wd).cpu().numpy()
+        assert np.all(got == want), (T, np.unique(got))
 
 
 def test_layer_from_hidden_states(ds4):

@@ -98,3 +98,40 @@ def test_the_seeded_router_keeps_the_workloads_routing_mix():
     top_drawn = np.bincount(oracle.route(L, wl.k)[0].ravel(), minlength=wl.E).max()
     top_router = np.bincount(oracle.route(R.astype(np.float32), wl.k)[0].ravel(), minlength=wl.E).max()
     assert 0.5 * top_drawn < top_router < 2.0 * top_drawn
+
+
+def _truncate_f32(v):
+    """fp32 rounding toward zero of fp64 values (the addition a truncating unit performs)."""
+    v = np.asarray(v, np.float64)
+    r = v.astype(np.float32)
+    up = np.abs(r.astype(np.float64)) > np.abs(v)
+    r[up] = np.nextafter(r[up], np.float32(0))
+    return r
+
+
+def test_tensor_core_bound_holds_for_block_sums_and_is_not_vacuous():
+    # the order the tensor-core router takes: 16-column blocks summed (here by halving, each
+    # addition truncated), added in increasing order into one accumulator (truncated), then the bias
+    from oracle.router import tensor_core_depth
+    rng = np.random.default_rng(5)
+    T, D, E = 3, 2048, 8
+    xb = _bits(rng.standard_normal((T, D)))
+    wb = _bits(0.02 * rng.standard_normal((E, D)))
+    b = (0.1 * rng.standard_normal(E)).astype(np.float32)
+    exact = router_logits(xb, wb, b)
+    bound = fp32_bound(xb, wb, b, depth=tensor_core_depth(D))
+    assert np.all(bound >= fp32_bound(xb, wb, b))  # the block order is the looser one
+    xv = bf16_to_f64(xb)
+    wv = bf16_to_f64(wb)
+    prod = (xv[:, None, :] * wv[None, :, :]).reshape(T, E, D // 16, 16)  # exact products
+    acc = np.zeros((T, E), np.float32)
+    for blk in range(D // 16):
+        p = prod[:, :, blk, :].astype(np.float32)
+        while p.shape[-1] > 1:
+            h = p.shape[-1] // 2
+            p = _truncate_f32(p[..., :h].astype(np.float64) + p[..., h:].astype(np.float64))
+        acc = _truncate_f32(acc.astype(np.float64) + p[..., 0].astype(np.float64))
+    got = _truncate_f32(acc.astype(np.float64) + b.astype(np.float64)[None, :]).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= bound)
+    assert np.max(np.abs(got - exact)) > 0
+    assert np.max(bound) < 0.02 * np.std(exact)
