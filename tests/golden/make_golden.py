@@ -15,7 +15,7 @@ import oracle  # noqa: E402
 def main():
     g = oracle.iq2_grid()
     with open(os.path.join(HERE, "iq2_grid.txt"), "w") as f:
-        f.write("# IQ2-style grid: 256 entries x 8 magnitudes (FORMAT.md), written by make_golden.py\n")
+        f.write("# the library's IQ2-style grid: 256 entries x 8 magnitudes, written by make_golden.py\n")
         f.write("# sha256 of the 2048 bytes: %s\n" % hashlib.sha256(g.tobytes()).hexdigest())
         for e in range(256):
             f.write(" ".join(str(int(v)) for v in g[e]) + "\n")
