@@ -814,47 +814,72 @@ __global__ void __launch_bounds__(kProducers) producer_dump_kernel(DeviceWeights
     }
 }
 
-// x (bf16) -> x16 (fp16) for rows of tensor-core groups and of the shared expert. One warp per
-// row: lane 0 resolves the row's token (or that the row is not on the tensor cores), then the
-// warp converts the token's D values, 8 per lane and step. A value beyond fp16's range flags the
-// row's expert (ovf[E]: the shared expert), whose results are then recomputed in fp32.
-__global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
+// x (bf16) -> x16 (fp16) for rows of tensor-core groups and of the shared expert, one warp per
+// token: lane j < k resolves the row of the token's j-th pair (or that its group is not on the
+// tensor cores), and the shared expert's row is P + token; the warp then reads the token's D values once, 32
+// columns x 8 per lane and group of four steps, and writes each group to every destination row. A
+// value beyond fp16's range flags each destination's expert (ovf[E]: the shared expert), whose
+// results are then recomputed in fp32.
+__global__ void __launch_bounds__(256, 4) gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ inv,
                                                      const int32_t *__restrict__ topk_idx,
                                                      const int32_t *__restrict__ counts,
                                                      const uint8_t *__restrict__ tc_ok, int gemm_min, int k, int D,
                                                      int P, int T, int shared, uint16_t *__restrict__ x16,
                                                      int32_t *__restrict__ ovf, int E) {
     pdl_wait();
+    constexpr int G = 4;  // 16-byte steps per lane held at once
     const int D8 = D / 8;
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
-    for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < P + T; row += warps) {
-        int tok = -1, owner = E;
-        if (lane == 0) {
-            if (row < P) {
-                const int pair = perm[row];
-                const int e = topk_idx[pair];
-                if (gemm_min > 0 && counts[e] >= gemm_min && tc_ok[e]) tok = pair / k;
-                owner = e;
-            } else if (shared) {
-                tok = row - P;
-            }
+    for (int tok = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < T; tok += warps) {
+        int row = -1, owner = E;  // this lane's destination row (routed pair j = lane) and its expert
+        if (lane < k) {
+            const int pair = tok * k + lane;
+            const int e = topk_idx[pair];
+            owner = e;
+            if (gemm_min > 0 && counts[e] >= gemm_min && tc_ok[e]) row = inv[pair];
         }
-        tok = __shfl_sync(0xffffffffu, tok, 0);
-        if (tok < 0) continue;
+        const unsigned rows = __ballot_sync(0xffffffffu, row >= 0);
+        if (!rows && !shared) continue;
         bool range_ok = true;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * D);
-        uint4 *dst = reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(row) * D);
-#pragma unroll 4
-        for (int c = lane; c < D8; c += 32) {
-            const uint4 v = __ldg(src + c);
-            const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        for (int c0 = 0; c0 < D8; c0 += 32 * G) {
+            uint4 v[G];
 #pragma unroll
-            for (int j = 0; j < 8; j++) range_ok &= fabsf(f[j]) <= 65504.0f;
-            dst[c] = make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+            for (int g = 0; g < G; g++) {
+                const int c = c0 + 32 * g + lane;
+                if (c < D8) {
+                    const uint4 b = __ldg(src + c);
+                    const float f[8] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
+                                        bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
+#pragma unroll
+                    for (int j = 0; j < 8; j++) range_ok &= fabsf(f[j]) <= 65504.0f;
+                    v[g] = make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+                }
+            }
+            for (unsigned m = rows; m; m &= m - 1) {
+                const int dl = __ffs(m) - 1;
+                const int r = __shfl_sync(0xffffffffu, row, dl);
+                uint4 *dst = reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(r) * D);
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const int c = c0 + 32 * g + lane;
+                    if (c < D8) dst[c] = v[g];
+                }
+            }
+            if (shared) {
+                uint4 *dst = reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(P + tok) * D);
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const int c = c0 + 32 * g + lane;
+                    if (c < D8) dst[c] = v[g];
+                }
+            }
         }
-        if (!__all_sync(0xffffffffu, range_ok) && lane == 0) ovf[owner] = 1;
+        if (!__all_sync(0xffffffffu, range_ok)) {
+            if (row >= 0) ovf[owner] = 1;
+            if (shared && lane == 0) ovf[E] = 1;
+        }
     }
 }
 
@@ -925,9 +950,9 @@ GemmParams make_params(const DeviceWeights &w, const Workspace &ws, int T, int k
 int launch_gather(const DeviceWeights &w, const Workspace &ws, const uint16_t *x, int T, int k, int gemm_min,
                   bool shared, void *stream) {
     const int P = T * k;
-    const int blocks = std::min((P + T + 7) / 8, sm_count_tc() * 8);  // a warp per row, 8 rows per CTA
+    const int blocks = std::min((T + 7) / 8, sm_count_tc() * 4);  // a warp per token, 8 tokens per CTA
     return launch_pdl(gather_kernel, dim3(blocks), dim3(256), 0, static_cast<cudaStream_t>(stream), x,
-                      static_cast<const int32_t *>(ws.perm), static_cast<const int32_t *>(ws.topk_idx),
+                      static_cast<const int32_t *>(ws.inv), static_cast<const int32_t *>(ws.topk_idx),
                       static_cast<const int32_t *>(ws.counts), static_cast<const uint8_t *>(w.tc_ok), gemm_min,
                       k, w.D, P, T, shared ? 1 : 0, ws.x16, ws.ovf, w.E);
 }
