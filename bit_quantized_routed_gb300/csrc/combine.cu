@@ -66,6 +66,10 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
         }
         __syncthreads();
         for (int c = threadIdx.x; c < D8; c += blockDim.x) {
+            // the residual's load is issued first and the slots' loads four at a time, so that
+            // several rows are in flight per thread
+            float4 *o = reinterpret_cast<float4 *>(p.out + static_cast<size_t>(t) * p.D) + 2 * c;
+            float4 a = o[0], b = o[1];
             float acc[8];
             if (p.shared) {
                 load8(p.y + static_cast<size_t>(p.P + t) * p.D, c, sh16, acc);
@@ -73,6 +77,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
 #pragma unroll
                 for (int i = 0; i < 8; i++) acc[i] = 0.0f;
             }
+#pragma unroll 4
             for (int s = 0; s < p.k; s++) {
                 float v[8];
                 load8(p.y + static_cast<size_t>(s_pos[s]) * p.D, c, s_f16[s] != 0, v);
@@ -80,8 +85,6 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
 #pragma unroll
                 for (int i = 0; i < 8; i++) acc[i] = fmaf(gw, v[i], acc[i]);
             }
-            float4 *o = reinterpret_cast<float4 *>(p.out + static_cast<size_t>(t) * p.D) + 2 * c;
-            float4 a = o[0], b = o[1];
             a.x += acc[0]; a.y += acc[1]; a.z += acc[2]; a.w += acc[3];
             b.x += acc[4]; b.y += acc[5]; b.z += acc[6]; b.w += acc[7];
             o[0] = a;
