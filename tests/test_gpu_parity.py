@@ -99,6 +99,18 @@ def test_group_one_expert_takes_all(ds4):
         assert np.array_equal(a.cpu().numpy(), b)
 
 
+@pytest.mark.parametrize("T,k,E", [(777, 3, 40), (1, 1, 8), (4097, 8, 256), (33, 5, 7)])
+def test_group_bitexact_ragged_pair_counts(ds4, T, k, E):
+    # pair counts that leave every warp's share, and its last batch of loads, partly empty
+    import torch
+    rng = np.random.default_rng(T * k + E)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ref = oracle.permute(idx, E)
+    got = ds4.ds4moe_group(torch.from_numpy(idx).cuda(), E)
+    for a, b in zip(got, ref):
+        assert np.array_equal(a.cpu().numpy(), b)
+
+
 # ---------------------------------------------------------------- device dequantisation
 
 @pytest.mark.parametrize("D,F", [(512, 768), (768, 512)])   # even and odd blocks per row (chunk permutation)
