@@ -9,6 +9,7 @@
 // sums are combined by xor-shuffles 16, 8, 4, 2, 1; the segment sums are added in increasing order,
 // then the bias. A CTA computes TT tokens x 4 experts with one warp per segment, so even one token
 // spreads the router's bytes over E / 4 x (D / 1024) warps, each with all its loads in flight at once.
+// Calls of 64 tokens or more (E a multiple of 128) run on the tensor cores instead (router_tc.cu).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
