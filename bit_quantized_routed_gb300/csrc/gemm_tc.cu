@@ -566,17 +566,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 tc_fence_after();
                 const uint32_t idesc = idesc_f16(BM * CTAS, mma_n(ti.ntok));
-                for (int kb = 0; kb < num_kb; kb++) {
-                    // both halves of the stage (producers' rows, token copy), tested together first
-                    if ((!mbar_test2(full_a(stage), full_b(stage), phase) &&
-                         (!wait(full_a(stage), phase) || !wait(full_b(stage), phase))) ||
-                        (PAIR && !wait(peer_full(stage), phase))) {
-                        ok = false;
-                        break;
-                    }
+                // one stage: wait for both halves (producers' rows, token copy; tested together
+                // first), the MMAs, the commit that frees the stage
+                auto stage_mmas = [&](int st, uint32_t ph, int kb) -> bool {
+                    if ((!mbar_test2(full_a(st), full_b(st), ph) && (!wait(full_a(st), ph) || !wait(full_b(st), ph))) ||
+                        (PAIR && !wait(peer_full(st), ph)))
+                        return false;
                     tc_fence_after();
                     // one add per operand descriptor: this thread shares its issue slots with producers
-                    const uint32_t a_lo = sw128_desc_lo(a_tile(stage, 0)), b_lo = sw128_desc_lo(b_tile(stage));
+                    const uint32_t a_lo = sw128_desc_lo(a_tile(st, 0)), b_lo = sw128_desc_lo(b_tile(st));
 #pragma unroll
                     for (int a = 0; a < NA; a++)
 #pragma unroll
@@ -590,16 +588,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         }
                     issued = true;
                     if (PAIR) {  // the stage is free in both CTAs once these MMAs are done
-                        tc_commit_pair(empty(stage));
-                        tc_commit_pair(map_shared(empty(stage), 1u));
+                        tc_commit_pair(empty(st));
+                        tc_commit_pair(map_shared(empty(st), 1u));
                     } else {
-                        tc_commit(empty(stage));
+                        tc_commit(empty(st));
                     }
+                    return true;
+                };
+                auto advance = [&]() {
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                };
+                // stages up to the ring's start, then whole turns of the ring with the stage index
+                // known at compile time (fewer instructions between stages), then the rest
+                int kb = 0;
+                for (; ok && kb < num_kb && stage != 0; kb++, advance()) ok = stage_mmas(stage, phase, kb);
+                for (; ok && kb + S <= num_kb; kb += S) {
+#pragma unroll
+                    for (int st = 0; st < S; st++)
+                        if (ok) ok = stage_mmas(st, phase, kb + st);
+                    phase ^= 1u;
                 }
+                for (; ok && kb < num_kb; kb++, advance()) ok = stage_mmas(stage, phase, kb);
                 if (!ok) break;
                 if (PAIR) {
                     tc_commit_pair(acc_full);
