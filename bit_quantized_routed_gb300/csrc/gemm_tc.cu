@@ -76,6 +76,10 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Bits 15 and 31 of the result: set for an fp16 half of hp that is +-inf or NaN (its magnitude
+// bits at or above 0x7c00; adding 0x0400 to each 15-bit magnitude carries into bit 15 exactly then).
+__device__ __forceinline__ uint32_t f16x2_overflow(uint32_t hp) { return ((hp & 0x7fff7fffu) + 0x04000400u) & 0x80008000u; }
+
 __device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -710,7 +714,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 break;
             }
             tc_fence_after();
-            bool range_ok = true;
+            // overflow bits of the tile's fp16 results: bit 15 / 31 of f16x2_overflow for a half that is
+            // +-inf or NaN (the value is beyond fp16's range after rounding)
+            uint32_t bad = 0;
+            bool range_ok_down = true;  // the down GEMM's per-value test (its register budget prefers it)
             static_assert(NA == 2, "the epilogue reads two accumulators");
             for (int c0 = 16 * colq; c0 < ti.ntok; c0 += 64) {
                 // 16 columns of both accumulators (gate and up, or the two down tiles), one wait
@@ -718,21 +725,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tmem_ld16_start(tmem + lane_addr + c0, v0);
                 tmem_ld16_start(tmem + lane_addr + BN + c0, v1);
                 tmem_wait_ld(v0, v1);
-                // two columns (tokens) per conversion: one packed fp32 -> fp16x2 round-to-nearest-even
+                // two columns (tokens) per conversion: one packed fp32 -> fp16x2 round-to-nearest-even;
+                // a chunk of 16 valid tokens (all but a ragged tile's last) takes no per-token checks
+                const int nv = min(16, ti.ntok - c0);  // valid tokens of the chunk, uniform over the warp
                 if (KIND == UP) {
                     uint16_t *dst = p.h16 + static_cast<size_t>(ti.row0 + c0) * F + ti.m * MR + tile_row0(0) + q * 32 + lane;
+                    if (nv == 16) {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float h0 = swiglu_fast(__uint_as_float(v0[j]), __uint_as_float(v1[j]));
-                        const float h1 = swiglu_fast(__uint_as_float(v0[j + 1]), __uint_as_float(v1[j + 1]));
-                        const uint32_t hp = pack_h2(h0, h1);
-                        if (c0 + j < ti.ntok) {
-                            range_ok &= fabsf(h0) <= 65504.0f;
+                        for (int j = 0; j < 16; j += 2) {
+                            const uint32_t hp = pack_h2(swiglu_fast(__uint_as_float(v0[j]), __uint_as_float(v1[j])),
+                                                        swiglu_fast(__uint_as_float(v0[j + 1]), __uint_as_float(v1[j + 1])));
+                            bad |= f16x2_overflow(hp);
                             dst[static_cast<size_t>(j) * F] = static_cast<uint16_t>(hp & 0xffffu);
-                        }
-                        if (c0 + j + 1 < ti.ntok) {
-                            range_ok &= fabsf(h1) <= 65504.0f;
                             dst[static_cast<size_t>(j + 1) * F] = static_cast<uint16_t>(hp >> 16);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const uint32_t hp = pack_h2(swiglu_fast(__uint_as_float(v0[j]), __uint_as_float(v1[j])),
+                                                        swiglu_fast(__uint_as_float(v0[j + 1]), __uint_as_float(v1[j + 1])));
+                            if (j < nv) {
+                                bad |= f16x2_overflow(hp) & (j + 1 < nv ? 0x80008000u : 0x00008000u);
+                                dst[static_cast<size_t>(j) * F] = static_cast<uint16_t>(hp & 0xffffu);
+                            }
+                            if (j + 1 < nv) dst[static_cast<size_t>(j + 1) * F] = static_cast<uint16_t>(hp >> 16);
                         }
                     }
                 } else {
@@ -746,17 +762,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             const float y1 = __uint_as_float(a ? v1[j + 1] : v0[j + 1]);
                             const uint32_t yp = pack_h2(y0, y1);
                             if (c0 + j < ti.ntok) {
-                                range_ok &= fabsf(y0) <= 65504.0f;
+                                range_ok_down &= fabsf(y0) <= 65504.0f;
                                 dst[static_cast<size_t>(j) * (2 * D)] = static_cast<uint16_t>(yp & 0xffffu);
                             }
                             if (c0 + j + 1 < ti.ntok) {
-                                range_ok &= fabsf(y1) <= 65504.0f;
+                                range_ok_down &= fabsf(y1) <= 65504.0f;
                                 dst[static_cast<size_t>(j + 1) * (2 * D)] = static_cast<uint16_t>(yp >> 16);
                             }
                         }
                     }
                 }
             }
+            const bool range_ok = bad == 0 && range_ok_down;
             if (!range_ok) p.ovf[ti.shared ? p.w.E : ti.e] = 1;  // recomputed in fp32 before the combine
             tc_fence_before();
             mbar_arrive(acc_empty);
