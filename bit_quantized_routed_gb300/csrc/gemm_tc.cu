@@ -277,8 +277,8 @@ __device__ __forceinline__ uint4 q4_to_f16x8(uint32_t word, float ds, float dm) 
 // Rows of the 4-bit variant (gate, up or down), half row: one 32-weight sub-block per stage.
 struct Q4Fmt {
     static constexpr int PF = 2;
-    static constexpr int PD = 0;
-    static constexpr int PE = 1;
+    static constexpr int PD = 8;  // L2 prefetch distance (stages), once per 144-byte block (4 stages)
+    static constexpr int PE = 4;
     struct Data {
         uint4 q;
         uint32_t dd, lo, hi;
@@ -295,7 +295,11 @@ struct Q4Fmt {
         v.hi = __ldg(reinterpret_cast<const uint32_t *>(blk + 12));
         return v;
     }
-    __device__ __forceinline__ void prefetch(int) const {}
+    __device__ __forceinline__ void prefetch(int kb) const {
+        const uint8_t *blk = row + (kb >> 2) * 144;
+        prefetch_l2(blk);
+        prefetch_l2(blk + 143);
+    }
     __device__ __forceinline__ void emit(const Data &v, uint32_t tile, int r, int kb) const {
         float ds, dm;
         q4_scales(v.dd, v.lo, v.hi, 2 * (kb & 3) + part, ds, dm);
