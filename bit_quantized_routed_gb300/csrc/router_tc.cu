@@ -202,12 +202,9 @@ bool router_tc_supported(int T, int D, int E) { return T >= 64 && E % kRtM == 0 
 
 int launch_router_tc(const uint16_t *x, const uint16_t *w, const float *bias, int T, int D, int E, float *logits,
                      void *stream) {
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem) != cudaSuccess)
-            return static_cast<int>(cudaGetLastError());
-        attr = true;
-    }
+    static int seen[64];  // per device: the kernel's shared-memory attribute is set
+    const int err = ensure_smem(reinterpret_cast<const void *>(router_tc_kernel), kRtSmem, seen);
+    if (err) return err;
     RouterMaps maps;
     if (encode_bf16_map(&maps.x, x, T, D) || encode_bf16_map(&maps.w, w, E, D)) return static_cast<int>(cudaErrorInvalidValue);
     const int blocks = (E / kRtM) * ((T + kRtN - 1) / kRtN);
