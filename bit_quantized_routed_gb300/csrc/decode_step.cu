@@ -816,14 +816,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(StepParams p) 
 #pragma unroll
             for (int r = 0; r < kRows2; r++) {
                 if (sval) {
-                    // sum_sb d sc_sb (q . h)_sb - dmin m_sb sum(h)_sb, in integers up to the two block factors
+                    // sum_sb d sc_sb (q . h)_sb - dmin m_sb sum(h)_sb, in integers up to the two block factors;
+                    // the two conversions go to the conversion unit, idle in this phase (rounded once)
                     const int a0 = q2k_idot(qw[r].x, hp), a1 = q2k_idot(qw[r].y, hp + 8);
                     const uint32_t sc = scw[r];
                     const int i1 = static_cast<int>(sc & 15u) * a0 + static_cast<int>((sc >> 8) & 15u) * a1;
                     const int i2 = static_cast<int>((sc >> 4) & 15u) * hs0 + static_cast<int>(sc >> 12) * hs1;
                     const float d = f16_to_f32(static_cast<uint16_t>(dd[r] & 0xffffu));
                     const float dmin = f16_to_f32(static_cast<uint16_t>(dd[r] >> 16));
-                    acc[r] = gh * fmaf(d, int_to_float(i1), -dmin * int_to_float(i2));
+                    acc[r] = gh * fmaf(d, __int2float_rn(i1), -dmin * __int2float_rn(i2));
                 }
                 if (w.has_shared) {
                     acc[r] = fmaf(bf16_lo(bw[r].x), hs.x, acc[r]);

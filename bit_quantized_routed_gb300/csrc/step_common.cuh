@@ -24,12 +24,6 @@ __device__ __forceinline__ uint32_t round_to_int_bits(float v) {
 // Exact int -> float for |v| < 2^22 with two full-rate operations (no conversion unit).
 __device__ __forceinline__ float small_int_to_float(int v) { return __int_as_float(0x4B400000 + v) - 12582912.0f; }
 
-// int -> float rounded once, for any int, with full-rate operations only (no conversion unit):
-// (v >> 12) * 4096 + (v & 4095), both parts exact.
-__device__ __forceinline__ float int_to_float(int v) {
-    return fmaf(small_int_to_float(v >> 12), 4096.0f, small_int_to_float(v & 4095));
-}
-
 // d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) or with bytes 2, 3 (hi): signed 16-bit a,
 // unsigned bytes b.
 __device__ __forceinline__ int dp2a_lo_su(uint32_t a, uint32_t b, int c) {
