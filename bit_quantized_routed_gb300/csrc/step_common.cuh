@@ -84,13 +84,13 @@ __device__ __forceinline__ uint32_t iq2_sg_off(uint32_t qy, int g, uint32_t lane
 // Sixteen Q2_K-style 2-bit codes (one u32: byte b holds weights 4b..4b+3) dotted with 16 int16 h
 // stored as hp[2j] = (h_j, h_4+j), hp[2j+1] = (h_8+j, h_12+j).
 __device__ __forceinline__ int q2k_idot(uint32_t qw, const uint32_t *hp) {
-    int a[4];
+    int a = 0;  // one accumulation chain: the callers have several rows in flight
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         const int c = static_cast<int>((qw >> (2 * j)) & 0x03030303u);  // weights j, 4+j, 8+j, 12+j
-        a[j] = __dp2a_hi(static_cast<int>(hp[2 * j + 1]), c, __dp2a_lo(static_cast<int>(hp[2 * j]), c, 0));
+        a = __dp2a_hi(static_cast<int>(hp[2 * j + 1]), c, __dp2a_lo(static_cast<int>(hp[2 * j]), c, a));
     }
-    return (a[0] + a[1]) + (a[2] + a[3]);
+    return a;
 }
 
 // Position of h element r (0..15) of a 16-column sub-block in the order q2k_idot reads it.
