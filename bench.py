@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -241,17 +242,33 @@ def algorithmic(wl, counts):
             "flops_up": flops_up, "flops_down": flops_down, "flops_call": flops_call}
 
 
-# headers whose inline code (waits, copies, MMA and decode helpers) the kernels compile in
-SHARED_HEADERS = ("common.cuh", "ptx.cuh", "step_common.cuh", "internal.h")
+def _include_closure(names):
+    """The kernel source files and every header they include, directly or through another
+    header (quoted includes, resolved against the including file's folder), in a fixed order."""
+    csrc = os.path.join(ROOT, "bit_quantized_routed_gb300", "csrc")
+    todo = [os.path.normpath(os.path.join(csrc, n)) for n in names]
+    seen = []
+    while todo:
+        f = todo.pop(0)
+        if f in seen:
+            continue
+        seen.append(f)
+        with open(f) as fh:
+            for line in fh:
+                m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
+                if m:
+                    todo.append(os.path.normpath(os.path.join(os.path.dirname(f), m.group(1))))
+    return sorted(seen)
 
 
 def src_sha(*names):
-    """Hash of a kernel's source file and the shared headers: a traffic record is reported only
-    while this matches the one taken with it."""
+    """Hash of a kernel's source file and the headers it includes: a traffic record is reported
+    only while this matches the one taken with it."""
     h = hashlib.sha256()
-    for n in names + SHARED_HEADERS:
-        with open(os.path.join(ROOT, "bit_quantized_routed_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+    for f in _include_closure(names):
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
