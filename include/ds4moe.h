@@ -46,7 +46,7 @@ enum ds4moe_status {
     DS4MOE_ECUDA = 3,        /* a CUDA runtime call failed (no device, launch error, ...) */
     DS4MOE_EBADDATA = 4,     /* input data rejected (non-finite weights, bad packed scale) */
     DS4MOE_ETIMEOUT = 5,     /* a bounded device-side wait gave up */
-    DS4MOE_EUNSUPPORTED = 6, /* shape or device not supported by this build */
+    DS4MOE_EUNSUPPORTED = 6, /* shape or device not supported by the library */
     DS4MOE_ERANGE = 7,       /* not returned by this version: tensor-core groups whose fp16 values
                                 overflow are recomputed in fp32 within the call */
     DS4MOE_ECAPACITY = 8     /* a call touched more experts than a pooled handle's slots */
