@@ -398,6 +398,30 @@ def test_single_token_kernel_nan_and_infinite_logits(ds4, mode, E):
     W.close()
 
 
+@pytest.mark.parametrize("T", [1, 3, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("E", [64, 300])   # the route kernel's register layouts of 2 and 10 logits per lane
+def test_separate_kernels_route_nan_and_infinite_logits_like_the_oracle(ds4, T, mode, E):
+    """Without the fused kernel (the route, grouping and expert kernels): top-k and gate weights on
+    NaN, +inf and -inf logits, through the whole layer, each token a different special row among
+    -inf logits."""
+    wl = synth.Workload("nang", T=T, D=1024, F=2048, E=E, k=8, seed=93 + T, shared=True)
+    lay = Layer(wl, quantized=False, experts=range(E))
+    W = lay.upload(ds4)
+    ds4.ds4moe_set_option(W, ds4.DS4MOE_OPT_SINGLE_STEP, 0)
+    rng = np.random.default_rng(T + E)
+    L = np.full((T, E), -np.inf, np.float32)
+    for t in range(T):
+        L[t, :8] = _SPECIAL_ROWS[t % len(_SPECIAL_ROWS)]
+        L[t] = L[t, np.argsort(rng.permutation(E))]   # the special values at scattered experts
+    lay.L = L
+    got = lay.run(ds4, W, mode=mode)
+    W.close()
+    ref, idx, g = lay.oracle_delta(mode=mode)
+    assert np.all(np.isfinite(g)) and np.all(np.isfinite(got))
+    assert norm_max_err(got, ref) <= FFN_TOL
+
+
 def test_single_token_kernel_equals_separate_kernels_and_is_deterministic(ds4):
     import torch
     wl = synth.WORKLOADS["decode_t1"]
